@@ -1,0 +1,427 @@
+/*
+ * mxq_oracle.c -- plain, slow, scalar CPU oracle for the MXFP8 / NVFP4
+ * quantizer contract.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  The product path
+ * (the CUDA library and its Python binding) never calls it, links it or
+ * shares any code, header, table or constant generator with it.
+ *
+ * Sources (page title, section):
+ *  - "Miles: end-to-end MXFP8 and per-token NVFP4 RL", formats section:
+ *      MXFP8 = E4M3 elements, 32 consecutive values share one E8M0
+ *      (power-of-two) scale, 1-D blocks; the decoded scale is rounded up so
+ *      the block maximum is not clipped.
+ *      NVFP4 = E2M1 elements with one E4M3 scale per 16 values, rounded to
+ *      the nearest representable value, plus one FP32 scale over a larger
+ *      tensor scope (two-level hierarchy).
+ *  - same page, MXFP8 recipe section: rowwise 1x32 and columnwise 32x1
+ *      blocks are quantized independently from the full-precision data.
+ *  - same page, NVFP4 recipe section: one FP32 activation scale per token,
+ *      computed online; gate/up weights share one FP32 scale.
+ *  - same page, backward-mode section: dequantized backward consumes BF16
+ *      dequantizations of the exact forward low-precision operands.
+ *  - "Using Quantization in RL", section "Two Ways to Configure Training
+ *      and Inference": a stored value is interpreted as code x scale.
+ *
+ * Design rules of this file:
+ *  - Every format is decoded from its bit pattern (sign / exponent /
+ *    mantissa fields), and every rounding is a brute-force nearest search
+ *    over the decoded table with ties resolved to the even code.  No bit
+ *    tricks are used to round.
+ *  - MXFP8 arithmetic is exact: block amax, the power-of-two scale and the
+ *    scaled element x * 2^-k are computed in binary64, where all of them are
+ *    exact for bf16 inputs.
+ *  - NVFP4 arithmetic is binary32, because the pages fix the second-level
+ *    scale as an FP32 number; every step is one IEEE binary32 operation
+ *    with round-to-nearest-even (compiled with -ffp-contract=off, no fast
+ *    math, FLT_EVAL_METHOD == 0).
+ *  - Readings of points the pages leave open (listed in the design notes):
+ *      scale exponent k = smallest integer with 448 * 2^k >= amax, clamped
+ *      to [-127, 127] (an all-zero block gets k = -127, scale byte 0x00);
+ *      NVFP4 FP32 scale is a decode scale S = amax / (6 * 448);
+ *      block scale sb = RNE_E4M3(amax_b / (6 * S)); element encode factor
+ *      enc = 1 / (E4M3(sb) * S) (0 when that product is 0, FLT_MAX-clamped);
+ *      packed E2M1: lower-index element in the low nibble.
+ *
+ * Logical layouts produced here (row-major, no padding, no swizzle):
+ *  - MXFP8 rowwise: codes [R x C], scales [R x C/32] (block j of row r at
+ *    r*(C/32)+j).
+ *  - MXFP8 columnwise of X [M x K]: codes stored transposed [K x M] (byte
+ *    (k, m) at k*M+m) and scales [K x M/32].
+ *  - NVFP4: codes [R x C/2] (two per byte), block scales [R x C/16].
+ *  - Swizzled scale layout: oracle_scale_swizzle() maps the logical matrix
+ *    to the 128x4-tile layout; it is a pure permutation with zero padding.
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#if !defined(FLT_EVAL_METHOD) || FLT_EVAL_METHOD != 0
+#error "the oracle needs binary32 arithmetic evaluated in binary32"
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Format decoders, from the bit fields.                                     */
+/* ------------------------------------------------------------------------ */
+
+/* bf16: 1 sign, 8 exponent (bias 127), 7 mantissa bits. */
+static double bf16_decode(uint16_t b) {
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xFF;
+    int m = b & 0x7F;
+    double v;
+    if (e == 0xFF) return m ? NAN : (sign ? -INFINITY : INFINITY);
+    if (e == 0) v = ldexp((double)m / 128.0, -126);           /* subnormal */
+    else v = ldexp(1.0 + (double)m / 128.0, e - 127);
+    return sign ? -v : v;
+}
+
+/* E4M3 ("fn"): 1 sign, 4 exponent (bias 7), 3 mantissa; S.1111.111 = NaN;
+ * no infinities; max finite 448. */
+static double e4m3_decode(uint8_t c) {
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa; no NaN/inf; max 6. */
+static double e2m1_decode(uint8_t c) {
+    int sign = (c >> 3) & 1;
+    int e = (c >> 1) & 0x3;
+    int m = c & 0x1;
+    double v;
+    if (e == 0) v = (double)m * 0.5;
+    else v = ldexp(1.0 + (double)m / 2.0, e - 1);
+    return sign ? -v : v;
+}
+
+/* E8M0 (unsigned): 2^(e-127) for e in [0, 254]; 0xFF = NaN. */
+static double e8m0_decode(uint8_t c) {
+    if (c == 0xFF) return NAN;
+    return ldexp(1.0, (int)c - 127);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Tables built by enumerating every code once.                              */
+/* ------------------------------------------------------------------------ */
+static double T_E4M3[256];
+static double T_E2M1[16];
+static int g_tables_ready = 0;
+
+static void build_tables(void) {
+    if (g_tables_ready) return;
+    for (int c = 0; c < 256; ++c) T_E4M3[c] = e4m3_decode((uint8_t)c);
+    for (int c = 0; c < 16; ++c) T_E2M1[c] = e2m1_decode((uint8_t)c);
+    g_tables_ready = 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Round-to-nearest-even by brute force over the non-negative codes.          */
+/* Saturate first (|v| > max -> max), then pick the nearest magnitude; on a   */
+/* tie the code with a 0 least-significant bit wins.  The sign bit of the    */
+/* input is kept, so a negative value that rounds to zero gives -0.          */
+/* ------------------------------------------------------------------------ */
+static uint8_t rne_e4m3(double v) {
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v);
+    if (a > 448.0) a = 448.0;
+    int best = 0;
+    double bestd = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {          /* 0x7F is NaN */
+        double d = fabs(T_E4M3[c] - a);
+        if (d < bestd || (d == bestd && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            bestd = d;
+        }
+    }
+    return (uint8_t)(best | (neg << 7));
+}
+
+static uint8_t rne_e2m1(double v) {
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v);
+    if (a > 6.0) a = 6.0;
+    int best = 0;
+    double bestd = INFINITY;
+    for (int c = 0; c <= 7; ++c) {
+        double d = fabs(T_E2M1[c] - a);
+        if (d < bestd || (d == bestd && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            bestd = d;
+        }
+    }
+    return (uint8_t)(best | (neg << 3));
+}
+
+/* Round a finite binary32 value to bf16, nearest, ties to even mantissa:
+ * the two candidates are the bf16 values that bracket it (truncation toward
+ * zero and the next bf16 away from zero); the nearer one wins, exactly
+ * compared in binary64.  Overflow past the largest bf16 goes to infinity
+ * as IEEE rounding does (the candidate above 0x7F7F is 0x7F80 = inf, and
+ * the halfway point to it is 2^128 - 2^119). */
+static uint16_t rne_bf16_from_f32(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u) {       /* inf / nan pass through */
+        uint16_t hi = (uint16_t)(u >> 16);
+        if (u & 0x007FFFFFu) hi |= 0x40;          /* keep NaN a NaN */
+        return hi;
+    }
+    uint16_t lo = (uint16_t)(u >> 16);            /* toward zero */
+    uint16_t up = (uint16_t)(lo + 1);             /* away from zero */
+    double x = fabs((double)f);
+    double vlo = fabs(bf16_decode(lo));
+    double vup;
+    if ((up & 0x7FFF) == 0x7F80) vup = ldexp(1.0, 128);  /* next step is inf */
+    else vup = fabs(bf16_decode(up));
+    double dlo = x - vlo, dup = vup - x;
+    if (dlo < dup) return lo;
+    if (dup < dlo) return up;
+    return (lo & 1) ? up : lo;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Exported codec probes (used by the pin tests).                            */
+/* ------------------------------------------------------------------------ */
+double oracle_decode_bf16(uint16_t b) { return bf16_decode(b); }
+double oracle_decode_e4m3(uint8_t c) { return e4m3_decode(c); }
+double oracle_decode_e2m1(uint8_t c) { return e2m1_decode(c); }
+double oracle_decode_e8m0(uint8_t c) { return e8m0_decode(c); }
+uint8_t oracle_rne_e4m3(double v) { build_tables(); return rne_e4m3(v); }
+uint8_t oracle_rne_e2m1(double v) { build_tables(); return rne_e2m1(v); }
+uint16_t oracle_rne_bf16(float f) { return rne_bf16_from_f32(f); }
+
+/* ------------------------------------------------------------------------ */
+/* MXFP8 (formats section + MXFP8 recipe section).                           */
+/* ------------------------------------------------------------------------ */
+
+/* E8M0 scale exponent for a block maximum a >= 0: the smallest k in
+ * [-127, 127] with 448 * 2^k >= a, i.e. the power-of-two scale "rounded
+ * up" so that a / 2^k never exceeds the E4M3 maximum.  Brute force over
+ * every representable scale. */
+static int mxfp8_scale_exponent(double a) {
+    for (int k = -127; k <= 127; ++k)
+        if (448.0 * ldexp(1.0, k) >= a) return k;
+    return 127;
+}
+
+int oracle_mxfp8_scale_exponent(double a) { return mxfp8_scale_exponent(a); }
+
+/* Encode one block of n values, read with a stride: returns the E8M0 byte
+ * and writes n E4M3 codes to out (contiguous). */
+static uint8_t mxfp8_encode_block(const uint16_t* x, int64_t stride, int n,
+                                  uint8_t* out) {
+    double a = 0.0;
+    for (int i = 0; i < n; ++i) {
+        double v = fabs(bf16_decode(x[(int64_t)i * stride]));
+        if (v > a) a = v;
+    }
+    int k = mxfp8_scale_exponent(a);
+    double inv = ldexp(1.0, -k);                /* exact power of two */
+    for (int i = 0; i < n; ++i)
+        out[i] = rne_e4m3(bf16_decode(x[(int64_t)i * stride]) * inv);
+    return (uint8_t)(k + 127);
+}
+
+/* Rowwise 1x32 blocks of X [R x C] (row stride ldx elements).
+ * codes [R x C], scales [R x C/32].  Returns 0, or -1 on a bad shape. */
+int oracle_mxfp8_quantize_rowwise(const uint16_t* x, int64_t R, int64_t C,
+                                  int64_t ldx, uint8_t* codes,
+                                  uint8_t* scales) {
+    if (C % 32 != 0 || R < 0 || ldx < C) return -1;
+    build_tables();
+    int64_t nb = C / 32;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t j = 0; j < nb; ++j)
+            scales[r * nb + j] = mxfp8_encode_block(
+                x + r * ldx + j * 32, 1, 32, codes + r * C + j * 32);
+    return 0;
+}
+
+/* Columnwise 32x1 blocks of X [M x K], quantized from X itself (never from
+ * the rowwise copy).  Output is stored transposed: codes_t [K x M] with
+ * byte (k, m) at k*M+m, scales_t [K x M/32].  Returns 0 or -1. */
+int oracle_mxfp8_quantize_colwise(const uint16_t* x, int64_t M, int64_t K,
+                                  int64_t ldx, uint8_t* codes_t,
+                                  uint8_t* scales_t) {
+    if (M % 32 != 0 || M < 0 || ldx < K) return -1;
+    build_tables();
+    int64_t nb = M / 32;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t j = 0; j < nb; ++j)
+            scales_t[k * nb + j] = mxfp8_encode_block(
+                x + (j * 32) * ldx + k, ldx, 32, codes_t + k * M + j * 32);
+    return 0;
+}
+
+/* Dequantize MXFP8: y = bf16( fl32( E4M3(code) * 2^(e-127) ) ), blocks of
+ * 32 along each row of codes [R x C]; scales [R x C/32] (logical layout).
+ * The binary32 product is formed exactly in binary64 and then rounded to
+ * binary32 (one rounding, as a binary32 multiply does), then to bf16. */
+int oracle_mxfp8_dequantize(const uint8_t* codes, const uint8_t* scales,
+                            int64_t R, int64_t C, uint16_t* y) {
+    if (C % 32 != 0) return -1;
+    int64_t nb = C / 32;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            double s = e8m0_decode(scales[r * nb + c / 32]);
+            float p = (float)(e4m3_decode(codes[r * C + c]) * s);
+            y[r * C + c] = rne_bf16_from_f32(p);
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4 (formats section + NVFP4 recipe section).                           */
+/* ------------------------------------------------------------------------ */
+
+/* max |x| over R rows of C values (exact; bf16 values are exact floats). */
+float oracle_bf16_amax(const uint16_t* x, int64_t R, int64_t C, int64_t ldx) {
+    double a = 0.0;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            double v = fabs(bf16_decode(x[r * ldx + c]));
+            if (v > a) a = v;
+        }
+    return (float)a;                      /* exact: a is a bf16 value */
+}
+
+/* Second-level FP32 scale: a decode scale, S = amax / (6 * 448). */
+float oracle_nvfp4_tensor_scale(float amax) {
+    const float fp4_max_times_e4m3_max = 2688.0f;  /* 6 * 448, exact */
+    return amax / fp4_max_times_e4m3_max;
+}
+
+/* Encode one 16-value block given the FP32 scale S.  Writes 16 E2M1 codes
+ * (one per byte, unpacked) and returns the E4M3 block-scale byte. */
+static uint8_t nvfp4_encode_block(const uint16_t* x, float S,
+                                  uint8_t* codes16) {
+    float ab = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+        float v = fabsf((float)bf16_decode(x[i]));
+        if (v > ab) ab = v;
+    }
+    uint8_t sb;
+    if (S == 0.0f) {
+        sb = 0x00;
+    } else {
+        float six_s = 6.0f * S;
+        float t = ab / six_s;
+        sb = rne_e4m3((double)t);
+    }
+    float d = (float)T_E4M3[sb] * S;   /* E4M3 value is exact in binary32 */
+    float enc;
+    if (d == 0.0f) {
+        enc = 0.0f;
+    } else {
+        enc = 1.0f / d;
+        if (enc > FLT_MAX) enc = FLT_MAX;
+    }
+    for (int i = 0; i < 16; ++i) {
+        float v = (float)bf16_decode(x[i]) * enc;
+        codes16[i] = rne_e2m1((double)v);
+    }
+    return sb;
+}
+
+/* Encode R rows of C values (C % 16 == 0) with FP32 scales: row r uses
+ * S[r * s_stride] (s_stride = 1: one scale per row, 0: one shared scale).
+ * codes [R x C/2] packed, lower-index element in the low nibble;
+ * scales [R x C/16]. */
+int oracle_nvfp4_encode_rows(const uint16_t* x, int64_t R, int64_t C,
+                             int64_t ldx, const float* S, int64_t s_stride,
+                             uint8_t* codes, uint8_t* scales) {
+    if (C % 16 != 0) return -1;
+    build_tables();
+    int64_t nb = C / 16;
+    uint8_t q[16];
+    for (int64_t r = 0; r < R; ++r) {
+        float s = S[r * s_stride];
+        for (int64_t j = 0; j < nb; ++j) {
+            scales[r * nb + j] = nvfp4_encode_block(x + r * ldx + j * 16, s, q);
+            for (int i = 0; i < 8; ++i)
+                codes[r * (C / 2) + j * 8 + i] =
+                    (uint8_t)((q[2 * i] & 0xF) | ((q[2 * i + 1] & 0xF) << 4));
+        }
+    }
+    return 0;
+}
+
+/* Per-token quantization: S_t = amax(row t) / 2688, then encode the row. */
+int oracle_nvfp4_quantize_per_token(const uint16_t* x, int64_t T, int64_t H,
+                                    int64_t ldx, uint8_t* codes,
+                                    uint8_t* scales, float* token_scales) {
+    if (H % 16 != 0) return -1;
+    for (int64_t t = 0; t < T; ++t)
+        token_scales[t] =
+            oracle_nvfp4_tensor_scale(oracle_bf16_amax(x + t * ldx, 1, H, H));
+    return oracle_nvfp4_encode_rows(x, T, H, ldx, token_scales, 1, codes,
+                                    scales);
+}
+
+/* Dequantize NVFP4: y = bf16( fl32( fl32(E2M1(c) * E4M3(sb)) * S ) ).
+ * codes [R x C/2], scales [R x C/16]; row r uses S[r * s_stride]. */
+int oracle_nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales,
+                            const float* S, int64_t s_stride, int64_t R,
+                            int64_t C, uint16_t* y) {
+    if (C % 16 != 0) return -1;
+    int64_t nb = C / 16;
+    for (int64_t r = 0; r < R; ++r) {
+        float s = S[r * s_stride];
+        for (int64_t c = 0; c < C; ++c) {
+            uint8_t byte = codes[r * (C / 2) + c / 2];
+            uint8_t q = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+            float bs = (float)e4m3_decode(scales[r * nb + c / 16]);
+            float p = (float)e2m1_decode(q) * bs;  /* exact (<= 6 bits) */
+            float v = p * s;
+            y[r * C + c] = rne_bf16_from_f32(v);
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Swizzled scale layout (not on the pages: the 128x4-tile layout that      */
+/* block-scaled tensor-core MMA reads).  Logical scale matrix [R x C] ->    */
+/* tiles of 128 rows x 4 columns, 512 bytes each, tile (rt, ct) at byte     */
+/* (rt * ceil(C/4) + ct) * 512; inside a tile, element (r, c) sits at        */
+/* (r % 32) * 16 + (r / 32) * 4 + c.  Padding bytes are 0x00.                */
+/* ------------------------------------------------------------------------ */
+int64_t oracle_swizzled_scale_bytes(int64_t R, int64_t C) {
+    int64_t rt = (R + 127) / 128, ct = (C + 3) / 4;
+    return rt * ct * 512;
+}
+
+int oracle_scale_swizzle(const uint8_t* logical, int64_t R, int64_t C,
+                         uint8_t* out) {
+    int64_t ct_n = (C + 3) / 4;
+    memset(out, 0, (size_t)oracle_swizzled_scale_bytes(R, C));
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            int64_t tile = (r / 128) * ct_n + (c / 4);
+            int64_t rr = r % 128, cc = c % 4;
+            out[tile * 512 + (rr % 32) * 16 + (rr / 32) * 4 + cc] =
+                logical[r * C + c];
+        }
+    return 0;
+}
+
+int oracle_scale_unswizzle(const uint8_t* swz, int64_t R, int64_t C,
+                           uint8_t* logical) {
+    int64_t ct_n = (C + 3) / 4;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            int64_t tile = (r / 128) * ct_n + (c / 4);
+            int64_t rr = r % 128, cc = c % 4;
+            logical[r * C + c] =
+                swz[tile * 512 + (rr % 32) * 16 + (rr / 32) * 4 + cc];
+        }
+    return 0;
+}
