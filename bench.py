@@ -1,0 +1,510 @@
+"""Benchmark of the MXFP8 / NVFP4 quantizer path on GB300.
+
+One step = one pass of every operation of the path over one batch of the
+activation workload X [8192 x 4096] bf16 (N(0,1) with 0.1% of entries x100):
+
+  1. mxfp8_quantize_rowcol   rowwise 1x32 + columnwise 32x1 copies, one pass,
+                             E8M0 scales in the swizzled tensor-core layout
+  2. dequantize_mxfp8        of the rowwise copy and of the columnwise copy
+  3. nvfp4_quantize_per_token X as 8192 tokens x 4096 hidden (FP32 scale per
+                             token, E4M3 per 16, packed E2M1)
+  4. dequantize_nvfp4        of (3), per-token scales
+  5. nvfp4_quantize_weight_shared  X as 4 gate/up pairs of [1024 x 4096]
+                             parts, each pair under one FP32 scale
+  6. dequantize_nvfp4        of (5), per-group scales
+
+value = algorithmic bytes of the step (bf16 read + codes / scales written,
+or codes / scales read + bf16 written) / device time, in GB/s.  Inputs are
+resident in HBM; every kernel reads data last touched at least one full
+step (~680 MB of traffic) earlier (three rotating input copies, two
+rotating output sets), so nothing is served from the 126 MB L2.
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (the oracle is the reference implementation of this path).
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("quantize GB/s and % of GB300 HBM peak (bytes in + codes/scales "
+          "out), bit-exact")
+UNIT = "GB/s"
+M, K = 8192, 4096
+PAIRS = 4                       # X viewed as 4 gate/up pairs
+PART_ROWS = M // (2 * PAIRS)    # 1024 rows per part
+WORKLOAD = ("MXFP8 rowwise+columnwise quantize (one pass) + both MXFP8 "
+            "dequantizes + NVFP4 per-token quantize/dequantize + NVFP4 "
+            "shared-scale weight quantize/dequantize of an activation "
+            "[8192 x 4096] bf16, N(0,1) with 0.1% entries x100")
+
+
+# --------------------------------------------------------------------------
+# Algorithmic bytes per operation.
+# --------------------------------------------------------------------------
+def op_bytes():
+    n = M * K
+    return {
+        "mxfp8_quantize_rowcol": n * 2 + 2 * (n + n // 32),
+        "dequantize_mxfp8_row": n + n // 32 + n * 2,
+        "dequantize_mxfp8_col": n + n // 32 + n * 2,
+        "nvfp4_quantize_per_token": n * 2 + n // 2 + n // 16 + 4 * M,
+        "dequantize_nvfp4_tokens": n // 2 + n // 16 + 4 * M + n * 2,
+        "nvfp4_quantize_weight_shared": n * 2 + n // 2 + n // 16 + 4 * PAIRS,
+        "dequantize_nvfp4_weights": n // 2 + n // 16 + 4 * PAIRS + n * 2,
+    }
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------
+# Clock sampling during the timed region.
+# --------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,"
+         "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# GPU arm.
+# --------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus and world > 1:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}")
+    return rank, world, local
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import nvfp4_quantizers_gb300 as q
+    import workloads as W
+    from nvfp4_quantizers_gb300 import build
+    build.build()
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    x_bits = W.mxfp8_random(M, K, seed=rank)
+    x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16)
+    X = [x_host.to(dev) for _ in range(3)]          # rotating input copies
+    stream = torch.cuda.Stream(dev)
+    lay = q.SCALE_SWIZZLED
+
+    def new_outputs():
+        return {
+            "rc": torch.empty((M, K), dtype=torch.uint8, device=dev),
+            "rs": torch.empty(q.scale_bytes(M, K // 32), dtype=torch.uint8, device=dev),
+            "cc": torch.empty((K, M), dtype=torch.uint8, device=dev),
+            "cs": torch.empty(q.scale_bytes(K, M // 32), dtype=torch.uint8, device=dev),
+            "tc": torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+            "ts": torch.empty(q.scale_bytes(M, K // 16), dtype=torch.uint8, device=dev),
+            "tS": torch.empty(M, dtype=torch.float32, device=dev),
+            "wc": torch.empty((PAIRS, 2 * PART_ROWS, K // 2), dtype=torch.uint8, device=dev),
+            "ws": torch.empty((PAIRS, q.scale_bytes(2 * PART_ROWS, K // 16)), dtype=torch.uint8, device=dev),
+            "wS": torch.empty(PAIRS, dtype=torch.float32, device=dev),
+        }
+
+    outs = [new_outputs(), new_outputs()]
+    y_row = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    y_col = torch.empty((K, M), dtype=torch.bfloat16, device=dev)
+    y_tok = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    y_w = torch.empty((PAIRS, 2 * PART_ROWS, K), dtype=torch.bfloat16, device=dev)
+    L = q.lib()
+    ws_bytes = int(L.nvfp4_quantize_weight_shared_workspace_size(PAIRS))
+    wsp = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    import ctypes
+    parts_tabs = []
+    for xi in X:
+        flat = xi.view(2 * PAIRS, PART_ROWS, K)
+        parts_tabs.append((ctypes.c_void_p * (2 * PAIRS))(
+            *[flat[i].data_ptr() for i in range(2 * PAIRS)]))
+    rows_tab = (ctypes.c_int64 * 2)(PART_ROWS, PART_ROWS)
+    s = ctypes.c_void_p(stream.cuda_stream)
+
+    def chk(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what}: {q.status_string(st)}")
+
+    names = list(op_bytes().keys())
+    ev = None
+
+    def step(i, record=None):
+        o_new, o_old = outs[i % 2], outs[(i + 1) % 2]
+        x0, x1, x2 = X[i % 3], X[(i + 1) % 3], X[(i + 2) % 3]
+        tab = parts_tabs[(i + 2) % 3]
+
+        def mark(j):
+            if record is not None:
+                record[j].record(stream)
+        mark(0)
+        chk(L.mxfp8_quantize_rowcol(x0.data_ptr(), M, K, K, o_new["rc"].data_ptr(),
+                                    o_new["rs"].data_ptr(), o_new["cc"].data_ptr(),
+                                    o_new["cs"].data_ptr(), lay, s), "rowcol")
+        mark(1)
+        chk(L.dequantize_mxfp8(o_old["rc"].data_ptr(), o_old["rs"].data_ptr(), M, K,
+                               lay, y_row.data_ptr(), s), "dq row")
+        mark(2)
+        chk(L.dequantize_mxfp8(o_old["cc"].data_ptr(), o_old["cs"].data_ptr(), K, M,
+                               lay, y_col.data_ptr(), s), "dq col")
+        mark(3)
+        chk(L.nvfp4_quantize_per_token(x1.data_ptr(), M, K, K, o_new["tc"].data_ptr(),
+                                       o_new["ts"].data_ptr(), o_new["tS"].data_ptr(),
+                                       lay, s), "per-token")
+        mark(4)
+        chk(L.dequantize_nvfp4(o_old["tc"].data_ptr(), o_old["ts"].data_ptr(),
+                               o_old["tS"].data_ptr(), q.S_PER_ROW, 1, M, K, lay,
+                               y_tok.data_ptr(), s), "dq tokens")
+        mark(5)
+        chk(L.nvfp4_quantize_weight_shared(
+            PAIRS, 2, ctypes.cast(tab, ctypes.c_void_p),
+            ctypes.cast(rows_tab, ctypes.c_void_p), K, o_new["wc"].data_ptr(),
+            o_new["ws"].data_ptr(), o_new["wS"].data_ptr(), None, lay,
+            wsp.data_ptr(), wsp.numel(), s), "weights")
+        mark(6)
+        chk(L.dequantize_nvfp4(o_old["wc"].data_ptr(), o_old["ws"].data_ptr(),
+                               o_old["wS"].data_ptr(), q.S_PER_BATCH, PAIRS,
+                               2 * PART_ROWS, K, lay, y_w.data_ptr(), s),
+            "dq weights")
+        mark(7)
+
+    # Our kernels per step: rowcol 1, dequant 2+1+1, per-token 1, weights
+    # (amax + encoder) per L2-sized chunk of groups.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    group_bytes = 2 * PART_ROWS * K * 2
+    chunk = max(1, min(64, int(0.4 * l2) // group_bytes))
+    n_chunks = -(-PAIRS // chunk)
+    launches_per_step = 1 + 2 + 1 + 1 + 2 * n_chunks + 1
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+
+    # Timed region: K steps, per-kernel events on the launching stream.
+    recs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)]
+            for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(args.steps):
+                step(args.warmup + i, recs[i])
+            end.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        wall = time.perf_counter() - t0
+    ms = start.elapsed_time(end)
+    ms_t = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    ob = op_bytes()
+    step_bytes = sum(ob.values())
+    per_kernel_ms = {}
+    for j, nm in enumerate(names):
+        per_kernel_ms[nm] = statistics.mean(
+            recs[i][j].elapsed_time(recs[i][j + 1]) for i in range(args.steps))
+    peak, peak_kind = measured_peak()
+    value = step_bytes * args.steps * world / (ms_max / 1e3) / 1e9
+
+    # e2e through the public API: pinned host input -> device -> the step's
+    # kernels -> quantized outputs back to pinned host memory.
+    e2e = run_e2e(q, dev, x_bits, args) if rank == 0 else None
+
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    total_ms = sum(per_kernel_ms.values())
+    kernels = {}
+    for nm in names:
+        t = per_kernel_ms[nm]
+        gbs = ob[nm] / (t / 1e3) / 1e9
+        kernels[nm] = {"us": round(t * 1e3, 2), "GB/s": round(gbs, 1),
+                       "frac": round(gbs / peak, 3),
+                       "share": round(t / total_ms, 3),
+                       "bytes": ob[nm]}
+    dom = max(names, key=lambda n: per_kernel_ms[n])
+    traffic = load_traffic(dom)
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD,
+            "M": M, "K": K, "scale_layout": "swizzled",
+            "weight_pairs": f"{PAIRS} x 2 x [{PART_ROWS} x {K}]",
+            "l2": ("inputs larger than L2: 3 rotating input copies and 2 "
+                   "rotating output sets, every kernel reads data last "
+                   "touched >= one step (~680 MB) earlier"),
+            "parallelism": f"weak: one independent replica per GPU x{world}",
+        },
+        "pct_hbm_peak": round(100 * value / world / peak, 1),
+        "roofline": {
+            "kernel": dom,
+            "bound": "hbm",
+            "achieved": kernels[dom]["GB/s"],
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": kernels[dom]["frac"],
+            "traffic": traffic,
+        },
+        "kernels": kernels,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args)
+    print(json.dumps(out), flush=True)
+
+
+def load_traffic(kernel_name):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary (profiles/traffic.json), or None when none was taken for the
+    current kernel."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        return d.get(kernel_name)
+    except Exception:
+        return None
+
+
+def run_e2e(q, dev, x_bits, args):
+    import torch
+    x_pin = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    res_shapes = None
+    hosts = None
+    n_e2e = max(3, min(20, args.steps // 50))
+
+    def once():
+        x = x_pin.to(dev, non_blocking=True)
+        r = q.mxfp8_quantize_rowcol(x)
+        q.dequantize_mxfp8(r.row_codes, r.row_scales)
+        q.dequantize_mxfp8(r.col_codes_t, r.col_scales_t)
+        t = q.nvfp4_quantize_per_token(x)
+        q.dequantize_nvfp4(t.codes, t.block_scales, t.scales)
+        parts = x.view(2 * PAIRS, PART_ROWS, K)
+        w = q.nvfp4_quantize_weight_shared(
+            [[parts[2 * g], parts[2 * g + 1]] for g in range(PAIRS)])
+        q.dequantize_nvfp4(w.codes, w.block_scales, w.scales)
+        return [r.row_codes, r.row_scales, r.col_codes_t, r.col_scales_t,
+                t.codes, t.block_scales, t.scales, w.codes, w.block_scales,
+                w.scales]
+
+    res = once()
+    hosts = [torch.empty(a.shape, dtype=a.dtype).pin_memory() for a in res]
+    for _ in range(2):
+        for h, a in zip(hosts, once()):
+            h.copy_(a, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        for h, a in zip(hosts, once()):
+            h.copy_(a, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    dt = (time.perf_counter() - t0) / n_e2e
+    step_bytes = sum(op_bytes().values())
+    d2h = sum(a.numel() * a.element_size() for a in res)
+    return {"value": round(step_bytes / dt / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": int(x_bits.nbytes),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(dt * 1e3, 3),
+            "steps": n_e2e}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline).
+# --------------------------------------------------------------------------
+def oracle_sample_step(x_rows):
+    """The step's operations run by the CPU oracle on a row slice of X."""
+    import oracle as O
+    rc, rs = O.mxfp8_quantize_rowwise(x_rows)
+    cc, cs = O.mxfp8_quantize_colwise(x_rows)
+    O.mxfp8_dequantize(rc, rs)
+    O.mxfp8_dequantize(cc, cs)
+    tc, ts, tS = O.nvfp4_quantize_per_token(x_rows)
+    O.nvfp4_dequantize(tc, ts, tS)
+    half = x_rows.shape[0] // 2
+    wc, wsc, wS = O.nvfp4_quantize_group([x_rows[:half], x_rows[half:]])
+    O.nvfp4_dequantize(wc, wsc, np.array([wS]))
+
+
+def oracle_timed(rows_total, threads):
+    """Time the oracle on `rows_total` rows of X split over `threads` threads
+    (32-row slices; ctypes releases the GIL inside the C oracle)."""
+    import oracle as O
+    import workloads as W
+    O.lib()
+    x = W.mxfp8_random(rows_total, K, seed=11)
+    slices = [x[i:i + 32] for i in range(0, rows_total, 32)]
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(oracle_sample_step, slices))
+    dt = time.perf_counter() - t0
+    frac = rows_total / M
+    return sum(op_bytes().values()) * frac / dt / 1e9, dt
+
+
+def cpu_baseline(args):
+    cores = os.cpu_count() or 1
+    rows = args.cpu_rows
+    v, dt = oracle_timed(rows, cores)
+    return {"value": round(v, 4), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": (f"the step's 8 operations on {rows} of the 8192 rows "
+                       f"of X ({rows * K} elements), 32-row slices over "
+                       f"{cores} threads, {dt:.1f} s")}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    cores = os.cpu_count() or 1
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_timed(32, cores)
+    vals, dts = [], []
+    for _ in range(args.steps):
+        v, dt = oracle_timed(rows, cores)
+        vals.append(v)
+        dts.append(dt)
+    value = statistics.mean(vals)
+    out = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.mean(dts), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "K": K,
+                   "sample_rows": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT,
+                         "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} of 8192 rows per step"},
+        "e2e": {"value": round(value, 4), "unit": UNIT,
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="libmxq", choices=["libmxq", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--ref-rows", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,238 @@
+/*
+ * mxq.h -- C ABI of libmxq, the GB300 (sm_103a) MXFP8 / NVFP4 quantizer
+ * library.
+ *
+ * Sources are cited as (page title, section):
+ *   [MILES]  "Miles: end-to-end MXFP8 and per-token NVFP4 RL"
+ *   [RLQ]    "Using Quantization in RL"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are plain pointers.  Unless stated otherwise every tensor
+ *    pointer is a DEVICE pointer on the current CUDA device; bf16 data is
+ *    passed as `const void*` holding IEEE bfloat16 values.  Only the
+ *    pointer table of nvfp4_quantize_weight_shared and its part_rows array
+ *    live in HOST memory.
+ *  - Every device pointer must be 16-byte aligned (MXQ_ERR_ALIGN).
+ *  - The caller owns every buffer.  The library never allocates or frees
+ *    memory and keeps no per-call state.  Calls that need scratch take a
+ *    caller-provided workspace and have a *_workspace_size query.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ *    work is enqueued on it; no entry point synchronizes.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    rejected call writes nothing and returns a non-zero mxq_status.  No
+ *    C++ exception crosses this ABI.
+ *  - Inputs must be finite bf16 values (NaN / Inf inputs are outside the
+ *    contract).
+ *  - Results are deterministic and bit-exact with respect to the algorithm
+ *    stated at each entry point: the same input bytes always give the same
+ *    output bytes, on any launch configuration.
+ *
+ * Scale layouts (argument `scale_layout`)
+ * ---------------------------------------
+ *  MXQ_SCALE_LINEAR:   the logical scale matrix [R x C] (one byte per
+ *                      block), row-major, no padding.
+ *  MXQ_SCALE_SWIZZLED: the 128x4-tile layout that block-scaled tensor-core
+ *                      MMA reads: R padded to a multiple of 128, C to a
+ *                      multiple of 4; tile (rt, ct) of 512 bytes at byte
+ *                      (rt * ceil(C/4) + ct) * 512; element (r, c) inside
+ *                      its tile at (r % 32) * 16 + ((r % 128) / 32) * 4 +
+ *                      (c % 4).  Padding bytes are written as 0x00.
+ *  mxq_scale_bytes() gives the buffer size of either layout.
+ */
+#ifndef MXQ_H
+#define MXQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int mxq_status;
+
+#define MXQ_OK            0  /* success                                    */
+#define MXQ_ERR_NULL      1  /* a required pointer is NULL                 */
+#define MXQ_ERR_SHAPE     2  /* a size is negative or not a block multiple */
+#define MXQ_ERR_ALIGN     3  /* a pointer or a leading dimension is not
+                                16-byte aligned                            */
+#define MXQ_ERR_LAYOUT    4  /* unknown scale_layout / scale mode          */
+#define MXQ_ERR_WORKSPACE 5  /* workspace NULL or smaller than required    */
+#define MXQ_ERR_CUDA      6  /* a CUDA call or kernel launch failed        */
+#define MXQ_ERR_TIMEOUT   7  /* a bounded device-side wait gave up         */
+#define MXQ_ERR_ARG       8  /* any other invalid argument                 */
+
+#define MXQ_SCALE_LINEAR   0
+#define MXQ_SCALE_SWIZZLED 1
+
+/* FP32 scale modes of dequantize_nvfp4. */
+#define MXQ_S_PER_ROW   0    /* S[b * rows + r]: one scale per row (token)  */
+#define MXQ_S_PER_BATCH 1    /* S[b]: one scale per batch entry (group)     */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mxq_status_string(mxq_status s);
+
+/* Library version, as 10000 * major + 100 * minor + patch. */
+int mxq_version(void);
+
+/* Bytes of a scale buffer for a logical [rows x cols] scale matrix in the
+ * given layout; -1 for a bad layout or negative size. */
+int64_t mxq_scale_bytes(int64_t rows, int64_t cols, int scale_layout);
+
+/* Returns and clears the error word that bounded device-side waits set
+ * when they give up (MXQ_ERR_TIMEOUT), then the last CUDA runtime error
+ * (MXQ_ERR_CUDA); MXQ_OK if neither is set.  Synchronizes the device. */
+mxq_status mxq_get_last_error(void);
+
+/* Host-side fault injection for tests of the error paths: mode 0 = off,
+ * 1 = every entry point fails its launch with MXQ_ERR_CUDA without
+ * launching, 2 = argument checks fail with MXQ_ERR_ARG.  Also read once
+ * from the environment variable MXQ_FAULT_INJECT ("launch" / "argcheck").
+ * Nothing faults on the GPU. */
+void mxq_set_fault_inject(int mode);
+
+/* --------------------------------------------------------------------- */
+/* MXFP8 quantize, rowwise and columnwise copies in one pass.             */
+/*                                                                       */
+/* [MILES] formats section: E4M3 elements, every 32 consecutive values    */
+/* share one E8M0 (power-of-two) scale, the block is one-dimensional, and */
+/* the decoded scale is rounded up so the block maximum is not clipped.   */
+/* [MILES] MXFP8 recipe section: rowwise 1x32 and columnwise 32x1 blocks  */
+/* are numerically different and are each quantized from the full-        */
+/* precision data; both copies are materialized by one quantization.      */
+/*                                                                       */
+/* Per block B (32 values): a = max|x|; k = smallest integer in           */
+/* [-127, 127] with 448 * 2^k >= a (a = 0 gives k = -127); scale byte =   */
+/* k + 127; code_i = E4M3 round-to-nearest-even of x_i * 2^-k (exact      */
+/* product, never saturates).                                             */
+/*                                                                       */
+/* x            bf16 [M x K], row stride ldx elements (ldx >= K,           */
+/*              ldx % 8 == 0).                                            */
+/* row_codes    u8 [M x K] (row stride K): blocks along K.                 */
+/* row_scales   E8M0, logical [M x K/32], in scale_layout.                 */
+/* col_codes_t  u8 [K x M]: the columnwise copy stored TRANSPOSED, byte    */
+/*              (k, m) at k * M + m, so each 32x1 block is 32 contiguous   */
+/*              bytes (the K-major operand of the backward GEMMs).         */
+/* col_scales_t E8M0, logical [K x M/32], in scale_layout.                 */
+/* Either pair may be NULL (both pointers of the pair) to skip that copy;  */
+/* at least one pair must be given.  K % 32 == 0; M % 32 == 0 when the     */
+/* columnwise copy is requested.  M == 0 or K == 0 is a no-op.            */
+/* --------------------------------------------------------------------- */
+mxq_status mxfp8_quantize_rowcol(const void* x, int64_t M, int64_t K,
+                                 int64_t ldx, uint8_t* row_codes,
+                                 uint8_t* row_scales, uint8_t* col_codes_t,
+                                 uint8_t* col_scales_t, int scale_layout,
+                                 void* stream);
+
+/* --------------------------------------------------------------------- */
+/* NVFP4 quantize with one FP32 scale per token.                          */
+/*                                                                       */
+/* [MILES] formats section: E2M1 elements, one E4M3 scale per 16 values   */
+/* rounded to the nearest representable value, and an FP32 scale over a   */
+/* larger scope.  [MILES] NVFP4 recipe section: that FP32 scale is one    */
+/* per token, computed online inside the same call that emits the packed  */
+/* FP4 values and the E4M3 block scales, so a token's bytes never depend  */
+/* on the rest of the batch.                                              */
+/*                                                                       */
+/* Per token t (all IEEE binary32, round-to-nearest-even, no FTZ):        */
+/*   S_t  = amax_t / 2688                        (2688 = 6 * 448)         */
+/*   sb   = E4M3_RNE( amax_b / (6 * S_t) )  per 16-block b (0 if S_t = 0) */
+/*   enc  = 1 / (E4M3(sb) * S_t)   (0 if that product is 0, else clamped  */
+/*                                  to FLT_MAX)                           */
+/*   code = E2M1_RNE( x * enc ), saturating at +-6, sign kept              */
+/* Two codes per byte, the lower-index element in the LOW nibble.         */
+/*                                                                       */
+/* x            bf16 [T x H], row stride ldx (ldx >= H, ldx % 8 == 0);     */
+/*              a ragged batch is passed flattened.                        */
+/* codes        u8 [T x H/2].                                              */
+/* block_scales E4M3, logical [T x H/16], in scale_layout.                 */
+/* token_scales f32 [T] (the decode scales S_t).                           */
+/* H % 16 == 0.  T == 0 is a no-op.                                       */
+/* --------------------------------------------------------------------- */
+mxq_status nvfp4_quantize_per_token(const void* x, int64_t T, int64_t H,
+                                    int64_t ldx, uint8_t* codes,
+                                    uint8_t* block_scales,
+                                    float* token_scales, int scale_layout,
+                                    void* stream);
+
+/* --------------------------------------------------------------------- */
+/* NVFP4 weight quantize with one FP32 scale shared by a group of parts.  */
+/*                                                                       */
+/* [MILES] NVFP4 recipe section: NVFP4 targets MoE expert weights; the    */
+/* gate and up projections are fused into one GEMM, so both must share    */
+/* the same FP32 scale during conversion and live weight update; the pair */
+/* is quantized together.                                                 */
+/*                                                                       */
+/* Group g consists of num_parts parts; part p is a bf16 [part_rows[p] x  */
+/* K] row-major matrix (row stride K) at device address                   */
+/* parts[g * num_parts + p].  S_g = max over all its parts of |x| / 2688  */
+/* (or group_scales_in[g] when that pointer is not NULL: a live update    */
+/* reusing a stored scale), then each row is encoded exactly as in        */
+/* nvfp4_quantize_per_token with S_g.  The output rows of a group are the */
+/* parts' rows concatenated (R = sum part_rows).                          */
+/*   gate/up pair: num_parts = 2, part_rows = {768, 768};                  */
+/*   down:         a second call with num_parts = 1.                      */
+/*                                                                       */
+/* parts          HOST array of num_groups * num_parts device pointers.    */
+/* part_rows      HOST array [num_parts].                                  */
+/* codes          u8 [num_groups x R x K/2].                                */
+/* block_scales   num_groups consecutive scale matrices, each logical      */
+/*                [R x K/16] in scale_layout, mxq_scale_bytes(R, K/16)     */
+/*                bytes apart.                                             */
+/* group_scales   f32 [num_groups] (out).                                  */
+/* group_scales_in f32 [num_groups] or NULL.                               */
+/* ws / ws_bytes  device workspace of at least                             */
+/*                nvfp4_quantize_weight_shared_workspace_size() bytes.     */
+/* K % 16 == 0; 1 <= num_parts <= 4.                                       */
+/* --------------------------------------------------------------------- */
+size_t nvfp4_quantize_weight_shared_workspace_size(int64_t num_groups);
+
+mxq_status nvfp4_quantize_weight_shared(
+    int64_t num_groups, int num_parts, const void* const* parts,
+    const int64_t* part_rows, int64_t K, uint8_t* codes,
+    uint8_t* block_scales, float* group_scales, const float* group_scales_in,
+    int scale_layout, void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------- */
+/* MXFP8 dequantize to bf16.                                              */
+/*                                                                       */
+/* [MILES] backward-mode section: dequantized backward feeds the BF16     */
+/* backward GEMMs with BF16 dequantizations of the exact low-precision    */
+/* operands of the forward pass.  [RLQ] "Two Ways to Configure Training   */
+/* and Inference": a stored value is code x scale.                        */
+/*                                                                       */
+/* y = bf16_RNE( fp32( E4M3(code) * 2^(scale - 127) ) ), blocks of 32      */
+/* along each row.  Exact for codes produced from bf16 data, except that  */
+/* a block of bf16-max magnitude overflows to +-inf (2^128).              */
+/* codes u8 [rows x cols]; scales logical [rows x cols/32] in              */
+/* scale_layout; y bf16 [rows x cols].  Dequantize the columnwise copy by */
+/* passing (col_codes_t, col_scales_t, K, M): the result is X^T.          */
+/* cols % 32 == 0.                                                        */
+/* --------------------------------------------------------------------- */
+mxq_status dequantize_mxfp8(const uint8_t* codes, const uint8_t* scales,
+                            int64_t rows, int64_t cols, int scale_layout,
+                            void* y, void* stream);
+
+/* --------------------------------------------------------------------- */
+/* NVFP4 dequantize to bf16.                                              */
+/*                                                                       */
+/* Same sources as dequantize_mxfp8.                                      */
+/* y = bf16_RNE( fp32( fp32(E2M1(c) * E4M3(sb)) * S ) ); the inner        */
+/* product is exact.  `batch` matrices of [rows x cols], stored back to   */
+/* back: codes [batch x rows x cols/2], block_scales batch consecutive    */
+/* scale matrices of mxq_scale_bytes(rows, cols/16) bytes, y [batch x rows */
+/* x cols].  S: s_mode MXQ_S_PER_ROW -> S[b * rows + r] (per-token data,  */
+/* batch = 1); MXQ_S_PER_BATCH -> S[b] (one weight group per batch        */
+/* entry).  cols % 16 == 0.                                                */
+/* --------------------------------------------------------------------- */
+mxq_status dequantize_nvfp4(const uint8_t* codes, const uint8_t* block_scales,
+                            const float* S, int s_mode, int64_t batch,
+                            int64_t rows, int64_t cols, int scale_layout,
+                            void* y, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXQ_H */

@@ -1,0 +1,294 @@
+"""ctypes binding of libmxq (include/mxq.h).
+
+Argument marshalling only: every step of every operation runs in the CUDA
+kernels of libmxq.so.  There is no fallback: if the library has not been
+built, or a call fails, a RuntimeError is raised.  PyTorch supplies device
+memory (outputs are allocated with ``torch.empty`` on the input's device)
+and the stream (``torch.cuda.current_stream()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import NamedTuple, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmxq.so")
+
+MXQ_OK = 0
+MXQ_ERR_NULL = 1
+MXQ_ERR_SHAPE = 2
+MXQ_ERR_ALIGN = 3
+MXQ_ERR_LAYOUT = 4
+MXQ_ERR_WORKSPACE = 5
+MXQ_ERR_CUDA = 6
+MXQ_ERR_TIMEOUT = 7
+MXQ_ERR_ARG = 8
+
+SCALE_LINEAR = 0
+SCALE_SWIZZLED = 1
+S_PER_ROW = 0
+S_PER_BATCH = 1
+
+_LAYOUTS = {"linear": SCALE_LINEAR, "swizzled": SCALE_SWIZZLED,
+            SCALE_LINEAR: SCALE_LINEAR, SCALE_SWIZZLED: SCALE_SWIZZLED}
+
+_lib = None
+_lock = threading.Lock()
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+
+
+class MxqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmxq.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libmxq.so not found at {LIB_PATH}; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        L.mxq_status_string.restype = ctypes.c_char_p
+        L.mxq_status_string.argtypes = [_int]
+        L.mxq_version.restype = _int
+        L.mxq_version.argtypes = []
+        L.mxq_scale_bytes.restype = _i64
+        L.mxq_scale_bytes.argtypes = [_i64, _i64, _int]
+        L.mxq_get_last_error.restype = _int
+        L.mxq_get_last_error.argtypes = []
+        L.mxq_set_fault_inject.restype = None
+        L.mxq_set_fault_inject.argtypes = [_int]
+        L.mxfp8_quantize_rowcol.restype = _int
+        L.mxfp8_quantize_rowcol.argtypes = [_p, _i64, _i64, _i64, _p, _p, _p,
+                                            _p, _int, _p]
+        L.nvfp4_quantize_per_token.restype = _int
+        L.nvfp4_quantize_per_token.argtypes = [_p, _i64, _i64, _i64, _p, _p,
+                                               _p, _int, _p]
+        L.nvfp4_quantize_weight_shared_workspace_size.restype = ctypes.c_size_t
+        L.nvfp4_quantize_weight_shared_workspace_size.argtypes = [_i64]
+        L.nvfp4_quantize_weight_shared.restype = _int
+        L.nvfp4_quantize_weight_shared.argtypes = [
+            _i64, _int, _p, _p, _i64, _p, _p, _p, _p, _int, _p,
+            ctypes.c_size_t, _p]
+        L.dequantize_mxfp8.restype = _int
+        L.dequantize_mxfp8.argtypes = [_p, _p, _i64, _i64, _int, _p, _p]
+        L.dequantize_nvfp4.restype = _int
+        L.dequantize_nvfp4.argtypes = [_p, _p, _p, _int, _i64, _i64, _i64,
+                                       _int, _p, _p]
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().mxq_status_string(int(status)).decode()
+
+
+def scale_bytes(rows: int, cols: int, scale_layout="swizzled") -> int:
+    n = lib().mxq_scale_bytes(int(rows), int(cols), _layout(scale_layout))
+    if n < 0:
+        raise ValueError("bad scale layout or size")
+    return int(n)
+
+
+def get_last_error() -> int:
+    """Synchronizes the device; returns the status of bounded device waits
+    (MXQ_ERR_TIMEOUT) or of the CUDA runtime (MXQ_ERR_CUDA)."""
+    return int(lib().mxq_get_last_error())
+
+
+def set_fault_inject(mode: int) -> None:
+    lib().mxq_set_fault_inject(int(mode))
+
+
+def _layout(scale_layout) -> int:
+    try:
+        return _LAYOUTS[scale_layout]
+    except KeyError:
+        raise ValueError(f"unknown scale layout {scale_layout!r}") from None
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != MXQ_OK:
+        raise MxqError(status, what)
+
+
+def _bf16_2d(x: torch.Tensor, name: str) -> torch.Tensor:
+    if x.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with unit column stride")
+    return x
+
+
+class Mxfp8Quantized(NamedTuple):
+    row_codes: torch.Tensor | None      # u8 [M, K]
+    row_scales: torch.Tensor | None     # E8M0 bytes, logical [M, K/32]
+    col_codes_t: torch.Tensor | None    # u8 [K, M] (columnwise copy, transposed)
+    col_scales_t: torch.Tensor | None   # E8M0 bytes, logical [K, M/32]
+    scale_layout: int
+
+
+class Nvfp4Quantized(NamedTuple):
+    codes: torch.Tensor                 # u8 [..., R, H/2]
+    block_scales: torch.Tensor          # E4M3 bytes
+    scales: torch.Tensor                # f32 per token [T] or per group [G]
+    scale_layout: int
+
+
+def mxfp8_quantize_rowcol(x: torch.Tensor, rowwise: bool = True,
+                          colwise: bool = True,
+                          scale_layout="swizzled") -> Mxfp8Quantized:
+    """MXFP8 rowwise (1x32) and/or columnwise (32x1) quantization of a bf16
+    [M, K] tensor in one pass (C: mxfp8_quantize_rowcol)."""
+    x = _bf16_2d(x, "x")
+    lay = _layout(scale_layout)
+    M, K = x.shape
+    dev = x.device
+    rc = rs = cc = cs = None
+    if rowwise:
+        rc = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        rs = torch.empty((scale_bytes(M, K // 32, lay),), dtype=torch.uint8,
+                         device=dev)
+    if colwise:
+        cc = torch.empty((K, M), dtype=torch.uint8, device=dev)
+        cs = torch.empty((scale_bytes(K, M // 32, lay),), dtype=torch.uint8,
+                         device=dev)
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    _check(lib().mxfp8_quantize_rowcol(
+        x.data_ptr(), M, K, x.stride(0), ptr(rc), ptr(rs), ptr(cc), ptr(cs),
+        lay, _stream(dev)), "mxfp8_quantize_rowcol")
+    return Mxfp8Quantized(rc, rs, cc, cs, lay)
+
+
+def nvfp4_quantize_per_token(x: torch.Tensor,
+                             scale_layout="swizzled") -> Nvfp4Quantized:
+    """NVFP4 quantization with one FP32 scale per token (row) of a bf16
+    [T, H] tensor (C: nvfp4_quantize_per_token)."""
+    x = _bf16_2d(x, "x")
+    lay = _layout(scale_layout)
+    T, H = x.shape
+    dev = x.device
+    codes = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
+    bs = torch.empty((scale_bytes(T, H // 16, lay),), dtype=torch.uint8,
+                     device=dev)
+    S = torch.empty((T,), dtype=torch.float32, device=dev)
+    _check(lib().nvfp4_quantize_per_token(
+        x.data_ptr(), T, H, x.stride(0), codes.data_ptr(), bs.data_ptr(),
+        S.data_ptr(), lay, _stream(dev)), "nvfp4_quantize_per_token")
+    return Nvfp4Quantized(codes, bs, S, lay)
+
+
+def nvfp4_quantize_weight_shared(groups: Sequence[Sequence[torch.Tensor]],
+                                 group_scales_in: torch.Tensor | None = None,
+                                 scale_layout="swizzled",
+                                 workspace: torch.Tensor | None = None
+                                 ) -> Nvfp4Quantized:
+    """NVFP4 weight quantization where all parts of a group share one FP32
+    scale (gate/up pair: two parts per group)
+    (C: nvfp4_quantize_weight_shared).
+
+    groups[g][p] is a contiguous bf16 [rows_p, K] CUDA tensor; every group
+    has the same part shapes.  Returns codes [G, R, K/2], block scales
+    [G, scale_bytes(R, K/16)] and S [G]."""
+    lay = _layout(scale_layout)
+    G = len(groups)
+    if G == 0:
+        raise ValueError("no groups")
+    P = len(groups[0])
+    shapes = [tuple(t.shape) for t in groups[0]]
+    K = shapes[0][1]
+    for grp in groups:
+        if [tuple(t.shape) for t in grp] != shapes:
+            raise ValueError("every group must have the same part shapes")
+        for t in grp:
+            _bf16_2d(t, "part")
+            if not t.is_contiguous():
+                raise ValueError("parts must be contiguous")
+    dev = groups[0][0].device
+    R = sum(s[0] for s in shapes)
+    ptrs = (ctypes.c_void_p * (G * P))(*[t.data_ptr() for grp in groups
+                                         for t in grp])
+    rows = (ctypes.c_int64 * P)(*[s[0] for s in shapes])
+    codes = torch.empty((G, R, K // 2), dtype=torch.uint8, device=dev)
+    sb = scale_bytes(R, K // 16, lay)
+    bs = torch.empty((G, sb), dtype=torch.uint8, device=dev)
+    S = torch.empty((G,), dtype=torch.float32, device=dev)
+    ws_bytes = int(lib().nvfp4_quantize_weight_shared_workspace_size(G))
+    if group_scales_in is None:
+        if workspace is None:
+            workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8,
+                                    device=dev)
+        ws_ptr, ws_len = workspace.data_ptr(), workspace.numel()
+        sin = None
+    else:
+        if group_scales_in.dtype != torch.float32 or group_scales_in.numel() != G:
+            raise ValueError("group_scales_in must be float32 [G]")
+        sin = group_scales_in.contiguous()
+        ws_ptr, ws_len = None, 0
+    _check(lib().nvfp4_quantize_weight_shared(
+        G, P, ctypes.cast(ptrs, ctypes.c_void_p), ctypes.cast(rows, ctypes.c_void_p),
+        K, codes.data_ptr(), bs.data_ptr(), S.data_ptr(),
+        None if sin is None else sin.data_ptr(), lay, ws_ptr, ws_len,
+        _stream(dev)), "nvfp4_quantize_weight_shared")
+    return Nvfp4Quantized(codes, bs, S, lay)
+
+
+def dequantize_mxfp8(codes: torch.Tensor, scales: torch.Tensor,
+                     scale_layout="swizzled") -> torch.Tensor:
+    """bf16 [rows, cols] from MXFP8 codes [rows, cols] and their E8M0 scales
+    (C: dequantize_mxfp8)."""
+    lay = _layout(scale_layout)
+    if codes.dtype != torch.uint8 or codes.dim() != 2 or not codes.is_contiguous():
+        raise ValueError("codes must be a contiguous uint8 [rows, cols] tensor")
+    rows, cols = codes.shape
+    y = torch.empty((rows, cols), dtype=torch.bfloat16, device=codes.device)
+    _check(lib().dequantize_mxfp8(codes.data_ptr(), scales.data_ptr(), rows,
+                                  cols, lay, y.data_ptr(),
+                                  _stream(codes.device)), "dequantize_mxfp8")
+    return y
+
+
+def dequantize_nvfp4(codes: torch.Tensor, block_scales: torch.Tensor,
+                     S: torch.Tensor, scale_layout="swizzled") -> torch.Tensor:
+    """bf16 from NVFP4 codes.  codes [rows, cols/2] with S per row [rows]
+    (activations), or codes [batch, rows, cols/2] with S per batch entry
+    [batch] (weight groups) (C: dequantize_nvfp4)."""
+    lay = _layout(scale_layout)
+    if codes.dtype != torch.uint8 or not codes.is_contiguous():
+        raise ValueError("codes must be a contiguous uint8 tensor")
+    if codes.dim() == 2:
+        batch, (rows, half) = 1, codes.shape
+        mode = S_PER_ROW
+        shape = (rows, half * 2)
+    elif codes.dim() == 3:
+        batch, rows, half = codes.shape
+        mode = S_PER_BATCH
+        shape = (batch, rows, half * 2)
+    else:
+        raise ValueError("codes must be 2-D or 3-D")
+    if S.dtype != torch.float32:
+        raise TypeError("S must be float32")
+    y = torch.empty(shape, dtype=torch.bfloat16, device=codes.device)
+    _check(lib().dequantize_nvfp4(codes.data_ptr(), block_scales.data_ptr(),
+                                  S.data_ptr(), mode, batch, rows, half * 2,
+                                  lay, y.data_ptr(), _stream(codes.device)),
+           "dequantize_nvfp4")
+    return y

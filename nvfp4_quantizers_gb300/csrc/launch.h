@@ -1,0 +1,59 @@
+// launch.h -- internal interface between the C ABI (api.cu) and the kernel
+// translation units.  Every launcher enqueues on `stream`, never
+// synchronizes, and returns the launch status.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mxq {
+
+// Host utilities (api.cu).
+int sm_count(int device);
+int64_t l2_bytes(int device);
+cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base,
+                              uint64_t inner, uint64_t outer,
+                              uint64_t outer_stride_bytes, uint32_t box_inner,
+                              uint32_t box_outer);
+
+// mxfp8.cu
+// Reads (and clears when set) the error word of the bounded device waits.
+cudaError_t mxfp8_take_wait_error(unsigned int* word);
+cudaError_t launch_mxfp8_rowcol(const void* x, int64_t M, int64_t K,
+                                int64_t ldx, uint8_t* row_codes,
+                                uint8_t* row_scales, uint8_t* col_codes,
+                                uint8_t* col_scales, int swizzled,
+                                cudaStream_t stream);
+
+// nvfp4.cu
+cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
+                                   int64_t ldx, uint8_t* codes,
+                                   uint8_t* scales, float* token_scales,
+                                   int swizzled, cudaStream_t stream);
+
+constexpr int kMaxParts = 4;
+
+cudaError_t launch_nvfp4_weight_shared(
+    int64_t num_groups, int num_parts, const void* const* parts,
+    const int64_t* part_rows, int64_t K, uint8_t* codes, uint8_t* scales,
+    float* group_scales, const float* group_scales_in, int swizzled,
+    uint32_t* amax_ws, cudaStream_t stream);
+
+// dequant.cu
+cudaError_t launch_dequant_mxfp8(const uint8_t* codes, const uint8_t* scales,
+                                 int64_t rows, int64_t cols, int swizzled,
+                                 void* y, cudaStream_t stream);
+cudaError_t launch_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales,
+                                 const float* S, int per_batch, int64_t batch,
+                                 int64_t rows, int64_t cols, int swizzled,
+                                 void* y, cudaStream_t stream);
+
+// Scale-matrix size in bytes for either layout.
+inline int64_t scale_bytes(int64_t rows, int64_t cols, int swizzled) {
+  if (!swizzled) return rows * cols;
+  return ((rows + 127) / 128) * 128 * ((cols + 3) / 4) * 4;
+}
+
+}  // namespace mxq

@@ -1,0 +1,149 @@
+"""Host-only checks of the C ABI (no GPU, no kernel launch).
+
+The library must load, export every function include/mxq.h declares, and
+reject bad arguments with the documented status codes before it touches
+the GPU (argument validation is host code that runs before any launch).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from nvfp4_quantizers_gb300 import build as B
+    B.build()
+    import nvfp4_quantizers_gb300 as q
+    lib = q.lib()
+    lib.mxq_set_fault_inject(0)
+    yield lib
+    lib.mxq_set_fault_inject(0)
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "mxq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_0-9]+)\s*\(", src)) -
+                  {"if", "sizeof", "defined"})
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert "mxfp8_quantize_rowcol" in names and len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(L):
+    import nvfp4_quantizers_gb300 as q
+    for s in range(9):
+        assert q.status_string(s).startswith("MXQ")
+    assert L.mxq_version() >= 100
+
+
+def test_scale_bytes(L):
+    import nvfp4_quantizers_gb300 as q
+    assert q.scale_bytes(256, 8, "swizzled") == 2048
+    assert q.scale_bytes(300, 5, "swizzled") == 384 * 8
+    assert q.scale_bytes(300, 5, "linear") == 1500
+    assert L.mxq_scale_bytes(1, 1, 7) == -1
+
+
+FAKE = 0x10000          # aligned fake device addresses: never dereferenced
+
+
+def test_mxfp8_argument_errors(L):
+    f = L.mxfp8_quantize_rowcol
+    import nvfp4_quantizers_gb300 as q
+    assert f(FAKE, 64, 64, 64, FAKE, FAKE, FAKE, FAKE, 9, None) == q.MXQ_ERR_LAYOUT
+    assert f(FAKE, 64, 64, 64, None, None, None, None, 1, None) == q.MXQ_ERR_NULL
+    assert f(FAKE, 64, 64, 64, FAKE, None, None, None, 1, None) == q.MXQ_ERR_NULL
+    assert f(None, 64, 64, 64, FAKE, FAKE, None, None, 1, None) == q.MXQ_ERR_NULL
+    assert f(FAKE, 64, 48, 48, FAKE, FAKE, None, None, 1, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, 48, 64, 64, FAKE, FAKE, FAKE, FAKE, 1, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, -1, 64, 64, FAKE, FAKE, None, None, 1, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, 64, 64, 32, FAKE, FAKE, None, None, 1, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE + 2, 64, 64, 64, FAKE, FAKE, None, None, 1, None) == q.MXQ_ERR_ALIGN
+    assert f(FAKE, 64, 64, 68, FAKE, FAKE, None, None, 1, None) == q.MXQ_ERR_ALIGN
+    assert f(FAKE, 64, 64, 64, FAKE + 8, FAKE, None, None, 1, None) == q.MXQ_ERR_ALIGN
+    # empty input: nothing to do, nothing launched
+    assert f(FAKE, 0, 64, 64, FAKE, FAKE, FAKE, FAKE, 1, None) == q.MXQ_OK
+    assert f(None, 64, 0, 0, FAKE, FAKE, None, None, 0, None) == q.MXQ_OK
+
+
+def test_nvfp4_argument_errors(L):
+    import nvfp4_quantizers_gb300 as q
+    f = L.nvfp4_quantize_per_token
+    assert f(FAKE, 4, 40, 40, FAKE, FAKE, FAKE, 1, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, 4, 32, 32, None, FAKE, FAKE, 1, None) == q.MXQ_ERR_NULL
+    assert f(FAKE, 4, 32, 36, FAKE, FAKE, FAKE, 1, None) == q.MXQ_ERR_ALIGN
+    assert f(FAKE, 4, 32, 32, FAKE, FAKE, FAKE + 4, 1, None) == q.MXQ_ERR_ALIGN
+    assert f(FAKE, 4, 32, 32, FAKE, FAKE, FAKE, 3, None) == q.MXQ_ERR_LAYOUT
+    assert f(None, 0, 32, 32, None, None, None, 1, None) == q.MXQ_OK
+
+    g = L.nvfp4_quantize_weight_shared
+    ptrs = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    rows = (ctypes.c_int64 * 2)(64, 64)
+    P = ctypes.cast(ptrs, ctypes.c_void_p)
+    R = ctypes.cast(rows, ctypes.c_void_p)
+    assert g(1, 5, P, R, 64, FAKE, FAKE, FAKE, None, 1, FAKE, 256, None) == q.MXQ_ERR_ARG
+    assert g(1, 2, P, R, 64, FAKE, FAKE, FAKE, None, 1, None, 0, None) == q.MXQ_ERR_WORKSPACE
+    assert g(1, 2, P, R, 64, FAKE, FAKE, FAKE, None, 1, FAKE, 0, None) == q.MXQ_ERR_WORKSPACE
+    assert g(1, 2, P, R, 40, FAKE, FAKE, FAKE, None, 1, FAKE, 256, None) == q.MXQ_ERR_SHAPE
+    assert g(1, 2, None, R, 64, FAKE, FAKE, FAKE, None, 1, FAKE, 256, None) == q.MXQ_ERR_NULL
+    assert L.nvfp4_quantize_weight_shared_workspace_size(128) == 512
+    assert L.nvfp4_quantize_weight_shared_workspace_size(0) == 0
+
+
+def test_dequant_argument_errors(L):
+    import nvfp4_quantizers_gb300 as q
+    assert L.dequantize_mxfp8(FAKE, FAKE, 4, 48, 1, FAKE, None) == q.MXQ_ERR_SHAPE
+    assert L.dequantize_mxfp8(None, FAKE, 4, 64, 1, FAKE, None) == q.MXQ_ERR_NULL
+    assert L.dequantize_mxfp8(FAKE, FAKE, 4, 64, 1, FAKE + 2, None) == q.MXQ_ERR_ALIGN
+    assert L.dequantize_nvfp4(FAKE, FAKE, FAKE, 5, 1, 4, 64, 1, FAKE, None) == q.MXQ_ERR_LAYOUT
+    assert L.dequantize_nvfp4(FAKE, FAKE, FAKE, 0, 1, 4, 24, 1, FAKE, None) == q.MXQ_ERR_SHAPE
+    assert L.dequantize_nvfp4(FAKE, FAKE, None, 0, 1, 4, 64, 1, FAKE, None) == q.MXQ_ERR_NULL
+    assert L.dequantize_nvfp4(FAKE, FAKE, FAKE, 0, 0, 4, 64, 1, FAKE, None) == q.MXQ_OK
+
+
+def test_fault_injection_returns_errors_without_launching(L):
+    import nvfp4_quantizers_gb300 as q
+    try:
+        L.mxq_set_fault_inject(2)
+        assert L.mxfp8_quantize_rowcol(FAKE, 64, 64, 64, FAKE, FAKE, None,
+                                       None, 1, None) == q.MXQ_ERR_ARG
+        assert L.dequantize_mxfp8(FAKE, FAKE, 4, 64, 1, FAKE, None) == q.MXQ_ERR_ARG
+        L.mxq_set_fault_inject(1)
+        # valid arguments, but the launch is reported failed and not issued
+        assert L.mxfp8_quantize_rowcol(FAKE, 64, 64, 64, FAKE, FAKE, None,
+                                       None, 1, None) == q.MXQ_ERR_CUDA
+        assert L.nvfp4_quantize_per_token(FAKE, 4, 32, 32, FAKE, FAKE, FAKE,
+                                          1, None) == q.MXQ_ERR_CUDA
+        assert L.dequantize_nvfp4(FAKE, FAKE, FAKE, 0, 1, 4, 64, 1, FAKE,
+                                  None) == q.MXQ_ERR_CUDA
+    finally:
+        L.mxq_set_fault_inject(0)
+
+
+def test_python_binding_raises_on_error(L):
+    import nvfp4_quantizers_gb300 as q
+    with pytest.raises(q.MxqError) as ei:
+        q._lib._check(q.MXQ_ERR_SHAPE, "op")
+    assert ei.value.status == q.MXQ_ERR_SHAPE
+    with pytest.raises(ValueError):
+        q.scale_bytes(4, 4, "bogus")
+
+
+def test_product_does_not_import_oracle():
+    """The product package shares no code with the oracle."""
+    pkg = os.path.join(ROOT, "nvfp4_quantizers_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".c")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text
+                assert "mxq_oracle" not in text and "liboracle" not in text
