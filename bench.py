@@ -461,9 +461,16 @@ def run_reference(args):
     if rank != 0:
         return
     cores = os.cpu_count() or 1
-    rows = args.ref_rows
+    # Size each step so that the whole run stays near a minute of wall time.
+    per_row = []
     for _ in range(args.warmup):
-        oracle_timed(32, cores)
+        v, dt = oracle_timed(32 * max(1, cores), cores)
+        per_row.append(dt / (32 * max(1, cores)))
+    rows = args.ref_rows
+    if rows <= 0:
+        budget_s = 60.0
+        rows = int(budget_s / max(args.steps, 1) / max(min(per_row), 1e-9))
+        rows = max(32, min(M, rows // 32 * 32))
     vals, dts = [], []
     for _ in range(args.steps):
         v, dt = oracle_timed(rows, cores)
@@ -491,11 +498,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="libmxq", choices=["libmxq", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=512)
-    ap.add_argument("--ref-rows", type=int, default=128)
+    ap.add_argument("--cpu-rows", type=int, default=4096)
+    ap.add_argument("--ref-rows", type=int, default=0,
+                    help="rows of X per reference step (0: sized to ~1 min)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
