@@ -46,6 +46,14 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
   asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
+// Packed max of magnitudes: each half of the result has magnitude
+// max(|a|, |b|) (its sign bit is the XOR of the inputs' and must be
+// cleared by the caller before the value is used as a magnitude).
+__device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 // max of the two halves of a packed word of non-negative bf16 values,
 // returned as the 16-bit pattern.
 __device__ __forceinline__ uint32_t bf16x2_hmax(uint32_t w) {

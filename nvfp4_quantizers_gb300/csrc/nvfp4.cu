@@ -40,7 +40,7 @@ namespace mxq {
 namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
-constexpr int ROW_WARPS = 8;                 // rows per 256-thread CTA
+constexpr int CTA_WARPS = 8;                 // 256 threads per CTA
 constexpr int kMaxGroupsPerLaunch = 64;
 
 struct RowOut {
@@ -52,90 +52,26 @@ struct RowOut {
   int swizzled;
 };
 
+// 16 bf16 values of one block (two 16-byte chunks).
+struct Blk {
+  uint4 a, b;
+};
+
+// max |x| of the 16 values of a block, as a bf16 bit pattern (the sign
+// bit left by max.xorsign.abs is cleared at the end).
+__device__ __forceinline__ uint32_t block_absmax(const Blk& v) {
+  const uint32_t m =
+      bf16x2_maxabs(bf16x2_maxabs(bf16x2_maxabs(v.a.x, v.a.y),
+                                  bf16x2_maxabs(v.a.z, v.a.w)),
+                    bf16x2_maxabs(bf16x2_maxabs(v.b.x, v.b.y),
+                                  bf16x2_maxabs(v.b.z, v.b.w)));
+  return bf16x2_hmax(m & 0x7FFF7FFFu);
+}
+
 __device__ __forceinline__ uint32_t chunk_absmax(const uint4& v) {
-  return bf16x2_hmax(bf16x2_max(bf16x2_absmax(v.x, v.y),
-                                bf16x2_absmax(v.z, v.w)));
-}
-
-// Encode ROUNDS x 32 chunks of one row (chunk c = chunk_base + r*32 + lane)
-// with FP32 scale S.  Lanes holding chunks beyond the row carry zeros.
-template <int ROUNDS>
-__device__ __forceinline__ void encode_rounds(const uint4 (&v)[ROUNDS],
-                                              int chunk_base, int nchunks,
-                                              float S, int lane,
-                                              bool write_codes,
-                                              const RowOut& o) {
-  const float six_s = __fmul_rn(6.0f, S);
-  const int64_t padded_cols = o.swizzled ? ((o.nblocks + 3) & ~int64_t(3))
-                                         : o.nblocks;
-#pragma unroll
-  for (int r = 0; r < ROUNDS; ++r) {
-    if (chunk_base + r * 32 >= nchunks) break;       // warp-uniform
-    const int c = chunk_base + r * 32 + lane;
-    uint32_t a = chunk_absmax(v[r]);
-    a = max(a, __shfl_xor_sync(FULL, a, 1));
-    const float ab = __uint_as_float(a << 16);
-    uint32_t sb = 0;
-    if (S != 0.0f) sb = cvt_e4m3x2(__fdiv_rn(ab, six_s), 0.0f) & 0xFFu;
-    const float d = __fmul_rn(e4m3_to_f32(sb), S);
-    float enc = 0.0f;
-    if (d != 0.0f) enc = fminf(__frcp_rn(d), FLT_MAX);
-    float q[8];
-    q[0] = __fmul_rn(bf16lo_to_f32(v[r].x), enc);
-    q[1] = __fmul_rn(bf16hi_to_f32(v[r].x), enc);
-    q[2] = __fmul_rn(bf16lo_to_f32(v[r].y), enc);
-    q[3] = __fmul_rn(bf16hi_to_f32(v[r].y), enc);
-    q[4] = __fmul_rn(bf16lo_to_f32(v[r].z), enc);
-    q[5] = __fmul_rn(bf16hi_to_f32(v[r].z), enc);
-    q[6] = __fmul_rn(bf16lo_to_f32(v[r].w), enc);
-    q[7] = __fmul_rn(bf16hi_to_f32(v[r].w), enc);
-    const uint32_t packed = cvt_e2m1x8(q);
-    if (write_codes && c < nchunks)
-      *reinterpret_cast<uint32_t*>(o.codes_row + (int64_t)c * 4) = packed;
-    // Lanes 0, 8, 16, 24 gather the scales of blocks b0..b0+3 (held by the
-    // even lanes l, l+2, l+4, l+6).
-    const uint32_t s1 = __shfl_down_sync(FULL, sb, 2);
-    const uint32_t s2 = __shfl_down_sync(FULL, sb, 4);
-    const uint32_t s3 = __shfl_down_sync(FULL, sb, 6);
-    if ((lane & 7) == 0) {
-      const int64_t b0 = c >> 1;
-      const uint32_t word = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-      if (o.swizzled) {
-        if (b0 < padded_cols)
-          *reinterpret_cast<uint32_t*>(
-              o.scales + swz_offset(o.row, b0, o.col_tiles)) = word;
-      } else if ((o.nblocks & 3) == 0) {
-        if (b0 < o.nblocks)
-          *reinterpret_cast<uint32_t*>(o.scales + o.row * o.nblocks + b0) =
-              word;
-      } else {
-        for (int j = 0; j < 4; ++j)
-          if (b0 + j < o.nblocks)
-            o.scales[o.row * o.nblocks + b0 + j] = (uint8_t)(word >> (8 * j));
-      }
-    }
-  }
-}
-
-template <int ROUNDS>
-__device__ __forceinline__ void load_rounds(uint4 (&v)[ROUNDS],
-                                            const uint16_t* row,
-                                            int chunk_base, int nchunks,
-                                            bool real, int lane) {
-#pragma unroll
-  for (int r = 0; r < ROUNDS; ++r) {
-    const int c = chunk_base + r * 32 + lane;
-    v[r] = (real && c < nchunks) ? ld_stream_v4(row + (int64_t)c * 8)
-                                 : make_uint4(0, 0, 0, 0);
-  }
-}
-
-template <int ROUNDS>
-__device__ __forceinline__ uint32_t rounds_absmax(const uint4 (&v)[ROUNDS]) {
-  uint32_t a = 0;
-#pragma unroll
-  for (int r = 0; r < ROUNDS; ++r) a = max(a, chunk_absmax(v[r]));
-  return a;
+  return bf16x2_hmax(bf16x2_maxabs(bf16x2_maxabs(v.x, v.y),
+                                   bf16x2_maxabs(v.z, v.w)) &
+                     0x7FFF7FFFu);
 }
 
 __device__ __forceinline__ uint32_t warp_max(uint32_t a) {
@@ -144,47 +80,185 @@ __device__ __forceinline__ uint32_t warp_max(uint32_t a) {
   return a;
 }
 
+__device__ __forceinline__ void load_block(Blk& v, const uint16_t* row,
+                                           int64_t b, bool valid) {
+  if (valid) {
+    v.a = ld_stream_v4(row + b * 16);
+    v.b = ld_stream_v4(row + b * 16 + 8);
+  } else {
+    v.a = make_uint4(0, 0, 0, 0);
+    v.b = v.a;
+  }
+}
+
+// Encode one 16-value block whose amax (bf16 bits) is `a` with FP32 scale
+// S (six_s = fl(6 S)); returns the packed codes (lo: values 0-7, hi:
+// values 8-15) and the E4M3 block-scale byte.
+__device__ __forceinline__ void encode_block(const Blk& v, uint32_t a, float S,
+                                             float six_s, uint32_t& lo,
+                                             uint32_t& hi, uint32_t& sb) {
+  sb = 0;
+  if (S != 0.0f)
+    sb = cvt_e4m3x2(__fdiv_rn(__uint_as_float(a << 16), six_s), 0.0f) & 0xFFu;
+  const float d = __fmul_rn(e4m3_to_f32(sb), S);
+  float enc = 0.0f;
+  if (d != 0.0f) enc = fminf(__frcp_rn(d), FLT_MAX);
+  float q[8];
+  q[0] = __fmul_rn(bf16lo_to_f32(v.a.x), enc);
+  q[1] = __fmul_rn(bf16hi_to_f32(v.a.x), enc);
+  q[2] = __fmul_rn(bf16lo_to_f32(v.a.y), enc);
+  q[3] = __fmul_rn(bf16hi_to_f32(v.a.y), enc);
+  q[4] = __fmul_rn(bf16lo_to_f32(v.a.z), enc);
+  q[5] = __fmul_rn(bf16hi_to_f32(v.a.z), enc);
+  q[6] = __fmul_rn(bf16lo_to_f32(v.a.w), enc);
+  q[7] = __fmul_rn(bf16hi_to_f32(v.a.w), enc);
+  lo = cvt_e2m1x8(q);
+  q[0] = __fmul_rn(bf16lo_to_f32(v.b.x), enc);
+  q[1] = __fmul_rn(bf16hi_to_f32(v.b.x), enc);
+  q[2] = __fmul_rn(bf16lo_to_f32(v.b.y), enc);
+  q[3] = __fmul_rn(bf16hi_to_f32(v.b.y), enc);
+  q[4] = __fmul_rn(bf16lo_to_f32(v.b.z), enc);
+  q[5] = __fmul_rn(bf16hi_to_f32(v.b.z), enc);
+  q[6] = __fmul_rn(bf16lo_to_f32(v.b.w), enc);
+  q[7] = __fmul_rn(bf16hi_to_f32(v.b.w), enc);
+  hi = cvt_e2m1x8(q);
+}
+
+// Store a lane's block: 8 bytes of codes, and (lanes 0, 4, 8, ...) the
+// 32-bit word holding the scales of blocks b0..b0+3 gathered from the
+// four consecutive lanes that own them.  `b` is the lane's block index;
+// all 32 lanes of the warp must call this together.
+__device__ __forceinline__ void store_block(const RowOut& o, int64_t b,
+                                            bool write_codes, uint32_t lo,
+                                            uint32_t hi, uint32_t sb, int lane) {
+  if (write_codes && b < o.nblocks) st_v2(o.codes_row + b * 8, lo, hi);
+  const uint32_t s1 = __shfl_down_sync(FULL, sb, 1);
+  const uint32_t s2 = __shfl_down_sync(FULL, sb, 2);
+  const uint32_t s3 = __shfl_down_sync(FULL, sb, 3);
+  if ((lane & 3) == 0) {
+    const uint32_t word = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    if (o.swizzled) {
+      if (b < ((o.nblocks + 3) & ~int64_t(3)))
+        *reinterpret_cast<uint32_t*>(o.scales +
+                                     swz_offset(o.row, b, o.col_tiles)) = word;
+    } else if ((o.nblocks & 3) == 0) {
+      if (b < o.nblocks)
+        *reinterpret_cast<uint32_t*>(o.scales + o.row * o.nblocks + b) = word;
+    } else {
+      for (int j = 0; j < 4; ++j)
+        if (b + j < o.nblocks)
+          o.scales[o.row * o.nblocks + b + j] = (uint8_t)(word >> (8 * j));
+    }
+  }
+}
+
+// One row of H values is spread over WPR warps; warp w of the row owns
+// blocks [w*R*32, (w+1)*R*32), lane l the blocks w*R*32 + r*32 + l.  The
+// row's amax is combined across its warps through shared memory and a
+// named barrier (id 1 + row slot, 32*WPR threads).
+template <int R, int WPR>
+__device__ __forceinline__ void encode_row_warps(
+    const uint16_t* row, bool real, float S_given, bool use_given,
+    const RowOut& o, int row_slot, int wpart, int lane, uint32_t* red,
+    float* S_used) {
+  const int64_t blk0 = (int64_t)wpart * R * 32;
+  Blk v[R];
+  uint32_t am[R];
+  uint32_t a = 0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int64_t b = blk0 + r * 32 + lane;
+    load_block(v[r], row, b, real && b < o.nblocks);
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    am[r] = block_absmax(v[r]);
+    a = max(a, am[r]);
+  }
+  float S = S_given;
+  if (!use_given) {
+    a = warp_max(a);
+    if (WPR > 1) {
+      if (lane == 0) red[row_slot * WPR + wpart] = a;
+      named_barrier_sync(1 + row_slot, 32 * WPR);
+      for (int w = 0; w < WPR; ++w) a = max(a, red[row_slot * WPR + w]);
+    }
+    S = __fdiv_rn(__uint_as_float(a << 16), kNvfp4ScaleDenom);
+  }
+  const float six_s = __fmul_rn(6.0f, S);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (blk0 + r * 32 >= o.nblocks) break;             // warp-uniform
+    uint32_t lo, hi, sb;
+    encode_block(v[r], am[r], S, six_s, lo, hi, sb);
+    store_block(o, blk0 + r * 32 + lane, real, lo, hi, sb, lane);
+  }
+  *S_used = S;
+}
+
 // ---------------------------------------------------------------------------
 // Per-token activations.
 // ---------------------------------------------------------------------------
-template <int ROUNDS>
-__global__ void __launch_bounds__(ROW_WARPS * 32)
+template <int R, int WPR>
+__global__ void __launch_bounds__(CTA_WARPS * 32)
     nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t T_pad,
                        int64_t H, int64_t ldx, uint8_t* __restrict__ codes,
                        uint8_t* __restrict__ scales, float* __restrict__ S_out,
                        int swizzled) {
-  const int lane = threadIdx.x & 31;
-  const int64_t t = (int64_t)blockIdx.x * ROW_WARPS + (threadIdx.x >> 5);
-  if (t >= T_pad) return;
+  constexpr int ROWS = CTA_WARPS / WPR;
+  __shared__ uint32_t red[CTA_WARPS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = warp / WPR, wpart = warp % WPR;
+  const int64_t t = (int64_t)blockIdx.x * ROWS + slot;
+  if (t >= T_pad) return;                 // uniform over the row's warps
   const bool real = t < T;
-  const int nchunks = (int)(H >> 3);
-  const uint16_t* row = x + t * ldx;
   RowOut o{codes + t * (H >> 1), scales, t, ((H >> 4) + 3) >> 2, H >> 4,
            swizzled};
   float S;
-  if ((int64_t)ROUNDS * 32 >= nchunks) {
-    uint4 v[ROUNDS];
-    load_rounds<ROUNDS>(v, row, 0, nchunks, real, lane);
-    const uint32_t a = warp_max(rounds_absmax<ROUNDS>(v));
-    S = __fdiv_rn(__uint_as_float(a << 16), kNvfp4ScaleDenom);
-    encode_rounds<ROUNDS>(v, 0, nchunks, S, lane, real, o);
-  } else {
-    // Long rows: amax pass, then a second (cache-served) pass to encode.
-    uint32_t a = 0;
-    for (int base = 0; base < nchunks; base += ROUNDS * 32) {
-      uint4 v[ROUNDS];
-      load_rounds<ROUNDS>(v, row, base, nchunks, real, lane);
-      a = max(a, rounds_absmax<ROUNDS>(v));
-    }
-    a = warp_max(a);
-    S = __fdiv_rn(__uint_as_float(a << 16), kNvfp4ScaleDenom);
-    for (int base = 0; base < nchunks; base += ROUNDS * 32) {
-      uint4 v[ROUNDS];
-      load_rounds<ROUNDS>(v, row, base, nchunks, real, lane);
-      encode_rounds<ROUNDS>(v, base, nchunks, S, lane, real, o);
-    }
+  encode_row_warps<R, WPR>(x + t * ldx, real, 0.0f, false, o, slot, wpart,
+                           lane, red, &S);
+  if (real && wpart == 0 && lane == 0) S_out[t] = S;
+}
+
+// Rows longer than 8 warps x 2048 values: one CTA per row, an amax pass and
+// a second (cache-served) pass that encodes.
+__global__ void __launch_bounds__(CTA_WARPS * 32)
+    nvfp4_token_long_kernel(const uint16_t* __restrict__ x, int64_t T,
+                            int64_t H, int64_t ldx,
+                            uint8_t* __restrict__ codes,
+                            uint8_t* __restrict__ scales,
+                            float* __restrict__ S_out, int swizzled) {
+  __shared__ uint32_t red[CTA_WARPS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = blockIdx.x;
+  const bool real = t < T;
+  const uint16_t* row = x + t * ldx;
+  RowOut o{codes + t * (H >> 1), scales, t, ((H >> 4) + 3) >> 2, H >> 4,
+           swizzled};
+  const int64_t span = CTA_WARPS * 32;
+  uint32_t a = 0;
+  for (int64_t b0 = 0; b0 < o.nblocks; b0 += span) {
+    const int64_t b = b0 + threadIdx.x;
+    Blk v;
+    load_block(v, row, b, real && b < o.nblocks);
+    a = max(a, block_absmax(v));
   }
-  if (real && lane == 0) S_out[t] = S;
+  a = warp_max(a);
+  if (lane == 0) red[warp] = a;
+  __syncthreads();
+  for (int w = 0; w < CTA_WARPS; ++w) a = max(a, red[w]);
+  const float S = __fdiv_rn(__uint_as_float(a << 16), kNvfp4ScaleDenom);
+  const float six_s = __fmul_rn(6.0f, S);
+  for (int64_t b0 = 0; b0 < o.nblocks; b0 += span) {
+    if (b0 + warp * 32 >= o.nblocks) continue;         // warp-uniform
+    const int64_t b = b0 + threadIdx.x;
+    Blk v;
+    load_block(v, row, b, real && b < o.nblocks);
+    uint32_t lo, hi, sb;
+    encode_block(v, block_absmax(v), S, six_s, lo, hi, sb);
+    store_block(o, b, real, lo, hi, sb, lane);
+  }
+  if (real && threadIdx.x == 0) S_out[t] = S;
 }
 
 // ---------------------------------------------------------------------------
@@ -243,13 +317,16 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-template <int ROUNDS>
-__global__ void __launch_bounds__(ROW_WARPS * 32)
+template <int R, int WPR>
+__global__ void __launch_bounds__(CTA_WARPS * 32)
     nvfp4_group_rows_kernel(const __grid_constant__ GroupTable tab,
                             const __grid_constant__ GroupParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t w = (int64_t)blockIdx.x * ROW_WARPS + (threadIdx.x >> 5);
-  if (w >= (int64_t)p.ng * p.R_pad) return;
+  constexpr int ROWS = CTA_WARPS / WPR;
+  __shared__ uint32_t red[CTA_WARPS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = warp / WPR, wpart = warp % WPR;
+  const int64_t w = (int64_t)blockIdx.x * ROWS + slot;
+  if (w >= (int64_t)p.ng * p.R_pad) return;       // uniform over the row
   const int gl = (int)(w / p.R_pad);
   const int64_t r = w - (int64_t)gl * p.R_pad;
   const int64_t g = p.g0 + gl;
@@ -263,26 +340,28 @@ __global__ void __launch_bounds__(ROW_WARPS * 32)
   const float S = p.S_in ? p.S_in[g]
                          : __fdiv_rn(__uint_as_float(p.amax[g]),
                                      kNvfp4ScaleDenom);
-  if (r == 0 && lane == 0) p.group_scales[g] = S;
-  const int nchunks = (int)(p.K >> 3);
+  if (r == 0 && wpart == 0 && lane == 0) p.group_scales[g] = S;
   RowOut o{p.codes + (g * p.R + r) * (p.K >> 1), p.scales + g * p.scale_stride,
            r, ((p.K >> 4) + 3) >> 2, p.K >> 4, p.swizzled};
-  for (int base = 0; base < nchunks; base += ROUNDS * 32) {
-    uint4 v[ROUNDS];
-    load_rounds<ROUNDS>(v, row, base, nchunks, real, lane);
-    encode_rounds<ROUNDS>(v, base, nchunks, S, lane, real, o);
-  }
+  float S_used;
+  encode_row_warps<R, WPR>(row, real, S, true, o, slot, wpart, lane, red,
+                           &S_used);
 }
 
-// Smallest supported ROUNDS >= the rounds a row needs (capped at 16; longer
-// rows loop).
-int pick_rounds(int64_t H) {
-  const int64_t need = ((H >> 3) + 31) / 32;
-  if (need <= 1) return 1;
-  if (need <= 2) return 2;
-  if (need <= 4) return 4;
-  if (need <= 8) return 8;
-  return 16;
+// Launch shape of the row encoders: R blocks per lane (R * 512 values per
+// warp) and WPR warps per row; 0 = rows too long (one CTA per row).
+struct RowShape {
+  int R, WPR;
+};
+RowShape pick_shape(int64_t H) {
+  const int64_t nb = H >> 4;
+  if (nb <= 32) return {1, 1};
+  if (nb <= 64) return {2, 1};
+  if (nb <= 128) return {4, 1};
+  if (nb <= 256) return {4, 2};
+  if (nb <= 512) return {4, 4};
+  if (nb <= 1024) return {4, 8};
+  return {0, 0};
 }
 
 }  // namespace
@@ -292,18 +371,24 @@ cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
                                    uint8_t* scales, float* token_scales,
                                    int swizzled, cudaStream_t stream) {
   const int64_t T_pad = swizzled ? (T + 127) / 128 * 128 : T;
-  const int64_t grid = (T_pad + ROW_WARPS - 1) / ROW_WARPS;
   const uint16_t* xs = static_cast<const uint16_t*>(x);
-#define MXQ_TOKEN_LAUNCH(R)                                                  \
-  nvfp4_token_kernel<R><<<(unsigned)grid, ROW_WARPS * 32, 0, stream>>>(      \
-      xs, T, T_pad, H, ldx, codes, scales, token_scales, swizzled)
-  switch (pick_rounds(H)) {
-    case 1: MXQ_TOKEN_LAUNCH(1); break;
-    case 2: MXQ_TOKEN_LAUNCH(2); break;
-    case 4: MXQ_TOKEN_LAUNCH(4); break;
-    case 8: MXQ_TOKEN_LAUNCH(8); break;
-    default: MXQ_TOKEN_LAUNCH(16); break;
+  const RowShape sh = pick_shape(H);
+  if (sh.R == 0) {
+    nvfp4_token_long_kernel<<<(unsigned)T_pad, CTA_WARPS * 32, 0, stream>>>(
+        xs, T, H, ldx, codes, scales, token_scales, swizzled);
+    return cudaGetLastError();
   }
+  const int rows_per_cta = CTA_WARPS / sh.WPR;
+  const unsigned grid = (unsigned)((T_pad + rows_per_cta - 1) / rows_per_cta);
+#define MXQ_TOKEN_LAUNCH(R_, W_)                                        \
+  nvfp4_token_kernel<R_, W_><<<grid, CTA_WARPS * 32, 0, stream>>>(      \
+      xs, T, T_pad, H, ldx, codes, scales, token_scales, swizzled)
+  if (sh.R == 1) MXQ_TOKEN_LAUNCH(1, 1);
+  else if (sh.R == 2) MXQ_TOKEN_LAUNCH(2, 1);
+  else if (sh.WPR == 1) MXQ_TOKEN_LAUNCH(4, 1);
+  else if (sh.WPR == 2) MXQ_TOKEN_LAUNCH(4, 2);
+  else if (sh.WPR == 4) MXQ_TOKEN_LAUNCH(4, 4);
+  else MXQ_TOKEN_LAUNCH(4, 8);
 #undef MXQ_TOKEN_LAUNCH
   return cudaGetLastError();
 }
@@ -346,6 +431,8 @@ cudaError_t launch_nvfp4_weight_shared(
   int64_t ctas_per_group = (group_chunks + 256 * 16 - 1) / (256 * 16);
   ctas_per_group = ctas_per_group < 1 ? 1 : (ctas_per_group > 65535 ? 65535 : ctas_per_group);
 
+  const RowShape sh = pick_shape(K);
+  if (sh.R == 0) return cudaErrorInvalidValue;   // K > 16384: not supported
   GroupTable tab;
   for (int64_t g0 = 0; g0 < num_groups; g0 += chunk) {
     const int ng = (int)((num_groups - g0) < chunk ? (num_groups - g0) : chunk);
@@ -366,16 +453,16 @@ cudaError_t launch_nvfp4_weight_shared(
       if (err != cudaSuccess) return err;
     }
     const int64_t rows = (int64_t)ng * p.R_pad;
-    const unsigned grid = (unsigned)((rows + ROW_WARPS - 1) / ROW_WARPS);
-#define MXQ_GROUP_LAUNCH(R) \
-  nvfp4_group_rows_kernel<R><<<grid, ROW_WARPS * 32, 0, stream>>>(tab, p)
-    switch (pick_rounds(K)) {
-      case 1: MXQ_GROUP_LAUNCH(1); break;
-      case 2: MXQ_GROUP_LAUNCH(2); break;
-      case 4: MXQ_GROUP_LAUNCH(4); break;
-      case 8: MXQ_GROUP_LAUNCH(8); break;
-      default: MXQ_GROUP_LAUNCH(16); break;
-    }
+    const int rows_per_cta = CTA_WARPS / sh.WPR;
+    const unsigned grid = (unsigned)((rows + rows_per_cta - 1) / rows_per_cta);
+#define MXQ_GROUP_LAUNCH(R_, W_) \
+  nvfp4_group_rows_kernel<R_, W_><<<grid, CTA_WARPS * 32, 0, stream>>>(tab, p)
+    if (sh.R == 1) MXQ_GROUP_LAUNCH(1, 1);
+    else if (sh.R == 2) MXQ_GROUP_LAUNCH(2, 1);
+    else if (sh.WPR == 1) MXQ_GROUP_LAUNCH(4, 1);
+    else if (sh.WPR == 2) MXQ_GROUP_LAUNCH(4, 2);
+    else if (sh.WPR == 4) MXQ_GROUP_LAUNCH(4, 4);
+    else MXQ_GROUP_LAUNCH(4, 8);
 #undef MXQ_GROUP_LAUNCH
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
