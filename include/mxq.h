@@ -195,6 +195,40 @@ mxq_status nvfp4_quantize_weight_shared(
     int scale_layout, void* ws, size_t ws_bytes, void* stream);
 
 /* --------------------------------------------------------------------- */
+/* NVFP4 weight quantize with a shared FP32 scale, allocating nothing.    */
+/*                                                                       */
+/* The pages have no counterpart to this entry point: it exists for       */
+/* callers that cannot allocate device memory -- plug-ins inside a host   */
+/* framework that owns every device allocation and offers no allocator,   */
+/* and latency-critical loops where a cudaMalloc (which may synchronize   */
+/* the device) is not allowed -- and so cannot provide the workspace of   */
+/* nvfp4_quantize_weight_shared.                                          */
+/*                                                                       */
+/* Same arguments, layouts and results as nvfp4_quantize_weight_shared,   */
+/* without ws / ws_bytes: the per-group scratch lives in a fixed device   */
+/* array inside the library (16 KiB, held on every GPU that loads the     */
+/* library until the process exits).                                      */
+/*  - num_groups must not exceed                                          */
+/*    nvfp4_quantize_weight_shared_noalloc_max_groups() (4096); larger    */
+/*    requests are rejected with MXQ_ERR_SHAPE before anything runs.      */
+/*  - The first call on a device looks up the array's device address      */
+/*    (cudaGetSymbolAddress) with that device current; make that first    */
+/*    call before any stream capture on the device.                       */
+/*  - Every call shares the array.  A call clears the words it uses on    */
+/*    its own stream before using them, so back-to-back calls on one      */
+/*    stream are correct; calls whose work overlaps on the GPU (unordered */
+/*    streams) race on the array.                                         */
+/*  - Calls no cudaMalloc, cudaFree or allocating routine.                */
+/* --------------------------------------------------------------------- */
+int64_t nvfp4_quantize_weight_shared_noalloc_max_groups(void);
+
+mxq_status nvfp4_quantize_weight_shared_noalloc(
+    int64_t num_groups, int num_parts, const void* const* parts,
+    const int64_t* part_rows, int64_t K, uint8_t* codes,
+    uint8_t* block_scales, float* group_scales, const float* group_scales_in,
+    int scale_layout, void* stream);
+
+/* --------------------------------------------------------------------- */
 /* MXFP8 dequantize to bf16.                                              */
 /*                                                                       */
 /* [MILES] backward-mode section: dequantized backward feeds the BF16     */

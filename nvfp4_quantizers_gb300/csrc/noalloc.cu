@@ -1,0 +1,117 @@
+// noalloc.cu -- nvfp4_quantize_weight_shared_noalloc: the shared-scale
+// NVFP4 weight quantizer without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at all: code that runs as a
+// plug-in inside a host framework that owns every device allocation and
+// gives its plug-ins no allocator, and latency-critical loops in which a
+// cudaMalloc (which may synchronize the device) is not allowed.  Such a
+// caller can still hand over its inputs and outputs, but not the small
+// scratch buffer that nvfp4_quantize_weight_shared needs for the per-group
+// amax words.  This entry point keeps that scratch in a fixed array in the
+// library's own device memory instead.
+//
+//  * The scratch is a file-scope device array of kNoAllocMaxGroups 32-bit
+//    words (16 KiB).  Every GPU that loads the library holds it until the
+//    process exits.
+//  * Host code cannot use the array's name as a device address (on the
+//    host it only stands in for the symbol).  The first call on a device
+//    looks the address up with cudaGetSymbolAddress, with that device
+//    current, and caches it; make that first call before any stream
+//    capture on the device.
+//  * All calls share the one array and it keeps the last call's contents:
+//    the words a call uses are cleared (cudaMemsetAsync on the call's
+//    stream) before its amax kernel runs.  Calls whose kernels overlap on
+//    the GPU (different streams, no ordering between them) race on the
+//    array; order them on one stream.
+//  * Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/mxq.h"
+#include "launch.h"
+
+namespace mxq {
+
+namespace {
+
+constexpr int64_t kNoAllocMaxGroups = 4096;
+static __device__ __align__(256) uint32_t g_noalloc_amax[kNoAllocMaxGroups];
+
+constexpr int kMaxDev = 64;
+std::mutex g_mu;
+uint32_t* g_addr[kMaxDev] = {};
+
+// Device address of g_noalloc_amax on the current device (looked up once
+// per device).
+cudaError_t noalloc_scratch(uint32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_amax);
+    if (e != cudaSuccess) return e;
+    g_addr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_addr[dev];
+  return cudaSuccess;
+}
+
+bool is_aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+}  // namespace
+
+}  // namespace mxq
+
+using namespace mxq;
+
+extern "C" {
+
+int64_t nvfp4_quantize_weight_shared_noalloc_max_groups(void) {
+  return kNoAllocMaxGroups;
+}
+
+mxq_status nvfp4_quantize_weight_shared_noalloc(
+    int64_t num_groups, int num_parts, const void* const* parts,
+    const int64_t* part_rows, int64_t K, uint8_t* codes,
+    uint8_t* block_scales, float* group_scales, const float* group_scales_in,
+    int scale_layout, void* stream) {
+  if (scale_layout != MXQ_SCALE_LINEAR && scale_layout != MXQ_SCALE_SWIZZLED)
+    return MXQ_ERR_LAYOUT;
+  if (num_groups < 0 || K < 0) return MXQ_ERR_SHAPE;
+  if (num_groups > kNoAllocMaxGroups) return MXQ_ERR_SHAPE;
+  if (num_parts < 1 || num_parts > kMaxParts) return MXQ_ERR_ARG;
+  if (num_groups == 0 || K == 0) return MXQ_OK;
+  if (!parts || !part_rows || !codes || !block_scales || !group_scales)
+    return MXQ_ERR_NULL;
+  if (K % 16 != 0 || K >= (1ll << 30)) return MXQ_ERR_SHAPE;
+  int64_t R = 0;
+  for (int i = 0; i < num_parts; ++i) {
+    if (part_rows[i] < 0) return MXQ_ERR_SHAPE;
+    R += part_rows[i];
+  }
+  if (R == 0) return MXQ_OK;
+  for (int64_t i = 0; i < num_groups * num_parts; ++i) {
+    if (part_rows[i % num_parts] > 0 && !parts[i]) return MXQ_ERR_NULL;
+    if (!is_aligned16(parts[i])) return MXQ_ERR_ALIGN;
+  }
+  if (!is_aligned16(codes) || !is_aligned16(block_scales) ||
+      !is_aligned16(group_scales) ||
+      (group_scales_in && !is_aligned16(group_scales_in)))
+    return MXQ_ERR_ALIGN;
+  uint32_t* scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return MXQ_ERR_CUDA;
+  cudaError_t e = launch_nvfp4_weight_shared(
+      num_groups, num_parts, parts, part_rows, K, codes, block_scales,
+      group_scales, group_scales_in, scale_layout == MXQ_SCALE_SWIZZLED,
+      scratch, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+}
+
+}  // extern "C"
