@@ -10,13 +10,13 @@
 //   NVFP4: y = bf16_RNE( (E2M1(c) * E4M3(sb)) * S )          (f32 products,
 //          the inner one exact)
 //
-// Design (sm_103a): pure streaming.  A thread converts 8 elements per step:
-// an 8-byte (MXFP8) or 4-byte (NVFP4) code load and one 16-byte bf16 store,
-// so a warp's loads and stores are both contiguous.  The codes widen
-// exactly through cvt.rn.f16x2.{e4m3x2,e2m1x2}; the scale multiply is one
-// binary32 multiply and the bf16 rounding one cvt.rn.bf16x2.f32.  The
-// (row, column) of a thread's chunk is advanced incrementally across the
-// grid-stride loop, so no per-element integer division is needed.
+// Design (sm_103a): pure streaming, grid-stride over 16-element units with
+// four 256-thread CTAs per SM.  A thread converts 16 values per step: a
+// 16-byte (MXFP8) or 8-byte (NVFP4) code load, one scale byte, and two
+// 16-byte bf16 stores.  The codes widen exactly through
+// cvt.rn.f16x2.{e4m3x2,e2m1x2}; the scale multiply is one binary32
+// multiply and the bf16 rounding one cvt.rn.bf16x2.f32.  Index math is
+// 32-bit whenever every index fits.
 #include "common.cuh"
 #include "launch.h"
 
@@ -25,148 +25,92 @@ namespace mxq {
 namespace {
 
 constexpr int DQ_THREADS = 256;
-constexpr int DQ_UNROLL = 4;
+constexpr int DQ_CTAS_PER_SM = 4;
 
-// Coordinates (batch entry, row, column) of a thread's current 8-element
-// chunk, advanced by a fixed grid stride with carries instead of divisions.
-struct Cursor {
-  int64_t bi, row, col;       // batch entry, row within it, column
-  int64_t dbi, drow, dcol;    // advance per grid-stride step
-  int64_t rows, cols;
-  __device__ __forceinline__ void advance() {
-    col += dcol;
-    row += drow;
-    bi += dbi;
-    if (col >= cols) { col -= cols; row += 1; }
-    if (row >= rows) { row -= rows; bi += 1; }
-  }
-};
-
-__device__ __forceinline__ Cursor make_cursor(int64_t chunk, int64_t stride,
-                                              int64_t rows, int64_t cols) {
-  Cursor c;
-  const int64_t e = chunk * 8, de = stride * 8;
-  const int64_t grow = e / cols, dgrow = de / cols;
-  c.col = e - grow * cols;
-  c.dcol = de - dgrow * cols;
-  c.bi = grow / rows;
-  c.row = grow - c.bi * rows;
-  c.dbi = dgrow / rows;
-  c.drow = dgrow - c.dbi * rows;
-  c.rows = rows;
-  c.cols = cols;
-  return c;
-}
-
+// MXFP8: a thread converts 16 codes (one 16-byte load, half a 1x32 block)
+// into 32 bytes of bf16 per step.  Idx is uint32_t when every index fits.
+template <typename Idx>
 __global__ void __launch_bounds__(DQ_THREADS)
     dequant_mxfp8_kernel(const uint8_t* __restrict__ codes,
-                         const uint8_t* __restrict__ scales, int64_t rows,
-                         int64_t cols, int swizzled,
-                         uint16_t* __restrict__ y) {
-  const int64_t nchunks = rows * cols / 8;
-  const int64_t stride = (int64_t)gridDim.x * DQ_THREADS;
-  int64_t i = (int64_t)blockIdx.x * DQ_THREADS + threadIdx.x;
-  if (i >= nchunks) return;
-  Cursor cur = make_cursor(i, stride, rows, cols);
-  const int64_t nb = cols >> 5, col_tiles = (nb + 3) >> 2;
-  for (; i < nchunks; i += stride * DQ_UNROLL) {
-    uint2 c[DQ_UNROLL];
-    uint32_t sbyte[DQ_UNROLL];
-    int64_t out[DQ_UNROLL];
-    bool ok[DQ_UNROLL];
-    Cursor k = cur;
+                         const uint8_t* __restrict__ scales, Idx rows,
+                         Idx cols, int swizzled, uint16_t* __restrict__ y) {
+  const Idx c16 = cols >> 4, nb = cols >> 5;
+  const Idx n16 = rows * c16;
+  const int64_t col_tiles = ((int64_t)nb + 3) >> 2;
+  for (Idx i = (Idx)blockIdx.x * DQ_THREADS + threadIdx.x; i < n16;
+       i += (Idx)gridDim.x * DQ_THREADS) {
+    const uint4 c = ld_stream_v4(codes + (int64_t)i * 16);
+    const Idx r = i / c16;
+    const Idx b = (i - r * c16) >> 1;
+    const uint32_t sbyte = swizzled ? scales[swz_offset(r, b, col_tiles)]
+                                    : scales[(int64_t)r * nb + b];
+    const float sc = e8m0_scale(sbyte);
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    uint32_t w[8];
 #pragma unroll
-    for (int u = 0; u < DQ_UNROLL; ++u) {
-      const int64_t j = i + u * stride;
-      ok[u] = j < nchunks;
-      if (ok[u]) {
-        asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
-                     : "=r"(c[u].x), "=r"(c[u].y)
-                     : "l"(codes + j * 8));
-        const int64_t b = k.col >> 5;
-        sbyte[u] = swizzled ? scales[swz_offset(k.row, b, col_tiles)]
-                            : scales[k.row * nb + b];
-        out[u] = j * 8;
-      }
-      k.advance();
+    for (int h = 0; h < 8; ++h) {
+      float a, bb;
+      e4m3x2_to_f32((cw[h >> 1] >> ((h & 1) * 16)) & 0xFFFFu, a, bb);
+      w[h] = f32x2_to_bf16x2(__fmul_rn(a, sc), __fmul_rn(bb, sc));
     }
-    cur = k;
-#pragma unroll
-    for (int u = 0; u < DQ_UNROLL; ++u) {
-      if (!ok[u]) continue;
-      const float sc = e8m0_scale(sbyte[u]);
-      uint32_t w[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const uint32_t two = ((h < 2 ? c[u].x : c[u].y) >> ((h & 1) * 16)) & 0xFFFFu;
-        float a, b;
-        e4m3x2_to_f32(two, a, b);
-        w[h] = f32x2_to_bf16x2(__fmul_rn(a, sc), __fmul_rn(b, sc));
-      }
-      st_v4(y + out[u], make_uint4(w[0], w[1], w[2], w[3]));
-    }
+    uint16_t* dst = y + (int64_t)i * 16;
+    st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
+    st_v4(dst + 8, make_uint4(w[4], w[5], w[6], w[7]));
   }
 }
 
+// NVFP4: a thread converts one 16-value block (8 bytes of codes) into 32
+// bytes of bf16 per step.  Rows are grouped in `batch` matrices of
+// rows_per_batch rows, each with its own scale matrix (scale_stride bytes
+// apart); S is per row (global row index) or per batch entry.
+template <typename Idx>
 __global__ void __launch_bounds__(DQ_THREADS)
     dequant_nvfp4_kernel(const uint8_t* __restrict__ codes,
                          const uint8_t* __restrict__ scales,
                          const float* __restrict__ S, int per_batch,
-                         int64_t rows_per_batch, int64_t total_rows,
-                         int64_t cols, int swizzled, int64_t scale_stride,
+                         Idx rows_per_batch, Idx total_rows, Idx cols,
+                         int swizzled, int64_t scale_stride,
                          uint16_t* __restrict__ y) {
-  const int64_t nchunks = total_rows * cols / 8;
-  const int64_t stride = (int64_t)gridDim.x * DQ_THREADS;
-  int64_t i = (int64_t)blockIdx.x * DQ_THREADS + threadIdx.x;
-  if (i >= nchunks) return;
-  Cursor cur = make_cursor(i, stride, rows_per_batch, cols);
-  const int64_t nb = cols >> 4, col_tiles = (nb + 3) >> 2;
-  for (; i < nchunks; i += stride * DQ_UNROLL) {
-    uint32_t c[DQ_UNROLL];
-    uint32_t sbyte[DQ_UNROLL];
-    float s32[DQ_UNROLL];
-    bool ok[DQ_UNROLL];
-    Cursor k = cur;
-#pragma unroll
-    for (int u = 0; u < DQ_UNROLL; ++u) {
-      const int64_t j = i + u * stride;
-      ok[u] = j < nchunks;
-      if (ok[u]) {
-        asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];"
-                     : "=r"(c[u])
-                     : "l"(codes + j * 4));
-        const int64_t b = k.col >> 4;
-        const int64_t grow = k.bi * rows_per_batch + k.row;
-        sbyte[u] = swizzled ? scales[k.bi * scale_stride +
-                                     swz_offset(k.row, b, col_tiles)]
-                            : scales[grow * nb + b];
-        s32[u] = per_batch ? S[k.bi] : S[grow];
-      }
-      k.advance();
+  const Idx nb = cols >> 4;
+  const Idx nblk = total_rows * nb;
+  const int64_t col_tiles = ((int64_t)nb + 3) >> 2;
+  const bool need_batch = swizzled || per_batch;
+  for (Idx i = (Idx)blockIdx.x * DQ_THREADS + threadIdx.x; i < nblk;
+       i += (Idx)gridDim.x * DQ_THREADS) {
+    uint2 c;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(c.x), "=r"(c.y)
+                 : "l"(codes + (int64_t)i * 8));
+    const Idx grow = i / nb;
+    const Idx b = i - grow * nb;
+    Idx bi = 0, r = grow;
+    if (need_batch) {
+      bi = grow / rows_per_batch;
+      r = grow - bi * rows_per_batch;
     }
-    cur = k;
+    const uint32_t sbyte =
+        swizzled ? scales[(int64_t)bi * scale_stride + swz_offset(r, b, col_tiles)]
+                 : scales[(int64_t)grow * nb + b];
+    const float s32 = per_batch ? S[bi] : S[grow];
+    const float bs = e4m3_to_f32(sbyte);
+    uint32_t w[8];
 #pragma unroll
-    for (int u = 0; u < DQ_UNROLL; ++u) {
-      if (!ok[u]) continue;
-      const float bs = e4m3_to_f32(sbyte[u]);
-      uint32_t w[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float a, b;
-        e2m1x2_to_f32(c[u] >> (8 * h), a, b);
-        w[h] = f32x2_to_bf16x2(__fmul_rn(__fmul_rn(a, bs), s32[u]),
-                               __fmul_rn(__fmul_rn(b, bs), s32[u]));
-      }
-      st_v4(y + (i + u * stride) * 8, make_uint4(w[0], w[1], w[2], w[3]));
+    for (int h = 0; h < 8; ++h) {
+      float a, bb;
+      e2m1x2_to_f32((h < 4 ? c.x : c.y) >> (8 * (h & 3)), a, bb);
+      w[h] = f32x2_to_bf16x2(__fmul_rn(__fmul_rn(a, bs), s32),
+                             __fmul_rn(__fmul_rn(bb, bs), s32));
     }
+    uint16_t* dst = y + (int64_t)i * 16;
+    st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
+    st_v4(dst + 8, make_uint4(w[4], w[5], w[6], w[7]));
   }
 }
 
-int64_t dq_grid(int64_t nchunks, int dev) {
-  const int64_t per_cta = (int64_t)DQ_THREADS * DQ_UNROLL;
-  int64_t g = (nchunks + per_cta - 1) / per_cta;
-  const int64_t cap = (int64_t)sm_count(dev) * 8;
-  return g < 1 ? 1 : (g > cap ? cap : g);
+unsigned dq_grid(int64_t units, int dev) {
+  int64_t g = (units + DQ_THREADS - 1) / DQ_THREADS;
+  const int64_t cap = (int64_t)sm_count(dev) * DQ_CTAS_PER_SM;
+  return (unsigned)(g < 1 ? 1 : (g > cap ? cap : g));
 }
 
 }  // namespace
@@ -177,10 +121,16 @@ cudaError_t launch_dequant_mxfp8(const uint8_t* codes, const uint8_t* scales,
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  const int64_t nchunks = rows * cols / 8;
-  dequant_mxfp8_kernel<<<(unsigned)dq_grid(nchunks, dev), DQ_THREADS, 0,
-                         stream>>>(codes, scales, rows, cols, swizzled,
-                                   static_cast<uint16_t*>(y));
+  const int64_t units = rows * (cols / 16);
+  const unsigned grid = dq_grid(units, dev);
+  uint16_t* out = static_cast<uint16_t*>(y);
+  // 32-bit indices when the largest index and the grid stride fit.
+  if (units + (int64_t)grid * DQ_THREADS < (1ll << 32))
+    dequant_mxfp8_kernel<uint32_t><<<grid, DQ_THREADS, 0, stream>>>(
+        codes, scales, (uint32_t)rows, (uint32_t)cols, swizzled, out);
+  else
+    dequant_mxfp8_kernel<int64_t><<<grid, DQ_THREADS, 0, stream>>>(
+        codes, scales, rows, cols, swizzled, out);
   return cudaGetLastError();
 }
 
@@ -192,12 +142,18 @@ cudaError_t launch_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales,
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   const int64_t total_rows = batch * rows;
-  const int64_t nchunks = total_rows * cols / 8;
-  dequant_nvfp4_kernel<<<(unsigned)dq_grid(nchunks, dev), DQ_THREADS, 0,
-                         stream>>>(codes, scales, S, per_batch, rows,
-                                   total_rows, cols, swizzled,
-                                   scale_bytes(rows, cols / 16, swizzled),
-                                   static_cast<uint16_t*>(y));
+  const int64_t units = total_rows * (cols / 16);
+  const unsigned grid = dq_grid(units, dev);
+  const int64_t stride = scale_bytes(rows, cols / 16, swizzled);
+  uint16_t* out = static_cast<uint16_t*>(y);
+  if (units + (int64_t)grid * DQ_THREADS < (1ll << 32))
+    dequant_nvfp4_kernel<uint32_t><<<grid, DQ_THREADS, 0, stream>>>(
+        codes, scales, S, per_batch, (uint32_t)rows, (uint32_t)total_rows,
+        (uint32_t)cols, swizzled, stride, out);
+  else
+    dequant_nvfp4_kernel<int64_t><<<grid, DQ_THREADS, 0, stream>>>(
+        codes, scales, S, per_batch, rows, total_rows, cols, swizzled, stride,
+        out);
   return cudaGetLastError();
 }
 

@@ -8,15 +8,18 @@
 // data and both copies are materialized by the same quantization.
 //
 // Design (sm_103a):
-//  * Persistent CTAs, 2 per SM.  A producer warp streams 128x128 bf16
-//    tiles (32 KB) into a 3-stage shared-memory ring with 2-D TMA
-//    (cp.async.bulk.tensor), completion tracked by mbarriers.
+//  * Persistent CTAs of 8 warps, 2 per SM.  128x128 bf16 tiles (32 KB)
+//    stream into a 3-stage shared-memory ring with 2-D TMA
+//    (cp.async.bulk.tensor), completion tracked by mbarriers; thread 0
+//    issues each load as soon as all warps have read the stage it refills.
 //  * 8 consumer warps read each staged tile twice from shared memory:
-//    rowwise, a lane owns 8 consecutive values of a row and 4 lanes form a
-//    1x32 block (amax by two xor-shuffles); columnwise, a lane owns two
-//    adjacent columns over 32 rows (amax on packed bf16x2), so the 32x1
-//    blocks come from the same staged tile as the 1x32 ones.
-//  * Row codes go out as 8-byte stores (a warp writes two full 128-byte
+//    rowwise, a lane owns whole 1x32 blocks (four 16-byte chunks, read in a
+//    lane-rotated order that keeps shared-memory phases conflict-free);
+//    columnwise, a lane owns two adjacent columns over 32 rows (amax on
+//    packed bf16x2), so the 32x1 blocks come from the same staged tile as
+//    the 1x32 ones.  All reads of a stage happen before the consumers hand
+//    it back, so the next TMA load overlaps the conversions.
+//  * Row codes go out as 8-byte stores (a warp covers eight full 128-byte
 //    row segments); the columnwise copy is written transposed, 32
 //    contiguous bytes per 32x1 block.
 //  * A 128x128 tile owns exactly one 512-byte tile of the swizzled row
@@ -38,7 +41,7 @@ constexpr int BM = 128;
 constexpr int BK = 128;
 constexpr int STAGES = 3;
 constexpr int CONSUMER_WARPS = 8;
-constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
+constexpr int THREADS = CONSUMER_WARPS * 32;
 constexpr uint32_t TILE_BYTES = BM * BK * 2;
 
 struct alignas(1024) Smem {
@@ -86,25 +89,18 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
 
   // ------------------------------------------------------------------ //
-  // Producer warp: one lane issues the TMA loads.                       //
+  // Prologue: thread 0 fills the ring with the first STAGES tiles.      //
   // ------------------------------------------------------------------ //
-  if (warp == CONSUMER_WARPS) {
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-        if (!mbar_wait(smem_addr(&s.empty[stage]), phase ^ 1, &s.abort,
-                       &g_mxfp8_wait_error))
-          break;
-        const int64_t tm = t / p.tiles_k, tk = t - tm * p.tiles_k;
-        const uint32_t full = smem_addr(&s.full[stage]);
-        mbar_arrive_expect_tx(full, TILE_BYTES);
-        tma_load_2d(smem_addr(s.tile[stage]), &tmap, (int32_t)(tk * BK),
-                    (int32_t)(tm * BM), full);
-        if (++stage == STAGES) { stage = 0; phase ^= 1; }
-      }
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < STAGES; ++st) {
+      const int64_t t = blockIdx.x + (int64_t)st * gridDim.x;
+      if (t >= p.num_tiles) break;
+      const int64_t tm = t / p.tiles_k, tk = t - tm * p.tiles_k;
+      const uint32_t full = smem_addr(&s.full[st]);
+      mbar_arrive_expect_tx(full, TILE_BYTES);
+      tma_load_2d(smem_addr(s.tile[st]), &tmap, (int32_t)(tk * BK),
+                  (int32_t)(tm * BM), full);
     }
-    return;
   }
 
   // ------------------------------------------------------------------ //
@@ -121,47 +117,109 @@ __global__ void __launch_bounds__(THREADS, 2)
                              &g_mxfp8_wait_error);
     const uint16_t* tile = s.tile[stage];
 
+    // Read everything this warp needs from the staged tile first, then hand
+    // the stage back to the producer so the next TMA load overlaps the
+    // conversions below.
+    //   rows: a lane owns whole 1x32 blocks: row w*16 + it*8 + lane/4,
+    //         block lane%4 (it = 0, 1).  Its four 16-byte chunks are read in
+    //         a lane-rotated order (chunk jj = (j + rot) % 4) so that the 8
+    //         lanes of each shared-memory phase hit 8 distinct 16-byte bank
+    //         groups; each chunk's codes are stored back at position jj.
+    //   cols: warp -> 32-row block mb; lane -> columns c, c+1 (packed).
+    const int rblk = lane & 3;
+    const int rot = (rblk >> 1) + 2 * ((lane >> 2) & 1);
+    const int mb = warp >> 1;
+    const int c = (warp & 1) * 64 + lane * 2;
+    uint4 rv[2][4];
+    uint32_t col[32];
     if (ok && p.do_row) {
-      // 16 rows per warp, two rows per step; lane -> (row, 16-byte chunk).
-      const int ch = lane & 15;
-#pragma unroll 2
-      for (int i = 0; i < 8; ++i) {
-        const int r = warp * 16 + i * 2 + (lane >> 4);
-        const uint4 v = *reinterpret_cast<const uint4*>(tile + r * BK + ch * 8);
-        uint32_t m = bf16x2_max(bf16x2_absmax(v.x, v.y), bf16x2_absmax(v.z, v.w));
-        uint32_t a = bf16x2_hmax(m);
-        a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int r = warp * 16 + it * 8 + (lane >> 2);
+        const uint16_t* src = tile + r * BK + rblk * 32;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          rv[it][j] = *reinterpret_cast<const uint4*>(src + ((j + rot) & 3) * 8);
+      }
+    }
+    if (ok && p.do_col) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        col[i] = *reinterpret_cast<const uint32_t*>(tile + (mb * 32 + i) * BK + c);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&s.empty[stage]));
+    // Refill: once all eight warps have read this stage, thread 0 loads the
+    // tile STAGES iterations ahead into it.
+    if (threadIdx.x == 0) {
+      const int64_t next = t + (int64_t)STAGES * gridDim.x;
+      if (next < p.num_tiles &&
+          mbar_wait(smem_addr(&s.empty[stage]), phase, &s.abort,
+                    &g_mxfp8_wait_error)) {
+        const int64_t nm = next / p.tiles_k, nk = next - nm * p.tiles_k;
+        const uint32_t full = smem_addr(&s.full[stage]);
+        mbar_arrive_expect_tx(full, TILE_BYTES);
+        tma_load_2d(smem_addr(s.tile[stage]), &tmap, (int32_t)(nk * BK),
+                    (int32_t)(nm * BM), full);
+      }
+    }
+    __syncwarp();
+
+    if (ok && p.do_row) {
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int r = warp * 16 + it * 8 + (lane >> 2);
+        const uint4* v = rv[it];
+        const uint32_t m =
+            bf16x2_maxabs(
+                bf16x2_maxabs(bf16x2_maxabs(v[0].x, v[0].y),
+                              bf16x2_maxabs(v[0].z, v[0].w)),
+                bf16x2_maxabs(bf16x2_maxabs(v[1].x, v[1].y),
+                              bf16x2_maxabs(v[1].z, v[1].w)));
+        const uint32_t m2 =
+            bf16x2_maxabs(
+                bf16x2_maxabs(bf16x2_maxabs(v[2].x, v[2].y),
+                              bf16x2_maxabs(v[2].z, v[2].w)),
+                bf16x2_maxabs(bf16x2_maxabs(v[3].x, v[3].y),
+                              bf16x2_maxabs(v[3].z, v[3].w)));
+        const uint32_t a = bf16x2_hmax(bf16x2_maxabs(m, m2) & 0x7FFF7FFFu);
         const uint32_t sbyte = e8m0_from_amax_bits(a);
         const float inv = e8m0_inv_scale(sbyte);
-        const uint32_t w0 =
-            cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(v.x), inv),
-                       __fmul_rn(bf16hi_to_f32(v.x), inv)) |
-            (cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(v.y), inv),
-                        __fmul_rn(bf16hi_to_f32(v.y), inv)) << 16);
-        const uint32_t w1 =
-            cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(v.z), inv),
-                       __fmul_rn(bf16hi_to_f32(v.z), inv)) |
-            (cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(v.w), inv),
-                        __fmul_rn(bf16hi_to_f32(v.w), inv)) << 16);
-        if (r < rows_valid && ch * 8 < cols_valid)
-          st_v2(p.row_codes + (m0 + r) * p.K + k0 + ch * 8, w0, w1);
-        if ((lane & 3) == 0)
-          s.rscale[par][stage_pos(r, ch >> 2, p.swizzled)] = (uint8_t)sbyte;
+        const bool store = r < rows_valid && rblk * 32 < cols_valid;
+        uint8_t* dst = p.row_codes + (m0 + r) * p.K + k0 + rblk * 32;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t w0 =
+              cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(v[j].x), inv),
+                         __fmul_rn(bf16hi_to_f32(v[j].x), inv)) |
+              (cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(v[j].y), inv),
+                          __fmul_rn(bf16hi_to_f32(v[j].y), inv)) << 16);
+          const uint32_t w1 =
+              cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(v[j].z), inv),
+                         __fmul_rn(bf16hi_to_f32(v[j].z), inv)) |
+              (cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(v[j].w), inv),
+                          __fmul_rn(bf16hi_to_f32(v[j].w), inv)) << 16);
+          if (store) st_v2(dst + ((j + rot) & 3) * 8, w0, w1);
+        }
+        s.rscale[par][stage_pos(r, rblk, p.swizzled)] = (uint8_t)sbyte;
       }
     }
 
     if (ok && p.do_col) {
-      // Warp -> 32-row block mb; lane -> columns c, c+1.
-      const int mb = warp >> 1;
-      const int c = (warp & 1) * 64 + lane * 2;
-      uint32_t col[32];
+      // amax over the 32 rows as four independent chains.
+      uint32_t m0r = bf16x2_maxabs(col[0], col[1]);
+      uint32_t m1r = bf16x2_maxabs(col[2], col[3]);
+      uint32_t m2r = bf16x2_maxabs(col[4], col[5]);
+      uint32_t m3r = bf16x2_maxabs(col[6], col[7]);
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        col[i] = *reinterpret_cast<const uint32_t*>(tile + (mb * 32 + i) * BK + c);
-      uint32_t m = col[0] & 0x7FFF7FFFu;
-#pragma unroll
-      for (int i = 1; i < 32; ++i) m = bf16x2_absmax(m, col[i]);
+      for (int i = 8; i < 32; i += 8) {
+        m0r = bf16x2_maxabs(m0r, bf16x2_maxabs(col[i], col[i + 1]));
+        m1r = bf16x2_maxabs(m1r, bf16x2_maxabs(col[i + 2], col[i + 3]));
+        m2r = bf16x2_maxabs(m2r, bf16x2_maxabs(col[i + 4], col[i + 5]));
+        m3r = bf16x2_maxabs(m3r, bf16x2_maxabs(col[i + 6], col[i + 7]));
+      }
+      const uint32_t m = bf16x2_maxabs(bf16x2_maxabs(m0r, m1r),
+                                       bf16x2_maxabs(m2r, m3r)) & 0x7FFF7FFFu;
       const uint32_t s_lo = e8m0_from_amax_bits(m & 0xFFFFu);
       const uint32_t s_hi = e8m0_from_amax_bits(m >> 16);
       const float inv_lo = e8m0_inv_scale(s_lo);
@@ -192,9 +250,6 @@ __global__ void __launch_bounds__(THREADS, 2)
       s.cscale[par][stage_pos(c + 1, mb, p.swizzled)] = (uint8_t)s_hi;
     }
 
-    // Release the stage to the producer (all lanes' smem reads are done).
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&s.empty[stage]));
     // All scale bytes of this tile are staged.
     named_barrier_sync(1, CONSUMER_WARPS * 32);
 
