@@ -150,9 +150,10 @@ int64_t mxq_scale_bytes(int64_t rows, int64_t cols, int scale_layout) {
 
 mxq_status mxq_get_last_error(void) {
   cudaError_t e = cudaDeviceSynchronize();
-  unsigned int word = 0;
+  unsigned int word = 0, word2 = 0;
   cudaError_t e2 = mxfp8_take_wait_error(&word);
-  if (e2 == cudaSuccess && word != 0) return MXQ_ERR_TIMEOUT;
+  if (e2 == cudaSuccess) e2 = nvfp4_take_wait_error(&word2);
+  if (e2 == cudaSuccess && (word != 0 || word2 != 0)) return MXQ_ERR_TIMEOUT;
   cudaError_t last = cudaGetLastError();
   if (e != cudaSuccess || e2 != cudaSuccess || last != cudaSuccess)
     return MXQ_ERR_CUDA;
@@ -215,7 +216,7 @@ mxq_status nvfp4_quantize_per_token(const void* x, int64_t T, int64_t H,
 
 size_t nvfp4_quantize_weight_shared_workspace_size(int64_t num_groups) {
   if (num_groups <= 0) return 0;
-  return (size_t)((num_groups * 4 + 255) / 256 * 256);
+  return nvfp4_weight_ws_bytes(num_groups);
 }
 
 mxq_status nvfp4_quantize_weight_shared(

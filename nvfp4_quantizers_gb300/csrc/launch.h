@@ -35,11 +35,18 @@ cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
 
 constexpr int kMaxParts = 4;
 
+// Workspace of the shared-scale weight quantizer: a 256-byte header (grid
+// barrier counter) followed by one 32-bit amax word per group.
+size_t nvfp4_weight_ws_bytes(int64_t num_groups);
+// Reads (and clears when set) the error word of the weight kernel's
+// bounded grid barrier.
+cudaError_t nvfp4_take_wait_error(unsigned int* word);
+
 cudaError_t launch_nvfp4_weight_shared(
     int64_t num_groups, int num_parts, const void* const* parts,
     const int64_t* part_rows, int64_t K, uint8_t* codes, uint8_t* scales,
     float* group_scales, const float* group_scales_in, int swizzled,
-    uint32_t* amax_ws, cudaStream_t stream);
+    uint32_t* ws, cudaStream_t stream);
 
 // dequant.cu
 cudaError_t launch_dequant_mxfp8(const uint8_t* codes, const uint8_t* scales,

@@ -10,9 +10,10 @@
 // amax words.  This entry point keeps that scratch in a fixed array in the
 // library's own device memory instead.
 //
-//  * The scratch is a file-scope device array of kNoAllocMaxGroups 32-bit
-//    words (16 KiB).  Every GPU that loads the library holds it until the
-//    process exits.
+//  * The scratch is a file-scope device array of 64 + kNoAllocMaxGroups
+//    32-bit words (16.25 KiB: a grid-barrier counter and one amax word per
+//    group).  Every GPU that loads the library holds it until the process
+//    exits.
 //  * Host code cannot use the array's name as a device address (on the
 //    host it only stands in for the symbol).  The first call on a device
 //    looks the address up with cudaGetSymbolAddress, with that device
@@ -20,7 +21,7 @@
 //    capture on the device.
 //  * All calls share the one array and it keeps the last call's contents:
 //    the words a call uses are cleared (cudaMemsetAsync on the call's
-//    stream) before its amax kernel runs.  Calls whose kernels overlap on
+//    stream) before its kernel runs.  Calls whose kernels overlap on
 //    the GPU (different streams, no ordering between them) race on the
 //    array; order them on one stream.
 //  * Nothing here calls cudaMalloc, cudaFree or any allocating routine.
@@ -37,7 +38,9 @@ namespace mxq {
 namespace {
 
 constexpr int64_t kNoAllocMaxGroups = 4096;
-static __device__ __align__(256) uint32_t g_noalloc_amax[kNoAllocMaxGroups];
+// 256-byte header (grid barrier counter) + one amax word per group.
+constexpr int64_t kNoAllocWords = 64 + kNoAllocMaxGroups;
+static __device__ __align__(256) uint32_t g_noalloc_amax[kNoAllocWords];
 
 constexpr int kMaxDev = 64;
 std::mutex g_mu;

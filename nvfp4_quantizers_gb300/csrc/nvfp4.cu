@@ -25,11 +25,9 @@
 // word of packed codes per chunk (the warp writes 128 contiguous bytes per
 // step); four block scales are gathered by shuffles into one 32-bit store
 // (four consecutive scale columns are contiguous in both layouts).
-// Weight groups take two kernels: a grid-wide amax of the group (CTA
-// partial maxima combined with an integer atomicMax on the float bits,
-// exact for non-negative values), then the row encoder with the group's S.
-// Groups are processed in chunks sized to a fraction of L2 so that the
-// encoder's second read of a chunk is served from L2, not HBM.
+// Weight groups use one persistent cooperative kernel (see below): an amax
+// phase and an encode phase per L2-sized chunk of groups, separated by a
+// bounded grid barrier, so the second read of a chunk is served from L2.
 #include <float.h>
 
 #include "common.cuh"
@@ -41,7 +39,6 @@ namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int CTA_WARPS = 8;                 // 256 threads per CTA
-constexpr int kMaxGroupsPerLaunch = 64;
 
 struct RowOut {
   uint8_t* codes_row;   // H/2 bytes of this row
@@ -262,8 +259,21 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 }
 
 // ---------------------------------------------------------------------------
-// Weight groups.
+// Weight groups: one persistent cooperative kernel.  For each chunk of
+// groups small enough to stay in L2: phase A reduces every group's amax
+// (64 KiB work units, CTA partial maxima combined with an integer atomicMax
+// on the float bits, exact for non-negative values); a grid-wide barrier;
+// phase B encodes the chunk's rows with their group's S, re-reading the
+// chunk from L2.  A CTA that finishes phase B of one chunk goes straight to
+// phase A of the next.
 // ---------------------------------------------------------------------------
+constexpr int kMaxGroupsPerLaunch = 256;
+constexpr int64_t kAmaxUnitChunks = 4096;     // 16-byte chunks per unit
+constexpr int kWsHeaderWords = 64;            // [0] = barrier counter
+
+// Error word of the bounded grid barrier of this translation unit.
+__device__ unsigned int g_nvfp4_wait_error = 0;
+
 struct GroupTable {
   const uint16_t* part[kMaxGroupsPerLaunch][kMaxParts];
 };
@@ -271,81 +281,136 @@ struct GroupTable {
 struct GroupParams {
   int num_parts;
   int64_t part_row0[kMaxParts + 1];   // prefix sums of the parts' rows
+  int64_t part_chunk0[kMaxParts + 1]; // prefix sums of the parts' 16-byte chunks
   int64_t R, R_pad, K;
   int64_t g0;                         // global index of local group 0
-  int ng;
+  int ng;                             // groups in this launch
+  int chunk;                          // groups per L2-sized chunk
+  int64_t units_per_group;            // phase-A units per group
   uint8_t* codes;                     // group g at g * R * K/2
   uint8_t* scales;                    // group g at g * scale_stride
   int64_t scale_stride;
   float* group_scales;
   const float* S_in;                  // NULL: S from amax
-  const uint32_t* amax;               // f32 bit patterns, global group index
+  uint32_t* ws;                       // [0] barrier, [64 + g] amax of group g
   int swizzled;
 };
 
-__global__ void __launch_bounds__(256)
-    nvfp4_group_amax_kernel(const __grid_constant__ GroupTable tab,
-                            const __grid_constant__ GroupParams p,
-                            uint32_t* __restrict__ amax) {
-  const int gl = blockIdx.y;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  uint32_t a = 0;
-  for (int pi = 0; pi < p.num_parts; ++pi) {
-    const uint16_t* base = tab.part[gl][pi];
-    const int64_t n = (p.part_row0[pi + 1] - p.part_row0[pi]) * p.K / 8;
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + 3 * stride < n; i += 4 * stride) {
-      const uint4 v0 = ld_stream_v4(base + i * 8);
-      const uint4 v1 = ld_stream_v4(base + (i + stride) * 8);
-      const uint4 v2 = ld_stream_v4(base + (i + 2 * stride) * 8);
-      const uint4 v3 = ld_stream_v4(base + (i + 3 * stride) * 8);
-      a = max(a, max(max(chunk_absmax(v0), chunk_absmax(v1)),
-                     max(chunk_absmax(v2), chunk_absmax(v3))));
-    }
-    for (; i < n; i += stride) a = max(a, chunk_absmax(ld_stream_v4(base + i * 8)));
-  }
-  a = warp_max(a);
-  __shared__ uint32_t red[8];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = a;
+// Grid-wide barrier for a cooperative launch: every CTA adds 1 to *ctr and
+// waits (bounded, ~1 s) until it reaches `target`.  On timeout it records 1
+// in g_nvfp4_wait_error, sets *abort and returns false; all threads of the
+// CTA still pass the same __syncthreads calls.
+__device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t target,
+                                             volatile int* abort) {
   __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t m = red[0];
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = max(m, red[w]);
-    // Non-negative float bit patterns order like their values.
-    atomicMax(&amax[p.g0 + gl], m << 16);
+  if (threadIdx.x == 0 && !*abort) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      uint32_t v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
+                   : "=r"(v)
+                   : "l"(ctr)
+                   : "memory");
+      if (v >= target) break;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(&g_nvfp4_wait_error, 1u);
+        *abort = 1;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
   }
+  __syncthreads();
+  return !*abort;
+}
+
+__device__ __forceinline__ const uint16_t* chunk_ptr(const GroupTable& tab,
+                                                     const GroupParams& p,
+                                                     int gl, int64_t q) {
+  int pi = 0;
+  while (pi + 1 < p.num_parts && q >= p.part_chunk0[pi + 1]) ++pi;
+  return tab.part[gl][pi] + (q - p.part_chunk0[pi]) * 8;
 }
 
 template <int R, int WPR>
 __global__ void __launch_bounds__(CTA_WARPS * 32)
-    nvfp4_group_rows_kernel(const __grid_constant__ GroupTable tab,
-                            const __grid_constant__ GroupParams p) {
+    nvfp4_weight_kernel(const __grid_constant__ GroupTable tab,
+                        const __grid_constant__ GroupParams p) {
   constexpr int ROWS = CTA_WARPS / WPR;
   __shared__ uint32_t red[CTA_WARPS];
+  __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slot = warp / WPR, wpart = warp % WPR;
-  const int64_t w = (int64_t)blockIdx.x * ROWS + slot;
-  if (w >= (int64_t)p.ng * p.R_pad) return;       // uniform over the row
-  const int gl = (int)(w / p.R_pad);
-  const int64_t r = w - (int64_t)gl * p.R_pad;
-  const int64_t g = p.g0 + gl;
-  const bool real = r < p.R;
-  const uint16_t* row = nullptr;
-  if (real) {
-    int pi = 0;
-    while (pi + 1 < p.num_parts && r >= p.part_row0[pi + 1]) ++pi;
-    row = tab.part[gl][pi] + (r - p.part_row0[pi]) * p.K;
+  if (threadIdx.x == 0) s_abort = 0;
+  __syncthreads();
+  const int64_t group_chunks = p.part_chunk0[p.num_parts];
+  uint32_t* amax = p.ws + kWsHeaderWords;
+  uint32_t gen = 0;
+  for (int c0 = 0; c0 < p.ng; c0 += p.chunk) {
+    const int nc = (p.ng - c0) < p.chunk ? (p.ng - c0) : p.chunk;
+    if (!p.S_in) {
+      // Phase A: amax of every group of the chunk.
+      const int64_t n_units = (int64_t)nc * p.units_per_group;
+      for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const int gl = c0 + (int)(u / p.units_per_group);
+        const int64_t q0 = (u % p.units_per_group) * kAmaxUnitChunks;
+        uint32_t a = 0;
+#pragma unroll
+        for (int j = 0; j < 16; j += 8) {
+          uint4 v[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int64_t q = q0 + threadIdx.x + (int64_t)(j + jj) * 256;
+            v[jj] = q < group_chunks ? ld_stream_v4(chunk_ptr(tab, p, gl, q))
+                                     : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) a = max(a, chunk_absmax(v[jj]));
+        }
+        a = warp_max(a);
+        if (lane == 0) red[warp] = a;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          uint32_t m = red[0];
+          for (int w = 1; w < CTA_WARPS; ++w) m = max(m, red[w]);
+          if (m) atomicMax(&amax[p.g0 + gl], m << 16);
+        }
+        __syncthreads();
+      }
+      ++gen;
+      grid_barrier(p.ws, gen * gridDim.x, &s_abort);
+    }
+    // Phase B: encode the chunk's rows (and the scale-tile padding rows).
+    const int64_t nrows = (int64_t)nc * p.R_pad;
+    for (int64_t base = (int64_t)blockIdx.x * ROWS; base < nrows;
+         base += (int64_t)gridDim.x * ROWS) {
+      const int64_t w = base + slot;
+      if (w >= nrows || s_abort) continue;             // uniform over the row
+      const int gl = c0 + (int)(w / p.R_pad);
+      const int64_t r = w - (int64_t)(gl - c0) * p.R_pad;
+      const int64_t g = p.g0 + gl;
+      const bool real = r < p.R;
+      const uint16_t* row = nullptr;
+      if (real) {
+        int pi = 0;
+        while (pi + 1 < p.num_parts && r >= p.part_row0[pi + 1]) ++pi;
+        row = tab.part[gl][pi] + (r - p.part_row0[pi]) * p.K;
+      }
+      const float S = p.S_in ? p.S_in[g]
+                             : __fdiv_rn(__uint_as_float(__ldcg(&amax[g])),
+                                         kNvfp4ScaleDenom);
+      if (r == 0 && wpart == 0 && lane == 0) p.group_scales[g] = S;
+      RowOut o{p.codes + (g * p.R + r) * (p.K >> 1),
+               p.scales + g * p.scale_stride, r, ((p.K >> 4) + 3) >> 2,
+               p.K >> 4, p.swizzled};
+      float S_used;
+      encode_row_warps<R, WPR>(row, real, S, true, o, slot, wpart, lane, red,
+                               &S_used);
+    }
   }
-  const float S = p.S_in ? p.S_in[g]
-                         : __fdiv_rn(__uint_as_float(p.amax[g]),
-                                     kNvfp4ScaleDenom);
-  if (r == 0 && wpart == 0 && lane == 0) p.group_scales[g] = S;
-  RowOut o{p.codes + (g * p.R + r) * (p.K >> 1), p.scales + g * p.scale_stride,
-           r, ((p.K >> 4) + 3) >> 2, p.K >> 4, p.swizzled};
-  float S_used;
-  encode_row_warps<R, WPR>(row, real, S, true, o, slot, wpart, lane, red,
-                           &S_used);
 }
 
 // Launch shape of the row encoders: R blocks per lane (R * 512 values per
@@ -393,49 +458,88 @@ cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
   return cudaGetLastError();
 }
 
+size_t nvfp4_weight_ws_bytes(int64_t num_groups) {
+  return (size_t)(((kWsHeaderWords + num_groups) * 4 + 255) / 256 * 256);
+}
+
+cudaError_t nvfp4_take_wait_error(unsigned int* word) {
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_nvfp4_wait_error, sizeof(*word));
+  if (e != cudaSuccess || *word == 0) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_nvfp4_wait_error, &zero, sizeof(zero));
+}
+
+namespace {
+
+template <int R, int WPR>
+cudaError_t launch_weight_coop(const GroupTable& tab, const GroupParams& p,
+                               int dev, cudaStream_t stream) {
+  static int occ[64] = {};
+  int n = (dev >= 0 && dev < 64) ? occ[dev] : 0;
+  if (n == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &n, nvfp4_weight_kernel<R, WPR>, CTA_WARPS * 32, 0);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    if (dev >= 0 && dev < 64) occ[dev] = n;
+  }
+  const unsigned grid = (unsigned)(n * sm_count(dev));
+  void* args[] = {const_cast<GroupTable*>(&tab), const_cast<GroupParams*>(&p)};
+  return cudaLaunchCooperativeKernel((const void*)nvfp4_weight_kernel<R, WPR>,
+                                     dim3(grid), dim3(CTA_WARPS * 32), args, 0,
+                                     stream);
+}
+
+}  // namespace
+
 cudaError_t launch_nvfp4_weight_shared(
     int64_t num_groups, int num_parts, const void* const* parts,
     const int64_t* part_rows, int64_t K, uint8_t* codes, uint8_t* scales,
     float* group_scales, const float* group_scales_in, int swizzled,
-    uint32_t* amax_ws, cudaStream_t stream) {
+    uint32_t* ws, cudaStream_t stream) {
+  const RowShape sh = pick_shape(K);
+  if (sh.R == 0) return cudaErrorInvalidValue;   // K > 16384: not supported
   GroupParams p;
   p.num_parts = num_parts;
   p.part_row0[0] = 0;
-  for (int i = 0; i < num_parts; ++i)
+  p.part_chunk0[0] = 0;
+  for (int i = 0; i < num_parts; ++i) {
     p.part_row0[i + 1] = p.part_row0[i] + part_rows[i];
-  for (int i = num_parts + 1; i <= kMaxParts; ++i)
+    p.part_chunk0[i + 1] = p.part_chunk0[i] + part_rows[i] * K / 8;
+  }
+  for (int i = num_parts + 1; i <= kMaxParts; ++i) {
     p.part_row0[i] = p.part_row0[num_parts];
+    p.part_chunk0[i] = p.part_chunk0[num_parts];
+  }
   p.R = p.part_row0[num_parts];
   p.R_pad = swizzled ? (p.R + 127) / 128 * 128 : p.R;
   p.K = K;
+  p.units_per_group =
+      (p.part_chunk0[num_parts] + kAmaxUnitChunks - 1) / kAmaxUnitChunks;
   p.codes = codes;
   p.scales = scales;
   p.scale_stride = scale_bytes(p.R, K / 16, swizzled);
   p.group_scales = group_scales;
   p.S_in = group_scales_in;
-  p.amax = amax_ws;
+  p.ws = ws;
   p.swizzled = swizzled;
 
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  // Groups per launch: the chunk read by the amax kernel should still be in
-  // L2 when the encoder reads it again.
+  // Groups per L2 chunk: what phase A reads should still be in L2 when
+  // phase B reads it again.
   const int64_t group_bytes = p.R * K * 2;
   int64_t chunk = kMaxGroupsPerLaunch;
   if (!group_scales_in && group_bytes > 0) {
     chunk = (int64_t)(0.4 * (double)l2_bytes(dev)) / group_bytes;
-    chunk = chunk < 1 ? 1 : (chunk > kMaxGroupsPerLaunch ? kMaxGroupsPerLaunch : chunk);
+    chunk = chunk < 1 ? 1 : chunk;
   }
-  const int64_t group_chunks = group_bytes / 16;
-  int64_t ctas_per_group = (group_chunks + 256 * 16 - 1) / (256 * 16);
-  ctas_per_group = ctas_per_group < 1 ? 1 : (ctas_per_group > 65535 ? 65535 : ctas_per_group);
-
-  const RowShape sh = pick_shape(K);
-  if (sh.R == 0) return cudaErrorInvalidValue;   // K > 16384: not supported
   GroupTable tab;
-  for (int64_t g0 = 0; g0 < num_groups; g0 += chunk) {
-    const int ng = (int)((num_groups - g0) < chunk ? (num_groups - g0) : chunk);
+  for (int64_t g0 = 0; g0 < num_groups; g0 += kMaxGroupsPerLaunch) {
+    const int ng = (int)((num_groups - g0) < kMaxGroupsPerLaunch
+                             ? (num_groups - g0)
+                             : kMaxGroupsPerLaunch);
     for (int gl = 0; gl < kMaxGroupsPerLaunch; ++gl)
       for (int pi = 0; pi < kMaxParts; ++pi)
         tab.part[gl][pi] =
@@ -444,27 +548,21 @@ cudaError_t launch_nvfp4_weight_shared(
                 : nullptr;
     p.g0 = g0;
     p.ng = ng;
+    p.chunk = (int)(chunk < ng ? chunk : ng);
     if (!group_scales_in) {
-      err = cudaMemsetAsync(amax_ws + g0, 0, (size_t)ng * 4, stream);
-      if (err != cudaSuccess) return err;
-      nvfp4_group_amax_kernel<<<dim3((unsigned)ctas_per_group, (unsigned)ng),
-                                256, 0, stream>>>(tab, p, amax_ws);
-      err = cudaGetLastError();
+      // Zero the barrier counter and this launch's amax words.
+      err = cudaMemsetAsync(ws, 0, kWsHeaderWords * 4, stream);
+      if (err == cudaSuccess)
+        err = cudaMemsetAsync(ws + kWsHeaderWords + g0, 0, (size_t)ng * 4,
+                              stream);
       if (err != cudaSuccess) return err;
     }
-    const int64_t rows = (int64_t)ng * p.R_pad;
-    const int rows_per_cta = CTA_WARPS / sh.WPR;
-    const unsigned grid = (unsigned)((rows + rows_per_cta - 1) / rows_per_cta);
-#define MXQ_GROUP_LAUNCH(R_, W_) \
-  nvfp4_group_rows_kernel<R_, W_><<<grid, CTA_WARPS * 32, 0, stream>>>(tab, p)
-    if (sh.R == 1) MXQ_GROUP_LAUNCH(1, 1);
-    else if (sh.R == 2) MXQ_GROUP_LAUNCH(2, 1);
-    else if (sh.WPR == 1) MXQ_GROUP_LAUNCH(4, 1);
-    else if (sh.WPR == 2) MXQ_GROUP_LAUNCH(4, 2);
-    else if (sh.WPR == 4) MXQ_GROUP_LAUNCH(4, 4);
-    else MXQ_GROUP_LAUNCH(4, 8);
-#undef MXQ_GROUP_LAUNCH
-    err = cudaGetLastError();
+    if (sh.R == 1) err = launch_weight_coop<1, 1>(tab, p, dev, stream);
+    else if (sh.R == 2) err = launch_weight_coop<2, 1>(tab, p, dev, stream);
+    else if (sh.WPR == 1) err = launch_weight_coop<4, 1>(tab, p, dev, stream);
+    else if (sh.WPR == 2) err = launch_weight_coop<4, 2>(tab, p, dev, stream);
+    else if (sh.WPR == 4) err = launch_weight_coop<4, 4>(tab, p, dev, stream);
+    else err = launch_weight_coop<4, 8>(tab, p, dev, stream);
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;
