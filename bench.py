@@ -244,13 +244,9 @@ def run_gpu(args):
             "dq weights")
         mark(7)
 
-    # Our kernels per step: rowcol 1, dequant 2+1+1, per-token 1, weights
-    # (amax + encoder) per L2-sized chunk of groups.
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    group_bytes = 2 * PART_ROWS * K * 2
-    chunk = max(1, min(64, int(0.4 * l2) // group_bytes))
-    n_chunks = -(-PAIRS // chunk)
-    launches_per_step = 1 + 2 + 1 + 1 + 2 * n_chunks + 1
+    # Our kernels per step: rowcol 1, dequant 2 + 1 + 1, per-token 1,
+    # weights 1 (one cooperative kernel per call of up to 256 groups).
+    launches_per_step = 1 + 2 + 1 + 1 + 1 + 1
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):

@@ -122,6 +122,26 @@ __device__ __forceinline__ void e2m1x2_to_f32(uint32_t byte, float& a,
   f16x2_to_f32(h2, a, b);
 }
 
+// Two IEEE binary32 multiplies (round to nearest even, no flush to zero)
+// in one packed f32x2 instruction: r0 = a0 * b0, r1 = a1 * b1.
+__device__ __forceinline__ void fmul2(float a0, float a1, float b0, float b1,
+                                      float& r0, float& r1) {
+  asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\t"
+      "mov.b64 pb, {%4, %5};\n\tmul.rn.f32x2 pd, pa, pb;\n\t"
+      "mov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// A packed bf16 pair scaled by (s_lo, s_hi) and rounded to two E4M3 codes
+// (low half -> low byte).
+__device__ __forceinline__ uint32_t bf16x2_scale_e4m3x2(uint32_t w, float s_lo,
+                                                        float s_hi) {
+  float a, b;
+  fmul2(bf16lo_to_f32(w), bf16hi_to_f32(w), s_lo, s_hi, a, b);
+  return cvt_e4m3x2(a, b);
+}
+
 // Two f32 -> packed bf16x2 (round to nearest even); `lo` in the low half.
 __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
   uint32_t r;

@@ -51,7 +51,8 @@ __global__ void __launch_bounds__(DQ_THREADS)
     for (int h = 0; h < 8; ++h) {
       float a, bb;
       e4m3x2_to_f32((cw[h >> 1] >> ((h & 1) * 16)) & 0xFFFFu, a, bb);
-      w[h] = f32x2_to_bf16x2(__fmul_rn(a, sc), __fmul_rn(bb, sc));
+      fmul2(a, bb, sc, sc, a, bb);
+      w[h] = f32x2_to_bf16x2(a, bb);
     }
     uint16_t* dst = y + (int64_t)i * 16;
     st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
@@ -98,8 +99,9 @@ __global__ void __launch_bounds__(DQ_THREADS)
     for (int h = 0; h < 8; ++h) {
       float a, bb;
       e2m1x2_to_f32((h < 4 ? c.x : c.y) >> (8 * (h & 3)), a, bb);
-      w[h] = f32x2_to_bf16x2(__fmul_rn(__fmul_rn(a, bs), s32),
-                             __fmul_rn(__fmul_rn(bb, bs), s32));
+      fmul2(a, bb, bs, bs, a, bb);      // exact: at most 6 significant bits
+      fmul2(a, bb, s32, s32, a, bb);
+      w[h] = f32x2_to_bf16x2(a, bb);
     }
     uint16_t* dst = y + (int64_t)i * 16;
     st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));

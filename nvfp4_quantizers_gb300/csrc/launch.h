@@ -16,7 +16,7 @@ int64_t l2_bytes(int device);
 cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base,
                               uint64_t inner, uint64_t outer,
                               uint64_t outer_stride_bytes, uint32_t box_inner,
-                              uint32_t box_outer);
+                              uint32_t box_outer, bool swizzle128);
 
 // mxfp8.cu
 // Reads (and clears when set) the error word of the bounded device waits.

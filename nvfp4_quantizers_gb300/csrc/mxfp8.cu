@@ -12,16 +12,17 @@
 //    stream into a 3-stage shared-memory ring with 2-D TMA
 //    (cp.async.bulk.tensor), completion tracked by mbarriers; thread 0
 //    issues each load as soon as all warps have read the stage it refills.
-//  * 8 consumer warps read each staged tile twice from shared memory:
-//    rowwise, a lane owns whole 1x32 blocks (four 16-byte chunks, read in a
-//    lane-rotated order that keeps shared-memory phases conflict-free);
-//    columnwise, a lane owns two adjacent columns over 32 rows (amax on
-//    packed bf16x2), so the 32x1 blocks come from the same staged tile as
-//    the 1x32 ones.  All reads of a stage happen before the consumers hand
-//    it back, so the next TMA load overlaps the conversions.
-//  * Row codes go out as 8-byte stores (a warp covers eight full 128-byte
-//    row segments); the columnwise copy is written transposed, 32
-//    contiguous bytes per 32x1 block.
+//  * Each tile arrives as two [128 x 64] halves with the 128-byte TMA
+//    swizzle (16-byte chunk q of row r stored at chunk q ^ (r % 8)), which
+//    makes both read patterns below free of shared-memory bank conflicts.
+//  * 8 warps read each staged tile twice: rowwise, a lane owns whole 1x32
+//    blocks; columnwise, a lane owns two adjacent columns over 32 rows
+//    (amax on packed bf16x2), so the 32x1 blocks come from the same staged
+//    tile as the 1x32 ones.  All reads of a stage happen before the warps
+//    hand it back, so the next TMA load overlaps the conversions.
+//  * Scaling uses packed f32x2 multiplies (exact: the scale is a power of
+//    two); row codes go out as two 16-byte stores per block; the columnwise
+//    copy is written transposed, 32 contiguous bytes per 32x1 block.
 //  * A 128x128 tile owns exactly one 512-byte tile of the swizzled row
 //    scales and one of the swizzled column scales; both are assembled in
 //    shared memory and written out as one coalesced 512-byte store each
@@ -42,6 +43,7 @@ constexpr int BK = 128;
 constexpr int STAGES = 3;
 constexpr int CONSUMER_WARPS = 8;
 constexpr int THREADS = CONSUMER_WARPS * 32;
+constexpr int HALF_COLS = 64;                 // one 128-byte swizzled TMA box
 constexpr uint32_t TILE_BYTES = BM * BK * 2;
 
 struct alignas(1024) Smem {
@@ -60,8 +62,16 @@ struct Params {
   uint8_t* col_codes;
   uint8_t* col_scales;
   int do_row, do_col, swizzled;
-  int64_t tiles_m, tiles_k, num_tiles;
+  uint32_t tiles_m, tiles_k, num_tiles;
 };
+
+// Element offset of (r, c) in a staged tile: two [128 x 64] halves of
+// 128-byte rows loaded with the 128-byte TMA swizzle, which stores 16-byte
+// chunk q of row r at chunk position q ^ (r % 8).
+__device__ __forceinline__ int tile_off(int r, int c) {
+  return (c >> 6) * (BM * HALF_COLS) + r * HALF_COLS +
+         ((((c & 63) >> 3) ^ (r & 7)) << 3) + (c & 7);
+}
 
 // Position of logical scale (r, c), r < 128, c < 4, inside the staged
 // 512-byte scale tile.
@@ -93,13 +103,15 @@ __global__ void __launch_bounds__(THREADS, 2)
   // ------------------------------------------------------------------ //
   if (threadIdx.x == 0) {
     for (int st = 0; st < STAGES; ++st) {
-      const int64_t t = blockIdx.x + (int64_t)st * gridDim.x;
+      const uint32_t t = blockIdx.x + (uint32_t)st * gridDim.x;
       if (t >= p.num_tiles) break;
-      const int64_t tm = t / p.tiles_k, tk = t - tm * p.tiles_k;
+      const uint32_t tm = t / p.tiles_k, tk = t - tm * p.tiles_k;
       const uint32_t full = smem_addr(&s.full[st]);
       mbar_arrive_expect_tx(full, TILE_BYTES);
       tma_load_2d(smem_addr(s.tile[st]), &tmap, (int32_t)(tk * BK),
                   (int32_t)(tm * BM), full);
+      tma_load_2d(smem_addr(s.tile[st] + BM * HALF_COLS), &tmap,
+                  (int32_t)(tk * BK + HALF_COLS), (int32_t)(tm * BM), full);
     }
   }
 
@@ -108,9 +120,9 @@ __global__ void __launch_bounds__(THREADS, 2)
   // ------------------------------------------------------------------ //
   int stage = 0, par = 0;
   uint32_t phase = 0;
-  for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-    const int64_t tm = t / p.tiles_k, tk = t - tm * p.tiles_k;
-    const int64_t m0 = tm * BM, k0 = tk * BK;
+  for (uint32_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    const uint32_t tm = t / p.tiles_k, tk = t - tm * p.tiles_k;
+    const int64_t m0 = (int64_t)tm * BM, k0 = (int64_t)tk * BK;
     const int rows_valid = (int)imin<int64_t>(BM, p.M - m0);
     const int cols_valid = (int)imin<int64_t>(BK, p.K - k0);
     const bool ok = mbar_wait(smem_addr(&s.full[stage]), phase, &s.abort,
@@ -118,16 +130,15 @@ __global__ void __launch_bounds__(THREADS, 2)
     const uint16_t* tile = s.tile[stage];
 
     // Read everything this warp needs from the staged tile first, then hand
-    // the stage back to the producer so the next TMA load overlaps the
-    // conversions below.
-    //   rows: a lane owns whole 1x32 blocks: row w*16 + it*8 + lane/4,
-    //         block lane%4 (it = 0, 1).  Its four 16-byte chunks are read in
-    //         a lane-rotated order (chunk jj = (j + rot) % 4) so that the 8
-    //         lanes of each shared-memory phase hit 8 distinct 16-byte bank
-    //         groups; each chunk's codes are stored back at position jj.
-    //   cols: warp -> 32-row block mb; lane -> columns c, c+1 (packed).
-    const int rblk = lane & 3;
-    const int rot = (rblk >> 1) + 2 * ((lane >> 2) & 1);
+    // the stage back so the next TMA load overlaps the conversions below.
+    //   rows: warp w owns rows 16w..16w+15; lane -> rows 16w + lane%8 and
+    //         16w + 8 + lane%8, 1x32 block lane/8.  The 8 lanes of a
+    //         shared-memory phase read 8 consecutive rows of one block,
+    //         which the 128-byte swizzle places in 8 different bank groups.
+    //   cols: warp -> 32-row block mb; lane -> columns c, c+1 (packed); a
+    //         warp reads one 128-byte swizzled row per step.
+    const int rlane = lane & 7;
+    const int rblk = lane >> 3;
     const int mb = warp >> 1;
     const int c = (warp & 1) * 64 + lane * 2;
     uint4 rv[2][4];
@@ -135,32 +146,33 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (ok && p.do_row) {
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
-        const int r = warp * 16 + it * 8 + (lane >> 2);
-        const uint16_t* src = tile + r * BK + rblk * 32;
+        const int r = warp * 16 + it * 8 + rlane;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          rv[it][j] = *reinterpret_cast<const uint4*>(src + ((j + rot) & 3) * 8);
+          rv[it][j] = *reinterpret_cast<const uint4*>(tile + tile_off(r, rblk * 32 + j * 8));
       }
     }
     if (ok && p.do_col) {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        col[i] = *reinterpret_cast<const uint32_t*>(tile + (mb * 32 + i) * BK + c);
+        col[i] = *reinterpret_cast<const uint32_t*>(tile + tile_off(mb * 32 + i, c));
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&s.empty[stage]));
     // Refill: once all eight warps have read this stage, thread 0 loads the
     // tile STAGES iterations ahead into it.
     if (threadIdx.x == 0) {
-      const int64_t next = t + (int64_t)STAGES * gridDim.x;
+      const uint32_t next = t + (uint32_t)STAGES * gridDim.x;
       if (next < p.num_tiles &&
           mbar_wait(smem_addr(&s.empty[stage]), phase, &s.abort,
                     &g_mxfp8_wait_error)) {
-        const int64_t nm = next / p.tiles_k, nk = next - nm * p.tiles_k;
+        const uint32_t nm = next / p.tiles_k, nk = next - nm * p.tiles_k;
         const uint32_t full = smem_addr(&s.full[stage]);
         mbar_arrive_expect_tx(full, TILE_BYTES);
         tma_load_2d(smem_addr(s.tile[stage]), &tmap, (int32_t)(nk * BK),
                     (int32_t)(nm * BM), full);
+        tma_load_2d(smem_addr(s.tile[stage] + BM * HALF_COLS), &tmap,
+                    (int32_t)(nk * BK + HALF_COLS), (int32_t)(nm * BM), full);
       }
     }
     __syncwarp();
@@ -168,7 +180,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (ok && p.do_row) {
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
-        const int r = warp * 16 + it * 8 + (lane >> 2);
+        const int r = warp * 16 + it * 8 + rlane;
         const uint4* v = rv[it];
         const uint32_t m =
             bf16x2_maxabs(
@@ -185,21 +197,18 @@ __global__ void __launch_bounds__(THREADS, 2)
         const uint32_t a = bf16x2_hmax(bf16x2_maxabs(m, m2) & 0x7FFF7FFFu);
         const uint32_t sbyte = e8m0_from_amax_bits(a);
         const float inv = e8m0_inv_scale(sbyte);
-        const bool store = r < rows_valid && rblk * 32 < cols_valid;
-        uint8_t* dst = p.row_codes + (m0 + r) * p.K + k0 + rblk * 32;
+        uint32_t w[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t w0 =
-              cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(v[j].x), inv),
-                         __fmul_rn(bf16hi_to_f32(v[j].x), inv)) |
-              (cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(v[j].y), inv),
-                          __fmul_rn(bf16hi_to_f32(v[j].y), inv)) << 16);
-          const uint32_t w1 =
-              cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(v[j].z), inv),
-                         __fmul_rn(bf16hi_to_f32(v[j].z), inv)) |
-              (cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(v[j].w), inv),
-                          __fmul_rn(bf16hi_to_f32(v[j].w), inv)) << 16);
-          if (store) st_v2(dst + ((j + rot) & 3) * 8, w0, w1);
+          w[2 * j] = bf16x2_scale_e4m3x2(v[j].x, inv, inv) |
+                     (bf16x2_scale_e4m3x2(v[j].y, inv, inv) << 16);
+          w[2 * j + 1] = bf16x2_scale_e4m3x2(v[j].z, inv, inv) |
+                         (bf16x2_scale_e4m3x2(v[j].w, inv, inv) << 16);
+        }
+        if (r < rows_valid && rblk * 32 < cols_valid) {
+          uint8_t* dst = p.row_codes + (m0 + r) * p.K + k0 + rblk * 32;
+          st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
+          st_v4(dst + 16, make_uint4(w[4], w[5], w[6], w[7]));
         }
         s.rscale[par][stage_pos(r, rblk, p.swizzled)] = (uint8_t)sbyte;
       }
@@ -227,16 +236,17 @@ __global__ void __launch_bounds__(THREADS, 2)
       uint32_t q_lo[8], q_hi[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const uint32_t a0 = col[4 * j], a1 = col[4 * j + 1];
-        const uint32_t a2 = col[4 * j + 2], a3 = col[4 * j + 3];
-        q_lo[j] = cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(a0), inv_lo),
-                             __fmul_rn(bf16lo_to_f32(a1), inv_lo)) |
-                  (cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(a2), inv_lo),
-                              __fmul_rn(bf16lo_to_f32(a3), inv_lo)) << 16);
-        q_hi[j] = cvt_e4m3x2(__fmul_rn(bf16hi_to_f32(a0), inv_hi),
-                             __fmul_rn(bf16hi_to_f32(a1), inv_hi)) |
-                  (cvt_e4m3x2(__fmul_rn(bf16hi_to_f32(a2), inv_hi),
-                              __fmul_rn(bf16hi_to_f32(a3), inv_hi)) << 16);
+        float l0, l1, l2, l3, h0, h1, h2, h3;
+        fmul2(bf16lo_to_f32(col[4 * j]), bf16lo_to_f32(col[4 * j + 1]), inv_lo,
+              inv_lo, l0, l1);
+        fmul2(bf16lo_to_f32(col[4 * j + 2]), bf16lo_to_f32(col[4 * j + 3]),
+              inv_lo, inv_lo, l2, l3);
+        fmul2(bf16hi_to_f32(col[4 * j]), bf16hi_to_f32(col[4 * j + 1]), inv_hi,
+              inv_hi, h0, h1);
+        fmul2(bf16hi_to_f32(col[4 * j + 2]), bf16hi_to_f32(col[4 * j + 3]),
+              inv_hi, inv_hi, h2, h3);
+        q_lo[j] = cvt_e4m3x2(l0, l1) | (cvt_e4m3x2(l2, l3) << 16);
+        q_hi[j] = cvt_e4m3x2(h0, h1) | (cvt_e4m3x2(h2, h3) << 16);
       }
       if (mb * 32 < rows_valid && c < cols_valid) {
         uint8_t* dst = p.col_codes + (k0 + c) * p.M + m0 + mb * 32;
@@ -300,7 +310,7 @@ cudaError_t launch_mxfp8_rowcol(const void* x, int64_t M, int64_t K,
                                 cudaStream_t stream) {
   CUtensorMap tmap;
   cudaError_t err = make_tmap_2d_bf16(&tmap, x, (uint64_t)K, (uint64_t)M,
-                                      (uint64_t)ldx * 2, BK, BM);
+                                      (uint64_t)ldx * 2, HALF_COLS, BM, true);
   if (err != cudaSuccess) return err;
   Params p;
   p.M = M;
@@ -312,8 +322,8 @@ cudaError_t launch_mxfp8_rowcol(const void* x, int64_t M, int64_t K,
   p.do_row = row_codes != nullptr;
   p.do_col = col_codes != nullptr;
   p.swizzled = swizzled;
-  p.tiles_m = (M + BM - 1) / BM;
-  p.tiles_k = (K + BK - 1) / BK;
+  p.tiles_m = (uint32_t)((M + BM - 1) / BM);
+  p.tiles_k = (uint32_t)((K + BK - 1) / BK);
   p.num_tiles = p.tiles_m * p.tiles_k;
 
   const size_t smem = mxfp8_rowcol_smem_bytes();
@@ -328,7 +338,7 @@ cudaError_t launch_mxfp8_rowcol(const void* x, int64_t M, int64_t K,
     if (err != cudaSuccess) return err;
     configured_dev = dev;
   }
-  const int64_t grid = imin<int64_t>(p.num_tiles, (int64_t)sm_count(dev) * 2);
+  const int64_t grid = imin<int64_t>((int64_t)p.num_tiles, (int64_t)sm_count(dev) * 2);
   mxfp8_rowcol_kernel<<<(unsigned)grid, THREADS, smem, stream>>>(tmap, p);
   return cudaGetLastError();
 }

@@ -101,23 +101,15 @@ __device__ __forceinline__ void encode_block(const Blk& v, uint32_t a, float S,
   float enc = 0.0f;
   if (d != 0.0f) enc = fminf(__frcp_rn(d), FLT_MAX);
   float q[8];
-  q[0] = __fmul_rn(bf16lo_to_f32(v.a.x), enc);
-  q[1] = __fmul_rn(bf16hi_to_f32(v.a.x), enc);
-  q[2] = __fmul_rn(bf16lo_to_f32(v.a.y), enc);
-  q[3] = __fmul_rn(bf16hi_to_f32(v.a.y), enc);
-  q[4] = __fmul_rn(bf16lo_to_f32(v.a.z), enc);
-  q[5] = __fmul_rn(bf16hi_to_f32(v.a.z), enc);
-  q[6] = __fmul_rn(bf16lo_to_f32(v.a.w), enc);
-  q[7] = __fmul_rn(bf16hi_to_f32(v.a.w), enc);
+  fmul2(bf16lo_to_f32(v.a.x), bf16hi_to_f32(v.a.x), enc, enc, q[0], q[1]);
+  fmul2(bf16lo_to_f32(v.a.y), bf16hi_to_f32(v.a.y), enc, enc, q[2], q[3]);
+  fmul2(bf16lo_to_f32(v.a.z), bf16hi_to_f32(v.a.z), enc, enc, q[4], q[5]);
+  fmul2(bf16lo_to_f32(v.a.w), bf16hi_to_f32(v.a.w), enc, enc, q[6], q[7]);
   lo = cvt_e2m1x8(q);
-  q[0] = __fmul_rn(bf16lo_to_f32(v.b.x), enc);
-  q[1] = __fmul_rn(bf16hi_to_f32(v.b.x), enc);
-  q[2] = __fmul_rn(bf16lo_to_f32(v.b.y), enc);
-  q[3] = __fmul_rn(bf16hi_to_f32(v.b.y), enc);
-  q[4] = __fmul_rn(bf16lo_to_f32(v.b.z), enc);
-  q[5] = __fmul_rn(bf16hi_to_f32(v.b.z), enc);
-  q[6] = __fmul_rn(bf16lo_to_f32(v.b.w), enc);
-  q[7] = __fmul_rn(bf16hi_to_f32(v.b.w), enc);
+  fmul2(bf16lo_to_f32(v.b.x), bf16hi_to_f32(v.b.x), enc, enc, q[0], q[1]);
+  fmul2(bf16lo_to_f32(v.b.y), bf16hi_to_f32(v.b.y), enc, enc, q[2], q[3]);
+  fmul2(bf16lo_to_f32(v.b.z), bf16hi_to_f32(v.b.z), enc, enc, q[4], q[5]);
+  fmul2(bf16lo_to_f32(v.b.w), bf16hi_to_f32(v.b.w), enc, enc, q[6], q[7]);
   hi = cvt_e2m1x8(q);
 }
 
@@ -268,7 +260,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 // phase A of the next.
 // ---------------------------------------------------------------------------
 constexpr int kMaxGroupsPerLaunch = 256;
-constexpr int64_t kAmaxUnitChunks = 4096;     // 16-byte chunks per unit
+constexpr int64_t kAmaxUnitChunks = 1024;     // 16-byte chunks per unit (16 KiB)
 constexpr int kWsHeaderWords = 64;            // [0] = barrier counter
 
 // Error word of the bounded grid barrier of this translation unit.
@@ -352,31 +344,60 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
   for (int c0 = 0; c0 < p.ng; c0 += p.chunk) {
     const int nc = (p.ng - c0) < p.chunk ? (p.ng - c0) : p.chunk;
     if (!p.S_in) {
-      // Phase A: amax of every group of the chunk.
+      // Phase A: amax of every group of the chunk.  Each CTA takes a
+      // contiguous range of 16 KiB units (so it spans at most a few groups),
+      // keeps a running max in registers and combines it across the CTA
+      // only when the group changes and at the end of its range.
       const int64_t n_units = (int64_t)nc * p.units_per_group;
-      for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const int gl = c0 + (int)(u / p.units_per_group);
-        const int64_t q0 = (u % p.units_per_group) * kAmaxUnitChunks;
-        uint32_t a = 0;
+      const int64_t u_begin = n_units * blockIdx.x / gridDim.x;
+      const int64_t u_end = n_units * (blockIdx.x + 1) / gridDim.x;
+      int cur = -1;
+      uint32_t a = 0;
+      for (int64_t u = u_begin; u < u_end; u += 2) {
+        const int gl0 = c0 + (int)(u / p.units_per_group);
+        const int gl1 = (u + 1 < u_end) ? c0 + (int)((u + 1) / p.units_per_group) : -1;
+        uint4 v[8];
 #pragma unroll
-        for (int j = 0; j < 16; j += 8) {
-          uint4 v[8];
+        for (int jj = 0; jj < 8; ++jj) {
+          const int64_t uu = u + (jj >> 2);
+          const int gl = (jj >> 2) ? gl1 : gl0;
+          const int64_t q = (uu % p.units_per_group) * kAmaxUnitChunks +
+                            threadIdx.x + (int64_t)(jj & 3) * 256;
+          v[jj] = (gl >= 0 && q < group_chunks)
+                      ? ld_stream_v4(chunk_ptr(tab, p, gl, q))
+                      : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int64_t q = q0 + threadIdx.x + (int64_t)(j + jj) * 256;
-            v[jj] = q < group_chunks ? ld_stream_v4(chunk_ptr(tab, p, gl, q))
-                                     : make_uint4(0, 0, 0, 0);
+        for (int half = 0; half < 2; ++half) {
+          const int gl = half ? gl1 : gl0;
+          if (gl < 0) break;                               // CTA-uniform
+          if (gl != cur) {                                 // CTA-uniform
+            if (cur >= 0) {
+              const uint32_t m = warp_max(a);
+              if (lane == 0) red[warp] = m;
+              __syncthreads();
+              if (threadIdx.x == 0) {
+                uint32_t mm = red[0];
+                for (int w = 1; w < CTA_WARPS; ++w) mm = max(mm, red[w]);
+                if (mm) atomicMax(&amax[p.g0 + cur], mm << 16);
+              }
+              __syncthreads();
+            }
+            cur = gl;
+            a = 0;
           }
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) a = max(a, chunk_absmax(v[jj]));
+          for (int jj = 0; jj < 4; ++jj) a = max(a, chunk_absmax(v[half * 4 + jj]));
         }
-        a = warp_max(a);
-        if (lane == 0) red[warp] = a;
+      }
+      if (cur >= 0) {                                      // CTA-uniform
+        const uint32_t m = warp_max(a);
+        if (lane == 0) red[warp] = m;
         __syncthreads();
         if (threadIdx.x == 0) {
-          uint32_t m = red[0];
-          for (int w = 1; w < CTA_WARPS; ++w) m = max(m, red[w]);
-          if (m) atomicMax(&amax[p.g0 + gl], m << 16);
+          uint32_t mm = red[0];
+          for (int w = 1; w < CTA_WARPS; ++w) mm = max(mm, red[w]);
+          if (mm) atomicMax(&amax[p.g0 + cur], mm << 16);
         }
         __syncthreads();
       }
@@ -532,7 +553,7 @@ cudaError_t launch_nvfp4_weight_shared(
   const int64_t group_bytes = p.R * K * 2;
   int64_t chunk = kMaxGroupsPerLaunch;
   if (!group_scales_in && group_bytes > 0) {
-    chunk = (int64_t)(0.4 * (double)l2_bytes(dev)) / group_bytes;
+    chunk = (int64_t)(0.55 * (double)l2_bytes(dev)) / group_bytes;
     chunk = chunk < 1 ? 1 : chunk;
   }
   GroupTable tab;
