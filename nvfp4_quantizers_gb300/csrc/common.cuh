@@ -299,6 +299,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Programmatic dependent launch.  Every kernel calls pdl_wait() before its
+// first global-memory access: it returns once the previous kernel on the
+// stream has completed and its writes are visible (and at once when the
+// kernel was launched without the programmatic-serialization attribute).
+// pdl_launch_dependents() lets the next kernel's CTAs be scheduled while
+// this grid drains; they still wait in their own pdl_wait().
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }

@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(DQ_THREADS)
   const Idx c16 = cols >> 4, nb = cols >> 5;
   const Idx n16 = rows * c16;
   const int64_t col_tiles = ((int64_t)nb + 3) >> 2;
+  pdl_wait();
   for (Idx i = (Idx)blockIdx.x * DQ_THREADS + threadIdx.x; i < n16;
        i += (Idx)gridDim.x * DQ_THREADS) {
     const uint4 c = ld_stream_v4(codes + (int64_t)i * 16);
@@ -58,6 +59,7 @@ __global__ void __launch_bounds__(DQ_THREADS)
     st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
     st_v4(dst + 8, make_uint4(w[4], w[5], w[6], w[7]));
   }
+  pdl_launch_dependents();
 }
 
 // NVFP4: a thread converts one 16-value block (8 bytes of codes) into 32
@@ -76,6 +78,7 @@ __global__ void __launch_bounds__(DQ_THREADS)
   const Idx nblk = total_rows * nb;
   const int64_t col_tiles = ((int64_t)nb + 3) >> 2;
   const bool need_batch = swizzled || per_batch;
+  pdl_wait();
   for (Idx i = (Idx)blockIdx.x * DQ_THREADS + threadIdx.x; i < nblk;
        i += (Idx)gridDim.x * DQ_THREADS) {
     uint2 c;
@@ -107,6 +110,7 @@ __global__ void __launch_bounds__(DQ_THREADS)
     st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
     st_v4(dst + 8, make_uint4(w[4], w[5], w[6], w[7]));
   }
+  pdl_launch_dependents();
 }
 
 unsigned dq_grid(int64_t units, int dev) {
@@ -128,12 +132,11 @@ cudaError_t launch_dequant_mxfp8(const uint8_t* codes, const uint8_t* scales,
   uint16_t* out = static_cast<uint16_t*>(y);
   // 32-bit indices when the largest index and the grid stride fit.
   if (units + (int64_t)grid * DQ_THREADS < (1ll << 32))
-    dequant_mxfp8_kernel<uint32_t><<<grid, DQ_THREADS, 0, stream>>>(
-        codes, scales, (uint32_t)rows, (uint32_t)cols, swizzled, out);
-  else
-    dequant_mxfp8_kernel<int64_t><<<grid, DQ_THREADS, 0, stream>>>(
-        codes, scales, rows, cols, swizzled, out);
-  return cudaGetLastError();
+    return launch_pdl(dequant_mxfp8_kernel<uint32_t>, dim3(grid),
+                      dim3(DQ_THREADS), 0, stream, false, codes, scales,
+                      (uint32_t)rows, (uint32_t)cols, swizzled, out);
+  return launch_pdl(dequant_mxfp8_kernel<int64_t>, dim3(grid), dim3(DQ_THREADS),
+                    0, stream, false, codes, scales, rows, cols, swizzled, out);
 }
 
 cudaError_t launch_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales,
@@ -149,14 +152,13 @@ cudaError_t launch_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales,
   const int64_t stride = scale_bytes(rows, cols / 16, swizzled);
   uint16_t* out = static_cast<uint16_t*>(y);
   if (units + (int64_t)grid * DQ_THREADS < (1ll << 32))
-    dequant_nvfp4_kernel<uint32_t><<<grid, DQ_THREADS, 0, stream>>>(
-        codes, scales, S, per_batch, (uint32_t)rows, (uint32_t)total_rows,
-        (uint32_t)cols, swizzled, stride, out);
-  else
-    dequant_nvfp4_kernel<int64_t><<<grid, DQ_THREADS, 0, stream>>>(
-        codes, scales, S, per_batch, rows, total_rows, cols, swizzled, stride,
-        out);
-  return cudaGetLastError();
+    return launch_pdl(dequant_nvfp4_kernel<uint32_t>, dim3(grid),
+                      dim3(DQ_THREADS), 0, stream, false, codes, scales, S,
+                      per_batch, (uint32_t)rows, (uint32_t)total_rows,
+                      (uint32_t)cols, swizzled, stride, out);
+  return launch_pdl(dequant_nvfp4_kernel<int64_t>, dim3(grid), dim3(DQ_THREADS),
+                    0, stream, false, codes, scales, S, per_batch, rows,
+                    total_rows, cols, swizzled, stride, out);
 }
 
 }  // namespace mxq

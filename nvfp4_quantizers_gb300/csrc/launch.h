@@ -8,6 +8,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace mxq {
 
 // Host utilities (api.cu).
@@ -56,6 +58,29 @@ cudaError_t launch_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales,
                                  const float* S, int per_batch, int64_t batch,
                                  int64_t rows, int64_t cols, int swizzled,
                                  void* y, cudaStream_t stream);
+
+// Launch `kernel` on `stream` with programmatic stream serialization (and
+// optionally as a cooperative grid), so its launch overlaps the tail of
+// the previous kernel on the stream; the kernel itself orders its memory
+// accesses after that kernel with griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                       size_t smem, cudaStream_t stream, bool cooperative,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cooperative ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Scale-matrix size in bytes for either layout.
 inline int64_t scale_bytes(int64_t rows, int64_t cols, int swizzled) {

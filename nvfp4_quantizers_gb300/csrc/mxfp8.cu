@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_wait();
 
   // ------------------------------------------------------------------ //
   // Prologue: thread 0 fills the ring with the first STAGES tiles.      //
@@ -290,6 +291,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (++stage == STAGES) { stage = 0; phase ^= 1; }
     par ^= 1;
   }
+  pdl_launch_dependents();
 }
 
 }  // namespace
@@ -339,8 +341,8 @@ cudaError_t launch_mxfp8_rowcol(const void* x, int64_t M, int64_t K,
     configured_dev = dev;
   }
   const int64_t grid = imin<int64_t>((int64_t)p.num_tiles, (int64_t)sm_count(dev) * 2);
-  mxfp8_rowcol_kernel<<<(unsigned)grid, THREADS, smem, stream>>>(tmap, p);
-  return cudaGetLastError();
+  return launch_pdl(mxfp8_rowcol_kernel, dim3((unsigned)grid), dim3(THREADS),
+                    smem, stream, false, tmap, p);
 }
 
 }  // namespace mxq

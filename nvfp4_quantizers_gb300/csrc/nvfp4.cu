@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slot = warp / WPR, wpart = warp % WPR;
   const int64_t t = (int64_t)blockIdx.x * ROWS + slot;
+  pdl_wait();
   if (t >= T_pad) return;                 // uniform over the row's warps
   const bool real = t < T;
   RowOut o{codes + t * (H >> 1), scales, t, ((H >> 4) + 3) >> 2, H >> 4,
@@ -207,6 +208,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
   encode_row_warps<R, WPR>(x + t * ldx, real, 0.0f, false, o, slot, wpart,
                            lane, red, &S);
   if (real && wpart == 0 && lane == 0) S_out[t] = S;
+  pdl_launch_dependents();
 }
 
 // Rows longer than 8 warps x 2048 values: one CTA per row, an amax pass and
@@ -222,6 +224,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
   const int64_t t = blockIdx.x;
   const bool real = t < T;
   const uint16_t* row = x + t * ldx;
+  pdl_wait();
   RowOut o{codes + t * (H >> 1), scales, t, ((H >> 4) + 3) >> 2, H >> 4,
            swizzled};
   const int64_t span = CTA_WARPS * 32;
@@ -248,6 +251,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
     store_block(o, b, real, lo, hi, sb, lane);
   }
   if (real && threadIdx.x == 0) S_out[t] = S;
+  pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -338,6 +342,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
   const int slot = warp / WPR, wpart = warp % WPR;
   if (threadIdx.x == 0) s_abort = 0;
   __syncthreads();
+  pdl_wait();
   const int64_t group_chunks = p.part_chunk0[p.num_parts];
   uint32_t* amax = p.ws + kWsHeaderWords;
   uint32_t gen = 0;
@@ -432,6 +437,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
                                &S_used);
     }
   }
+  pdl_launch_dependents();
 }
 
 // Launch shape of the row encoders: R blocks per lane (R * 512 values per
@@ -460,23 +466,23 @@ cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
   const uint16_t* xs = static_cast<const uint16_t*>(x);
   const RowShape sh = pick_shape(H);
   if (sh.R == 0) {
-    nvfp4_token_long_kernel<<<(unsigned)T_pad, CTA_WARPS * 32, 0, stream>>>(
-        xs, T, H, ldx, codes, scales, token_scales, swizzled);
-    return cudaGetLastError();
+    return launch_pdl(nvfp4_token_long_kernel, dim3((unsigned)T_pad),
+                      dim3(CTA_WARPS * 32), 0, stream, false, xs, T, H, ldx,
+                      codes, scales, token_scales, swizzled);
   }
   const int rows_per_cta = CTA_WARPS / sh.WPR;
   const unsigned grid = (unsigned)((T_pad + rows_per_cta - 1) / rows_per_cta);
-#define MXQ_TOKEN_LAUNCH(R_, W_)                                        \
-  nvfp4_token_kernel<R_, W_><<<grid, CTA_WARPS * 32, 0, stream>>>(      \
-      xs, T, T_pad, H, ldx, codes, scales, token_scales, swizzled)
-  if (sh.R == 1) MXQ_TOKEN_LAUNCH(1, 1);
-  else if (sh.R == 2) MXQ_TOKEN_LAUNCH(2, 1);
-  else if (sh.WPR == 1) MXQ_TOKEN_LAUNCH(4, 1);
-  else if (sh.WPR == 2) MXQ_TOKEN_LAUNCH(4, 2);
-  else if (sh.WPR == 4) MXQ_TOKEN_LAUNCH(4, 4);
-  else MXQ_TOKEN_LAUNCH(4, 8);
+#define MXQ_TOKEN_LAUNCH(R_, W_)                                          \
+  launch_pdl(nvfp4_token_kernel<R_, W_>, dim3(grid), dim3(CTA_WARPS * 32), \
+             0, stream, false, xs, T, T_pad, H, ldx, codes, scales,        \
+             token_scales, swizzled)
+  if (sh.R == 1) return MXQ_TOKEN_LAUNCH(1, 1);
+  if (sh.R == 2) return MXQ_TOKEN_LAUNCH(2, 1);
+  if (sh.WPR == 1) return MXQ_TOKEN_LAUNCH(4, 1);
+  if (sh.WPR == 2) return MXQ_TOKEN_LAUNCH(4, 2);
+  if (sh.WPR == 4) return MXQ_TOKEN_LAUNCH(4, 4);
+  return MXQ_TOKEN_LAUNCH(4, 8);
 #undef MXQ_TOKEN_LAUNCH
-  return cudaGetLastError();
 }
 
 size_t nvfp4_weight_ws_bytes(int64_t num_groups) {
@@ -505,10 +511,8 @@ cudaError_t launch_weight_coop(const GroupTable& tab, const GroupParams& p,
     if (dev >= 0 && dev < 64) occ[dev] = n;
   }
   const unsigned grid = (unsigned)(n * sm_count(dev));
-  void* args[] = {const_cast<GroupTable*>(&tab), const_cast<GroupParams*>(&p)};
-  return cudaLaunchCooperativeKernel((const void*)nvfp4_weight_kernel<R, WPR>,
-                                     dim3(grid), dim3(CTA_WARPS * 32), args, 0,
-                                     stream);
+  return launch_pdl(nvfp4_weight_kernel<R, WPR>, dim3(grid),
+                    dim3(CTA_WARPS * 32), 0, stream, true, tab, p);
 }
 
 }  // namespace
