@@ -137,6 +137,23 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 # GPU arm.
 # --------------------------------------------------------------------------
+def max_over_ranks(value, dist, device):
+    """Max of a per-rank float over all ranks (the rank-local value when not
+    distributed)."""
+    import torch
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(step_bytes, steps, world, ms_max):
+    """Whole-job GB/s: every rank processes `step_bytes` per step, and the
+    job takes as long as its slowest rank."""
+    return step_bytes * steps * world / (ms_max / 1e3) / 1e9
+
+
 def dist_setup(n_gpus):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -281,10 +298,7 @@ def run_gpu(args):
             dist.barrier()
         wall = time.perf_counter() - t0
     ms = start.elapsed_time(end)
-    ms_t = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = max_over_ranks(ms, dist if world > 1 else None, dev)
     ob = op_bytes()
     step_bytes = sum(ob.values())
     dom = "mxfp8_quantize_rowcol"
@@ -305,7 +319,7 @@ def run_gpu(args):
         per_kernel_ms[nm] = statistics.mean(
             recs8[i][j].elapsed_time(recs8[i][j + 1]) for i in range(nb))
     peak, peak_kind = measured_peak()
-    value = step_bytes * args.steps * world / (ms_max / 1e3) / 1e9
+    value = weak_scaling_value(step_bytes, args.steps, world, ms_max)
 
     # e2e through the public API: pinned host input -> device -> the step's
     # kernels -> quantized outputs back to pinned host memory.

@@ -332,7 +332,7 @@ __device__ __forceinline__ const uint16_t* chunk_ptr(const GroupTable& tab,
 }
 
 template <int R, int WPR>
-__global__ void __launch_bounds__(CTA_WARPS * 32)
+__global__ void __launch_bounds__(CTA_WARPS * 32, 4)
     nvfp4_weight_kernel(const __grid_constant__ GroupTable tab,
                         const __grid_constant__ GroupParams p) {
   constexpr int ROWS = CTA_WARPS / WPR;
@@ -358,42 +358,33 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
       const int64_t u_end = n_units * (blockIdx.x + 1) / gridDim.x;
       int cur = -1;
       uint32_t a = 0;
-      for (int64_t u = u_begin; u < u_end; u += 2) {
-        const int gl0 = c0 + (int)(u / p.units_per_group);
-        const int gl1 = (u + 1 < u_end) ? c0 + (int)((u + 1) / p.units_per_group) : -1;
-        uint4 v[8];
+      for (int64_t u = u_begin; u < u_end; ++u) {
+        const int gl = c0 + (int)(u / p.units_per_group);
+        const int64_t q0 = (u % p.units_per_group) * kAmaxUnitChunks;
+        uint4 v[4];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int64_t uu = u + (jj >> 2);
-          const int gl = (jj >> 2) ? gl1 : gl0;
-          const int64_t q = (uu % p.units_per_group) * kAmaxUnitChunks +
-                            threadIdx.x + (int64_t)(jj & 3) * 256;
-          v[jj] = (gl >= 0 && q < group_chunks)
-                      ? ld_stream_v4(chunk_ptr(tab, p, gl, q))
-                      : make_uint4(0, 0, 0, 0);
+        for (int jj = 0; jj < 4; ++jj) {
+          const int64_t q = q0 + threadIdx.x + (int64_t)jj * 256;
+          v[jj] = q < group_chunks ? ld_stream_v4(chunk_ptr(tab, p, gl, q))
+                                   : make_uint4(0, 0, 0, 0);
         }
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int gl = half ? gl1 : gl0;
-          if (gl < 0) break;                               // CTA-uniform
-          if (gl != cur) {                                 // CTA-uniform
-            if (cur >= 0) {
-              const uint32_t m = warp_max(a);
-              if (lane == 0) red[warp] = m;
-              __syncthreads();
-              if (threadIdx.x == 0) {
-                uint32_t mm = red[0];
-                for (int w = 1; w < CTA_WARPS; ++w) mm = max(mm, red[w]);
-                if (mm) atomicMax(&amax[p.g0 + cur], mm << 16);
-              }
-              __syncthreads();
+        if (gl != cur) {                                   // CTA-uniform
+          if (cur >= 0) {
+            const uint32_t m = warp_max(a);
+            if (lane == 0) red[warp] = m;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+              uint32_t mm = red[0];
+              for (int w = 1; w < CTA_WARPS; ++w) mm = max(mm, red[w]);
+              if (mm) atomicMax(&amax[p.g0 + cur], mm << 16);
             }
-            cur = gl;
-            a = 0;
+            __syncthreads();
           }
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) a = max(a, chunk_absmax(v[half * 4 + jj]));
+          cur = gl;
+          a = 0;
         }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) a = max(a, chunk_absmax(v[jj]));
       }
       if (cur >= 0) {                                      // CTA-uniform
         const uint32_t m = warp_max(a);
