@@ -265,6 +265,48 @@ mxq_status dequantize_nvfp4(const uint8_t* codes, const uint8_t* block_scales,
                             int64_t rows, int64_t cols, int scale_layout,
                             void* y, void* stream);
 
+/* --------------------------------------------------------------------- */
+/* Block-scaled GEMM consumers (5th-generation tensor cores).             */
+/*                                                                       */
+/* [MILES] MXFP8 recipe section: forward, weight-gradient and data-       */
+/* gradient GEMMs consume the MXFP8 copies.  [MILES] experiments section: */
+/* the per-token NVFP4 GEMM applies the per-token FP32 scale in the       */
+/* kernel epilogue rather than as a separate operation.                   */
+/*                                                                       */
+/* mxq_gemm_mxfp8: C[m, n] = sum_k A[m, k] * B[k, n] with fp32             */
+/* accumulation, where A is the rowwise MXFP8 copy of an [M x K] tensor    */
+/* (a_codes [M x K], a_scales swizzled E8M0 [M x K/32]) and B is given as  */
+/* B^T [N x K]: the columnwise copy of a [K x N] tensor (col_codes_t,      */
+/* col_scales_t), or the rowwise copy of an [N x K] weight.  Scales must   */
+/* be in MXQ_SCALE_SWIZZLED layout.  C is fp32 [M x N], row stride ldc    */
+/* (ldc >= N, ldc % 4 == 0).  M % 128 == 0, N % 128 == 0, K % 128 == 0.    */
+/* --------------------------------------------------------------------- */
+mxq_status mxq_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
+                          const uint8_t* bt_codes, const uint8_t* bt_scales,
+                          int64_t M, int64_t N, int64_t K, float* C,
+                          int64_t ldc, void* stream);
+
+/* mxq_gemm_nvfp4_grouped: expert-grouped NVFP4 GEMM.  A holds the routed  */
+/* activations of all groups, grouped contiguously: rows                  */
+/* group_offsets[g] .. group_offsets[g+1] (HOST array of num_groups + 1    */
+/* entries, group_offsets[0] == 0, every entry a multiple of 128: pad each */
+/* group) use weight W_g.  a_codes [M_total x K/2], a_scales swizzled E4M3 */
+/* [M_total x K/16], a_token_scales f32 [M_total] (as produced by          */
+/* nvfp4_quantize_per_token).  w_codes [num_groups x N x K/2], w_scales    */
+/* num_groups swizzled scale matrices of mxq_scale_bytes(N, K/16) bytes,   */
+/* w_group_scales f32 [num_groups] (as produced by                         */
+/* nvfp4_quantize_weight_shared).                                          */
+/*   C[r, n] = a_token_scales[r] * w_group_scales[g] *                     */
+/*             sum_k (E2M1 x E4M3)(a[r, k]) * (E2M1 x E4M3)(w_g[n, k])     */
+/* with fp32 accumulation; C fp32 [M_total x N], row stride ldc.           */
+/* N % 128 == 0, K % 256 == 0, num_groups <= 256.                          */
+/* --------------------------------------------------------------------- */
+mxq_status mxq_gemm_nvfp4_grouped(
+    const uint8_t* a_codes, const uint8_t* a_scales, const float* a_token_scales,
+    const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
+    const uint8_t* w_scales, const float* w_group_scales, int64_t N, int64_t K,
+    float* C, int64_t ldc, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -9,7 +9,8 @@ from ._lib import (  # noqa: F401
     MXQ_ERR_ALIGN, MXQ_ERR_ARG, MXQ_ERR_CUDA, MXQ_ERR_LAYOUT, MXQ_ERR_NULL,
     MXQ_ERR_SHAPE, MXQ_ERR_TIMEOUT, MXQ_ERR_WORKSPACE, MXQ_OK, SCALE_LINEAR,
     SCALE_SWIZZLED, S_PER_BATCH, S_PER_ROW, Mxfp8Quantized, MxqError,
-    Nvfp4Quantized, dequantize_mxfp8, dequantize_nvfp4, get_last_error, lib,
+    Nvfp4Quantized, dequantize_mxfp8, dequantize_nvfp4, gemm_mxfp8,
+    gemm_nvfp4_grouped, get_last_error, lib,
     mxfp8_quantize_rowcol, nvfp4_quantize_per_token,
     nvfp4_quantize_weight_shared, scale_bytes, set_fault_inject,
     status_string)

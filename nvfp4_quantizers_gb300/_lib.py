@@ -84,6 +84,12 @@ def lib() -> ctypes.CDLL:
             ctypes.c_size_t, _p]
         L.dequantize_mxfp8.restype = _int
         L.dequantize_mxfp8.argtypes = [_p, _p, _i64, _i64, _int, _p, _p]
+        L.mxq_gemm_mxfp8.restype = _int
+        L.mxq_gemm_mxfp8.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p,
+                                     _i64, _p]
+        L.mxq_gemm_nvfp4_grouped.restype = _int
+        L.mxq_gemm_nvfp4_grouped.argtypes = [_p, _p, _p, _p, _i64, _p, _p, _p,
+                                             _i64, _i64, _p, _i64, _p]
         L.dequantize_nvfp4.restype = _int
         L.dequantize_nvfp4.argtypes = [_p, _p, _p, _int, _i64, _i64, _i64,
                                        _int, _p, _p]
@@ -292,3 +298,42 @@ def dequantize_nvfp4(codes: torch.Tensor, block_scales: torch.Tensor,
                                   lay, y.data_ptr(), _stream(codes.device)),
            "dequantize_nvfp4")
     return y
+
+
+def gemm_mxfp8(a_codes: torch.Tensor, a_scales: torch.Tensor,
+               bt_codes: torch.Tensor, bt_scales: torch.Tensor) -> torch.Tensor:
+    """fp32 C [M, N] = A @ B from the rowwise MXFP8 copy of A [M, K] and
+    B^T [N, K] (the columnwise copy of B [K, N]); swizzled scales
+    (C: mxq_gemm_mxfp8)."""
+    M, K = a_codes.shape
+    N = bt_codes.shape[0]
+    if bt_codes.shape[1] != K:
+        raise ValueError("A and B^T must share K")
+    C = torch.empty((M, N), dtype=torch.float32, device=a_codes.device)
+    _check(lib().mxq_gemm_mxfp8(a_codes.data_ptr(), a_scales.data_ptr(),
+                                bt_codes.data_ptr(), bt_scales.data_ptr(), M, N,
+                                K, C.data_ptr(), N, _stream(a_codes.device)),
+           "mxq_gemm_mxfp8")
+    return C
+
+
+def gemm_nvfp4_grouped(a_codes: torch.Tensor, a_scales: torch.Tensor,
+                       a_token_scales: torch.Tensor, group_offsets,
+                       w_codes: torch.Tensor, w_scales: torch.Tensor,
+                       w_group_scales: torch.Tensor) -> torch.Tensor:
+    """Expert-grouped NVFP4 GEMM with the per-token and per-group FP32
+    scales applied in the epilogue (C: mxq_gemm_nvfp4_grouped).
+    group_offsets: num_groups + 1 row offsets, multiples of 128."""
+    offs = [int(v) for v in group_offsets]
+    G = len(offs) - 1
+    M_total, half = a_codes.shape
+    K = half * 2
+    N = w_codes.shape[1]
+    off_arr = (ctypes.c_int64 * len(offs))(*offs)
+    C = torch.empty((M_total, N), dtype=torch.float32, device=a_codes.device)
+    _check(lib().mxq_gemm_nvfp4_grouped(
+        a_codes.data_ptr(), a_scales.data_ptr(), a_token_scales.data_ptr(),
+        ctypes.cast(off_arr, ctypes.c_void_p), G, w_codes.data_ptr(),
+        w_scales.data_ptr(), w_group_scales.data_ptr(), N, K, C.data_ptr(), N,
+        _stream(a_codes.device)), "mxq_gemm_nvfp4_grouped")
+    return C

@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmxq.so")
-SOURCES = ["api.cu", "mxfp8.cu", "nvfp4.cu", "dequant.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "mxfp8.cu", "nvfp4.cu", "dequant.cu", "noalloc.cu",
+           "gemm.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [

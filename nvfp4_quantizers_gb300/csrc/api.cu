@@ -120,6 +120,23 @@ cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_tmap_2d_bytes(CUtensorMap* map, const void* base,
+                               uint64_t inner, uint64_t outer,
+                               uint64_t outer_stride_bytes, uint32_t box_inner,
+                               uint32_t box_outer) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {outer_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace mxq
 
 using namespace mxq;
@@ -153,9 +170,11 @@ int64_t mxq_scale_bytes(int64_t rows, int64_t cols, int scale_layout) {
 mxq_status mxq_get_last_error(void) {
   cudaError_t e = cudaDeviceSynchronize();
   unsigned int word = 0, word2 = 0;
+  unsigned int word3 = 0;
   cudaError_t e2 = mxfp8_take_wait_error(&word);
   if (e2 == cudaSuccess) e2 = nvfp4_take_wait_error(&word2);
-  if (e2 == cudaSuccess && (word != 0 || word2 != 0)) return MXQ_ERR_TIMEOUT;
+  if (e2 == cudaSuccess) e2 = gemm_take_wait_error(&word3);
+  if (e2 == cudaSuccess && (word | word2 | word3) != 0) return MXQ_ERR_TIMEOUT;
   cudaError_t last = cudaGetLastError();
   if (e != cudaSuccess || e2 != cudaSuccess || last != cudaSuccess)
     return MXQ_ERR_CUDA;
@@ -300,6 +319,63 @@ mxq_status dequantize_nvfp4(const uint8_t* codes, const uint8_t* block_scales,
   return from_cuda(launch_dequant_nvfp4(
       codes, block_scales, S, s_mode == MXQ_S_PER_BATCH, batch, rows, cols,
       scale_layout == MXQ_SCALE_SWIZZLED, y, static_cast<cudaStream_t>(stream)));
+}
+
+mxq_status mxq_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
+                          const uint8_t* bt_codes, const uint8_t* bt_scales,
+                          int64_t M, int64_t N, int64_t K, float* C,
+                          int64_t ldc, void* stream) {
+  const int fm = fault_mode();
+  if (fm == 2) return MXQ_ERR_ARG;
+  if (M < 0 || N < 0 || K < 0 || ldc < N) return MXQ_ERR_SHAPE;
+  if (M == 0 || N == 0) return MXQ_OK;
+  if (!a_codes || !a_scales || !bt_codes || !bt_scales || !C)
+    return MXQ_ERR_NULL;
+  if (M % 128 != 0 || N % 128 != 0 || K % 128 != 0 || K == 0)
+    return MXQ_ERR_SHAPE;
+  if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31))
+    return MXQ_ERR_SHAPE;
+  if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(bt_codes) ||
+      !aligned16(bt_scales) || !aligned16(C) || ldc % 4 != 0)
+    return MXQ_ERR_ALIGN;
+  if (fm == 1) return MXQ_ERR_CUDA;
+  return from_cuda(launch_gemm_mxfp8(a_codes, a_scales, bt_codes, bt_scales, M,
+                                     N, K, C, ldc,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+mxq_status mxq_gemm_nvfp4_grouped(
+    const uint8_t* a_codes, const uint8_t* a_scales, const float* a_token_scales,
+    const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
+    const uint8_t* w_scales, const float* w_group_scales, int64_t N, int64_t K,
+    float* C, int64_t ldc, void* stream) {
+  const int fm = fault_mode();
+  if (fm == 2) return MXQ_ERR_ARG;
+  if (num_groups < 0 || num_groups > 256 || N < 0 || K < 0 || ldc < N)
+    return MXQ_ERR_SHAPE;
+  if (num_groups == 0 || N == 0) return MXQ_OK;
+  if (!group_offsets) return MXQ_ERR_NULL;
+  if (group_offsets[0] != 0) return MXQ_ERR_SHAPE;
+  for (int64_t g = 0; g < num_groups; ++g)
+    if (group_offsets[g + 1] < group_offsets[g] ||
+        group_offsets[g + 1] % 128 != 0)
+      return MXQ_ERR_SHAPE;
+  if (group_offsets[num_groups] == 0) return MXQ_OK;
+  if (!a_codes || !a_scales || !a_token_scales || !w_codes || !w_scales ||
+      !w_group_scales || !C)
+    return MXQ_ERR_NULL;
+  if (N % 128 != 0 || K % 256 != 0 || K == 0) return MXQ_ERR_SHAPE;
+  if (group_offsets[num_groups] >= (1ll << 31) || num_groups * N >= (1ll << 31) ||
+      K >= (1ll << 31))
+    return MXQ_ERR_SHAPE;
+  if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) ||
+      !aligned16(w_scales) || !aligned16(C) || ldc % 4 != 0)
+    return MXQ_ERR_ALIGN;
+  if (fm == 1) return MXQ_ERR_CUDA;
+  return from_cuda(launch_gemm_nvfp4_grouped(
+      a_codes, a_scales, a_token_scales, group_offsets, num_groups, w_codes,
+      w_scales, w_group_scales, N, K, C, ldc,
+      static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -1,0 +1,439 @@
+// gemm.cu -- block-scaled GEMM consumers of the quantizer outputs, on the
+// 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// "Miles: end-to-end MXFP8 and per-token NVFP4 RL", MXFP8 recipe section:
+// forward, weight-gradient and data-gradient GEMMs consume the MXFP8
+// copies; experiments section: the per-token NVFP4 GEMM applies the
+// per-token FP32 scale in the kernel epilogue instead of a separate op.
+//
+//   MXFP8:  C[m, n] = sum_k A[m, k] * B[k, n], A given rowwise (1x32 E8M0
+//           blocks along K) and B given as B^T [N x K] (its columnwise
+//           copy, also 1x32 blocks along K); fp32 accumulation and output.
+//   NVFP4:  grouped over experts: rows off[e] .. off[e+1] of A use expert
+//           e's weight W_e [N x K]; C[r, n] = S_tok[r] * S_w[e] *
+//           sum_k a[r, k] w_e[n, k], where a and w are E2M1 x E4M3 block
+//           values and the two FP32 scales are applied in the epilogue.
+//
+// Design (one 128 x 128 output tile per CTA, 4 warps):
+//  * warp 0 lane 0 streams K-stages into a 4-deep shared-memory ring: the
+//    A and B code tiles by 2-D TMA with the 128-byte swizzle (one 128-byte
+//    row per matrix row), and the matching 512-byte scale tiles, which the
+//    quantizers already store in the 128x4 layout the tensor core reads, by
+//    1-D bulk copies; completion on mbarriers.
+//  * warp 1 lane 0 copies each stage's scale tiles into tensor memory
+//    (tcgen05.cp 32x128b.warpx4) and issues the block-scaled MMAs
+//    (tcgen05.mma kind::mxf8f6f4 block_scale, or kind::mxf4nvf4 with
+//    4 E4M3 scales per 64 values); the fp32 accumulator lives in tensor
+//    memory; tcgen05.commit frees each stage when its MMAs are done.
+//  * all 4 warps then read the accumulator with tcgen05.ld (each warp its
+//    32 lanes = 32 rows), scale (NVFP4) and store fp32 C.
+// Every wait is bounded; on timeout the kernel records the error word and
+// skips the remaining work (still freeing its tensor memory).
+#include "common.cuh"
+#include "launch.h"
+
+namespace mxq {
+
+__device__ unsigned int g_gemm_wait_error = 0;
+
+namespace {
+
+constexpr int GM = 128;              // tile rows (A) = MMA M
+constexpr int GN = 128;              // tile cols (B rows) = MMA N
+constexpr int GKB = 128;             // bytes of K per stage per row
+constexpr int GSTAGES = 4;
+constexpr int GTHREADS = 128;
+constexpr uint32_t kTmemCols = 256;  // accumulator 128 + scales 8/stage
+constexpr uint32_t kSfCol0 = 128;
+
+struct alignas(1024) GemmSmem {
+  uint8_t a[GSTAGES][GM * GKB];
+  uint8_t b[GSTAGES][GN * GKB];
+  alignas(16) uint8_t sfa[GSTAGES][4][512];
+  alignas(16) uint8_t sfb[GSTAGES][4][512];
+  alignas(8) uint64_t full[GSTAGES];
+  alignas(8) uint64_t empty[GSTAGES];
+  alignas(8) uint64_t done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// ---------------------------------------------------------------------------
+// tcgen05 / bulk-copy wrappers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile(
+      "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+          dst_smem),
+      "r"(ncols)
+      : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(
+                   taddr),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];" ::"r"(bar)
+      : "memory");
+}
+// 32 rows x 128 bits of shared memory (32 x 16 bytes, a 512-byte scale tile)
+// into tensor memory, replicated to the four 32-lane quarters.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr),
+               "l"(sdesc)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d, uint64_t adesc,
+                                            uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d, uint64_t adesc,
+                                            uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns of tensor memory -> registers.
+__device__ __forceinline__ void tc_ld_32x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, "
+      "%7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, "
+      "%21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+        "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
+        "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src,
+                                         uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor (sm_100 family): start address, leading
+// and stride byte offsets (all >> 4), version 1 at bit 46, layout type at
+// bits 61-63 (0 = no swizzle, 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo,
+                                              uint32_t sbo, uint32_t layout) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) |
+         ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) |
+         ((uint64_t)layout << 61);
+}
+
+// Instruction descriptor of a block-scaled MMA, M = 128, N = GN, both
+// operands K-major: format codes a_fmt / b_fmt, scale format (1 = E8M0,
+// 0 = E4M3), and the byte of each 32-bit scale cell to use (sf_id).
+__device__ __forceinline__ uint32_t idesc_block_scaled(uint32_t a_fmt,
+                                                       uint32_t b_fmt,
+                                                       uint32_t sf_e8m0,
+                                                       uint32_t sf_id) {
+  return (sf_id << 4) | (a_fmt << 7) | (b_fmt << 10) |
+         ((uint32_t)(GN >> 3) << 17) | (sf_e8m0 << 23) |
+         ((uint32_t)(GM >> 4) << 24) | (sf_id << 29);
+}
+
+struct GemmParams {
+  // tile -> operands
+  int kind;                 // 0 = MXFP8, 1 = NVFP4 grouped
+  int64_t M, N, K;          // K in elements
+  int64_t k_stages;         // K / elements per stage
+  const uint8_t* a_sf;      // swizzled scales of A
+  const uint8_t* b_sf;      // swizzled scales of B (group 0)
+  int64_t a_sf_ct;          // scale tiles per 128 rows of A (= K / 128 or K / 64)
+  int64_t b_sf_ct;
+  int64_t b_sf_group_stride;   // bytes between the scale matrices of groups
+  int64_t b_rows_group_stride; // rows between the groups' weights in the B map
+  // NVFP4 grouped
+  const float* s_tok;
+  const float* s_w;
+  int num_groups;
+  int64_t tile_end[257];    // prefix sums of the M-tiles of each group
+  int64_t row_off[257];     // first row of each group
+  int64_t tiles_n;
+  float* C;
+  int64_t ldc;
+};
+
+__global__ void __launch_bounds__(GTHREADS, 1)
+    gemm_block_scaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                             const __grid_constant__ CUtensorMap tmap_b,
+                             const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t gsmem_raw[];
+  GemmSmem& s = *reinterpret_cast<GemmSmem*>(
+      (reinterpret_cast<uintptr_t>(gsmem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Tile coordinates: (group, m-tile within the group, n-tile).
+  const int64_t tile = blockIdx.x;
+  const int64_t mt_all = tile / p.tiles_n;
+  const int64_t nt = tile - mt_all * p.tiles_n;
+  int grp = 0;
+  if (p.kind == 1)
+    while (grp + 1 < p.num_groups && mt_all >= p.tile_end[grp]) ++grp;
+  const int64_t mt_in = p.kind == 1 ? mt_all - (grp ? p.tile_end[grp - 1] : 0)
+                                    : mt_all;
+  const int64_t m0 = (p.kind == 1 ? p.row_off[grp] : 0) + mt_in * GM;
+  const int64_t n0 = nt * GN;
+
+  if (warp == 0) tmem_alloc(smem_addr(&s.tmem_base), kTmemCols);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < GSTAGES; ++i) {
+      mbar_init(smem_addr(&s.full[i]), 1);
+      mbar_init(smem_addr(&s.empty[i]), 1);
+    }
+    mbar_init(smem_addr(&s.done), 1);
+    s.abort = 0;
+    fence_barrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  pdl_wait();
+
+  const int n_sf = p.kind == 1 ? 4 : 1;      // scale tiles per stage
+  const uint32_t stage_bytes = 2 * GM * GKB + 2 * 512 * n_sf;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- producer ----------------
+    for (int64_t kt = 0; kt < p.k_stages; ++kt) {
+      const int st = (int)(kt % GSTAGES);
+      const uint32_t ph = (uint32_t)((kt / GSTAGES) & 1);
+      if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1, &s.abort,
+                     &g_gemm_wait_error))
+        break;
+      const uint32_t full = smem_addr(&s.full[st]);
+      mbar_arrive_expect_tx(full, stage_bytes);
+      tma_load_2d(smem_addr(s.a[st]), &tmap_a, (int32_t)(kt * GKB),
+                  (int32_t)m0, full);
+      tma_load_2d(smem_addr(s.b[st]), &tmap_b, (int32_t)(kt * GKB),
+                  (int32_t)(grp * p.b_rows_group_stride + n0), full);
+      for (int j = 0; j < n_sf; ++j) {
+        const int64_t ct = kt * n_sf + j;
+        bulk_g2s(smem_addr(s.sfa[st][j]),
+                 p.a_sf + ((m0 / 128) * p.a_sf_ct + ct) * 512, 512, full);
+        bulk_g2s(smem_addr(s.sfb[st][j]),
+                 p.b_sf + grp * p.b_sf_group_stride +
+                     ((n0 / 128) * p.b_sf_ct + ct) * 512,
+                 512, full);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    for (int64_t kt = 0; kt < p.k_stages; ++kt) {
+      const int st = (int)(kt % GSTAGES);
+      const uint32_t ph = (uint32_t)((kt / GSTAGES) & 1);
+      if (!mbar_wait(smem_addr(&s.full[st]), ph, &s.abort, &g_gemm_wait_error))
+        break;
+      tc_fence_after();
+      const uint32_t sf_col = tmem + kSfCol0 + (uint32_t)st * 32;
+      for (int j = 0; j < n_sf; ++j) {
+        tc_cp_sf(sf_col + j * 4, smem_desc(smem_addr(s.sfa[st][j]), 16, 128, 0));
+        tc_cp_sf(sf_col + 16 + j * 4,
+                 smem_desc(smem_addr(s.sfb[st][j]), 16, 128, 0));
+      }
+      const uint32_t a_addr = smem_addr(s.a[st]);
+      const uint32_t b_addr = smem_addr(s.b[st]);
+      // Four MMAs per stage, each 32 bytes of K further along the
+      // 128-byte swizzled rows.
+      for (int j = 0; j < 4; ++j) {
+        const uint64_t ad = smem_desc(a_addr + j * 32, 16, 1024, 2);
+        const uint64_t bd = smem_desc(b_addr + j * 32, 16, 1024, 2);
+        const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
+        if (p.kind == 0) {
+          // 8-bit operands: K = 32 per MMA, one E8M0 scale per row per
+          // MMA: byte j of the stage's 32-bit scale cell.
+          tc_mma_mxf8(tmem, ad, bd, idesc_block_scaled(0, 0, 1, (uint32_t)j),
+                      sf_col, sf_col + 16, acc);
+        } else {
+          // 4-bit operands: K = 64 per MMA, four E4M3 scales per row (one
+          // 32-bit cell = one scale tile column group j).
+          tc_mma_nvf4(tmem, ad, bd, idesc_block_scaled(1, 1, 0, 0),
+                      sf_col + j * 4, sf_col + 16 + j * 4, acc);
+        }
+      }
+      tc_commit(smem_addr(&s.empty[st]));
+    }
+    tc_commit(smem_addr(&s.done));
+  }
+  __syncwarp();
+
+  // ---------------- epilogue: 4 warps x 32 rows ----------------
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&s.done), 0,
+                                                     &s.abort,
+                                                     &g_gemm_wait_error));
+  tc_fence_after();
+  if (ok) {
+    const int64_t row = m0 + warp * 32 + lane;
+    float rs = 1.0f;
+    if (p.kind == 1) rs = __fmul_rn(p.s_tok[row], p.s_w[grp]);
+    float* crow = p.C + row * p.ldc + n0;
+    for (int c = 0; c < GN; c += 32) {
+      uint32_t r[32];
+      tc_ld_32x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, r);
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        float4 v;
+        v.x = __uint_as_float(r[i]);
+        v.y = __uint_as_float(r[i + 1]);
+        v.z = __uint_as_float(r[i + 2]);
+        v.w = __uint_as_float(r[i + 3]);
+        if (p.kind == 1) {
+          v.x = __fmul_rn(v.x, rs);
+          v.y = __fmul_rn(v.y, rs);
+          v.z = __fmul_rn(v.z, rs);
+          v.w = __fmul_rn(v.w, rs);
+        }
+        *reinterpret_cast<float4*>(crow + c + i) = v;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  pdl_launch_dependents();
+}
+
+size_t gemm_smem_bytes() { return sizeof(GemmSmem) + 1024; }
+
+cudaError_t make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner,
+                            uint64_t outer, uint64_t stride_bytes) {
+  return make_tmap_2d_bytes(map, base, inner, outer, stride_bytes, GKB, GM);
+}
+
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb,
+                        const GemmParams& p, int64_t tiles,
+                        cudaStream_t stream) {
+  const size_t smem = gemm_smem_bytes();
+  static int configured[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    err = cudaFuncSetAttribute(gemm_block_scaled_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+    if (err != cudaSuccess) return err;
+    configured[dev] = 1;
+  }
+  return launch_pdl(gemm_block_scaled_kernel, dim3((unsigned)tiles),
+                    dim3(GTHREADS), smem, stream, false, ta, tb, p);
+}
+
+}  // namespace
+
+cudaError_t gemm_take_wait_error(unsigned int* word) {
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_gemm_wait_error, sizeof(*word));
+  if (e != cudaSuccess || *word == 0) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_gemm_wait_error, &zero, sizeof(zero));
+}
+
+cudaError_t launch_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
+                              const uint8_t* bt_codes,
+                              const uint8_t* bt_scales, int64_t M, int64_t N,
+                              int64_t K, float* C, int64_t ldc,
+                              cudaStream_t stream) {
+  CUtensorMap ta, tb;
+  cudaError_t err = make_tmap_2d_u8(&ta, a_codes, (uint64_t)K, (uint64_t)M,
+                                    (uint64_t)K);
+  if (err != cudaSuccess) return err;
+  err = make_tmap_2d_u8(&tb, bt_codes, (uint64_t)K, (uint64_t)N, (uint64_t)K);
+  if (err != cudaSuccess) return err;
+  GemmParams p = {};
+  p.kind = 0;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.k_stages = K / GKB;                 // 128 fp8 values per stage
+  p.a_sf = a_scales;
+  p.b_sf = bt_scales;
+  p.a_sf_ct = (K / 32 + 3) / 4;         // 4 scale columns per tile
+  p.b_sf_ct = p.a_sf_ct;
+  p.b_sf_group_stride = 0;
+  p.b_rows_group_stride = 0;
+  p.num_groups = 1;
+  p.tiles_n = N / GN;
+  p.C = C;
+  p.ldc = ldc;
+  return launch_gemm(ta, tb, p, (M / GM) * p.tiles_n, stream);
+}
+
+cudaError_t launch_gemm_nvfp4_grouped(
+    const uint8_t* a_codes, const uint8_t* a_scales, const float* a_s,
+    const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
+    const uint8_t* w_scales, const float* w_s, int64_t N, int64_t K, float* C,
+    int64_t ldc, cudaStream_t stream) {
+  const int64_t m_total = group_offsets[num_groups];
+  CUtensorMap ta, tb;
+  // Packed E2M1: K/2 bytes per row; all groups' weights as one
+  // [num_groups * N x K/2] byte matrix.
+  cudaError_t err = make_tmap_2d_u8(&ta, a_codes, (uint64_t)(K / 2),
+                                    (uint64_t)m_total, (uint64_t)(K / 2));
+  if (err != cudaSuccess) return err;
+  err = make_tmap_2d_u8(&tb, w_codes, (uint64_t)(K / 2),
+                        (uint64_t)(num_groups * N), (uint64_t)(K / 2));
+  if (err != cudaSuccess) return err;
+  GemmParams p = {};
+  p.kind = 1;
+  p.M = m_total;
+  p.N = N;
+  p.K = K;
+  p.k_stages = K / 256;                 // 256 fp4 values (128 bytes) per stage
+  p.a_sf = a_scales;
+  p.b_sf = w_scales;
+  p.a_sf_ct = (K / 16 + 3) / 4;
+  p.b_sf_ct = p.a_sf_ct;
+  p.b_sf_group_stride = scale_bytes(N, K / 16, 1);
+  p.b_rows_group_stride = N;
+  p.s_tok = a_s;
+  p.s_w = w_s;
+  p.num_groups = (int)num_groups;
+  int64_t tiles_m = 0;
+  for (int64_t g = 0; g < num_groups; ++g) {
+    p.row_off[g] = group_offsets[g];
+    tiles_m += (group_offsets[g + 1] - group_offsets[g]) / GM;
+    p.tile_end[g] = tiles_m;
+  }
+  p.tiles_n = N / GN;
+  p.C = C;
+  p.ldc = ldc;
+  if (tiles_m == 0) return cudaSuccess;
+  return launch_gemm(ta, tb, p, tiles_m * p.tiles_n, stream);
+}
+
+}  // namespace mxq

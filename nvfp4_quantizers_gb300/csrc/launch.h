@@ -15,6 +15,10 @@ namespace mxq {
 // Host utilities (api.cu).
 int sm_count(int device);
 int64_t l2_bytes(int device);
+cudaError_t make_tmap_2d_bytes(CUtensorMap* map, const void* base,
+                               uint64_t inner, uint64_t outer,
+                               uint64_t outer_stride_bytes, uint32_t box_inner,
+                               uint32_t box_outer);
 cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base,
                               uint64_t inner, uint64_t outer,
                               uint64_t outer_stride_bytes, uint32_t box_inner,
@@ -81,6 +85,19 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
   cfg.numAttrs = cooperative ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+
+// gemm.cu
+cudaError_t gemm_take_wait_error(unsigned int* word);
+cudaError_t launch_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
+                              const uint8_t* bt_codes,
+                              const uint8_t* bt_scales, int64_t M, int64_t N,
+                              int64_t K, float* C, int64_t ldc,
+                              cudaStream_t stream);
+cudaError_t launch_gemm_nvfp4_grouped(
+    const uint8_t* a_codes, const uint8_t* a_scales, const float* a_s,
+    const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
+    const uint8_t* w_scales, const float* w_s, int64_t N, int64_t K, float* C,
+    int64_t ldc, cudaStream_t stream);
 
 // Scale-matrix size in bytes for either layout.
 inline int64_t scale_bytes(int64_t rows, int64_t cols, int swizzled) {

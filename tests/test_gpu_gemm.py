@@ -1,0 +1,105 @@
+"""GPU parity of the tcgen05 block-scaled GEMM consumers.
+
+The reference is the oracle GEMM: float64 accumulation over operands
+dequantized exactly from the same codes and scales (MXFP8: E4M3 x 2^k;
+NVFP4: E2M1 x E4M3, with the per-token and per-group FP32 scales applied
+after the sum).  The kernel accumulates in fp32, so the bar is a relative
+Frobenius error of 1e-3, the benchmark spec's tolerance; an error in the scale
+layout (the swizzled 128x4 tiles the tensor core reads) shows up as
+factor-of-two errors far above it.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from gpu_util import dev_bf16, host_u8
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def mxq():
+    if not torch.cuda.is_available():
+        pytest.fail("the GPU tests need a CUDA device")
+    from nvfp4_quantizers_gb300 import build
+    build.build()
+    import nvfp4_quantizers_gb300 as q
+    q.lib()
+    return q
+
+
+def rel_fro(c, ref):
+    return float(np.linalg.norm(c - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def _mxfp8_case(q, M, K, N, seed, scale_spread=0):
+    rng = np.random.default_rng(seed)
+    a = rng.standard_normal((M, K))
+    b = 0.02 * rng.standard_normal((K, N))
+    if scale_spread:
+        # distinct power-of-two magnitudes per 32-block make every scale
+        # byte matter
+        a *= np.exp2(rng.integers(-scale_spread, scale_spread, (M, K // 32))
+                     ).repeat(32, axis=1)
+        b *= np.exp2(rng.integers(-scale_spread, scale_spread, (K // 32, N))
+                     ).repeat(32, axis=0)
+    A = W.to_bf16_bits(a)
+    B = W.to_bf16_bits(b)
+    qa = q.mxfp8_quantize_rowcol(dev_bf16(A), rowwise=True, colwise=False)
+    qb = q.mxfp8_quantize_rowcol(dev_bf16(B), rowwise=False, colwise=True)
+    C = q.gemm_mxfp8(qa.row_codes, qa.row_scales, qb.col_codes_t,
+                     qb.col_scales_t)
+    torch.cuda.synchronize()
+    ac, asc = host_u8(qa.row_codes), O.scale_unswizzle(host_u8(qa.row_scales), M, K // 32)
+    bc, bsc = host_u8(qb.col_codes_t), O.scale_unswizzle(host_u8(qb.col_scales_t), N, K // 32)
+    ref = O.gemm_mxfp8(ac, asc, bc, bsc)
+    return C.cpu().numpy().astype(np.float64), ref
+
+
+@pytest.mark.parametrize("M,K,N", [(128, 128, 128), (256, 512, 384)])
+def test_gemm_mxfp8_small(mxq, M, K, N):
+    C, ref = _mxfp8_case(mxq, M, K, N, seed=M + K + N)
+    err = rel_fro(C, ref)
+    assert err <= TOL, err
+
+
+def test_gemm_mxfp8_scale_layout(mxq):
+    """Per-block magnitudes spread over 2^-6 .. 2^6: a permuted or
+    misread scale tile would be off by powers of two."""
+    C, ref = _mxfp8_case(mxq, 256, 256, 256, seed=3, scale_spread=6)
+    assert rel_fro(C, ref) <= TOL
+
+
+def _nvfp4_grouped_case(q, rows_per_group, K, N, seed):
+    rng = np.random.default_rng(seed)
+    G = len(rows_per_group)
+    offs = np.concatenate([[0], np.cumsum(rows_per_group)])
+    a = rng.standard_normal((int(offs[-1]), K)) * np.exp2(
+        rng.integers(-4, 4, (int(offs[-1]), 1)))
+    A = W.to_bf16_bits(a)
+    Wts = [W.to_bf16_bits(0.02 * rng.standard_normal((N, K))) for _ in range(G)]
+    ta = q.nvfp4_quantize_per_token(dev_bf16(A))
+    tw = q.nvfp4_quantize_weight_shared([[dev_bf16(w)] for w in Wts])
+    C = q.gemm_nvfp4_grouped(ta.codes, ta.block_scales, ta.scales, offs,
+                             tw.codes, tw.block_scales, tw.scales)
+    torch.cuda.synchronize()
+    Mt = int(offs[-1])
+    a_sc = O.scale_unswizzle(host_u8(ta.block_scales), Mt, K // 16)
+    w_sc = np.stack([O.scale_unswizzle(host_u8(tw.block_scales[g]), N, K // 16)
+                     for g in range(G)])
+    ref = O.gemm_nvfp4_grouped(host_u8(ta.codes), a_sc, ta.scales.cpu().numpy(),
+                               offs, host_u8(tw.codes), w_sc,
+                               tw.scales.cpu().numpy())
+    return C.cpu().numpy().astype(np.float64), ref
+
+
+@pytest.mark.parametrize("rows,K,N", [([128], 256, 128),
+                                      ([128, 256, 0, 128], 512, 256)])
+def test_gemm_nvfp4_grouped_small(mxq, rows, K, N):
+    C, ref = _nvfp4_grouped_case(mxq, rows, K, N, seed=sum(rows) + K)
+    err = rel_fro(C, ref)
+    assert err <= TOL, err
