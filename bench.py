@@ -383,19 +383,109 @@ def run_gpu(args):
         "e2e": e2e,
         "wall_s_timed_region": round(wall, 3),
     }
+    out["gemm"] = run_gemm(q, W, dev, stream)
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args)
     print(json.dumps(out), flush=True)
 
 
+def tensor_peaks():
+    """fp8 and fp4 dense tensor peaks: the measured bf16 GEMM rate times the
+    nominal fp8/bf16 (2x) and fp4/bf16 (6x) ratios."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16 = float(json.load(f)["bf16_tflops"])
+        kind = "measured bf16 x nominal ratio"
+    except Exception:
+        bf16, kind = 1900.0, "fallback bf16 x nominal ratio"
+    return {"fp8": 2 * bf16, "fp4": 6 * bf16, "kind": kind}
+
+
+def run_gemm(q, W, dev, stream, reps=20):
+    """The block-scaled GEMM consumers on the workloads they are specified
+    for: MXFP8 A [2048 x 2048] x B [2048 x 8192]; NVFP4 4096 tokens routed
+    top-8 over 128 experts against gate/up [1536 x 2048] weights."""
+    import torch
+    peaks = tensor_peaks()
+    out = {}
+    A, B = W.gemm_mxfp8_inputs(2048, 2048, 8192)
+    qa = q.mxfp8_quantize_rowcol(torch.from_numpy(A.view(np.int16)).view(
+        torch.bfloat16).to(dev), rowwise=True, colwise=False)
+    qb = q.mxfp8_quantize_rowcol(torch.from_numpy(B.view(np.int16)).view(
+        torch.bfloat16).to(dev), rowwise=False, colwise=True)
+
+    def t_mx():
+        return q.gemm_mxfp8(qa.row_codes, qa.row_scales, qb.col_codes_t,
+                            qb.col_scales_t)
+    ms = _time_fn(t_mx, stream, reps)
+    fl = 2.0 * 2048 * 2048 * 8192
+    out["mxfp8_2048x2048x8192"] = {
+        "us": round(ms * 1e3, 2), "TFLOP/s": round(fl / ms / 1e9, 1),
+        "peak_fp8": round(peaks["fp8"], 1),
+        "frac": round(fl / ms / 1e9 / peaks["fp8"], 3), "bound": "tensor"}
+    E, H, F = 128, 2048, 768
+    tokens = W.gemm_tokens(4096, H)
+    route = W.topk_routing(4096, E, 8)
+    rows_by_e = [np.nonzero((route == e).any(axis=1))[0] for e in range(E)]
+    padded = [((len(r) + 127) // 128) * 128 for r in rows_by_e]
+    offs = np.concatenate([[0], np.cumsum(padded)])
+    gathered = np.zeros((int(offs[-1]), H), np.uint16)
+    for e in range(E):
+        gathered[offs[e]:offs[e] + len(rows_by_e[e])] = tokens[rows_by_e[e]]
+    ta = q.nvfp4_quantize_per_token(torch.from_numpy(gathered.view(np.int16))
+                                    .view(torch.bfloat16).to(dev))
+    wts = torch.from_numpy(np.stack(
+        [np.concatenate(W.moe_expert(e, hidden=H, ffn=F)[:2])
+         for e in range(E)]).view(np.int16)).view(torch.bfloat16).to(dev)
+    tw = q.nvfp4_quantize_weight_shared([[wts[e]] for e in range(E)])
+    del wts
+
+    def t_nv():
+        return q.gemm_nvfp4_grouped(ta.codes, ta.block_scales, ta.scales, offs,
+                                    tw.codes, tw.block_scales, tw.scales)
+    ms = _time_fn(t_nv, stream, reps)
+    fl_routed = 2.0 * 32768 * 2 * F * H
+    fl_padded = 2.0 * int(offs[-1]) * 2 * F * H
+    out["nvfp4_grouped_4096tok_top8_128x1536x2048"] = {
+        "us": round(ms * 1e3, 2),
+        "TFLOP/s_routed": round(fl_routed / ms / 1e9, 1),
+        "TFLOP/s_padded": round(fl_padded / ms / 1e9, 1),
+        "padded_rows": int(offs[-1]), "routed_rows": 32768,
+        "peak_fp4": round(peaks["fp4"], 1),
+        "frac": round(fl_padded / ms / 1e9 / peaks["fp4"], 3),
+        "bound": "tensor"}
+    out["peaks_kind"] = peaks["kind"]
+    return out
+
+
+def _time_fn(fn, stream, reps):
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def load_traffic(kernel_name):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary (profiles/traffic.json), or None when none was taken for the
-    current kernel."""
+    """DRAM bytes (read + write) per launch of the dominant kernel from the
+    committed ncu summary (profiles/traffic.json), or None when no capture
+    was taken for the kernel as it is now (its source hash differs)."""
+    import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            d = json.load(f)
-        return d.get(kernel_name)
+            d = json.load(f)[kernel_name]
+        with open(os.path.join(ROOT, d["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != d["source_sha256"]:
+                return None
+        return int(d["dram_bytes_per_launch"])
     except Exception:
         return None
 

@@ -103,3 +103,61 @@ def test_gemm_nvfp4_grouped_small(mxq, rows, K, N):
     C, ref = _nvfp4_grouped_case(mxq, rows, K, N, seed=sum(rows) + K)
     err = rel_fro(C, ref)
     assert err <= TOL, err
+
+
+def test_gemm_mxfp8_full_size_sampled(mxq):
+    """A [2048 x 2048] N(0,1) times B [2048 x 8192] N(0, 0.02), B consumed
+    through its columnwise copy; 256 sampled rows of C vs the oracle."""
+    M, K, N = 2048, 2048, 8192
+    A, B = W.gemm_mxfp8_inputs(M, K, N)
+    qa = mxq.mxfp8_quantize_rowcol(dev_bf16(A), rowwise=True, colwise=False)
+    qb = mxq.mxfp8_quantize_rowcol(dev_bf16(B), rowwise=False, colwise=True)
+    C = mxq.gemm_mxfp8(qa.row_codes, qa.row_scales, qb.col_codes_t,
+                       qb.col_scales_t)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(0).choice(M, 256, replace=False))
+    ac = host_u8(qa.row_codes)[rows]
+    asc = O.scale_unswizzle(host_u8(qa.row_scales), M, K // 32)[rows]
+    bc = host_u8(qb.col_codes_t)
+    bsc = O.scale_unswizzle(host_u8(qb.col_scales_t), N, K // 32)
+    ref = O.gemm_mxfp8(ac, asc, bc, bsc)
+    got = C.cpu().numpy()[rows].astype(np.float64)
+    assert rel_fro(got, ref) <= TOL
+
+
+def test_gemm_nvfp4_grouped_moe_sampled(mxq):
+    """4096 tokens (hidden 2048), top-8 of 128 experts, gate/up weights
+    [1536 x 2048] per expert: tokens gathered by expert into 128-row-padded
+    groups, quantized per token, multiplied by each expert's NVFP4 weight
+    with both FP32 scales in the epilogue.  Four experts are checked row by
+    row against the oracle."""
+    E, H, F = 128, 2048, 768
+    tokens = W.gemm_tokens(4096, H)
+    route = W.topk_routing(4096, E, 8)
+    rows_by_e = [np.nonzero((route == e).any(axis=1))[0] for e in range(E)]
+    sizes = [len(r) for r in rows_by_e]
+    padded = [((s + 127) // 128) * 128 for s in sizes]
+    offs = np.concatenate([[0], np.cumsum(padded)])
+    gathered = np.zeros((int(offs[-1]), H), np.uint16)
+    for e in range(E):
+        gathered[offs[e]:offs[e] + sizes[e]] = tokens[rows_by_e[e]]
+    ta = mxq.nvfp4_quantize_per_token(dev_bf16(gathered))
+    experts = [W.moe_expert(e, hidden=H, ffn=F) for e in range(E)]
+    tw = mxq.nvfp4_quantize_weight_shared(
+        [[dev_bf16(g), dev_bf16(u)] for g, u, _ in experts])
+    del experts
+    C = mxq.gemm_nvfp4_grouped(ta.codes, ta.block_scales, ta.scales, offs,
+                               tw.codes, tw.block_scales, tw.scales)
+    torch.cuda.synchronize()
+    Mt = int(offs[-1])
+    a_codes = host_u8(ta.codes)
+    a_sc = O.scale_unswizzle(host_u8(ta.block_scales), Mt, H // 16)
+    a_S = ta.scales.cpu().numpy()
+    Cn = C.cpu().numpy()
+    for e in (0, 17, 64, 127):
+        r0, r1 = int(offs[e]), int(offs[e]) + sizes[e]
+        w_sc = O.scale_unswizzle(host_u8(tw.block_scales[e]), 2 * F, H // 16)
+        ref = O.gemm_nvfp4_grouped(a_codes[r0:r1], a_sc[r0:r1], a_S[r0:r1],
+                                   [0, r1 - r0], host_u8(tw.codes[e])[None],
+                                   w_sc[None], tw.scales.cpu().numpy()[e:e + 1])
+        assert rel_fro(Cn[r0:r1].astype(np.float64), ref) <= TOL, e
