@@ -14,21 +14,29 @@
 //           sum_k a[r, k] w_e[n, k], where a and w are E2M1 x E4M3 block
 //           values and the two FP32 scales are applied in the epilogue.
 //
-// Design (one 128 x 128 output tile per CTA, 4 warps):
+// Design (persistent, one CTA per SM, 128 x 128 output tiles, 7 warps):
 //  * warp 0 lane 0 streams K-stages into a 4-deep shared-memory ring: the
 //    A and B code tiles by 2-D TMA with the 128-byte swizzle (one 128-byte
 //    row per matrix row), and the matching 512-byte scale tiles, which the
 //    quantizers already store in the 128x4 layout the tensor core reads, by
 //    1-D bulk copies; completion on mbarriers.
+//  * warp 2 polls the stage and accumulator barriers and hands each ready
+//    stage to warp 1 through a named barrier, so that the MMA-issuing
+//    thread never waits on shared memory between MMAs;
 //  * warp 1 lane 0 copies each stage's scale tiles into tensor memory
 //    (tcgen05.cp 32x128b.warpx4) and issues the block-scaled MMAs
 //    (tcgen05.mma kind::mxf8f6f4 block_scale, or kind::mxf4nvf4 with
 //    4 E4M3 scales per 64 values); the fp32 accumulator lives in tensor
-//    memory; tcgen05.commit frees each stage when its MMAs are done.
-//  * all 4 warps then read the accumulator with tcgen05.ld (each warp its
-//    32 lanes = 32 rows), scale (NVFP4) and store fp32 C.
+//    memory, double-buffered so that the epilogue of one tile overlaps the
+//    MMAs of the next; tcgen05.commit frees each stage when its MMAs are
+//    done and hands each finished accumulator to the epilogue.
+//  * warps 3-6 read the accumulator with tcgen05.ld (each warp its 32-lane
+//    quarter = 32 rows), scale (NVFP4), store fp32 C and release the
+//    accumulator buffer.
 // Every wait is bounded; on timeout the kernel records the error word and
 // skips the remaining work (still freeing its tensor memory).
+//  * C leaves through 32 x 32 fp32 TMA stores from 128-byte-swizzled
+//    staging boxes (whole 128-byte rows per global write).
 #include "common.cuh"
 #include "launch.h"
 
@@ -42,18 +50,22 @@ constexpr int GM = 128;              // tile rows (A) = MMA M
 constexpr int GN = 128;              // tile cols (B rows) = MMA N
 constexpr int GKB = 128;             // bytes of K per stage per row
 constexpr int GSTAGES = 4;
-constexpr int GTHREADS = 128;
-constexpr uint32_t kTmemCols = 256;  // accumulator 128 + scales 8/stage
-constexpr uint32_t kSfCol0 = 128;
+constexpr int GTHREADS = 224;  // producer, MMA issuer, waiter, 4 epilogue warps
+constexpr uint32_t kTmemCols = 512;  // 2 accumulators x 128 + scale columns
+constexpr uint32_t kSfCol0 = 256;    // 32 scale columns per stage
 
 struct alignas(1024) GemmSmem {
   uint8_t a[GSTAGES][GM * GKB];
   uint8_t b[GSTAGES][GN * GKB];
+  // Epilogue staging: per epilogue warp two 32 x 32 fp32 boxes in the
+  // 128-byte-swizzled layout the C tensor map stores from.
+  uint8_t cst[4][2][32 * 128];
   alignas(16) uint8_t sfa[GSTAGES][4][512];
   alignas(16) uint8_t sfb[GSTAGES][4][512];
   alignas(8) uint64_t full[GSTAGES];
   alignas(8) uint64_t empty[GSTAGES];
-  alignas(8) uint64_t done;
+  alignas(8) uint64_t acc_full[2];
+  alignas(8) uint64_t acc_empty[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -143,6 +155,46 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src,
       : "memory");
 }
 
+// Stage handoff between the waiter warp and the MMA warp: both warps
+// (converged) meet at named barrier 1; the result is the OR of the abort
+// flags the two warps bring.
+__device__ __forceinline__ bool stage_handoff(bool abort_in) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 64, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)abort_in)
+      : "memory");
+  return r != 0;
+}
+
+// Shared -> global 2-D tensor store, tracked by the issuing thread's bulk
+// groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map,
+                                             uint32_t src, int32_t x,
+                                             int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, "
+      "%2}], [%3];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most one committed store group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Generic-proxy shared-memory writes -> visible to the bulk-copy engine.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor (sm_100 family): start address, leading
 // and stride byte offsets (all >> 4), version 1 at bit 46, layout type at
 // bits 61-63 (0 = no swizzle, 2 = 128-byte swizzle).
@@ -184,30 +236,42 @@ struct GemmParams {
   int64_t tile_end[257];    // prefix sums of the M-tiles of each group
   int64_t row_off[257];     // first row of each group
   int64_t tiles_n;
+  int64_t n_tiles;
   float* C;
   int64_t ldc;
 };
 
+struct Tile {
+  int64_t m0, n0;
+  int grp;
+};
+
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, int64_t tile) {
+  const int64_t mt_all = tile / p.tiles_n;
+  const int64_t nt = tile - mt_all * p.tiles_n;
+  Tile t;
+  t.grp = 0;
+  if (p.kind == 1)
+    while (t.grp + 1 < p.num_groups && mt_all >= p.tile_end[t.grp]) ++t.grp;
+  const int64_t mt_in =
+      p.kind == 1 ? mt_all - (t.grp ? p.tile_end[t.grp - 1] : 0) : mt_all;
+  t.m0 = (p.kind == 1 ? p.row_off[t.grp] : 0) + mt_in * GM;
+  t.n0 = nt * GN;
+  return t;
+}
+
+// Persistent: CTA b handles tiles b, b + grid, ...  Two fp32 accumulators
+// in tensor memory let the epilogue warps drain tile i while the MMA warp
+// already accumulates tile i + 1.
 __global__ void __launch_bounds__(GTHREADS, 1)
     gemm_block_scaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
                              const __grid_constant__ CUtensorMap tmap_b,
+                             const __grid_constant__ CUtensorMap tmap_c,
                              const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t gsmem_raw[];
   GemmSmem& s = *reinterpret_cast<GemmSmem*>(
       (reinterpret_cast<uintptr_t>(gsmem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // Tile coordinates: (group, m-tile within the group, n-tile).
-  const int64_t tile = blockIdx.x;
-  const int64_t mt_all = tile / p.tiles_n;
-  const int64_t nt = tile - mt_all * p.tiles_n;
-  int grp = 0;
-  if (p.kind == 1)
-    while (grp + 1 < p.num_groups && mt_all >= p.tile_end[grp]) ++grp;
-  const int64_t mt_in = p.kind == 1 ? mt_all - (grp ? p.tile_end[grp - 1] : 0)
-                                    : mt_all;
-  const int64_t m0 = (p.kind == 1 ? p.row_off[grp] : 0) + mt_in * GM;
-  const int64_t n0 = nt * GN;
 
   if (warp == 0) tmem_alloc(smem_addr(&s.tmem_base), kTmemCols);
   if (threadIdx.x == 0) {
@@ -215,7 +279,10 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       mbar_init(smem_addr(&s.full[i]), 1);
       mbar_init(smem_addr(&s.empty[i]), 1);
     }
-    mbar_init(smem_addr(&s.done), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&s.acc_full[i]), 1);
+      mbar_init(smem_addr(&s.acc_empty[i]), 4);
+    }
     s.abort = 0;
     fence_barrier_init();
   }
@@ -228,102 +295,188 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   const int n_sf = p.kind == 1 ? 4 : 1;      // scale tiles per stage
   const uint32_t stage_bytes = 2 * GM * GKB + 2 * 512 * n_sf;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- producer ----------------
-    for (int64_t kt = 0; kt < p.k_stages; ++kt) {
-      const int st = (int)(kt % GSTAGES);
-      const uint32_t ph = (uint32_t)((kt / GSTAGES) & 1);
-      if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1, &s.abort,
-                     &g_gemm_wait_error))
-        break;
-      const uint32_t full = smem_addr(&s.full[st]);
-      mbar_arrive_expect_tx(full, stage_bytes);
-      tma_load_2d(smem_addr(s.a[st]), &tmap_a, (int32_t)(kt * GKB),
-                  (int32_t)m0, full);
-      tma_load_2d(smem_addr(s.b[st]), &tmap_b, (int32_t)(kt * GKB),
-                  (int32_t)(grp * p.b_rows_group_stride + n0), full);
-      for (int j = 0; j < n_sf; ++j) {
-        const int64_t ct = kt * n_sf + j;
-        bulk_g2s(smem_addr(s.sfa[st][j]),
-                 p.a_sf + ((m0 / 128) * p.a_sf_ct + ct) * 512, 512, full);
-        bulk_g2s(smem_addr(s.sfb[st][j]),
-                 p.b_sf + grp * p.b_sf_group_stride +
-                     ((n0 / 128) * p.b_sf_ct + ct) * 512,
-                 512, full);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- producer ----------------
+      int64_t it = 0;
+      for (int64_t tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile(p, tile);
+        for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
+          const int st = (int)(it % GSTAGES);
+          const uint32_t ph = (uint32_t)((it / GSTAGES) & 1);
+          if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1, &s.abort,
+                         &g_gemm_wait_error))
+            break;
+          const uint32_t full = smem_addr(&s.full[st]);
+          mbar_arrive_expect_tx(full, stage_bytes);
+          tma_load_2d(smem_addr(s.a[st]), &tmap_a, (int32_t)(kt * GKB),
+                      (int32_t)t.m0, full);
+          tma_load_2d(smem_addr(s.b[st]), &tmap_b, (int32_t)(kt * GKB),
+                      (int32_t)(t.grp * p.b_rows_group_stride + t.n0), full);
+          for (int j = 0; j < n_sf; ++j) {
+            const int64_t ct = kt * n_sf + j;
+            bulk_g2s(smem_addr(s.sfa[st][j]),
+                     p.a_sf + ((t.m0 / 128) * p.a_sf_ct + ct) * 512, 512, full);
+            bulk_g2s(smem_addr(s.sfb[st][j]),
+                     p.b_sf + t.grp * p.b_sf_group_stride +
+                         ((t.n0 / 128) * p.b_sf_ct + ct) * 512,
+                     512, full);
+          }
+        }
+        if (s.abort) break;
       }
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    for (int64_t kt = 0; kt < p.k_stages; ++kt) {
-      const int st = (int)(kt % GSTAGES);
-      const uint32_t ph = (uint32_t)((kt / GSTAGES) & 1);
-      if (!mbar_wait(smem_addr(&s.full[st]), ph, &s.abort, &g_gemm_wait_error))
-        break;
-      tc_fence_after();
-      const uint32_t sf_col = tmem + kSfCol0 + (uint32_t)st * 32;
-      for (int j = 0; j < n_sf; ++j) {
-        tc_cp_sf(sf_col + j * 4, smem_desc(smem_addr(s.sfa[st][j]), 16, 128, 0));
-        tc_cp_sf(sf_col + 16 + j * 4,
-                 smem_desc(smem_addr(s.sfb[st][j]), 16, 128, 0));
-      }
-      const uint32_t a_addr = smem_addr(s.a[st]);
-      const uint32_t b_addr = smem_addr(s.b[st]);
-      // Four MMAs per stage, each 32 bytes of K further along the
-      // 128-byte swizzled rows.
-      for (int j = 0; j < 4; ++j) {
-        const uint64_t ad = smem_desc(a_addr + j * 32, 16, 1024, 2);
-        const uint64_t bd = smem_desc(b_addr + j * 32, 16, 1024, 2);
-        const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
-        if (p.kind == 0) {
-          // 8-bit operands: K = 32 per MMA, one E8M0 scale per row per
-          // MMA: byte j of the stage's 32-bit scale cell.
-          tc_mma_mxf8(tmem, ad, bd, idesc_block_scaled(0, 0, 1, (uint32_t)j),
-                      sf_col, sf_col + 16, acc);
-        } else {
-          // 4-bit operands: K = 64 per MMA, four E4M3 scales per row (one
-          // 32-bit cell = one scale tile column group j).
-          tc_mma_nvf4(tmem, ad, bd, idesc_block_scaled(1, 1, 0, 0),
-                      sf_col + j * 4, sf_col + 16 + j * 4, acc);
+    // The issuing thread touches no shared memory between MMAs: while the
+    // tensor core streams operands out of shared memory, an mbarrier poll
+    // from this thread stalls behind those reads and the MMA queue runs
+    // dry.  The waiter warp polls instead and hands each ready stage over
+    // through a named barrier, which carries the abort flag as well.
+    int64_t it = 0;
+    int local = 0;
+    bool aborted = false;
+    for (int64_t tile = blockIdx.x; tile < p.n_tiles && !aborted;
+         tile += gridDim.x, ++local) {
+      const int buf = local & 1;
+      const uint32_t d = tmem + (uint32_t)buf * GN;
+      for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
+        __syncwarp();
+        if (stage_handoff(false)) {
+          aborted = true;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const int st = (int)(it % GSTAGES);
+          const uint32_t sf_col = tmem + kSfCol0 + (uint32_t)st * 32;
+          for (int j = 0; j < n_sf; ++j) {
+            tc_cp_sf(sf_col + j * 4,
+                     smem_desc(smem_addr(s.sfa[st][j]), 16, 128, 0));
+            tc_cp_sf(sf_col + 16 + j * 4,
+                     smem_desc(smem_addr(s.sfb[st][j]), 16, 128, 0));
+          }
+          const uint32_t a_addr = smem_addr(s.a[st]);
+          const uint32_t b_addr = smem_addr(s.b[st]);
+          // Four MMAs per stage, each 32 bytes of K further along the
+          // 128-byte swizzled rows.
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t ad = smem_desc(a_addr + j * 32, 16, 1024, 2);
+            const uint64_t bd = smem_desc(b_addr + j * 32, 16, 1024, 2);
+            const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
+            if (p.kind == 0) {
+              // 8-bit operands: K = 32 per MMA, one E8M0 scale per row per
+              // MMA: byte j of the stage's 32-bit scale cell.
+              tc_mma_mxf8(d, ad, bd, idesc_block_scaled(0, 0, 1, (uint32_t)j),
+                          sf_col, sf_col + 16, acc);
+            } else {
+              // 4-bit operands: K = 64 per MMA, four E4M3 scales per row (one
+              // 32-bit cell = scale tile j).
+              tc_mma_nvf4(d, ad, bd, idesc_block_scaled(1, 1, 0, 0),
+                          sf_col + j * 4, sf_col + 16 + j * 4, acc);
+            }
+          }
+          tc_commit(smem_addr(&s.empty[st]));
+          if (kt == p.k_stages - 1) tc_commit(smem_addr(&s.acc_full[buf]));
         }
       }
-      tc_commit(smem_addr(&s.empty[st]));
     }
-    tc_commit(smem_addr(&s.done));
+  } else if (warp == 2) {
+    // ---------------- waiter ----------------
+    // Mirrors the issuer's loop: before a tile's first stage it waits until
+    // the epilogue has released the accumulator buffer, before every stage
+    // until the stage's operands have landed; then one handoff.
+    int64_t it = 0;
+    int local = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; tile < p.n_tiles && ok;
+         tile += gridDim.x, ++local) {
+      const int buf = local & 1;
+      const uint32_t acc_ph = (uint32_t)((local >> 1) & 1);
+      if (lane == 0)
+        ok = mbar_wait(smem_addr(&s.acc_empty[buf]), acc_ph ^ 1, &s.abort,
+                       &g_gemm_wait_error);
+      for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
+        const int st = (int)(it % GSTAGES);
+        const uint32_t ph = (uint32_t)((it / GSTAGES) & 1);
+        if (lane == 0 && ok)
+          ok = mbar_wait(smem_addr(&s.full[st]), ph, &s.abort,
+                         &g_gemm_wait_error);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        if (stage_handoff(!ok)) {
+          ok = false;
+          break;
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 3-6, one 32-lane quarter each ------
+    // Tensor-memory lane quarter = warp id mod 4; lane = tile row.  Each
+    // 32 x 32 fp32 box goes registers -> swizzled staging -> TMA store, so
+    // global writes are whole 128-byte rows; the two staging boxes of a
+    // warp alternate.
+    const int q = warp & 3;
+    int local = 0;
+    uint32_t nbox = 0;
+    for (int64_t tile = blockIdx.x; tile < p.n_tiles;
+         tile += gridDim.x, ++local) {
+      const int buf = local & 1;
+      const uint32_t acc_ph = (uint32_t)((local >> 1) & 1);
+      const bool ok = __all_sync(
+          0xffffffffu, mbar_wait(smem_addr(&s.acc_full[buf]), acc_ph,
+                                 &s.abort, &g_gemm_wait_error));
+      if (!ok) break;
+      tc_fence_after();
+      const Tile t = decode_tile(p, tile);
+      float rs = 1.0f;
+      if (p.kind == 1)
+        rs = __fmul_rn(p.s_tok[t.m0 + q * 32 + lane], p.s_w[t.grp]);
+      for (int c = 0; c < GN; c += 32, ++nbox) {
+        uint32_t r[32];
+        tc_ld_32x32(tmem + ((uint32_t)(q * 32) << 16) +
+                        (uint32_t)(buf * GN + c),
+                    r);
+        if (c == GN - 32) {
+          // Last read of this accumulator: hand it back to the MMA warp.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&s.acc_empty[buf]));
+        }
+        uint8_t* box = s.cst[q][nbox & 1];
+        if (lane == 0) bulk_wait_read_1();   // the box's previous store
+        __syncwarp();
+        uint8_t* row = box + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float4 v;
+          v.x = __uint_as_float(r[4 * j]);
+          v.y = __uint_as_float(r[4 * j + 1]);
+          v.z = __uint_as_float(r[4 * j + 2]);
+          v.w = __uint_as_float(r[4 * j + 3]);
+          if (p.kind == 1) {
+            v.x = __fmul_rn(v.x, rs);
+            v.y = __fmul_rn(v.y, rs);
+            v.z = __fmul_rn(v.z, rs);
+            v.w = __fmul_rn(v.w, rs);
+          }
+          *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmap_c, smem_addr(box), (int32_t)(t.n0 + c),
+                       (int32_t)(t.m0 + q * 32));
+          bulk_commit();
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();
   }
   __syncwarp();
-
-  // ---------------- epilogue: 4 warps x 32 rows ----------------
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&s.done), 0,
-                                                     &s.abort,
-                                                     &g_gemm_wait_error));
-  tc_fence_after();
-  if (ok) {
-    const int64_t row = m0 + warp * 32 + lane;
-    float rs = 1.0f;
-    if (p.kind == 1) rs = __fmul_rn(p.s_tok[row], p.s_w[grp]);
-    float* crow = p.C + row * p.ldc + n0;
-    for (int c = 0; c < GN; c += 32) {
-      uint32_t r[32];
-      tc_ld_32x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, r);
-#pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        float4 v;
-        v.x = __uint_as_float(r[i]);
-        v.y = __uint_as_float(r[i + 1]);
-        v.z = __uint_as_float(r[i + 2]);
-        v.w = __uint_as_float(r[i + 3]);
-        if (p.kind == 1) {
-          v.x = __fmul_rn(v.x, rs);
-          v.y = __fmul_rn(v.y, rs);
-          v.z = __fmul_rn(v.z, rs);
-          v.w = __fmul_rn(v.w, rs);
-        }
-        *reinterpret_cast<float4*>(crow + c + i) = v;
-      }
-    }
-  }
   tc_fence_before();
   __syncthreads();
+  tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
   pdl_launch_dependents();
 }
@@ -335,9 +488,19 @@ cudaError_t make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner,
   return make_tmap_2d_bytes(map, base, inner, outer, stride_bytes, GKB, GM);
 }
 
+// fp32 C [rows x cols] with row stride ldc floats, stored in 32 x 32 boxes.
+cudaError_t make_tmap_c(CUtensorMap* map, float* C, int64_t rows,
+                        int64_t cols, int64_t ldc) {
+  return make_tmap_2d_f32(map, C, (uint64_t)cols, (uint64_t)rows,
+                          (uint64_t)ldc * 4, 32, 32);
+}
+
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb,
                         const GemmParams& p, int64_t tiles,
                         cudaStream_t stream) {
+  CUtensorMap tc;
+  cudaError_t cerr = make_tmap_c(&tc, p.C, p.M, p.N, p.ldc);
+  if (cerr != cudaSuccess) return cerr;
   const size_t smem = gemm_smem_bytes();
   static int configured[64] = {};
   int dev = 0;
@@ -350,8 +513,11 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb,
     if (err != cudaSuccess) return err;
     configured[dev] = 1;
   }
-  return launch_pdl(gemm_block_scaled_kernel, dim3((unsigned)tiles),
-                    dim3(GTHREADS), smem, stream, false, ta, tb, p);
+  GemmParams pp = p;
+  pp.n_tiles = tiles;
+  const int64_t grid = imin<int64_t>(tiles, (int64_t)sm_count(dev));
+  return launch_pdl(gemm_block_scaled_kernel, dim3((unsigned)grid),
+                    dim3(GTHREADS), smem, stream, false, ta, tb, tc, pp);
 }
 
 }  // namespace

@@ -23,6 +23,11 @@ cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base,
                               uint64_t inner, uint64_t outer,
                               uint64_t outer_stride_bytes, uint32_t box_inner,
                               uint32_t box_outer, bool swizzle128);
+// fp32 matrix, 128-byte swizzle (box_inner * 4 <= 128).
+cudaError_t make_tmap_2d_f32(CUtensorMap* map, const void* base,
+                             uint64_t inner, uint64_t outer,
+                             uint64_t outer_stride_bytes, uint32_t box_inner,
+                             uint32_t box_outer);
 
 // mxfp8.cu
 // Reads (and clears when set) the error word of the bounded device waits.

@@ -105,6 +105,32 @@ def test_gemm_nvfp4_grouped_small(mxq, rows, K, N):
     assert err <= TOL, err
 
 
+def test_gemm_mxfp8_many_tiles_per_cta(mxq):
+    """320 output tiles over at most 152 persistent CTAs: every CTA runs
+    two or three tiles, alternating its two tensor-memory accumulators,
+    and the 3-stage K loop wraps the 4-deep operand ring across tiles.
+    Every element of C is checked."""
+    C, ref = _mxfp8_case(mxq, 2048, 384, 2560, seed=11)
+    assert rel_fro(C, ref) <= TOL
+    # no tile may be left unwritten or written twice with the wrong data:
+    # a per-tile check catches an error hidden by the global norm
+    for i in range(0, 2048, 128):
+        for j in range(0, 2560, 128):
+            assert rel_fro(C[i:i + 128, j:j + 128],
+                           ref[i:i + 128, j:j + 128]) <= TOL, (i, j)
+
+
+def test_gemm_nvfp4_grouped_many_tiles_per_cta(mxq):
+    """Ragged expert groups (one empty) giving 38 row tiles x 8 column
+    tiles = 304 tiles, K = 512 (two stages per tile): several tiles per
+    persistent CTA, tiles that straddle group boundaries in the schedule."""
+    rows = [128 * 7, 0, 128 * 13, 256, 128 * 5, 128 * 11]
+    C, ref = _nvfp4_grouped_case(mxq, rows, 512, 1024, seed=5)
+    assert rel_fro(C, ref) <= TOL
+    for i in range(0, C.shape[0], 128):
+        assert rel_fro(C[i:i + 128], ref[i:i + 128]) <= TOL, i
+
+
 def test_gemm_mxfp8_full_size_sampled(mxq):
     """A [2048 x 2048] N(0,1) times B [2048 x 8192] N(0, 0.02), B consumed
     through its columnwise copy; 256 sampled rows of C vs the oracle."""
