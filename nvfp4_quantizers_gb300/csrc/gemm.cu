@@ -155,6 +155,41 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src,
       : "memory");
 }
 
+// 2-D TMA load delivered to the same shared-memory offset (and completing
+// on the same mbarrier offset) in every CTA of the cluster named in mask.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst,
+                                               const CUtensorMap* map,
+                                               int32_t x, int32_t y,
+                                               uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_"
+      "tx::bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar),
+      "h"(mask)
+      : "memory");
+}
+// Arrive on the mbarrier at this offset in every CTA of mask once all
+// previously issued tcgen05 operations of this thread have completed.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
+      "multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA in the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
 // Stage handoff between the waiter warp and the MMA warp: both warps
 // (converged) meet at named barrier 1; the result is the OR of the abort
 // flags the two warps bring.
@@ -189,10 +224,6 @@ __device__ __forceinline__ void bulk_wait_read_1() {
 }
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-// Generic-proxy shared-memory writes -> visible to the bulk-copy engine.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor (sm_100 family): start address, leading
@@ -246,13 +277,17 @@ struct Tile {
   int grp;
 };
 
-__device__ __forceinline__ Tile decode_tile(const GemmParams& p, int64_t tile) {
+// Tile index -> operand coordinates.  Each thread visits its tiles in
+// increasing order, so the group is found by advancing a cursor (*grp)
+// that the caller keeps across calls, instead of scanning from group 0.
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, int64_t tile,
+                                            int* grp) {
   const int64_t mt_all = tile / p.tiles_n;
   const int64_t nt = tile - mt_all * p.tiles_n;
   Tile t;
-  t.grp = 0;
   if (p.kind == 1)
-    while (t.grp + 1 < p.num_groups && mt_all >= p.tile_end[t.grp]) ++t.grp;
+    while (*grp + 1 < p.num_groups && mt_all >= p.tile_end[*grp]) ++*grp;
+  t.grp = *grp;
   const int64_t mt_in =
       p.kind == 1 ? mt_all - (t.grp ? p.tile_end[t.grp - 1] : 0) : mt_all;
   t.m0 = (p.kind == 1 ? p.row_off[t.grp] : 0) + mt_in * GM;
@@ -260,9 +295,13 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int64_t tile) {
   return t;
 }
 
-// Persistent: CTA b handles tiles b, b + grid, ...  Two fp32 accumulators
-// in tensor memory let the epilogue warps drain tile i while the MMA warp
-// already accumulates tile i + 1.
+// Persistent: cluster c of CL CTAs handles tile groups u = c, c + grid/CL,
+// ...; CTA rank r of the cluster takes tile u * CL + r.  The CL tiles of a
+// group share their A rows (tiles_n is a multiple of CL), so with CL = 2
+// each CTA loads half of the A stage and multicasts it to both.  Two fp32
+// accumulators in tensor memory let the epilogue warps drain tile i while
+// the MMA warp already accumulates tile i + 1.
+template <int CL>
 __global__ void __launch_bounds__(GTHREADS, 1)
     gemm_block_scaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
                              const __grid_constant__ CUtensorMap tmap_b,
@@ -277,7 +316,8 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < GSTAGES; ++i) {
       mbar_init(smem_addr(&s.full[i]), 1);
-      mbar_init(smem_addr(&s.empty[i]), 1);
+      // freed by the MMA commits of every CTA that writes this slot
+      mbar_init(smem_addr(&s.empty[i]), CL);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&s.acc_full[i]), 1);
@@ -289,7 +329,14 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The peer's multicast loads and commits target this CTA's barriers:
+  // they must be initialised cluster-wide before anyone issues one.
+  if (CL > 1) cluster_sync();
   const uint32_t tmem = s.tmem_base;
+  const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
+  const uint16_t cmask = (uint16_t)((1u << CL) - 1u);
+  const int64_t n_units = p.n_tiles / CL;
+  const int64_t unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
   pdl_wait();
 
   const int n_sf = p.kind == 1 ? 4 : 1;      // scale tiles per stage
@@ -299,8 +346,9 @@ __global__ void __launch_bounds__(GTHREADS, 1)
     if (lane == 0) {
       // ---------------- producer ----------------
       int64_t it = 0;
-      for (int64_t tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x) {
-        const Tile t = decode_tile(p, tile);
+      int grp_cursor = 0;
+      for (int64_t u = unit0; u < n_units; u += unit_step) {
+        const Tile t = decode_tile(p, u * CL + crank, &grp_cursor);
         for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
           const int st = (int)(it % GSTAGES);
           const uint32_t ph = (uint32_t)((it / GSTAGES) & 1);
@@ -309,21 +357,39 @@ __global__ void __launch_bounds__(GTHREADS, 1)
             break;
           const uint32_t full = smem_addr(&s.full[st]);
           mbar_arrive_expect_tx(full, stage_bytes);
-          tma_load_2d(smem_addr(s.a[st]), &tmap_a, (int32_t)(kt * GKB),
-                      (int32_t)t.m0, full);
+          if (CL == 1) {
+            tma_load_2d(smem_addr(s.a[st]), &tmap_a, (int32_t)(kt * GKB),
+                        (int32_t)t.m0, full);
+          } else {
+            // rows [crank * 64, crank * 64 + 64) of the A stage, to both CTAs
+            tma_load_2d_mc(smem_addr(s.a[st]) + crank * (GM / CL) * GKB,
+                           &tmap_a, (int32_t)(kt * GKB),
+                           (int32_t)(t.m0 + crank * (GM / CL)), full, cmask);
+          }
           tma_load_2d(smem_addr(s.b[st]), &tmap_b, (int32_t)(kt * GKB),
                       (int32_t)(t.grp * p.b_rows_group_stride + t.n0), full);
-          for (int j = 0; j < n_sf; ++j) {
-            const int64_t ct = kt * n_sf + j;
-            bulk_g2s(smem_addr(s.sfa[st][j]),
-                     p.a_sf + ((t.m0 / 128) * p.a_sf_ct + ct) * 512, 512, full);
-            bulk_g2s(smem_addr(s.sfb[st][j]),
-                     p.b_sf + t.grp * p.b_sf_group_stride +
-                         ((t.n0 / 128) * p.b_sf_ct + ct) * 512,
-                     512, full);
-          }
+          // The stage's n_sf scale tiles are consecutive in the swizzled
+          // layout (same 128-row block, consecutive column tiles): one copy
+          // per operand.
+          const int64_t ct = kt * n_sf;
+          bulk_g2s(smem_addr(s.sfa[st][0]),
+                   p.a_sf + ((t.m0 / 128) * p.a_sf_ct + ct) * 512,
+                   512u * n_sf, full);
+          bulk_g2s(smem_addr(s.sfb[st][0]),
+                   p.b_sf + t.grp * p.b_sf_group_stride +
+                       ((t.n0 / 128) * p.b_sf_ct + ct) * 512,
+                   512u * n_sf, full);
         }
         if (s.abort) break;
+      }
+      if (CL > 1) {
+        // Wait until both CTAs' MMAs have released every slot, so that no
+        // commit from the peer is still headed for this CTA's barriers
+        // when it exits.
+        for (int64_t j = it > GSTAGES ? it - GSTAGES : 0; j < it; ++j)
+          mbar_wait(smem_addr(&s.empty[j % GSTAGES]),
+                    (uint32_t)((j / GSTAGES) & 1), &s.abort,
+                    &g_gemm_wait_error);
       }
     }
   } else if (warp == 1) {
@@ -336,8 +402,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
     int64_t it = 0;
     int local = 0;
     bool aborted = false;
-    for (int64_t tile = blockIdx.x; tile < p.n_tiles && !aborted;
-         tile += gridDim.x, ++local) {
+    for (int64_t u = unit0; u < n_units && !aborted; u += unit_step, ++local) {
       const int buf = local & 1;
       const uint32_t d = tmem + (uint32_t)buf * GN;
       for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
@@ -376,7 +441,10 @@ __global__ void __launch_bounds__(GTHREADS, 1)
                           sf_col + j * 4, sf_col + 16 + j * 4, acc);
             }
           }
-          tc_commit(smem_addr(&s.empty[st]));
+          if (CL == 1)
+            tc_commit(smem_addr(&s.empty[st]));
+          else
+            tc_commit_mc(smem_addr(&s.empty[st]), cmask);
           if (kt == p.k_stages - 1) tc_commit(smem_addr(&s.acc_full[buf]));
         }
       }
@@ -389,8 +457,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
     int64_t it = 0;
     int local = 0;
     bool ok = true;
-    for (int64_t tile = blockIdx.x; tile < p.n_tiles && ok;
-         tile += gridDim.x, ++local) {
+    for (int64_t u = unit0; u < n_units && ok; u += unit_step, ++local) {
       const int buf = local & 1;
       const uint32_t acc_ph = (uint32_t)((local >> 1) & 1);
       if (lane == 0)
@@ -418,9 +485,9 @@ __global__ void __launch_bounds__(GTHREADS, 1)
     // warp alternate.
     const int q = warp & 3;
     int local = 0;
+    int grp_cursor = 0;
     uint32_t nbox = 0;
-    for (int64_t tile = blockIdx.x; tile < p.n_tiles;
-         tile += gridDim.x, ++local) {
+    for (int64_t u = unit0; u < n_units; u += unit_step, ++local) {
       const int buf = local & 1;
       const uint32_t acc_ph = (uint32_t)((local >> 1) & 1);
       const bool ok = __all_sync(
@@ -428,7 +495,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
                                  &s.abort, &g_gemm_wait_error));
       if (!ok) break;
       tc_fence_after();
-      const Tile t = decode_tile(p, tile);
+      const Tile t = decode_tile(p, u * CL + crank, &grp_cursor);
       float rs = 1.0f;
       if (p.kind == 1)
         rs = __fmul_rn(p.s_tok[t.m0 + q * 32 + lane], p.s_w[t.grp]);
@@ -477,6 +544,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (CL > 1) cluster_sync();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
   pdl_launch_dependents();
 }
@@ -484,8 +552,10 @@ __global__ void __launch_bounds__(GTHREADS, 1)
 size_t gemm_smem_bytes() { return sizeof(GemmSmem) + 1024; }
 
 cudaError_t make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner,
-                            uint64_t outer, uint64_t stride_bytes) {
-  return make_tmap_2d_bytes(map, base, inner, outer, stride_bytes, GKB, GM);
+                            uint64_t outer, uint64_t stride_bytes,
+                            uint32_t box_rows) {
+  return make_tmap_2d_bytes(map, base, inner, outer, stride_bytes, GKB,
+                            box_rows);
 }
 
 // fp32 C [rows x cols] with row stride ldc floats, stored in 32 x 32 boxes.
@@ -495,29 +565,78 @@ cudaError_t make_tmap_c(CUtensorMap* map, float* C, int64_t rows,
                           (uint64_t)ldc * 4, 32, 32);
 }
 
-cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb,
+// A operand as a byte matrix [a_rows x a_row_bytes].
+struct AOperand {
+  const uint8_t* base;
+  int64_t row_bytes, rows;
+};
+
+template <int CL>
+cudaError_t launch_gemm_cl(const AOperand& a, const CUtensorMap& tb,
+                           const CUtensorMap& tc, const GemmParams& pp,
+                           int dev, cudaStream_t stream) {
+  auto kern = gemm_block_scaled_kernel<CL>;
+  const size_t smem = gemm_smem_bytes();
+  static int configured[64] = {};
+  static int max_clusters[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(GTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CL > 1 ? 2 : 1;
+  if (!configured[dev]) {
+    cudaError_t err = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    int n = sm_count(dev) / CL;
+    if (CL > 1) {
+      // clusters that fit on the GPU at once (GPCs may leave SMs unpaired)
+      cfg.gridDim = dim3((unsigned)(n * CL));
+      int fit = 0;
+      if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess &&
+          fit > 0)
+        n = imin(n, fit);
+      else
+        cudaGetLastError();
+    }
+    max_clusters[dev] = n;
+    configured[dev] = 1;
+  }
+  CUtensorMap ta;
+  cudaError_t err = make_tmap_2d_u8(&ta, a.base, (uint64_t)a.row_bytes,
+                                    (uint64_t)a.rows, (uint64_t)a.row_bytes,
+                                    (uint32_t)(GM / CL));
+  if (err != cudaSuccess) return err;
+  const int64_t units = imin<int64_t>(pp.n_tiles / CL, max_clusters[dev]);
+  cfg.gridDim = dim3((unsigned)(units * CL));
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, pp);
+}
+
+// Tiles of one row block are paired across a 2-CTA cluster when the
+// column-tile count is even; otherwise one CTA per cluster.
+cudaError_t launch_gemm(const AOperand& a, const CUtensorMap& tb,
                         const GemmParams& p, int64_t tiles,
                         cudaStream_t stream) {
   CUtensorMap tc;
-  cudaError_t cerr = make_tmap_c(&tc, p.C, p.M, p.N, p.ldc);
-  if (cerr != cudaSuccess) return cerr;
-  const size_t smem = gemm_smem_bytes();
-  static int configured[64] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  cudaError_t err = make_tmap_c(&tc, p.C, p.M, p.N, p.ldc);
   if (err != cudaSuccess) return err;
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    err = cudaFuncSetAttribute(gemm_block_scaled_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
-    if (err != cudaSuccess) return err;
-    configured[dev] = 1;
-  }
+  int dev = 0;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
   GemmParams pp = p;
   pp.n_tiles = tiles;
-  const int64_t grid = imin<int64_t>(tiles, (int64_t)sm_count(dev));
-  return launch_pdl(gemm_block_scaled_kernel, dim3((unsigned)grid),
-                    dim3(GTHREADS), smem, stream, false, ta, tb, tc, pp);
+  if (p.tiles_n % 2 == 0)
+    return launch_gemm_cl<2>(a, tb, tc, pp, dev, stream);
+  return launch_gemm_cl<1>(a, tb, tc, pp, dev, stream);
 }
 
 }  // namespace
@@ -534,11 +653,9 @@ cudaError_t launch_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
                               const uint8_t* bt_scales, int64_t M, int64_t N,
                               int64_t K, float* C, int64_t ldc,
                               cudaStream_t stream) {
-  CUtensorMap ta, tb;
-  cudaError_t err = make_tmap_2d_u8(&ta, a_codes, (uint64_t)K, (uint64_t)M,
-                                    (uint64_t)K);
-  if (err != cudaSuccess) return err;
-  err = make_tmap_2d_u8(&tb, bt_codes, (uint64_t)K, (uint64_t)N, (uint64_t)K);
+  CUtensorMap tb;
+  cudaError_t err = make_tmap_2d_u8(&tb, bt_codes, (uint64_t)K, (uint64_t)N,
+                                    (uint64_t)K, GN);
   if (err != cudaSuccess) return err;
   GemmParams p = {};
   p.kind = 0;
@@ -556,7 +673,8 @@ cudaError_t launch_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
   p.tiles_n = N / GN;
   p.C = C;
   p.ldc = ldc;
-  return launch_gemm(ta, tb, p, (M / GM) * p.tiles_n, stream);
+  return launch_gemm(AOperand{a_codes, K, M}, tb, p, (M / GM) * p.tiles_n,
+                     stream);
 }
 
 cudaError_t launch_gemm_nvfp4_grouped(
@@ -565,14 +683,12 @@ cudaError_t launch_gemm_nvfp4_grouped(
     const uint8_t* w_scales, const float* w_s, int64_t N, int64_t K, float* C,
     int64_t ldc, cudaStream_t stream) {
   const int64_t m_total = group_offsets[num_groups];
-  CUtensorMap ta, tb;
+  CUtensorMap tb;
   // Packed E2M1: K/2 bytes per row; all groups' weights as one
   // [num_groups * N x K/2] byte matrix.
-  cudaError_t err = make_tmap_2d_u8(&ta, a_codes, (uint64_t)(K / 2),
-                                    (uint64_t)m_total, (uint64_t)(K / 2));
-  if (err != cudaSuccess) return err;
-  err = make_tmap_2d_u8(&tb, w_codes, (uint64_t)(K / 2),
-                        (uint64_t)(num_groups * N), (uint64_t)(K / 2));
+  cudaError_t err = make_tmap_2d_u8(&tb, w_codes, (uint64_t)(K / 2),
+                                    (uint64_t)(num_groups * N),
+                                    (uint64_t)(K / 2), GN);
   if (err != cudaSuccess) return err;
   GemmParams p = {};
   p.kind = 1;
@@ -599,7 +715,8 @@ cudaError_t launch_gemm_nvfp4_grouped(
   p.C = C;
   p.ldc = ldc;
   if (tiles_m == 0) return cudaSuccess;
-  return launch_gemm(ta, tb, p, tiles_m * p.tiles_n, stream);
+  return launch_gemm(AOperand{a_codes, K / 2, m_total}, tb, p,
+                     tiles_m * p.tiles_n, stream);
 }
 
 }  // namespace mxq
