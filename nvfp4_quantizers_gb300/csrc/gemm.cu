@@ -47,25 +47,28 @@ __device__ unsigned int g_gemm_wait_error = 0;
 namespace {
 
 constexpr int GM = 128;              // tile rows (A) = MMA M
-constexpr int GN = 128;              // tile cols (B rows) = MMA N
+constexpr int GN = 256;              // tile cols (B rows) = MMA N
 constexpr int GKB = 128;             // bytes of K per stage per row
-constexpr int GSTAGES = 4;
-constexpr int GTHREADS = 224;  // producer, MMA issuer, waiter, 4 epilogue warps
-constexpr uint32_t kTmemCols = 512;  // 2 accumulators x 128 + scale columns
-constexpr uint32_t kSfCol0 = 256;    // 32 scale columns per stage
+constexpr int GSTAGES = 3;
+constexpr int kEpiWarps = 8;         // 4 lane quarters x 2 column halves
+constexpr int GTHREADS = 32 * (3 + kEpiWarps);  // producer, MMA, waiter, epilogue
+constexpr uint32_t kTmemCols = 512;  // accumulator 256 + scale columns
+constexpr uint32_t kSfCol0 = 256;    // 64 scale columns per stage
+constexpr uint32_t kSfColsPerStage = 64;
 
 struct alignas(1024) GemmSmem {
   uint8_t a[GSTAGES][GM * GKB];
   uint8_t b[GSTAGES][GN * GKB];
-  // Epilogue staging: per epilogue warp two 32 x 32 fp32 boxes in the
+  // Epilogue staging: one 32 x 32 fp32 box per epilogue warp in the
   // 128-byte-swizzled layout the C tensor map stores from.
-  uint8_t cst[4][2][32 * 128];
+  uint8_t cst[kEpiWarps][32 * 128];
+  // scale tiles of the stage: A [tile j], B [128-row block][tile j]
   alignas(16) uint8_t sfa[GSTAGES][4][512];
-  alignas(16) uint8_t sfb[GSTAGES][4][512];
+  alignas(16) uint8_t sfb[GSTAGES][2][4][512];
   alignas(8) uint64_t full[GSTAGES];
   alignas(8) uint64_t empty[GSTAGES];
-  alignas(8) uint64_t acc_full[2];
-  alignas(8) uint64_t acc_empty[2];
+  alignas(8) uint64_t acc_full;
+  alignas(8) uint64_t acc_empty;
   uint32_t tmem_base;
   int abort;
 };
@@ -128,6 +131,27 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d, uint64_t adesc,
       "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns of tensor memory -> registers
+// (completion: tc_wait_ld).
+__device__ __forceinline__ void tc_ld_32x32_async(uint32_t taddr,
+                                                  uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, "
+      "%7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, "
+      "%21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+        "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
+        "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 // 32 lanes x 32 consecutive 32-bit columns of tensor memory -> registers.
 __device__ __forceinline__ void tc_ld_32x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -218,9 +242,9 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map,
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// Wait until at most one committed store group still reads shared memory.
-__device__ __forceinline__ void bulk_wait_read_1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+// Wait until no committed store group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -298,9 +322,12 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int64_t tile,
 // Persistent: cluster c of CL CTAs handles tile groups u = c, c + grid/CL,
 // ...; CTA rank r of the cluster takes tile u * CL + r.  The CL tiles of a
 // group share their A rows (tiles_n is a multiple of CL), so with CL = 2
-// each CTA loads half of the A stage and multicasts it to both.  Two fp32
-// accumulators in tensor memory let the epilogue warps drain tile i while
-// the MMA warp already accumulates tile i + 1.
+// each CTA loads half of the A stage and multicasts it to both.
+//
+// One 128 x 256 fp32 accumulator in tensor memory.  The eight epilogue
+// warps copy it to registers (128 values per thread) and hand it back to
+// the MMA warp at once, then scale and store while the next tile's MMAs
+// already run.
 template <int CL>
 __global__ void __launch_bounds__(GTHREADS, 1)
     gemm_block_scaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -319,10 +346,8 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       // freed by the MMA commits of every CTA that writes this slot
       mbar_init(smem_addr(&s.empty[i]), CL);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_addr(&s.acc_full[i]), 1);
-      mbar_init(smem_addr(&s.acc_empty[i]), 4);
-    }
+    mbar_init(smem_addr(&s.acc_full), 1);
+    mbar_init(smem_addr(&s.acc_empty), kEpiWarps);
     s.abort = 0;
     fence_barrier_init();
   }
@@ -339,8 +364,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   const int64_t unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
   pdl_wait();
 
-  const int n_sf = p.kind == 1 ? 4 : 1;      // scale tiles per stage
-  const uint32_t stage_bytes = 2 * GM * GKB + 2 * 512 * n_sf;
+  const int n_sf = p.kind == 1 ? 4 : 1;  // scale tiles per stage and row block
 
   if (warp == 0) {
     if (lane == 0) {
@@ -349,6 +373,11 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       int grp_cursor = 0;
       for (int64_t u = unit0; u < n_units; u += unit_step) {
         const Tile t = decode_tile(p, u * CL + crank, &grp_cursor);
+        // B row blocks of this tile that exist (the last column tile may
+        // hold only 128 columns); rows past them are never stored.
+        const int nrb = t.n0 + 128 < p.N ? 2 : 1;
+        const uint32_t stage_bytes =
+            (uint32_t)(GM * GKB + GN * GKB + 512 * n_sf * (1 + nrb));
         for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
           const int st = (int)(it % GSTAGES);
           const uint32_t ph = (uint32_t)((it / GSTAGES) & 1);
@@ -368,17 +397,17 @@ __global__ void __launch_bounds__(GTHREADS, 1)
           }
           tma_load_2d(smem_addr(s.b[st]), &tmap_b, (int32_t)(kt * GKB),
                       (int32_t)(t.grp * p.b_rows_group_stride + t.n0), full);
-          // The stage's n_sf scale tiles are consecutive in the swizzled
-          // layout (same 128-row block, consecutive column tiles): one copy
-          // per operand.
+          // The stage's n_sf scale tiles of one 128-row block are
+          // consecutive in the swizzled layout: one copy per row block.
           const int64_t ct = kt * n_sf;
           bulk_g2s(smem_addr(s.sfa[st][0]),
                    p.a_sf + ((t.m0 / 128) * p.a_sf_ct + ct) * 512,
                    512u * n_sf, full);
-          bulk_g2s(smem_addr(s.sfb[st][0]),
-                   p.b_sf + t.grp * p.b_sf_group_stride +
-                       ((t.n0 / 128) * p.b_sf_ct + ct) * 512,
-                   512u * n_sf, full);
+          for (int rb = 0; rb < nrb; ++rb)
+            bulk_g2s(smem_addr(s.sfb[st][rb][0]),
+                     p.b_sf + t.grp * p.b_sf_group_stride +
+                         ((t.n0 / 128 + rb) * p.b_sf_ct + ct) * 512,
+                     512u * n_sf, full);
         }
         if (s.abort) break;
       }
@@ -400,11 +429,8 @@ __global__ void __launch_bounds__(GTHREADS, 1)
     // dry.  The waiter warp polls instead and hands each ready stage over
     // through a named barrier, which carries the abort flag as well.
     int64_t it = 0;
-    int local = 0;
     bool aborted = false;
-    for (int64_t u = unit0; u < n_units && !aborted; u += unit_step, ++local) {
-      const int buf = local & 1;
-      const uint32_t d = tmem + (uint32_t)buf * GN;
+    for (int64_t u = unit0; u < n_units && !aborted; u += unit_step) {
       for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
         __syncwarp();
         if (stage_handoff(false)) {
@@ -414,12 +440,18 @@ __global__ void __launch_bounds__(GTHREADS, 1)
         if (lane == 0) {
           tc_fence_after();
           const int st = (int)(it % GSTAGES);
-          const uint32_t sf_col = tmem + kSfCol0 + (uint32_t)st * 32;
+          // Scale columns of the stage: A tile j at 4j, B (row block rb,
+          // tile j) at 16 + 8j + 4rb.  Scale columns of a B row block the
+          // tile does not have keep stale values; they only feed output
+          // columns that are never stored.
+          const uint32_t sf_col =
+              tmem + kSfCol0 + (uint32_t)st * kSfColsPerStage;
           for (int j = 0; j < n_sf; ++j) {
             tc_cp_sf(sf_col + j * 4,
                      smem_desc(smem_addr(s.sfa[st][j]), 16, 128, 0));
-            tc_cp_sf(sf_col + 16 + j * 4,
-                     smem_desc(smem_addr(s.sfb[st][j]), 16, 128, 0));
+            for (int rb = 0; rb < 2; ++rb)
+              tc_cp_sf(sf_col + 16 + j * 8 + rb * 4,
+                       smem_desc(smem_addr(s.sfb[st][rb][j]), 16, 128, 0));
           }
           const uint32_t a_addr = smem_addr(s.a[st]);
           const uint32_t b_addr = smem_addr(s.b[st]);
@@ -432,37 +464,36 @@ __global__ void __launch_bounds__(GTHREADS, 1)
             if (p.kind == 0) {
               // 8-bit operands: K = 32 per MMA, one E8M0 scale per row per
               // MMA: byte j of the stage's 32-bit scale cell.
-              tc_mma_mxf8(d, ad, bd, idesc_block_scaled(0, 0, 1, (uint32_t)j),
-                          sf_col, sf_col + 16, acc);
+              tc_mma_mxf8(tmem, ad, bd,
+                          idesc_block_scaled(0, 0, 1, (uint32_t)j), sf_col,
+                          sf_col + 16, acc);
             } else {
               // 4-bit operands: K = 64 per MMA, four E4M3 scales per row (one
               // 32-bit cell = scale tile j).
-              tc_mma_nvf4(d, ad, bd, idesc_block_scaled(1, 1, 0, 0),
-                          sf_col + j * 4, sf_col + 16 + j * 4, acc);
+              tc_mma_nvf4(tmem, ad, bd, idesc_block_scaled(1, 1, 0, 0),
+                          sf_col + j * 4, sf_col + 16 + j * 8, acc);
             }
           }
           if (CL == 1)
             tc_commit(smem_addr(&s.empty[st]));
           else
             tc_commit_mc(smem_addr(&s.empty[st]), cmask);
-          if (kt == p.k_stages - 1) tc_commit(smem_addr(&s.acc_full[buf]));
+          if (kt == p.k_stages - 1) tc_commit(smem_addr(&s.acc_full));
         }
       }
     }
   } else if (warp == 2) {
     // ---------------- waiter ----------------
     // Mirrors the issuer's loop: before a tile's first stage it waits until
-    // the epilogue has released the accumulator buffer, before every stage
-    // until the stage's operands have landed; then one handoff.
+    // the epilogue has taken the accumulator, before every stage until the
+    // stage's operands have landed; then one handoff.
     int64_t it = 0;
     int local = 0;
     bool ok = true;
     for (int64_t u = unit0; u < n_units && ok; u += unit_step, ++local) {
-      const int buf = local & 1;
-      const uint32_t acc_ph = (uint32_t)((local >> 1) & 1);
       if (lane == 0)
-        ok = mbar_wait(smem_addr(&s.acc_empty[buf]), acc_ph ^ 1, &s.abort,
-                       &g_gemm_wait_error);
+        ok = mbar_wait(smem_addr(&s.acc_empty), (uint32_t)((local & 1) ^ 1),
+                       &s.abort, &g_gemm_wait_error);
       for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
         const int st = (int)(it % GSTAGES);
         const uint32_t ph = (uint32_t)((it / GSTAGES) & 1);
@@ -478,49 +509,53 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue: warps 3-6, one 32-lane quarter each ------
-    // Tensor-memory lane quarter = warp id mod 4; lane = tile row.  Each
-    // 32 x 32 fp32 box goes registers -> swizzled staging -> TMA store, so
-    // global writes are whole 128-byte rows; the two staging boxes of a
-    // warp alternate.
-    const int q = warp & 3;
+    // ---------------- epilogue: warps 3-10 ----------------
+    // Tensor-memory lane quarter q = warp id mod 4 (lane = tile row),
+    // column half h.  Each thread takes its row's 128 accumulator values
+    // into registers and releases the accumulator; then every 32 x 32 fp32
+    // box goes registers -> swizzled staging -> TMA store (whole 128-byte
+    // rows).
+    const int e = warp - 3;
+    const int q = warp & 3, h = e >> 2;
+    uint8_t* box = s.cst[e];
     int local = 0;
     int grp_cursor = 0;
-    uint32_t nbox = 0;
     for (int64_t u = unit0; u < n_units; u += unit_step, ++local) {
-      const int buf = local & 1;
-      const uint32_t acc_ph = (uint32_t)((local >> 1) & 1);
       const bool ok = __all_sync(
-          0xffffffffu, mbar_wait(smem_addr(&s.acc_full[buf]), acc_ph,
-                                 &s.abort, &g_gemm_wait_error));
+          0xffffffffu,
+          mbar_wait(smem_addr(&s.acc_full), (uint32_t)(local & 1), &s.abort,
+                    &g_gemm_wait_error));
       if (!ok) break;
       tc_fence_after();
+      uint32_t r[128];
+      const uint32_t taddr =
+          tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc_ld_32x32_async(taddr + c * 32, r + c * 32);
+      tc_wait_ld();
+      // The accumulator may be overwritten once all eight warps hold it.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&s.acc_empty));
+
       const Tile t = decode_tile(p, u * CL + crank, &grp_cursor);
       float rs = 1.0f;
       if (p.kind == 1)
         rs = __fmul_rn(p.s_tok[t.m0 + q * 32 + lane], p.s_w[t.grp]);
-      for (int c = 0; c < GN; c += 32, ++nbox) {
-        uint32_t r[32];
-        tc_ld_32x32(tmem + ((uint32_t)(q * 32) << 16) +
-                        (uint32_t)(buf * GN + c),
-                    r);
-        if (c == GN - 32) {
-          // Last read of this accumulator: hand it back to the MMA warp.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&s.acc_empty[buf]));
-        }
-        uint8_t* box = s.cst[q][nbox & 1];
-        if (lane == 0) bulk_wait_read_1();   // the box's previous store
+      const int64_t x0 = t.n0 + h * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (x0 + c * 32 >= p.N) break;  // columns past N: not stored
+        if (lane == 0) bulk_wait_read_0();  // the box's previous store
         __syncwarp();
         uint8_t* row = box + lane * 128;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           float4 v;
-          v.x = __uint_as_float(r[4 * j]);
-          v.y = __uint_as_float(r[4 * j + 1]);
-          v.z = __uint_as_float(r[4 * j + 2]);
-          v.w = __uint_as_float(r[4 * j + 3]);
+          v.x = __uint_as_float(r[c * 32 + 4 * j]);
+          v.y = __uint_as_float(r[c * 32 + 4 * j + 1]);
+          v.z = __uint_as_float(r[c * 32 + 4 * j + 2]);
+          v.w = __uint_as_float(r[c * 32 + 4 * j + 3]);
           if (p.kind == 1) {
             v.x = __fmul_rn(v.x, rs);
             v.y = __fmul_rn(v.y, rs);
@@ -532,7 +567,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmap_c, smem_addr(box), (int32_t)(t.n0 + c),
+          tma_store_2d(&tmap_c, smem_addr(box), (int32_t)(x0 + c * 32),
                        (int32_t)(t.m0 + q * 32));
           bulk_commit();
         }
@@ -670,7 +705,7 @@ cudaError_t launch_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
   p.b_sf_group_stride = 0;
   p.b_rows_group_stride = 0;
   p.num_groups = 1;
-  p.tiles_n = N / GN;
+  p.tiles_n = (N + GN - 1) / GN;
   p.C = C;
   p.ldc = ldc;
   return launch_gemm(AOperand{a_codes, K, M}, tb, p, (M / GM) * p.tiles_n,
@@ -711,7 +746,7 @@ cudaError_t launch_gemm_nvfp4_grouped(
     tiles_m += (group_offsets[g + 1] - group_offsets[g]) / GM;
     p.tile_end[g] = tiles_m;
   }
-  p.tiles_n = N / GN;
+  p.tiles_n = (N + GN - 1) / GN;
   p.C = C;
   p.ldc = ldc;
   if (tiles_m == 0) return cudaSuccess;
