@@ -401,6 +401,21 @@ def tensor_peaks():
     return {"fp8": 2 * bf16, "fp4": 6 * bf16, "kind": kind}
 
 
+def gemm_roofline(us, flops, nbytes, tensor_peak_tflops):
+    """Both ceilings of a GEMM launch: tensor time at the dtype's peak and
+    HBM time for its algorithmic bytes (operands, scales and fp32 C once).
+    The larger one binds; frac = that time / the measured time."""
+    hbm = measured_peak()[0]
+    t_tensor = flops / (tensor_peak_tflops * 1e12) * 1e6
+    t_hbm = nbytes / (hbm * 1e9) * 1e6
+    bound = "tensor" if t_tensor >= t_hbm else "hbm"
+    return {"us": round(us, 2), "TFLOP/s": round(flops / us / 1e6, 1),
+            "GB/s": round(nbytes / us / 1e3, 1), "bytes": int(nbytes),
+            "tensor_frac": round(t_tensor / us, 3),
+            "hbm_frac": round(t_hbm / us, 3), "bound": bound,
+            "frac": round(max(t_tensor, t_hbm) / us, 3)}
+
+
 def run_gemm(q, W, dev, stream, reps=20):
     """The block-scaled GEMM consumers on the workloads they are specified
     for: MXFP8 A [2048 x 2048] x B [2048 x 8192]; NVFP4 4096 tokens routed
@@ -419,10 +434,12 @@ def run_gemm(q, W, dev, stream, reps=20):
                             qb.col_scales_t)
     ms = _time_fn(t_mx, stream, reps)
     fl = 2.0 * 2048 * 2048 * 8192
-    out["mxfp8_2048x2048x8192"] = {
-        "us": round(ms * 1e3, 2), "TFLOP/s": round(fl / ms / 1e9, 1),
-        "peak_fp8": round(peaks["fp8"], 1),
-        "frac": round(fl / ms / 1e9 / peaks["fp8"], 3), "bound": "tensor"}
+    # codes and E8M0 scales of A and B^T, fp32 C
+    nb = 2048 * 2048 * (1 + 1 / 32) + 8192 * 2048 * (1 + 1 / 32) + \
+        2048 * 8192 * 4
+    out["mxfp8_2048x2048x8192"] = dict(
+        gemm_roofline(ms * 1e3, fl, nb, peaks["fp8"]),
+        peak_fp8=round(peaks["fp8"], 1))
     E, H, F = 128, 2048, 768
     tokens = W.gemm_tokens(4096, H)
     route = W.topk_routing(4096, E, 8)
@@ -446,14 +463,16 @@ def run_gemm(q, W, dev, stream, reps=20):
     ms = _time_fn(t_nv, stream, reps)
     fl_routed = 2.0 * 32768 * 2 * F * H
     fl_padded = 2.0 * int(offs[-1]) * 2 * F * H
-    out["nvfp4_grouped_4096tok_top8_128x1536x2048"] = {
-        "us": round(ms * 1e3, 2),
-        "TFLOP/s_routed": round(fl_routed / ms / 1e9, 1),
-        "TFLOP/s_padded": round(fl_padded / ms / 1e9, 1),
-        "padded_rows": int(offs[-1]), "routed_rows": 32768,
-        "peak_fp4": round(peaks["fp4"], 1),
-        "frac": round(fl_padded / ms / 1e9 / peaks["fp4"], 3),
-        "bound": "tensor"}
+    Mp = int(offs[-1])
+    # packed E2M1 + E4M3 scales of the gathered tokens and of all experts'
+    # gate/up weights, per-token and per-expert FP32 scales, fp32 C
+    nb = Mp * H * (0.5 + 1 / 16) + 4 * Mp + \
+        E * 2 * F * H * (0.5 + 1 / 16) + 4 * E + Mp * 2 * F * 4
+    out["nvfp4_grouped_4096tok_top8_128x1536x2048"] = dict(
+        gemm_roofline(ms * 1e3, fl_padded, nb, peaks["fp4"]),
+        **{"TFLOP/s_routed": round(fl_routed / ms / 1e9, 1),
+           "padded_rows": Mp, "routed_rows": 32768,
+           "peak_fp4": round(peaks["fp4"], 1)})
     out["peaks_kind"] = peaks["kind"]
     return out
 
@@ -565,15 +584,30 @@ def oracle_timed(rows_total, threads):
     return sum(op_bytes().values()) * frac / dt / 1e9, dt
 
 
-def cpu_baseline(args):
+def cpu_baseline(args, min_s=10.0, max_passes=40):
+    """The oracle over `cpu_rows` rows of X, repeated until at least min_s
+    seconds of CPU work have run (at most max_passes passes)."""
+    import oracle as O
+    import workloads as W
+    O.lib()
     cores = os.cpu_count() or 1
     rows = args.cpu_rows
-    v, dt = oracle_timed(rows, cores)
+    x = W.mxfp8_random(rows, K, seed=11)
+    slices = [x[i:i + 32] for i in range(0, rows, 32)]
+    passes, total = 0, 0.0
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        while passes < max_passes and (passes == 0 or total < min_s):
+            t0 = time.perf_counter()
+            list(ex.map(oracle_sample_step, slices))
+            total += time.perf_counter() - t0
+            passes += 1
+    v = sum(op_bytes().values()) * (rows / M) * passes / total / 1e9
     return {"value": round(v, 4), "unit": UNIT, "cores": cores,
             "kind": "oracle",
-            "sample": (f"the step's 8 operations on {rows} of the 8192 rows "
-                       f"of X ({rows * K} elements), 32-row slices over "
-                       f"{cores} threads, {dt:.1f} s")}
+            "sample": (f"{passes} passes of the step's 8 operations over "
+                       f"{rows} of the 8192 rows of X ({rows * K} elements "
+                       f"per pass), 32-row slices over {cores} threads, "
+                       f"{total:.1f} s")}
 
 
 def run_reference(args):
@@ -622,7 +656,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="libmxq", choices=["libmxq", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=4096)
+    ap.add_argument("--cpu-rows", type=int, default=8192)
     ap.add_argument("--ref-rows", type=int, default=0,
                     help="rows of X per reference step (0: sized to ~1 min)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
