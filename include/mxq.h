@@ -206,7 +206,7 @@ mxq_status nvfp4_quantize_weight_shared(
 /*                                                                       */
 /* Same arguments, layouts and results as nvfp4_quantize_weight_shared,   */
 /* without ws / ws_bytes: the per-group scratch lives in a fixed device   */
-/* array inside the library (16.25 KiB, held on every GPU that loads the  */
+/* array inside the library (32.25 KiB, held on every GPU that loads the  */
 /* library until the process exits).                                      */
 /*  - num_groups must not exceed                                          */
 /*    nvfp4_quantize_weight_shared_noalloc_max_groups() (4096); larger    */

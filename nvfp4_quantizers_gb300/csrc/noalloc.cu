@@ -10,10 +10,10 @@
 // amax words.  This entry point keeps that scratch in a fixed array in the
 // library's own device memory instead.
 //
-//  * The scratch is a file-scope device array of 64 + kNoAllocMaxGroups
-//    32-bit words (16.25 KiB: a grid-barrier counter and one amax word per
-//    group).  Every GPU that loads the library holds it until the process
-//    exits.
+//  * The scratch is a file-scope device array of 64 + 2 * kNoAllocMaxGroups
+//    32-bit words (32.25 KiB: a task counter, one amax word and one
+//    progress counter per group).  Every GPU that loads the library holds
+//    it until the process exits.
 //  * Host code cannot use the array's name as a device address (on the
 //    host it only stands in for the symbol).  The first call on a device
 //    looks the address up with cudaGetSymbolAddress, with that device
@@ -38,8 +38,9 @@ namespace mxq {
 namespace {
 
 constexpr int64_t kNoAllocMaxGroups = 4096;
-// 256-byte header (grid barrier counter) + one amax word per group.
-constexpr int64_t kNoAllocWords = 64 + kNoAllocMaxGroups;
+// 256-byte header (task counter) + an amax word and a progress counter per
+// group.
+constexpr int64_t kNoAllocWords = 64 + 2 * kNoAllocMaxGroups;
 static __device__ __align__(256) uint32_t g_noalloc_amax[kNoAllocWords];
 
 constexpr int kMaxDev = 64;

@@ -17,17 +17,15 @@
 //                                      FLT_MAX otherwise)
 //   q   = E2M1_RNE( x enc )           (saturating at +-6, sign kept)
 //
-// Design (sm_103a): HBM-streaming, one warp per row.  A lane loads 16-byte
-// chunks (8 bf16) with coalesced non-allocating loads, all chunks of the
-// row in flight at once (H = 2048: 8 loads of 16 B per lane); the row
-// amax is a 5-step xor-shuffle reduction and a 16-block's amax one more
-// shuffle between the two lanes that hold it.  Each lane emits one 32-bit
-// word of packed codes per chunk (the warp writes 128 contiguous bytes per
-// step); four block scales are gathered by shuffles into one 32-bit store
-// (four consecutive scale columns are contiguous in both layouts).
-// Weight groups use one persistent cooperative kernel (see below): an amax
-// phase and an encode phase per L2-sized chunk of groups, separated by a
-// bounded grid barrier, so the second read of a chunk is served from L2.
+// Design (sm_103a): HBM-streaming.  Per-token rows: one lane per 16-value
+// block, R blocks per lane with all of a lane's loads in flight at once
+// (non-allocating 16-byte loads), WPR warps per row joined by a named
+// barrier for the row amax; the block's scale and codes come from binary32
+// IEEE intrinsics and cvt.rn.satfinite.e2m1x2; one 8-byte code store per
+// block, four block scales gathered by shuffles into one 32-bit store (four
+// consecutive scale columns are contiguous in both layouts).  Weight groups
+// use one persistent task-list kernel (see below): all amax tasks, then all
+// encode tasks, so the second read of a group is served from L2.
 #include <float.h>
 
 #include "common.cuh"
@@ -255,19 +253,28 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 }
 
 // ---------------------------------------------------------------------------
-// Weight groups: one persistent cooperative kernel.  For each chunk of
-// groups small enough to stay in L2: phase A reduces every group's amax
-// (64 KiB work units, CTA partial maxima combined with an integer atomicMax
-// on the float bits, exact for non-negative values); a grid-wide barrier;
-// phase B encodes the chunk's rows with their group's S, re-reading the
-// chunk from L2.  A CTA that finishes phase B of one chunk goes straight to
-// phase A of the next.
+// Weight groups: one persistent kernel working through a task list.  Per
+// group g there are nA amax tasks (32 KiB of the group each) and nE encode
+// tasks (ROWS rows each); an encode task needs its group's S, i.e. every
+// amax task of the group.  The list holds all amax tasks, then all encode
+// tasks; CTAs take tasks in list order from an atomic counter, so an encode
+// task only ever waits (bounded) for amax tasks that running CTAs already
+// hold, and the data read by the amax tasks is still in L2 when the encode
+// tasks read it again.  (Interleaving the next group's amax tasks with the
+// encode tasks, to overlap HBM-bound and ALU-bound work, measured slower:
+// the encode tasks then wait for amax tasks handed out just before them.)
+//
+// Workspace: [1 + launch] the task counter of each launch; [64 + g] the
+// amax of group g (float bits, merged with atomicMax); [64 + G + g] the
+// number of group g's amax tasks that have merged their maximum (atomicAdd
+// after a fence).  Plain single-shot atomics: a compare-and-swap loop on
+// one word per group serialises the hundreds of CTAs that finish together.
 // ---------------------------------------------------------------------------
 constexpr int kMaxGroupsPerLaunch = 256;
-constexpr int64_t kAmaxUnitChunks = 1024;     // 16-byte chunks per unit (16 KiB)
-constexpr int kWsHeaderWords = 64;            // [0] = barrier counter
+constexpr int64_t kTaskChunks = 2048;         // 16-byte chunks per amax task
+constexpr int kWsHeaderWords = 64;            // [1 + launch] = task counters
 
-// Error word of the bounded grid barrier of this translation unit.
+// Error word of the bounded waits of this translation unit.
 __device__ unsigned int g_nvfp4_wait_error = 0;
 
 struct GroupTable {
@@ -281,47 +288,17 @@ struct GroupParams {
   int64_t R, R_pad, K;
   int64_t g0;                         // global index of local group 0
   int ng;                             // groups in this launch
-  int chunk;                          // groups per L2-sized chunk
-  int64_t units_per_group;            // phase-A units per group
+  int64_t nA, nE;                     // amax / encode tasks per group
   uint8_t* codes;                     // group g at g * R * K/2
   uint8_t* scales;                    // group g at g * scale_stride
   int64_t scale_stride;
   float* group_scales;
   const float* S_in;                  // NULL: S from amax
-  uint32_t* ws;                       // [0] barrier, [64 + g] amax of group g
+  uint32_t* ws;                       // [64 + g] amax words
+  uint32_t* counter;                  // this launch's task counter
+  uint32_t* done;                     // finished amax tasks per group
   int swizzled;
 };
-
-// Grid-wide barrier for a cooperative launch: every CTA adds 1 to *ctr and
-// waits (bounded, ~1 s) until it reaches `target`.  On timeout it records 1
-// in g_nvfp4_wait_error, sets *abort and returns false; all threads of the
-// CTA still pass the same __syncthreads calls.
-__device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t target,
-                                             volatile int* abort) {
-  __syncthreads();
-  if (threadIdx.x == 0 && !*abort) {
-    __threadfence();
-    atomicAdd(ctr, 1u);
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-      uint32_t v;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
-                   : "=r"(v)
-                   : "l"(ctr)
-                   : "memory");
-      if (v >= target) break;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        atomicOr(&g_nvfp4_wait_error, 1u);
-        *abort = 1;
-        break;
-      }
-      __nanosleep(64);
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  return !*abort;
-}
 
 __device__ __forceinline__ const uint16_t* chunk_ptr(const GroupTable& tab,
                                                      const GroupParams& p,
@@ -331,6 +308,18 @@ __device__ __forceinline__ const uint16_t* chunk_ptr(const GroupTable& tab,
   return tab.part[gl][pi] + (q - p.part_chunk0[pi]) * 8;
 }
 
+// Task t of the list -> (is_amax, local group, index within the group).
+// Task t of the list -> (is_amax, local group, index within the group).
+__device__ __forceinline__ void task_of(const GroupParams& p, int64_t t,
+                                        bool* is_a, int* gl, int64_t* idx) {
+  const int64_t na_all = p.S_in ? 0 : (int64_t)p.ng * p.nA;
+  *is_a = t < na_all;
+  if (!*is_a) t -= na_all;
+  const int64_t per = *is_a ? p.nA : p.nE;
+  *gl = (int)(t / per);
+  *idx = t - (int64_t)*gl * per;
+}
+
 template <int R, int WPR>
 __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
     nvfp4_weight_kernel(const __grid_constant__ GroupTable tab,
@@ -338,77 +327,97 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
   constexpr int ROWS = CTA_WARPS / WPR;
   __shared__ uint32_t red[CTA_WARPS];
   __shared__ int s_abort;
+  __shared__ int64_t s_task;
+  __shared__ float s_S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slot = warp / WPR, wpart = warp % WPR;
   if (threadIdx.x == 0) s_abort = 0;
   __syncthreads();
   pdl_wait();
   const int64_t group_chunks = p.part_chunk0[p.num_parts];
-  uint32_t* amax = p.ws + kWsHeaderWords;
-  uint32_t gen = 0;
-  for (int c0 = 0; c0 < p.ng; c0 += p.chunk) {
-    const int nc = (p.ng - c0) < p.chunk ? (p.ng - c0) : p.chunk;
-    if (!p.S_in) {
-      // Phase A: amax of every group of the chunk.  Each CTA takes a
-      // contiguous range of 16 KiB units (so it spans at most a few groups),
-      // keeps a running max in registers and combines it across the CTA
-      // only when the group changes and at the end of its range.
-      const int64_t n_units = (int64_t)nc * p.units_per_group;
-      const int64_t u_begin = n_units * blockIdx.x / gridDim.x;
-      const int64_t u_end = n_units * (blockIdx.x + 1) / gridDim.x;
-      int cur = -1;
-      uint32_t a = 0;
-      for (int64_t u = u_begin; u < u_end; ++u) {
-        const int gl = c0 + (int)(u / p.units_per_group);
-        const int64_t q0 = (u % p.units_per_group) * kAmaxUnitChunks;
-        uint4 v[4];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int64_t q = q0 + threadIdx.x + (int64_t)jj * 256;
-          v[jj] = q < group_chunks ? ld_stream_v4(chunk_ptr(tab, p, gl, q))
-                                   : make_uint4(0, 0, 0, 0);
-        }
-        if (gl != cur) {                                   // CTA-uniform
-          if (cur >= 0) {
-            const uint32_t m = warp_max(a);
-            if (lane == 0) red[warp] = m;
-            __syncthreads();
-            if (threadIdx.x == 0) {
-              uint32_t mm = red[0];
-              for (int w = 1; w < CTA_WARPS; ++w) mm = max(mm, red[w]);
-              if (mm) atomicMax(&amax[p.g0 + cur], mm << 16);
-            }
-            __syncthreads();
-          }
-          cur = gl;
-          a = 0;
-        }
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) a = max(a, chunk_absmax(v[jj]));
-      }
-      if (cur >= 0) {                                      // CTA-uniform
-        const uint32_t m = warp_max(a);
-        if (lane == 0) red[warp] = m;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          uint32_t mm = red[0];
-          for (int w = 1; w < CTA_WARPS; ++w) mm = max(mm, red[w]);
-          if (mm) atomicMax(&amax[p.g0 + cur], mm << 16);
-        }
-        __syncthreads();
-      }
-      ++gen;
-      grid_barrier(p.ws, gen * gridDim.x, &s_abort);
+  uint32_t* amax = p.ws + kWsHeaderWords;      // unused when S_in is given
+  const int64_t total = (int64_t)p.ng * (p.S_in ? p.nE : p.nA + p.nE);
+  int64_t t_static = blockIdx.x;
+  while (true) {
+    int64_t t;
+    if (p.S_in) {
+      t = t_static;                   // no amax: a static round robin
+      t_static += gridDim.x;
+    } else {
+      if (threadIdx.x == 0) s_task = (int64_t)atomicAdd(p.counter, 1u);
+      __syncthreads();
+      t = s_task;
+      __syncthreads();
     }
-    // Phase B: encode the chunk's rows (and the scale-tile padding rows).
-    const int64_t nrows = (int64_t)nc * p.R_pad;
-    for (int64_t base = (int64_t)blockIdx.x * ROWS; base < nrows;
-         base += (int64_t)gridDim.x * ROWS) {
-      const int64_t w = base + slot;
-      if (w >= nrows || s_abort) continue;             // uniform over the row
-      const int gl = c0 + (int)(w / p.R_pad);
-      const int64_t r = w - (int64_t)(gl - c0) * p.R_pad;
-      const int64_t g = p.g0 + gl;
+    if (t >= total) break;
+    bool is_a;
+    int gl;
+    int64_t idx;
+    task_of(p, t, &is_a, &gl, &idx);
+    if (is_a) {
+      // ---- amax of 64 KiB of group gl ----
+      uint32_t a = 0;
+      const int64_t q0 = idx * kTaskChunks;
+#pragma unroll
+      for (int rr = 0; rr < (int)(kTaskChunks / (CTA_WARPS * 32 * 8)); ++rr) {
+        uint4 v[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int64_t q = q0 + (int64_t)(rr * 8 + jj) * (CTA_WARPS * 32) +
+                            threadIdx.x;
+          v[jj] = (q < group_chunks && !s_abort)
+                      ? ld_stream_v4(chunk_ptr(tab, p, gl, q))
+                      : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) a = max(a, chunk_absmax(v[jj]));
+      }
+      const uint32_t m = warp_max(a);
+      if (lane == 0) red[warp] = m;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        uint32_t mm = red[0];
+        for (int w = 1; w < CTA_WARPS; ++w) mm = max(mm, red[w]);
+        if (mm) atomicMax(&amax[p.g0 + gl], mm << 16);
+        __threadfence();              // the maximum lands before the count
+        atomicAdd(&p.done[p.g0 + gl], 1u);
+      }
+      __syncthreads();
+      continue;
+    }
+    // ---- encode ROWS rows of group gl ----
+    const int64_t g = p.g0 + gl;
+    if (threadIdx.x == 0) {
+      float S = 0.0f;
+      if (p.S_in) {
+        S = p.S_in[g];
+      } else {
+        // wait until every amax task of the group has merged its maximum
+        // Poll with relaxed loads and a back-off (acquire loads in a tight
+        // loop slow down the streaming loads of the other CTAs on the SM),
+        // then one acquire fence.
+        const uint64_t t0 = global_timer_ns();
+        while (true) {
+          const uint32_t nd = *reinterpret_cast<volatile uint32_t*>(&p.done[g]);
+          if ((int64_t)nd >= p.nA || s_abort) break;
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_nvfp4_wait_error, 1u);
+            s_abort = 1;
+            break;
+          }
+          __nanosleep(256);
+        }
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        S = __fdiv_rn(
+            __uint_as_float(*reinterpret_cast<volatile uint32_t*>(&amax[g])),
+            kNvfp4ScaleDenom);
+      }
+      s_S = S;
+    }
+    __syncthreads();
+    const float S = s_S;
+    const int64_t r = idx * ROWS + slot;
+    if (r < p.R_pad && !s_abort) {                      // uniform over the row
       const bool real = r < p.R;
       const uint16_t* row = nullptr;
       if (real) {
@@ -416,9 +425,6 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
         while (pi + 1 < p.num_parts && r >= p.part_row0[pi + 1]) ++pi;
         row = tab.part[gl][pi] + (r - p.part_row0[pi]) * p.K;
       }
-      const float S = p.S_in ? p.S_in[g]
-                             : __fdiv_rn(__uint_as_float(__ldcg(&amax[g])),
-                                         kNvfp4ScaleDenom);
       if (r == 0 && wpart == 0 && lane == 0) p.group_scales[g] = S;
       RowOut o{p.codes + (g * p.R + r) * (p.K >> 1),
                p.scales + g * p.scale_stride, r, ((p.K >> 4) + 3) >> 2,
@@ -427,6 +433,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
       encode_row_warps<R, WPR>(row, real, S, true, o, slot, wpart, lane, red,
                                &S_used);
     }
+    __syncthreads();                  // s_S and red are reused by the next task
   }
   pdl_launch_dependents();
 }
@@ -477,7 +484,7 @@ cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
 }
 
 size_t nvfp4_weight_ws_bytes(int64_t num_groups) {
-  return (size_t)(((kWsHeaderWords + num_groups) * 4 + 255) / 256 * 256);
+  return (size_t)(((kWsHeaderWords + 2 * num_groups) * 4 + 255) / 256 * 256);
 }
 
 cudaError_t nvfp4_take_wait_error(unsigned int* word) {
@@ -490,8 +497,8 @@ cudaError_t nvfp4_take_wait_error(unsigned int* word) {
 namespace {
 
 template <int R, int WPR>
-cudaError_t launch_weight_coop(const GroupTable& tab, const GroupParams& p,
-                               int dev, cudaStream_t stream) {
+cudaError_t launch_weight_tasks(const GroupTable& tab, const GroupParams& p,
+                                int dev, cudaStream_t stream) {
   static int occ[64] = {};
   int n = (dev >= 0 && dev < 64) ? occ[dev] : 0;
   if (n == 0) {
@@ -502,8 +509,10 @@ cudaError_t launch_weight_coop(const GroupTable& tab, const GroupParams& p,
     if (dev >= 0 && dev < 64) occ[dev] = n;
   }
   const unsigned grid = (unsigned)(n * sm_count(dev));
+  // No co-residency is needed: a CTA only waits for tasks that running
+  // CTAs hold.
   return launch_pdl(nvfp4_weight_kernel<R, WPR>, dim3(grid),
-                    dim3(CTA_WARPS * 32), 0, stream, true, tab, p);
+                    dim3(CTA_WARPS * 32), 0, stream, false, tab, p);
 }
 
 }  // namespace
@@ -530,8 +539,9 @@ cudaError_t launch_nvfp4_weight_shared(
   p.R = p.part_row0[num_parts];
   p.R_pad = swizzled ? (p.R + 127) / 128 * 128 : p.R;
   p.K = K;
-  p.units_per_group =
-      (p.part_chunk0[num_parts] + kAmaxUnitChunks - 1) / kAmaxUnitChunks;
+  p.nA = (p.part_chunk0[num_parts] + kTaskChunks - 1) / kTaskChunks;
+  p.nE = (p.R_pad + (CTA_WARPS / sh.WPR) - 1) / (CTA_WARPS / sh.WPR);
+  p.done = ws ? ws + kWsHeaderWords + num_groups : nullptr;
   p.codes = codes;
   p.scales = scales;
   p.scale_stride = scale_bytes(p.R, K / 16, swizzled);
@@ -543,13 +553,13 @@ cudaError_t launch_nvfp4_weight_shared(
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  // Groups per L2 chunk: what phase A reads should still be in L2 when
-  // phase B reads it again.
-  const int64_t group_bytes = p.R * K * 2;
-  int64_t chunk = kMaxGroupsPerLaunch;
-  if (!group_scales_in && group_bytes > 0) {
-    chunk = (int64_t)(0.55 * (double)l2_bytes(dev)) / group_bytes;
-    chunk = chunk < 1 ? 1 : chunk;
+  const int64_t n_launch =
+      (num_groups + kMaxGroupsPerLaunch - 1) / kMaxGroupsPerLaunch;
+  if (!group_scales_in) {
+    if (n_launch > kWsHeaderWords - 1) return cudaErrorInvalidValue;
+    // Zero the task counters and every group's amax and count words.
+    err = cudaMemsetAsync(ws, 0, (kWsHeaderWords + 2 * num_groups) * 4, stream);
+    if (err != cudaSuccess) return err;
   }
   GroupTable tab;
   for (int64_t g0 = 0; g0 < num_groups; g0 += kMaxGroupsPerLaunch) {
@@ -564,21 +574,13 @@ cudaError_t launch_nvfp4_weight_shared(
                 : nullptr;
     p.g0 = g0;
     p.ng = ng;
-    p.chunk = (int)(chunk < ng ? chunk : ng);
-    if (!group_scales_in) {
-      // Zero the barrier counter and this launch's amax words.
-      err = cudaMemsetAsync(ws, 0, kWsHeaderWords * 4, stream);
-      if (err == cudaSuccess)
-        err = cudaMemsetAsync(ws + kWsHeaderWords + g0, 0, (size_t)ng * 4,
-                              stream);
-      if (err != cudaSuccess) return err;
-    }
-    if (sh.R == 1) err = launch_weight_coop<1, 1>(tab, p, dev, stream);
-    else if (sh.R == 2) err = launch_weight_coop<2, 1>(tab, p, dev, stream);
-    else if (sh.WPR == 1) err = launch_weight_coop<4, 1>(tab, p, dev, stream);
-    else if (sh.WPR == 2) err = launch_weight_coop<4, 2>(tab, p, dev, stream);
-    else if (sh.WPR == 4) err = launch_weight_coop<4, 4>(tab, p, dev, stream);
-    else err = launch_weight_coop<4, 8>(tab, p, dev, stream);
+    p.counter = ws ? ws + 1 + g0 / kMaxGroupsPerLaunch : nullptr;
+    if (sh.R == 1) err = launch_weight_tasks<1, 1>(tab, p, dev, stream);
+    else if (sh.R == 2) err = launch_weight_tasks<2, 1>(tab, p, dev, stream);
+    else if (sh.WPR == 1) err = launch_weight_tasks<4, 1>(tab, p, dev, stream);
+    else if (sh.WPR == 2) err = launch_weight_tasks<4, 2>(tab, p, dev, stream);
+    else if (sh.WPR == 4) err = launch_weight_tasks<4, 4>(tab, p, dev, stream);
+    else err = launch_weight_tasks<4, 8>(tab, p, dev, stream);
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;

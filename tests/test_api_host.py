@@ -95,7 +95,8 @@ def test_nvfp4_argument_errors(L):
     assert g(1, 2, P, R, 64, FAKE, FAKE, FAKE, None, 1, FAKE, 0, None) == q.MXQ_ERR_WORKSPACE
     assert g(1, 2, P, R, 40, FAKE, FAKE, FAKE, None, 1, FAKE, 256, None) == q.MXQ_ERR_SHAPE
     assert g(1, 2, None, R, 64, FAKE, FAKE, FAKE, None, 1, FAKE, 256, None) == q.MXQ_ERR_NULL
-    assert L.nvfp4_quantize_weight_shared_workspace_size(128) == 768
+    # 256-byte header + an amax word and a progress counter per group
+    assert L.nvfp4_quantize_weight_shared_workspace_size(128) == 1280
     assert L.nvfp4_quantize_weight_shared_workspace_size(0) == 0
 
 
