@@ -380,3 +380,37 @@ def gemm_nvfp4_grouped(a_codes, a_scales, a_S, offsets, w_codes, w_scales,
         C[r0:r1] = acc * (a_S[r0:r1, None].astype(np.float64)
                           * float(w_S[e]))
     return C
+
+
+# --------------------------------------------------------------------------
+# MoE expert forward up to the activation ("Miles: end-to-end MXFP8 and
+# per-token NVFP4 RL", NVFP4 recipe section: SwiGLU MoE layers fuse the gate
+# and up projections into one GEMM under one FP32 weight scale).  SwiGLU is
+# taken in its standard form h = silu(gate) * up, silu(z) = z * sigmoid(z),
+# evaluated in float64 on the float64 GEMM result.
+# --------------------------------------------------------------------------
+def silu(z: np.ndarray) -> np.ndarray:
+    """z * sigmoid(z) = z / (1 + exp(-z)), float64 (exp overflow -> 0)."""
+    z = np.asarray(z, np.float64)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def gather_rows(x: np.ndarray, row_index: np.ndarray) -> np.ndarray:
+    """Row t of the result is x[row_index[t]], or a zero row where the index
+    is outside [0, len(x)) (the padding rows of an expert group)."""
+    out = np.zeros((len(row_index),) + x.shape[1:], x.dtype)
+    ok = (row_index >= 0) & (row_index < x.shape[0])
+    out[ok] = x[row_index[ok]]
+    return out
+
+
+def moe_gate_up_swiglu(a_codes, a_scales, a_S, offsets, w_codes, w_scales,
+                       w_S) -> np.ndarray:
+    """Grouped gate/up GEMM (expert e's weight = [gate_e ; up_e], 2F x K,
+    one FP32 scale per expert) with both FP32 scales, then SwiGLU:
+    h[r, j] = silu(C[r, j]) * C[r, F + j]."""
+    F = w_codes.shape[1] // 2
+    C = gemm_nvfp4_grouped(a_codes, a_scales, a_S, offsets, w_codes,
+                           w_scales, w_S)
+    return silu(C[:, :F]) * C[:, F:]

@@ -554,3 +554,78 @@ def test_gemm_nvfp4_grouped_closed_form(orc):
     ref[:4] = (a[:4] * 448) @ (w[0] * 448).T * 0.5 * 2.0
     ref[4:] = (a[4:] * 448) @ (w[1] * 448).T * 0.5 * 0.25
     assert np.array_equal(C, ref)
+
+
+# --------------------------------------------------------------------------
+# MoE gate/up + SwiGLU oracle: closed forms and structure.
+# --------------------------------------------------------------------------
+def test_silu_closed_forms(orc):
+    """silu(0) = 0; sigmoid(ln 3) = 3/4; silu(-z) = silu(z) - z; silu(z)/z
+    -> 1 and silu(-z) -> 0 for large z."""
+    assert orc.silu(0.0) == 0.0
+    assert abs(orc.silu(np.log(3.0)) - 0.75 * np.log(3.0)) < 1e-15
+    z = np.random.default_rng(7).normal(0, 4, 1000)
+    assert np.max(np.abs(orc.silu(-z) - (orc.silu(z) - z))) < 1e-12
+    assert abs(orc.silu(40.0) / 40.0 - 1.0) < 1e-15
+    assert abs(orc.silu(-40.0)) < 1e-15
+    assert orc.silu(-1e4) == 0.0 and orc.silu(1e4) == 1e4
+
+
+def test_gather_rows_pads_with_zero_rows(orc):
+    x = np.arange(12, dtype=np.uint16).reshape(4, 3) + 1
+    idx = np.array([2, -1, 0, 4, 3])
+    g = orc.gather_rows(x, idx)
+    assert np.array_equal(g, np.array([[7, 8, 9], [0, 0, 0], [1, 2, 3],
+                                       [0, 0, 0], [10, 11, 12]]))
+
+
+def test_moe_swiglu_structure(orc):
+    """Exact small-integer operands: gate columns equal to 0 give h = 0;
+    gate columns with a large positive value give h = g * u (silu(g) = g to
+    1e-15); large negative give |h| < 1e-12 |u|; up columns equal to 0 give
+    h = 0.  Swapping the gate and up halves changes h, and the two FP32
+    scales multiply both halves before the activation."""
+    rng = np.random.default_rng(8)
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4])
+    F, K = 4, 32
+    a = rng.choice(mags, (6, K)) * np.where(rng.random((6, K)) < .5, -1, 1)
+    a[:, 0] = 6.0
+    a[:, 16] = 6.0
+    w = rng.choice(mags, (2, 2 * F, K))
+    w[:, :, 0] = 6.0
+    w[:, :, 16] = 6.0
+    w[:, 0, 1:16] = 0.0            # gate column 0: g = 6*6*448*448*S... > 0
+    w[:, 0, 17:] = 0.0
+    w[:, F + 1, :] = 0.0           # up column 1: u = 0
+    S1 = np.array([1.0 / 448], np.float32)
+    enc = [orc.nvfp4_encode_rows(W.to_bf16_bits(w[e]), S1) for e in range(2)]
+    wc = np.stack([c for c, _ in enc])
+    wsc = np.stack([s for _, s in enc])
+    ac, asc = orc.nvfp4_encode_rows(W.to_bf16_bits(a), S1)
+    aS = np.full(6, 0.5, np.float32)
+    wS = np.array([2.0, 0.25], np.float32)
+    off = np.array([0, 4, 6])
+    h = orc.moe_gate_up_swiglu(ac, asc, aS, off, wc, wsc, wS)
+    # exact gate/up products (decoded operands are value * 448)
+    full = np.zeros((6, 2 * F))
+    full[:4] = (a[:4] * 448) @ (w[0] * 448).T * 0.5 * 2.0
+    full[4:] = (a[4:] * 448) @ (w[1] * 448).T * 0.5 * 0.25
+    g, u = full[:, :F], full[:, F:]
+    assert np.all(g[:, 0] > 1e5)
+    assert np.allclose(h[:, 0], g[:, 0] * u[:, 0], rtol=1e-15, atol=0)
+    assert np.all(h[:, 1] == 0)
+    big_neg = g < -50
+    assert np.all(np.abs(h[big_neg]) <= 1e-12 * np.abs(u[big_neg]))
+    zero_g = g == 0
+    assert np.all(h[zero_g] == 0)
+    # In the O(1) range (tiny FP32 scales) silu is far from linear: swapping
+    # the gate and up halves must change h.
+    aS_small = np.full(6, 2.0 ** -11, np.float32)
+    wS_small = np.array([2.0 ** -11, 2.0 ** -10], np.float32)
+    swapped = np.concatenate([wc[:, F:], wc[:, :F]], axis=1)
+    swapped_s = np.concatenate([wsc[:, F:], wsc[:, :F]], axis=1)
+    h1 = orc.moe_gate_up_swiglu(ac, asc, aS_small, off, wc, wsc, wS_small)
+    h2 = orc.moe_gate_up_swiglu(ac, asc, aS_small, off, swapped, swapped_s,
+                                wS_small)
+    assert 0.01 < np.median(np.abs(h1[:, 2:])) < 100
+    assert not np.allclose(h1, h2, rtol=1e-3)
