@@ -157,6 +157,28 @@ mxq_status nvfp4_quantize_per_token(const void* x, int64_t T, int64_t H,
                                     void* stream);
 
 /* --------------------------------------------------------------------- */
+/* NVFP4 per-token quantize of gathered rows (routing gather fused in).    */
+/*                                                                       */
+/* [MILES] NVFP4 recipe section (SwiGLU MoE layers: the tokens routed to  */
+/* an expert form that expert's rows of the gate/up GEMM) and experiments */
+/* section (per-token NVFP4 activation quantize): output row t is the     */
+/* per-token quantization of x row row_index[t], exactly as               */
+/* nvfp4_quantize_per_token would produce it for that row.                 */
+/*                                                                       */
+/* x            bf16 [T_src x H] (row stride ldx), device.                */
+/* row_index    int32 [T], device (4-byte aligned).  An index outside     */
+/*              [0, T_src) gives a zero row (codes 0, block scales 0,     */
+/*              token scale 0): the padding rows of an expert group.      */
+/* codes, block_scales, token_scales: as nvfp4_quantize_per_token, for T  */
+/*              output rows.                                              */
+/* --------------------------------------------------------------------- */
+mxq_status nvfp4_quantize_per_token_gather(
+    const void* x, int64_t T_src, int64_t H, int64_t ldx,
+    const int32_t* row_index, int64_t T, uint8_t* codes,
+    uint8_t* block_scales, float* token_scales, int scale_layout,
+    void* stream);
+
+/* --------------------------------------------------------------------- */
 /* NVFP4 weight quantize with one FP32 scale shared by a group of parts.  */
 /*                                                                       */
 /* [MILES] NVFP4 recipe section: NVFP4 targets MoE expert weights; the    */
@@ -306,6 +328,39 @@ mxq_status mxq_gemm_nvfp4_grouped(
     const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
     const uint8_t* w_scales, const float* w_group_scales, int64_t N, int64_t K,
     float* C, int64_t ldc, void* stream);
+
+/* --------------------------------------------------------------------- */
+/* MoE expert forward up to the activation: grouped NVFP4 gate/up GEMM    */
+/* with SwiGLU in the epilogue.                                           */
+/*                                                                       */
+/* [MILES] NVFP4 recipe section: in SwiGLU MoE layers the gate and up     */
+/* projections are one GEMM whose two halves share an FP32 weight scale;  */
+/* experiments section: the per-token FP32 scale is applied in the GEMM   */
+/* epilogue.  SwiGLU is its standard form, silu(gate) * up with           */
+/* silu(z) = z / (1 + e^-z).                                              */
+/*                                                                       */
+/*   rows off[e] .. off[e+1] of A use expert e; with                       */
+/*   s = S_tok[r] * S_w[e], g = s * (a . gate_e[j]), u = s * (a . up_e[j]): */
+/*   h[r, j] = bf16( silu(g) * u ),  j < F.                               */
+/*                                                                       */
+/* a_*            per-token NVFP4 operand (e.g. from                       */
+/*                nvfp4_quantize_per_token_gather), swizzled scales,      */
+/*                rows = group_offsets[num_groups].                       */
+/* group_offsets  HOST int64 [num_groups + 1], ascending multiples of 128. */
+/* w_codes        u8 [num_groups x 2F x K/2]: per expert the F gate rows  */
+/*                then the F up rows (nvfp4_quantize_weight_shared with   */
+/*                parts {gate, up}); w_scales: per expert a swizzled      */
+/*                [2F x K/16] matrix, mxq_scale_bytes(2F, K/16) apart;    */
+/*                w_group_scales f32 [num_groups].                         */
+/* h              bf16 [rows x F], row stride ldh elements (ldh % 8 == 0). */
+/* F % 128 == 0, K % 256 == 0, num_groups <= 256.                         */
+/* binary32 arithmetic (expf, IEEE divide) before the bf16 rounding.      */
+/* --------------------------------------------------------------------- */
+mxq_status mxq_moe_gate_up_swiglu_nvfp4(
+    const uint8_t* a_codes, const uint8_t* a_scales, const float* a_token_scales,
+    const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
+    const uint8_t* w_scales, const float* w_group_scales, int64_t F, int64_t K,
+    void* h, int64_t ldh, void* stream);
 
 #ifdef __cplusplus
 }

@@ -10,9 +10,9 @@ from ._lib import (  # noqa: F401
     MXQ_ERR_SHAPE, MXQ_ERR_TIMEOUT, MXQ_ERR_WORKSPACE, MXQ_OK, SCALE_LINEAR,
     SCALE_SWIZZLED, S_PER_BATCH, S_PER_ROW, Mxfp8Quantized, MxqError,
     Nvfp4Quantized, dequantize_mxfp8, dequantize_nvfp4, gemm_mxfp8,
-    gemm_nvfp4_grouped, get_last_error, lib,
+    gemm_nvfp4_grouped, get_last_error, lib, moe_gate_up_swiglu,
     mxfp8_quantize_rowcol, nvfp4_quantize_per_token,
-    nvfp4_quantize_weight_shared, scale_bytes, set_fault_inject,
-    status_string)
+    nvfp4_quantize_per_token_gather, nvfp4_quantize_weight_shared,
+    scale_bytes, set_fault_inject, status_string)
 
 __version__ = "0.1.0"

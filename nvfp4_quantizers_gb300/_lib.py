@@ -76,6 +76,9 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_quantize_per_token.restype = _int
         L.nvfp4_quantize_per_token.argtypes = [_p, _i64, _i64, _i64, _p, _p,
                                                _p, _int, _p]
+        L.nvfp4_quantize_per_token_gather.restype = _int
+        L.nvfp4_quantize_per_token_gather.argtypes = [
+            _p, _i64, _i64, _i64, _p, _i64, _p, _p, _p, _int, _p]
         L.nvfp4_quantize_weight_shared_workspace_size.restype = ctypes.c_size_t
         L.nvfp4_quantize_weight_shared_workspace_size.argtypes = [_i64]
         L.nvfp4_quantize_weight_shared.restype = _int
@@ -90,6 +93,9 @@ def lib() -> ctypes.CDLL:
         L.mxq_gemm_nvfp4_grouped.restype = _int
         L.mxq_gemm_nvfp4_grouped.argtypes = [_p, _p, _p, _p, _i64, _p, _p, _p,
                                              _i64, _i64, _p, _i64, _p]
+        L.mxq_moe_gate_up_swiglu_nvfp4.restype = _int
+        L.mxq_moe_gate_up_swiglu_nvfp4.argtypes = [
+            _p, _p, _p, _p, _i64, _p, _p, _p, _i64, _i64, _p, _i64, _p]
         L.dequantize_nvfp4.restype = _int
         L.dequantize_nvfp4.argtypes = [_p, _p, _p, _int, _i64, _i64, _i64,
                                        _int, _p, _p]
@@ -199,6 +205,31 @@ def nvfp4_quantize_per_token(x: torch.Tensor,
     _check(lib().nvfp4_quantize_per_token(
         x.data_ptr(), T, H, x.stride(0), codes.data_ptr(), bs.data_ptr(),
         S.data_ptr(), lay, _stream(dev)), "nvfp4_quantize_per_token")
+    return Nvfp4Quantized(codes, bs, S, lay)
+
+
+def nvfp4_quantize_per_token_gather(x: torch.Tensor, row_index: torch.Tensor,
+                                    scale_layout="swizzled") -> Nvfp4Quantized:
+    """Per-token NVFP4 quantization of gathered rows: output row t is row
+    row_index[t] of the bf16 [T_src, H] tensor x, or a zero row where the
+    index is outside [0, T_src) (C: nvfp4_quantize_per_token_gather)."""
+    x = _bf16_2d(x, "x")
+    if (row_index.dtype != torch.int32 or row_index.dim() != 1
+            or row_index.device != x.device or not row_index.is_contiguous()):
+        raise ValueError("row_index must be a contiguous int32 vector on "
+                         "x's device")
+    lay = _layout(scale_layout)
+    T_src, H = x.shape
+    T = row_index.numel()
+    dev = x.device
+    codes = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
+    bs = torch.empty((scale_bytes(T, H // 16, lay),), dtype=torch.uint8,
+                     device=dev)
+    S = torch.empty((T,), dtype=torch.float32, device=dev)
+    _check(lib().nvfp4_quantize_per_token_gather(
+        x.data_ptr(), T_src, H, x.stride(0), row_index.data_ptr(), T,
+        codes.data_ptr(), bs.data_ptr(), S.data_ptr(), lay, _stream(dev)),
+        "nvfp4_quantize_per_token_gather")
     return Nvfp4Quantized(codes, bs, S, lay)
 
 
@@ -337,3 +368,26 @@ def gemm_nvfp4_grouped(a_codes: torch.Tensor, a_scales: torch.Tensor,
         w_scales.data_ptr(), w_group_scales.data_ptr(), N, K, C.data_ptr(), N,
         _stream(a_codes.device)), "mxq_gemm_nvfp4_grouped")
     return C
+
+
+def moe_gate_up_swiglu(a_codes: torch.Tensor, a_scales: torch.Tensor,
+                       a_token_scales: torch.Tensor, group_offsets,
+                       w_codes: torch.Tensor, w_scales: torch.Tensor,
+                       w_group_scales: torch.Tensor) -> torch.Tensor:
+    """Grouped NVFP4 gate/up GEMM with SwiGLU in the epilogue
+    (C: mxq_moe_gate_up_swiglu_nvfp4).  w_codes [G, 2F, K/2] holds each
+    expert's F gate rows then its F up rows; returns bf16 h [rows, F],
+    h = silu(gate) * up with both FP32 scales applied first."""
+    offs = [int(v) for v in group_offsets]
+    G = len(offs) - 1
+    M_total, half = a_codes.shape
+    K = half * 2
+    F = w_codes.shape[1] // 2
+    off_arr = (ctypes.c_int64 * len(offs))(*offs)
+    h = torch.empty((M_total, F), dtype=torch.bfloat16, device=a_codes.device)
+    _check(lib().mxq_moe_gate_up_swiglu_nvfp4(
+        a_codes.data_ptr(), a_scales.data_ptr(), a_token_scales.data_ptr(),
+        ctypes.cast(off_arr, ctypes.c_void_p), G, w_codes.data_ptr(),
+        w_scales.data_ptr(), w_group_scales.data_ptr(), F, K, h.data_ptr(), F,
+        _stream(a_codes.device)), "mxq_moe_gate_up_swiglu_nvfp4")
+    return h

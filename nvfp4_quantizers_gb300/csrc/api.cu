@@ -249,7 +249,32 @@ mxq_status nvfp4_quantize_per_token(const void* x, int64_t T, int64_t H,
     return MXQ_ERR_ALIGN;
   if (fm == 1) return MXQ_ERR_CUDA;
   return from_cuda(launch_nvfp4_per_token(
-      x, T, H, ldx, codes, block_scales, token_scales,
+      x, T, H, ldx, nullptr, T, codes, block_scales, token_scales,
+      scale_layout == MXQ_SCALE_SWIZZLED, static_cast<cudaStream_t>(stream)));
+}
+
+mxq_status nvfp4_quantize_per_token_gather(
+    const void* x, int64_t T_src, int64_t H, int64_t ldx,
+    const int32_t* row_index, int64_t T, uint8_t* codes,
+    uint8_t* block_scales, float* token_scales, int scale_layout,
+    void* stream) {
+  const int fm = fault_mode();
+  if (fm == 2) return MXQ_ERR_ARG;
+  if (!valid_layout(scale_layout)) return MXQ_ERR_LAYOUT;
+  if (T < 0 || T_src < 0 || H < 0 || ldx < H) return MXQ_ERR_SHAPE;
+  if (T == 0 || H == 0) return MXQ_OK;
+  if (!row_index || !codes || !block_scales || !token_scales)
+    return MXQ_ERR_NULL;
+  if (T_src > 0 && !x) return MXQ_ERR_NULL;
+  if (H % 16 != 0 || H >= (1ll << 30) || T_src >= (1ll << 31))
+    return MXQ_ERR_SHAPE;
+  if ((x && !aligned16(x)) || ldx % 8 != 0 || !aligned16(codes) ||
+      !aligned16(block_scales) || !aligned16(token_scales) ||
+      (reinterpret_cast<uintptr_t>(row_index) & 3u) != 0)
+    return MXQ_ERR_ALIGN;
+  if (fm == 1) return MXQ_ERR_CUDA;
+  return from_cuda(launch_nvfp4_per_token(
+      x, T, H, ldx, row_index, T_src, codes, block_scales, token_scales,
       scale_layout == MXQ_SCALE_SWIZZLED, static_cast<cudaStream_t>(stream)));
 }
 
@@ -393,6 +418,40 @@ mxq_status mxq_gemm_nvfp4_grouped(
   return from_cuda(launch_gemm_nvfp4_grouped(
       a_codes, a_scales, a_token_scales, group_offsets, num_groups, w_codes,
       w_scales, w_group_scales, N, K, C, ldc,
+      static_cast<cudaStream_t>(stream)));
+}
+
+mxq_status mxq_moe_gate_up_swiglu_nvfp4(
+    const uint8_t* a_codes, const uint8_t* a_scales, const float* a_token_scales,
+    const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
+    const uint8_t* w_scales, const float* w_group_scales, int64_t F, int64_t K,
+    void* h, int64_t ldh, void* stream) {
+  const int fm = fault_mode();
+  if (fm == 2) return MXQ_ERR_ARG;
+  if (num_groups < 0 || num_groups > 256 || F < 0 || K < 0 || ldh < F)
+    return MXQ_ERR_SHAPE;
+  if (num_groups == 0 || F == 0) return MXQ_OK;
+  if (!group_offsets) return MXQ_ERR_NULL;
+  if (group_offsets[0] != 0) return MXQ_ERR_SHAPE;
+  for (int64_t g = 0; g < num_groups; ++g)
+    if (group_offsets[g + 1] < group_offsets[g] ||
+        group_offsets[g + 1] % 128 != 0)
+      return MXQ_ERR_SHAPE;
+  if (group_offsets[num_groups] == 0) return MXQ_OK;
+  if (!a_codes || !a_scales || !a_token_scales || !w_codes || !w_scales ||
+      !w_group_scales || !h)
+    return MXQ_ERR_NULL;
+  if (F % 128 != 0 || K % 256 != 0 || K == 0) return MXQ_ERR_SHAPE;
+  if (group_offsets[num_groups] >= (1ll << 31) ||
+      num_groups * 2 * F >= (1ll << 31) || K >= (1ll << 31))
+    return MXQ_ERR_SHAPE;
+  if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) ||
+      !aligned16(w_scales) || !aligned16(h) || ldh % 8 != 0)
+    return MXQ_ERR_ALIGN;
+  if (fm == 1) return MXQ_ERR_CUDA;
+  return from_cuda(launch_moe_gate_up_swiglu(
+      a_codes, a_scales, a_token_scales, group_offsets, num_groups, w_codes,
+      w_scales, w_group_scales, F, K, h, ldh,
       static_cast<cudaStream_t>(stream)));
 }
 

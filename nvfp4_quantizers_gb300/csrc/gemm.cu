@@ -292,6 +292,8 @@ struct GemmParams {
   int64_t row_off[257];     // first row of each group
   int64_t tiles_n;
   int64_t n_tiles;
+  int64_t tile_cols;        // output columns per tile: 256, or 128 (SwiGLU)
+  int64_t b_up_row;         // SwiGLU: row of the up half in a group's weights
   float* C;
   int64_t ldc;
 };
@@ -315,7 +317,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int64_t tile,
   const int64_t mt_in =
       p.kind == 1 ? mt_all - (t.grp ? p.tile_end[t.grp - 1] : 0) : mt_all;
   t.m0 = (p.kind == 1 ? p.row_off[t.grp] : 0) + mt_in * GM;
-  t.n0 = nt * GN;
+  t.n0 = nt * p.tile_cols;
   return t;
 }
 
@@ -328,7 +330,12 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int64_t tile,
 // warps copy it to registers (128 values per thread) and hand it back to
 // the MMA warp at once, then scale and store while the next tile's MMAs
 // already run.
-template <int CL>
+//
+// EPI = 0: C tile = the 128 x 256 accumulator (x S_tok x S_w for NVFP4),
+// fp32.  EPI = 1 (SwiGLU, NVFP4 gate/up weights [gate ; up] per group): the
+// B stage holds 128 gate rows and the 128 matching up rows, so one tile
+// gives 128 output columns h = silu(s g) * (s u), s = S_tok x S_w, bf16.
+template <int CL, int EPI>
 __global__ void __launch_bounds__(GTHREADS, 1)
     gemm_block_scaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
                              const __grid_constant__ CUtensorMap tmap_b,
@@ -375,7 +382,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
         const Tile t = decode_tile(p, u * CL + crank, &grp_cursor);
         // B row blocks of this tile that exist (the last column tile may
         // hold only 128 columns); rows past them are never stored.
-        const int nrb = t.n0 + 128 < p.N ? 2 : 1;
+        const int nrb = (EPI == 1 || t.n0 + 128 < p.N) ? 2 : 1;
         const uint32_t stage_bytes =
             (uint32_t)(GM * GKB + GN * GKB + 512 * n_sf * (1 + nrb));
         for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
@@ -395,19 +402,32 @@ __global__ void __launch_bounds__(GTHREADS, 1)
                            &tmap_a, (int32_t)(kt * GKB),
                            (int32_t)(t.m0 + crank * (GM / CL)), full, cmask);
           }
-          tma_load_2d(smem_addr(s.b[st]), &tmap_b, (int32_t)(kt * GKB),
-                      (int32_t)(t.grp * p.b_rows_group_stride + t.n0), full);
+          const int64_t brow = t.grp * p.b_rows_group_stride + t.n0;
+          if (EPI == 0) {
+            tma_load_2d(smem_addr(s.b[st]), &tmap_b, (int32_t)(kt * GKB),
+                        (int32_t)brow, full);
+          } else {
+            // gate rows n0.. and up rows up_row + n0.. (128-row boxes)
+            tma_load_2d(smem_addr(s.b[st]), &tmap_b, (int32_t)(kt * GKB),
+                        (int32_t)brow, full);
+            tma_load_2d(smem_addr(s.b[st]) + 128 * GKB, &tmap_b,
+                        (int32_t)(kt * GKB), (int32_t)(brow + p.b_up_row),
+                        full);
+          }
           // The stage's n_sf scale tiles of one 128-row block are
           // consecutive in the swizzled layout: one copy per row block.
           const int64_t ct = kt * n_sf;
           bulk_g2s(smem_addr(s.sfa[st][0]),
                    p.a_sf + ((t.m0 / 128) * p.a_sf_ct + ct) * 512,
                    512u * n_sf, full);
-          for (int rb = 0; rb < nrb; ++rb)
+          for (int rb = 0; rb < nrb; ++rb) {
+            const int64_t rblk =
+                EPI == 0 ? t.n0 / 128 + rb : (t.n0 + rb * p.b_up_row) / 128;
             bulk_g2s(smem_addr(s.sfb[st][rb][0]),
                      p.b_sf + t.grp * p.b_sf_group_stride +
-                         ((t.n0 / 128 + rb) * p.b_sf_ct + ct) * 512,
+                         (rblk * p.b_sf_ct + ct) * 512,
                      512u * n_sf, full);
+          }
         }
         if (s.abort) break;
       }
@@ -528,10 +548,23 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       if (!ok) break;
       tc_fence_after();
       uint32_t r[128];
-      const uint32_t taddr =
-          tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      if (EPI == 0) {
+        // columns h*128 .. h*128+127
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc_ld_32x32_async(taddr + c * 32, r + c * 32);
+        for (int c = 0; c < 4; ++c)
+          tc_ld_32x32_async(lane_base + (uint32_t)(h * 128 + c * 32),
+                            r + c * 32);
+      } else {
+        // gate columns h*64.. (r[0..63]) and up columns 128 + h*64..
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tc_ld_32x32_async(lane_base + (uint32_t)(h * 64 + c * 32),
+                            r + c * 32);
+          tc_ld_32x32_async(lane_base + (uint32_t)(128 + h * 64 + c * 32),
+                            r + 64 + c * 32);
+        }
+      }
       tc_wait_ld();
       // The accumulator may be overwritten once all eight warps hold it.
       tc_fence_before();
@@ -542,32 +575,65 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       float rs = 1.0f;
       if (p.kind == 1)
         rs = __fmul_rn(p.s_tok[t.m0 + q * 32 + lane], p.s_w[t.grp]);
-      const int64_t x0 = t.n0 + h * 128;
+      uint8_t* row = box + lane * 128;
+      if (EPI == 0) {
+        const int64_t x0 = t.n0 + h * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (x0 + c * 32 >= p.N) break;  // columns past N: not stored
-        if (lane == 0) bulk_wait_read_0();  // the box's previous store
+        for (int c = 0; c < 4; ++c) {
+          if (x0 + c * 32 >= p.N) break;  // columns past N: not stored
+          if (lane == 0) bulk_wait_read_0();  // the box's previous store
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float4 v;
+            v.x = __uint_as_float(r[c * 32 + 4 * j]);
+            v.y = __uint_as_float(r[c * 32 + 4 * j + 1]);
+            v.z = __uint_as_float(r[c * 32 + 4 * j + 2]);
+            v.w = __uint_as_float(r[c * 32 + 4 * j + 3]);
+            if (p.kind == 1) {
+              v.x = __fmul_rn(v.x, rs);
+              v.y = __fmul_rn(v.y, rs);
+              v.z = __fmul_rn(v.z, rs);
+              v.w = __fmul_rn(v.w, rs);
+            }
+            *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) = v;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmap_c, smem_addr(box), (int32_t)(x0 + c * 32),
+                         (int32_t)(t.m0 + q * 32));
+            bulk_commit();
+          }
+        }
+      } else {
+        // h = silu(s g) * (s u) in binary32 (expf, IEEE divide), to bf16;
+        // one 32 x 64 bf16 box per warp.
+        if (lane == 0) bulk_wait_read_0();
         __syncwarp();
-        uint8_t* row = box + lane * 128;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          float4 v;
-          v.x = __uint_as_float(r[c * 32 + 4 * j]);
-          v.y = __uint_as_float(r[c * 32 + 4 * j + 1]);
-          v.z = __uint_as_float(r[c * 32 + 4 * j + 2]);
-          v.w = __uint_as_float(r[c * 32 + 4 * j + 3]);
-          if (p.kind == 1) {
-            v.x = __fmul_rn(v.x, rs);
-            v.y = __fmul_rn(v.y, rs);
-            v.z = __fmul_rn(v.z, rs);
-            v.w = __fmul_rn(v.w, rs);
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float o[2];
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const int col = j * 8 + k * 2 + e2;
+              const float g = __fmul_rn(__uint_as_float(r[col]), rs);
+              const float uu = __fmul_rn(__uint_as_float(r[64 + col]), rs);
+              const float sg = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+              o[e2] = __fmul_rn(sg, uu);
+            }
+            w[k] = f32x2_to_bf16x2(o[0], o[1]);
           }
-          *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) = v;
+          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmap_c, smem_addr(box), (int32_t)(x0 + c * 32),
+          tma_store_2d(&tmap_c, smem_addr(box), (int32_t)(t.n0 + h * 64),
                        (int32_t)(t.m0 + q * 32));
           bulk_commit();
         }
@@ -606,11 +672,11 @@ struct AOperand {
   int64_t row_bytes, rows;
 };
 
-template <int CL>
+template <int CL, int EPI>
 cudaError_t launch_gemm_cl(const AOperand& a, const CUtensorMap& tb,
                            const CUtensorMap& tc, const GemmParams& pp,
                            int dev, cudaStream_t stream) {
-  auto kern = gemm_block_scaled_kernel<CL>;
+  auto kern = gemm_block_scaled_kernel<CL, EPI>;
   const size_t smem = gemm_smem_bytes();
   static int configured[64] = {};
   static int max_clusters[64] = {};
@@ -658,20 +724,44 @@ cudaError_t launch_gemm_cl(const AOperand& a, const CUtensorMap& tb,
 
 // Tiles of one row block are paired across a 2-CTA cluster when the
 // column-tile count is even; otherwise one CTA per cluster.
+template <int EPI>
 cudaError_t launch_gemm(const AOperand& a, const CUtensorMap& tb,
-                        const GemmParams& p, int64_t tiles,
-                        cudaStream_t stream) {
-  CUtensorMap tc;
-  cudaError_t err = make_tmap_c(&tc, p.C, p.M, p.N, p.ldc);
-  if (err != cudaSuccess) return err;
+                        const CUtensorMap& tc, const GemmParams& p,
+                        int64_t tiles, cudaStream_t stream) {
   int dev = 0;
-  err = cudaGetDevice(&dev);
+  cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   GemmParams pp = p;
   pp.n_tiles = tiles;
   if (p.tiles_n % 2 == 0)
-    return launch_gemm_cl<2>(a, tb, tc, pp, dev, stream);
-  return launch_gemm_cl<1>(a, tb, tc, pp, dev, stream);
+    return launch_gemm_cl<2, EPI>(a, tb, tc, pp, dev, stream);
+  return launch_gemm_cl<1, EPI>(a, tb, tc, pp, dev, stream);
+}
+
+// Grouped NVFP4 parameters shared by the plain and the SwiGLU GEMM.
+void grouped_params(GemmParams& p, const uint8_t* a_scales, const float* a_s,
+                    const int64_t* group_offsets, int64_t num_groups,
+                    const uint8_t* w_scales, const float* w_s, int64_t w_rows,
+                    int64_t K, int64_t* tiles_m) {
+  p.kind = 1;
+  p.M = group_offsets[num_groups];
+  p.K = K;
+  p.k_stages = K / 256;                 // 256 fp4 values (128 bytes) per stage
+  p.a_sf = a_scales;
+  p.b_sf = w_scales;
+  p.a_sf_ct = (K / 16 + 3) / 4;
+  p.b_sf_ct = p.a_sf_ct;
+  p.b_sf_group_stride = scale_bytes(w_rows, K / 16, 1);
+  p.b_rows_group_stride = w_rows;
+  p.s_tok = a_s;
+  p.s_w = w_s;
+  p.num_groups = (int)num_groups;
+  *tiles_m = 0;
+  for (int64_t g = 0; g < num_groups; ++g) {
+    p.row_off[g] = group_offsets[g];
+    *tiles_m += (group_offsets[g + 1] - group_offsets[g]) / GM;
+    p.tile_end[g] = *tiles_m;
+  }
 }
 
 }  // namespace
@@ -706,10 +796,14 @@ cudaError_t launch_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
   p.b_rows_group_stride = 0;
   p.num_groups = 1;
   p.tiles_n = (N + GN - 1) / GN;
+  p.tile_cols = GN;
   p.C = C;
   p.ldc = ldc;
-  return launch_gemm(AOperand{a_codes, K, M}, tb, p, (M / GM) * p.tiles_n,
-                     stream);
+  CUtensorMap tc;
+  err = make_tmap_c(&tc, C, M, N, ldc);
+  if (err != cudaSuccess) return err;
+  return launch_gemm<0>(AOperand{a_codes, K, M}, tb, tc, p,
+                        (M / GM) * p.tiles_n, stream);
 }
 
 cudaError_t launch_gemm_nvfp4_grouped(
@@ -717,41 +811,59 @@ cudaError_t launch_gemm_nvfp4_grouped(
     const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
     const uint8_t* w_scales, const float* w_s, int64_t N, int64_t K, float* C,
     int64_t ldc, cudaStream_t stream) {
-  const int64_t m_total = group_offsets[num_groups];
-  CUtensorMap tb;
   // Packed E2M1: K/2 bytes per row; all groups' weights as one
   // [num_groups * N x K/2] byte matrix.
+  CUtensorMap tb;
   cudaError_t err = make_tmap_2d_u8(&tb, w_codes, (uint64_t)(K / 2),
                                     (uint64_t)(num_groups * N),
                                     (uint64_t)(K / 2), GN);
   if (err != cudaSuccess) return err;
   GemmParams p = {};
-  p.kind = 1;
-  p.M = m_total;
-  p.N = N;
-  p.K = K;
-  p.k_stages = K / 256;                 // 256 fp4 values (128 bytes) per stage
-  p.a_sf = a_scales;
-  p.b_sf = w_scales;
-  p.a_sf_ct = (K / 16 + 3) / 4;
-  p.b_sf_ct = p.a_sf_ct;
-  p.b_sf_group_stride = scale_bytes(N, K / 16, 1);
-  p.b_rows_group_stride = N;
-  p.s_tok = a_s;
-  p.s_w = w_s;
-  p.num_groups = (int)num_groups;
   int64_t tiles_m = 0;
-  for (int64_t g = 0; g < num_groups; ++g) {
-    p.row_off[g] = group_offsets[g];
-    tiles_m += (group_offsets[g + 1] - group_offsets[g]) / GM;
-    p.tile_end[g] = tiles_m;
-  }
+  grouped_params(p, a_scales, a_s, group_offsets, num_groups, w_scales, w_s,
+                 N, K, &tiles_m);
+  p.N = N;
   p.tiles_n = (N + GN - 1) / GN;
+  p.tile_cols = GN;
   p.C = C;
   p.ldc = ldc;
   if (tiles_m == 0) return cudaSuccess;
-  return launch_gemm(AOperand{a_codes, K / 2, m_total}, tb, p,
-                     tiles_m * p.tiles_n, stream);
+  CUtensorMap tc;
+  err = make_tmap_c(&tc, C, p.M, N, ldc);
+  if (err != cudaSuccess) return err;
+  return launch_gemm<0>(AOperand{a_codes, K / 2, p.M}, tb, tc, p,
+                        tiles_m * p.tiles_n, stream);
+}
+
+cudaError_t launch_moe_gate_up_swiglu(
+    const uint8_t* a_codes, const uint8_t* a_scales, const float* a_s,
+    const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
+    const uint8_t* w_scales, const float* w_s, int64_t F, int64_t K,
+    void* out, int64_t ldo, cudaStream_t stream) {
+  // weights: [num_groups * 2F x K/2] bytes, gate rows then up rows per
+  // group, loaded as 128-row boxes (gate block and matching up block)
+  CUtensorMap tb;
+  cudaError_t err = make_tmap_2d_u8(&tb, w_codes, (uint64_t)(K / 2),
+                                    (uint64_t)(num_groups * 2 * F),
+                                    (uint64_t)(K / 2), 128);
+  if (err != cudaSuccess) return err;
+  GemmParams p = {};
+  int64_t tiles_m = 0;
+  grouped_params(p, a_scales, a_s, group_offsets, num_groups, w_scales, w_s,
+                 2 * F, K, &tiles_m);
+  p.N = F;                              // output columns
+  p.tiles_n = F / 128;
+  p.tile_cols = 128;
+  p.b_up_row = F;
+  p.C = nullptr;
+  p.ldc = ldo;
+  if (tiles_m == 0) return cudaSuccess;
+  CUtensorMap tc;                       // bf16 h [rows x F], 32 x 64 boxes
+  err = make_tmap_2d_bf16(&tc, out, (uint64_t)F, (uint64_t)p.M,
+                          (uint64_t)ldo * 2, 64, 32, true);
+  if (err != cudaSuccess) return err;
+  return launch_gemm<1>(AOperand{a_codes, K / 2, p.M}, tb, tc, p,
+                        tiles_m * p.tiles_n, stream);
 }
 
 }  // namespace mxq

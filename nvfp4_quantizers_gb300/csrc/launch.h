@@ -39,8 +39,11 @@ cudaError_t launch_mxfp8_rowcol(const void* x, int64_t M, int64_t K,
                                 cudaStream_t stream);
 
 // nvfp4.cu
+// row_index: NULL, or a device int32 [T]: output row t quantizes x row
+// row_index[t] (indices outside [0, T_src) give a zero row).
 cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
-                                   int64_t ldx, uint8_t* codes,
+                                   int64_t ldx, const int32_t* row_index,
+                                   int64_t T_src, uint8_t* codes,
                                    uint8_t* scales, float* token_scales,
                                    int swizzled, cudaStream_t stream);
 
@@ -103,6 +106,12 @@ cudaError_t launch_gemm_nvfp4_grouped(
     const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
     const uint8_t* w_scales, const float* w_s, int64_t N, int64_t K, float* C,
     int64_t ldc, cudaStream_t stream);
+// h = silu(gate) * up over the grouped gate/up GEMM, bf16 [rows x F].
+cudaError_t launch_moe_gate_up_swiglu(
+    const uint8_t* a_codes, const uint8_t* a_scales, const float* a_s,
+    const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
+    const uint8_t* w_scales, const float* w_s, int64_t F, int64_t K,
+    void* out, int64_t ldo, cudaStream_t stream);
 
 // Scale-matrix size in bytes for either layout.
 inline int64_t scale_bytes(int64_t rows, int64_t cols, int swizzled) {

@@ -145,7 +145,7 @@ __device__ __forceinline__ void store_block(const RowOut& o, int64_t b,
 // named barrier (id 1 + row slot, 32*WPR threads).
 template <int R, int WPR>
 __device__ __forceinline__ void encode_row_warps(
-    const uint16_t* row, bool real, float S_given, bool use_given,
+    const uint16_t* row, bool load, bool write, float S_given, bool use_given,
     const RowOut& o, int row_slot, int wpart, int lane, uint32_t* red,
     float* S_used) {
   const int64_t blk0 = (int64_t)wpart * R * 32;
@@ -155,7 +155,7 @@ __device__ __forceinline__ void encode_row_warps(
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int64_t b = blk0 + r * 32 + lane;
-    load_block(v[r], row, b, real && b < o.nblocks);
+    load_block(v[r], row, b, load && b < o.nblocks);
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -178,7 +178,7 @@ __device__ __forceinline__ void encode_row_warps(
     if (blk0 + r * 32 >= o.nblocks) break;             // warp-uniform
     uint32_t lo, hi, sb;
     encode_block(v[r], am[r], S, six_s, lo, hi, sb);
-    store_block(o, blk0 + r * 32 + lane, real, lo, hi, sb, lane);
+    store_block(o, blk0 + r * 32 + lane, write, lo, hi, sb, lane);
   }
   *S_used = S;
 }
@@ -189,7 +189,9 @@ __device__ __forceinline__ void encode_row_warps(
 template <int R, int WPR>
 __global__ void __launch_bounds__(CTA_WARPS * 32)
     nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t T_pad,
-                       int64_t H, int64_t ldx, uint8_t* __restrict__ codes,
+                       int64_t H, int64_t ldx,
+                       const int32_t* __restrict__ row_index, int64_t T_src,
+                       uint8_t* __restrict__ codes,
                        uint8_t* __restrict__ scales, float* __restrict__ S_out,
                        int swizzled) {
   constexpr int ROWS = CTA_WARPS / WPR;
@@ -200,11 +202,17 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
   pdl_wait();
   if (t >= T_pad) return;                 // uniform over the row's warps
   const bool real = t < T;
+  int64_t src = t;
+  bool load = real;
+  if (row_index && real) {                // gather: row t <- x[row_index[t]]
+    src = row_index[t];
+    load = src >= 0 && src < T_src;       // other indices: a zero row
+  }
   RowOut o{codes + t * (H >> 1), scales, t, ((H >> 4) + 3) >> 2, H >> 4,
            swizzled};
   float S;
-  encode_row_warps<R, WPR>(x + t * ldx, real, 0.0f, false, o, slot, wpart,
-                           lane, red, &S);
+  encode_row_warps<R, WPR>(load ? x + src * ldx : x, load, real, 0.0f, false,
+                           o, slot, wpart, lane, red, &S);
   if (real && wpart == 0 && lane == 0) S_out[t] = S;
   pdl_launch_dependents();
 }
@@ -214,14 +222,21 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 __global__ void __launch_bounds__(CTA_WARPS * 32)
     nvfp4_token_long_kernel(const uint16_t* __restrict__ x, int64_t T,
                             int64_t H, int64_t ldx,
-                            uint8_t* __restrict__ codes,
+                            const int32_t* __restrict__ row_index,
+                            int64_t T_src, uint8_t* __restrict__ codes,
                             uint8_t* __restrict__ scales,
                             float* __restrict__ S_out, int swizzled) {
   __shared__ uint32_t red[CTA_WARPS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = blockIdx.x;
   const bool real = t < T;
-  const uint16_t* row = x + t * ldx;
+  int64_t src = t;
+  bool load = real;
+  if (row_index && real) {                // gather: row t <- x[row_index[t]]
+    src = row_index[t];
+    load = src >= 0 && src < T_src;
+  }
+  const uint16_t* row = load ? x + src * ldx : x;
   pdl_wait();
   RowOut o{codes + t * (H >> 1), scales, t, ((H >> 4) + 3) >> 2, H >> 4,
            swizzled};
@@ -230,7 +245,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
   for (int64_t b0 = 0; b0 < o.nblocks; b0 += span) {
     const int64_t b = b0 + threadIdx.x;
     Blk v;
-    load_block(v, row, b, real && b < o.nblocks);
+    load_block(v, row, b, load && b < o.nblocks);
     a = max(a, block_absmax(v));
   }
   a = warp_max(a);
@@ -243,7 +258,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
     if (b0 + warp * 32 >= o.nblocks) continue;         // warp-uniform
     const int64_t b = b0 + threadIdx.x;
     Blk v;
-    load_block(v, row, b, real && b < o.nblocks);
+    load_block(v, row, b, load && b < o.nblocks);
     uint32_t lo, hi, sb;
     encode_block(v, block_absmax(v), S, six_s, lo, hi, sb);
     store_block(o, b, real, lo, hi, sb, lane);
@@ -430,8 +445,8 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
                p.scales + g * p.scale_stride, r, ((p.K >> 4) + 3) >> 2,
                p.K >> 4, p.swizzled};
       float S_used;
-      encode_row_warps<R, WPR>(row, real, S, true, o, slot, wpart, lane, red,
-                               &S_used);
+      encode_row_warps<R, WPR>(row, real, real, S, true, o, slot, wpart, lane,
+                               red, &S_used);
     }
     __syncthreads();                  // s_S and red are reused by the next task
   }
@@ -457,7 +472,8 @@ RowShape pick_shape(int64_t H) {
 }  // namespace
 
 cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
-                                   int64_t ldx, uint8_t* codes,
+                                   int64_t ldx, const int32_t* row_index,
+                                   int64_t T_src, uint8_t* codes,
                                    uint8_t* scales, float* token_scales,
                                    int swizzled, cudaStream_t stream) {
   const int64_t T_pad = swizzled ? (T + 127) / 128 * 128 : T;
@@ -466,14 +482,14 @@ cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
   if (sh.R == 0) {
     return launch_pdl(nvfp4_token_long_kernel, dim3((unsigned)T_pad),
                       dim3(CTA_WARPS * 32), 0, stream, false, xs, T, H, ldx,
-                      codes, scales, token_scales, swizzled);
+                      row_index, T_src, codes, scales, token_scales, swizzled);
   }
   const int rows_per_cta = CTA_WARPS / sh.WPR;
   const unsigned grid = (unsigned)((T_pad + rows_per_cta - 1) / rows_per_cta);
 #define MXQ_TOKEN_LAUNCH(R_, W_)                                          \
   launch_pdl(nvfp4_token_kernel<R_, W_>, dim3(grid), dim3(CTA_WARPS * 32), \
-             0, stream, false, xs, T, T_pad, H, ldx, codes, scales,        \
-             token_scales, swizzled)
+             0, stream, false, xs, T, T_pad, H, ldx, row_index, T_src,     \
+             codes, scales, token_scales, swizzled)
   if (sh.R == 1) return MXQ_TOKEN_LAUNCH(1, 1);
   if (sh.R == 2) return MXQ_TOKEN_LAUNCH(2, 1);
   if (sh.WPR == 1) return MXQ_TOKEN_LAUNCH(4, 1);

@@ -111,6 +111,27 @@ def test_dequant_argument_errors(L):
     assert L.dequantize_nvfp4(FAKE, FAKE, FAKE, 0, 0, 4, 64, 1, FAKE, None) == q.MXQ_OK
 
 
+def test_moe_entry_point_argument_errors(L):
+    import nvfp4_quantizers_gb300 as q
+    g = L.nvfp4_quantize_per_token_gather
+    assert g(FAKE, 10, 64, 64, None, 4, FAKE, FAKE, FAKE, 1, None) == q.MXQ_ERR_NULL
+    assert g(FAKE, 10, 40, 40, FAKE, 4, FAKE, FAKE, FAKE, 1, None) == q.MXQ_ERR_SHAPE
+    assert g(FAKE, 10, 64, 64, FAKE + 2, 4, FAKE, FAKE, FAKE, 1, None) == q.MXQ_ERR_ALIGN
+    assert g(FAKE, 10, 64, 64, FAKE, 4, FAKE, FAKE, FAKE, 7, None) == q.MXQ_ERR_LAYOUT
+    assert g(FAKE, 10, 64, 64, FAKE, 0, None, None, None, 1, None) == q.MXQ_OK
+    f = L.mxq_moe_gate_up_swiglu_nvfp4
+    offs = (ctypes.c_int64 * 3)(0, 128, 256)
+    O = ctypes.cast(offs, ctypes.c_void_p)
+    assert f(FAKE, FAKE, FAKE, O, 2, FAKE, FAKE, FAKE, 192, 256, FAKE, 192, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, O, 2, FAKE, FAKE, FAKE, 128, 128, FAKE, 128, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, O, 2, FAKE, FAKE, FAKE, 128, 256, None, 128, None) == q.MXQ_ERR_NULL
+    assert f(FAKE, FAKE, FAKE, O, 2, FAKE, FAKE, FAKE, 128, 256, FAKE, 132, None) == q.MXQ_ERR_ALIGN
+    bad = (ctypes.c_int64 * 3)(0, 100, 256)
+    assert f(FAKE, FAKE, FAKE, ctypes.cast(bad, ctypes.c_void_p), 2, FAKE, FAKE,
+             FAKE, 128, 256, FAKE, 128, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, O, 0, FAKE, FAKE, FAKE, 128, 256, FAKE, 128, None) == q.MXQ_OK
+
+
 def test_fault_injection_returns_errors_without_launching(L):
     import nvfp4_quantizers_gb300 as q
     try:

@@ -283,3 +283,19 @@ def topk_routing(n_tokens=4096, n_experts=128, k=8, seed=0) -> np.ndarray:
 def gemm_tokens(n_tokens=4096, H=2048, seed=0):
     return to_bf16_bits(_rng(seed, 15).standard_normal((n_tokens, H),
                                                        dtype=np.float32))
+
+
+def expert_gather_index(route: np.ndarray, n_experts: int, pad: int = 128):
+    """Rows of the grouped expert GEMM from top-k routing: expert e's group
+    lists (in token order) the tokens routed to it, padded with -1 entries
+    to a multiple of `pad` rows.  Returns (row_index int32 [rows],
+    offsets int64 [n_experts + 1], group sizes before padding)."""
+    idx, offs, sizes = [], [0], []
+    for e in range(n_experts):
+        toks = np.nonzero((route == e).any(axis=1))[0]
+        sizes.append(len(toks))
+        padded = -(-len(toks) // pad) * pad
+        idx.append(np.concatenate([toks, np.full(padded - len(toks), -1)]))
+        offs.append(offs[-1] + padded)
+    return (np.concatenate(idx).astype(np.int32), np.array(offs, np.int64),
+            np.array(sizes))
