@@ -473,6 +473,39 @@ def run_gemm(q, W, dev, stream, reps=20):
         **{"TFLOP/s_routed": round(fl_routed / ms / 1e9, 1),
            "padded_rows": Mp, "routed_rows": 32768,
            "peak_fp4": round(peaks["fp4"], 1)})
+    # MoE expert forward up to the activation: routing gather fused into
+    # the per-token quantizer, then the gate/up GEMM with SwiGLU (bf16 h).
+    idx, offs2, _ = W.expert_gather_index(route, E)
+    tok_dev = torch.from_numpy(tokens.view(np.int16)).view(
+        torch.bfloat16).to(dev)
+    idx_dev = torch.from_numpy(idx).to(dev)
+
+    def t_gq():
+        return q.nvfp4_quantize_per_token_gather(tok_dev, idx_dev)
+    ms_gq = _time_fn(t_gq, stream, reps)
+    tg = t_gq()
+
+    def t_sw():
+        return q.moe_gate_up_swiglu(tg.codes, tg.block_scales, tg.scales,
+                                    offs2, tw.codes, tw.block_scales,
+                                    tw.scales)
+    ms_sw = _time_fn(t_sw, stream, reps)
+    Mp2 = int(offs2[-1])
+    # gather-quantize: the unique tokens read once, gathered codes, block
+    # scales and token scales written
+    nb_gq = 4096 * H * 2 + Mp2 * H * (0.5 + 1 / 16) + 4 * Mp2
+    # SwiGLU GEMM: operands as above, bf16 h [rows x F]
+    nb_sw = Mp2 * H * (0.5 + 1 / 16) + 4 * Mp2 + \
+        E * 2 * F * H * (0.5 + 1 / 16) + 4 * E + Mp2 * F * 2
+    out["moe_gate_up_swiglu_4096tok_top8_128x768x2048"] = dict(
+        gemm_roofline(ms_sw * 1e3, 2.0 * Mp2 * 2 * F * H, nb_sw,
+                      peaks["fp4"]),
+        **{"gather_quantize_us": round(ms_gq * 1e3, 2),
+           "gather_quantize_GB/s": round(nb_gq / ms_gq / 1e6, 1),
+           "gather_quantize_hbm_frac": round(
+               nb_gq / ms_gq / 1e6 / measured_peak()[0], 3),
+           "forward_us": round((ms_gq + ms_sw) * 1e3, 2),
+           "padded_rows": Mp2, "output": "bf16 h [rows x 768]"})
     out["peaks_kind"] = peaks["kind"]
     return out
 

@@ -354,7 +354,8 @@ mxq_status mxq_gemm_nvfp4_grouped(
 /*                w_group_scales f32 [num_groups].                         */
 /* h              bf16 [rows x F], row stride ldh elements (ldh % 8 == 0). */
 /* F % 128 == 0, K % 256 == 0, num_groups <= 256.                         */
-/* binary32 arithmetic (expf, IEEE divide) before the bf16 rounding.      */
+/* binary32 arithmetic before the bf16 rounding; silu uses a fast         */
+/* exponential and divide (relative error below 2^-20, far inside bf16).  */
 /* --------------------------------------------------------------------- */
 mxq_status mxq_moe_gate_up_swiglu_nvfp4(
     const uint8_t* a_codes, const uint8_t* a_scales, const float* a_token_scales,

@@ -334,7 +334,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int64_t tile,
 // EPI = 0: C tile = the 128 x 256 accumulator (x S_tok x S_w for NVFP4),
 // fp32.  EPI = 1 (SwiGLU, NVFP4 gate/up weights [gate ; up] per group): the
 // B stage holds 128 gate rows and the 128 matching up rows, so one tile
-// gives 128 output columns h = silu(s g) * (s u), s = S_tok x S_w, bf16.
+// gives 128 output columns h = silu(s g) * (s u), s = S_tok x S_w, bf16
+// (binary32 with a fast exponential and divide before the bf16 rounding).
 template <int CL, int EPI>
 __global__ void __launch_bounds__(GTHREADS, 1)
     gemm_block_scaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -607,8 +608,10 @@ __global__ void __launch_bounds__(GTHREADS, 1)
           }
         }
       } else {
-        // h = silu(s g) * (s u) in binary32 (expf, IEEE divide), to bf16;
-        // one 32 x 64 bf16 box per warp.
+        // h = silu(s g) * (s u) in binary32, to bf16; one 32 x 64 bf16 box
+        // per warp.  The fast exponential and divide (relative error below
+        // 2^-20) are far inside the bf16 rounding (2^-9); for very negative
+        // g, 1 + e^-g overflows and sigmoid comes out 0, the limit.
         if (lane == 0) bulk_wait_read_0();
         __syncwarp();
 #pragma unroll
@@ -616,16 +619,18 @@ __global__ void __launch_bounds__(GTHREADS, 1)
           uint32_t w[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            float o[2];
-#pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-              const int col = j * 8 + k * 2 + e2;
-              const float g = __fmul_rn(__uint_as_float(r[col]), rs);
-              const float uu = __fmul_rn(__uint_as_float(r[64 + col]), rs);
-              const float sg = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
-              o[e2] = __fmul_rn(sg, uu);
-            }
-            w[k] = f32x2_to_bf16x2(o[0], o[1]);
+            const int col = j * 8 + k * 2;
+            float g0, g1, u0, u1;
+            fmul2(__uint_as_float(r[col]), __uint_as_float(r[col + 1]), rs,
+                  rs, g0, g1);
+            fmul2(__uint_as_float(r[64 + col]),
+                  __uint_as_float(r[64 + col + 1]), rs, rs, u0, u1);
+            const float s0 = __fdividef(1.0f, 1.0f + __expf(-g0));
+            const float s1 = __fdividef(1.0f, 1.0f + __expf(-g1));
+            float h0, h1;
+            fmul2(g0, g1, s0, s1, h0, h1);
+            fmul2(h0, h1, u0, u1, h0, h1);
+            w[k] = f32x2_to_bf16x2(h0, h1);
           }
           *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) =
               make_uint4(w[0], w[1], w[2], w[3]);

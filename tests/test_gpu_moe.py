@@ -7,7 +7,8 @@ the GEMM epilogue).
 
 The gather quantizer is byte-exact against the oracle applied to the
 gathered rows.  The SwiGLU GEMM writes bf16: the kernel accumulates in fp32
-and evaluates silu with expf and an IEEE divide, so each output is within
+and evaluates silu with a fast exponential and divide (relative error below
+2^-20), so each output is within
 one bf16 ulp (2^-7 relative) of the float64 oracle rounded the same way,
 except where the value is tiny against the row's scale (cancellation in the
 fp32 sums): an absolute floor of 1e-3 of the output's RMS covers those.
