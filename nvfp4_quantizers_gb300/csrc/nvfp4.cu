@@ -286,7 +286,8 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 // one word per group serialises the hundreds of CTAs that finish together.
 // ---------------------------------------------------------------------------
 constexpr int kMaxGroupsPerLaunch = 256;
-constexpr int64_t kTaskChunks = 2048;         // 16-byte chunks per amax task
+constexpr int64_t kTaskChunks = 4096;         // 16-byte chunks per amax task
+constexpr int kRowSetsPerTask = 2;            // encode task: 2 x ROWS rows
 constexpr int kWsHeaderWords = 64;            // [1 + launch] = task counters
 
 // Error word of the bounded waits of this translation unit.
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
   constexpr int ROWS = CTA_WARPS / WPR;
   __shared__ uint32_t red[CTA_WARPS];
   __shared__ int s_abort;
-  __shared__ int64_t s_task;
+  __shared__ int64_t s_task[2];
   __shared__ float s_S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slot = warp / WPR, wpart = warp % WPR;
@@ -353,16 +354,21 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
   uint32_t* amax = p.ws + kWsHeaderWords;      // unused when S_in is given
   const int64_t total = (int64_t)p.ng * (p.S_in ? p.nE : p.nA + p.nE);
   int64_t t_static = blockIdx.x;
+  // The next task's index is fetched while the current task runs (slot
+  // buf ^ 1); the barrier that ends every task publishes it.
+  if (!p.S_in && threadIdx.x == 0) s_task[0] = (int64_t)atomicAdd(p.counter, 1u);
+  __syncthreads();
+  int buf = 0;
   while (true) {
     int64_t t;
     if (p.S_in) {
       t = t_static;                   // no amax: a static round robin
       t_static += gridDim.x;
     } else {
-      if (threadIdx.x == 0) s_task = (int64_t)atomicAdd(p.counter, 1u);
-      __syncthreads();
-      t = s_task;
-      __syncthreads();
+      t = s_task[buf];
+      if (t < total && threadIdx.x == 0)
+        s_task[buf ^ 1] = (int64_t)atomicAdd(p.counter, 1u);
+      buf ^= 1;
     }
     if (t >= total) break;
     bool is_a;
@@ -431,7 +437,8 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
     }
     __syncthreads();
     const float S = s_S;
-    const int64_t r = idx * ROWS + slot;
+    for (int rs = 0; rs < kRowSetsPerTask; ++rs) {
+    const int64_t r = (idx * kRowSetsPerTask + rs) * ROWS + slot;
     if (r < p.R_pad && !s_abort) {                      // uniform over the row
       const bool real = r < p.R;
       const uint16_t* row = nullptr;
@@ -447,6 +454,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
       float S_used;
       encode_row_warps<R, WPR>(row, real, real, S, true, o, slot, wpart, lane,
                                red, &S_used);
+    }
     }
     __syncthreads();                  // s_S and red are reused by the next task
   }
@@ -556,7 +564,8 @@ cudaError_t launch_nvfp4_weight_shared(
   p.R_pad = swizzled ? (p.R + 127) / 128 * 128 : p.R;
   p.K = K;
   p.nA = (p.part_chunk0[num_parts] + kTaskChunks - 1) / kTaskChunks;
-  p.nE = (p.R_pad + (CTA_WARPS / sh.WPR) - 1) / (CTA_WARPS / sh.WPR);
+  const int64_t rows_per_task = kRowSetsPerTask * (CTA_WARPS / sh.WPR);
+  p.nE = (p.R_pad + rows_per_task - 1) / rows_per_task;
   p.done = ws ? ws + kWsHeaderWords + num_groups : nullptr;
   p.codes = codes;
   p.scales = scales;
