@@ -119,11 +119,11 @@ __device__ __forceinline__ void store_block(const RowOut& o, int64_t b,
                                             bool write_codes, uint32_t lo,
                                             uint32_t hi, uint32_t sb, int lane) {
   if (write_codes && b < o.nblocks) st_v2(o.codes_row + b * 8, lo, hi);
-  const uint32_t s1 = __shfl_down_sync(FULL, sb, 1);
-  const uint32_t s2 = __shfl_down_sync(FULL, sb, 2);
-  const uint32_t s3 = __shfl_down_sync(FULL, sb, 3);
+  // lanes 4i .. 4i+3 hold four consecutive block scales: two shuffles
+  // assemble them, lowest block in the lowest byte, in lane 4i
+  const uint32_t pair = sb | (__shfl_down_sync(FULL, sb, 1) << 8);
+  const uint32_t word = pair | (__shfl_down_sync(FULL, pair, 2) << 16);
   if ((lane & 3) == 0) {
-    const uint32_t word = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
     if (o.swizzled) {
       if (b < ((o.nblocks + 3) & ~int64_t(3)))
         *reinterpret_cast<uint32_t*>(o.scales +
