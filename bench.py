@@ -214,6 +214,15 @@ def run_gpu(args):
             *[flat[i].data_ptr() for i in range(2 * PAIRS)]))
     rows_tab = (ctypes.c_int64 * 2)(PART_ROWS, PART_ROWS)
     s = ctypes.c_void_p(stream.cuda_stream)
+    # The step's three chains (MXFP8 quantize -> both dequantizations;
+    # per-token quantize -> dequantize; weights -> dequantize) touch
+    # different buffers: after the rowcol kernel (timed alone for the
+    # roofline line), the other two chains fork onto their own streams and
+    # join before the next step.
+    side = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    s_side = [ctypes.c_void_p(x.cuda_stream) for x in side]
+    ev_fork = torch.cuda.Event()
+    ev_join = [torch.cuda.Event(), torch.cuda.Event()]
 
     def chk(st, what):
         if st != 0:
@@ -222,8 +231,9 @@ def run_gpu(args):
     names = list(op_bytes().keys())
     ev = None
 
-    def step(i, record=None, only=None):
+    def step(i, record=None, only=None, concurrent=False):
         o_new, o_old = outs[i % 2], outs[(i + 1) % 2]
+        s1, s2 = (s_side[0], s_side[1]) if concurrent else (s, s)
         x0, x1, x2 = X[i % 3], X[(i + 1) % 3], X[(i + 2) % 3]
         tab = parts_tabs[(i + 2) % 3]
 
@@ -239,6 +249,10 @@ def run_gpu(args):
                                     o_new["rs"].data_ptr(), o_new["cc"].data_ptr(),
                                     o_new["cs"].data_ptr(), lay, s), "rowcol")
         mark(1)
+        if concurrent:
+            ev_fork.record(stream)
+            side[0].wait_event(ev_fork)
+            side[1].wait_event(ev_fork)
         chk(L.dequantize_mxfp8(o_old["rc"].data_ptr(), o_old["rs"].data_ptr(), M, K,
                                lay, y_row.data_ptr(), s), "dq row")
         mark(2)
@@ -247,22 +261,27 @@ def run_gpu(args):
         mark(3)
         chk(L.nvfp4_quantize_per_token(x1.data_ptr(), M, K, K, o_new["tc"].data_ptr(),
                                        o_new["ts"].data_ptr(), o_new["tS"].data_ptr(),
-                                       lay, s), "per-token")
+                                       lay, s1), "per-token")
         mark(4)
         chk(L.dequantize_nvfp4(o_old["tc"].data_ptr(), o_old["ts"].data_ptr(),
                                o_old["tS"].data_ptr(), q.S_PER_ROW, 1, M, K, lay,
-                               y_tok.data_ptr(), s), "dq tokens")
+                               y_tok.data_ptr(), s1), "dq tokens")
         mark(5)
         chk(L.nvfp4_quantize_weight_shared(
             PAIRS, 2, ctypes.cast(tab, ctypes.c_void_p),
             ctypes.cast(rows_tab, ctypes.c_void_p), K, o_new["wc"].data_ptr(),
             o_new["ws"].data_ptr(), o_new["wS"].data_ptr(), None, lay,
-            wsp.data_ptr(), wsp.numel(), s), "weights")
+            wsp.data_ptr(), wsp.numel(), s2), "weights")
         mark(6)
         chk(L.dequantize_nvfp4(o_old["wc"].data_ptr(), o_old["ws"].data_ptr(),
                                o_old["wS"].data_ptr(), q.S_PER_BATCH, PAIRS,
-                               2 * PART_ROWS, K, lay, y_w.data_ptr(), s),
+                               2 * PART_ROWS, K, lay, y_w.data_ptr(), s2),
             "dq weights")
+        if concurrent:
+            ev_join[0].record(side[0])
+            ev_join[1].record(side[1])
+            stream.wait_event(ev_join[0])
+            stream.wait_event(ev_join[1])
         mark(7)
 
     # Our kernels per step: rowcol 1, dequant 2 + 1 + 1, per-token 1,
@@ -271,7 +290,7 @@ def run_gpu(args):
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            step(i)
+            step(i, concurrent=not args.serial)
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
@@ -291,7 +310,8 @@ def run_gpu(args):
         with torch.cuda.stream(stream):
             start.record(stream)
             for i in range(args.steps):
-                step(args.warmup + i, recs[i], only=(0, 1))
+                step(args.warmup + i, recs[i], only=(0, 1),
+                     concurrent=not args.serial)
             end.record(stream)
         torch.cuda.synchronize(dev)
         if world > 1:
@@ -363,6 +383,9 @@ def run_gpu(args):
                    "rotating output sets, every kernel reads data last "
                    "touched >= one step (~680 MB) earlier"),
             "parallelism": f"weak: one independent replica per GPU x{world}",
+            "streams": ("1 (serial)" if args.serial else
+                        "3: rowcol alone, then its dequantizations, the "
+                        "per-token chain and the weight chain concurrently"),
         },
         "pct_hbm_peak": round(100 * value / world / peak, 1),
         "roofline": {
@@ -705,6 +728,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=0,
                     help="rows of X per reference step (0: sized to ~1 min)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--serial", action="store_true",
+                    help="run the step's three chains on one stream")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
