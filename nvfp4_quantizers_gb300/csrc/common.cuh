@@ -199,10 +199,34 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return v;
 }
 
+// 32-byte global store (sm_100 family); p must be 32-byte aligned.  One
+// instruction writes a whole 32-byte sector, where two 16-byte stores
+// would each write half of it.
+__device__ __forceinline__ void st_v8(void* p, uint4 a, uint4 b) {
+  asm volatile(
+      "st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+      "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z),
+      "r"(b.w)
+      : "memory");
+}
+
+// 32 bytes written as one 32-byte store when `wide` (the caller checked
+// 32-byte alignment of the buffer), else as two 16-byte stores.
+__device__ __forceinline__ void st_32B(void* p, uint4 a, uint4 b, bool wide);
+
 __device__ __forceinline__ void st_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p),
                "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+__device__ __forceinline__ void st_32B(void* p, uint4 a, uint4 b, bool wide) {
+  if (wide) {
+    st_v8(p, a, b);
+  } else {
+    st_v4(p, a);
+    st_v4(static_cast<uint8_t*>(p) + 16, b);
+  }
 }
 
 __device__ __forceinline__ void st_v2(void* p, uint32_t a, uint32_t b) {

@@ -33,7 +33,8 @@ template <typename Idx>
 __global__ void __launch_bounds__(DQ_THREADS)
     dequant_mxfp8_kernel(const uint8_t* __restrict__ codes,
                          const uint8_t* __restrict__ scales, Idx rows,
-                         Idx cols, int swizzled, uint16_t* __restrict__ y) {
+                         Idx cols, int swizzled, int wide,
+                         uint16_t* __restrict__ y) {
   const Idx c16 = cols >> 4, nb = cols >> 5;
   const Idx n16 = rows * c16;
   const int64_t col_tiles = ((int64_t)nb + 3) >> 2;
@@ -55,9 +56,8 @@ __global__ void __launch_bounds__(DQ_THREADS)
       fmul2(a, bb, sc, sc, a, bb);
       w[h] = f32x2_to_bf16x2(a, bb);
     }
-    uint16_t* dst = y + (int64_t)i * 16;
-    st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
-    st_v4(dst + 8, make_uint4(w[4], w[5], w[6], w[7]));
+    st_32B(y + (int64_t)i * 16, make_uint4(w[0], w[1], w[2], w[3]),
+           make_uint4(w[4], w[5], w[6], w[7]), wide);
   }
   pdl_launch_dependents();
 }
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(DQ_THREADS)
                          const uint8_t* __restrict__ scales,
                          const float* __restrict__ S, int per_batch,
                          Idx rows_per_batch, Idx total_rows, Idx cols,
-                         int swizzled, int64_t scale_stride,
+                         int swizzled, int64_t scale_stride, int wide,
                          uint16_t* __restrict__ y) {
   const Idx nb = cols >> 4;
   const Idx nblk = total_rows * nb;
@@ -106,9 +106,8 @@ __global__ void __launch_bounds__(DQ_THREADS)
       fmul2(a, bb, s32, s32, a, bb);
       w[h] = f32x2_to_bf16x2(a, bb);
     }
-    uint16_t* dst = y + (int64_t)i * 16;
-    st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
-    st_v4(dst + 8, make_uint4(w[4], w[5], w[6], w[7]));
+    st_32B(y + (int64_t)i * 16, make_uint4(w[0], w[1], w[2], w[3]),
+           make_uint4(w[4], w[5], w[6], w[7]), wide);
   }
   pdl_launch_dependents();
 }
@@ -130,13 +129,16 @@ cudaError_t launch_dequant_mxfp8(const uint8_t* codes, const uint8_t* scales,
   const int64_t units = rows * (cols / 16);
   const unsigned grid = dq_grid(units, dev);
   uint16_t* out = static_cast<uint16_t*>(y);
+  // a unit's 16 outputs are 32 bytes at a multiple of 32 bytes from y
+  const int wide = (reinterpret_cast<uintptr_t>(y) & 31u) == 0;
   // 32-bit indices when the largest index and the grid stride fit.
   if (units + (int64_t)grid * DQ_THREADS < (1ll << 32))
     return launch_pdl(dequant_mxfp8_kernel<uint32_t>, dim3(grid),
                       dim3(DQ_THREADS), 0, stream, false, codes, scales,
-                      (uint32_t)rows, (uint32_t)cols, swizzled, out);
+                      (uint32_t)rows, (uint32_t)cols, swizzled, wide, out);
   return launch_pdl(dequant_mxfp8_kernel<int64_t>, dim3(grid), dim3(DQ_THREADS),
-                    0, stream, false, codes, scales, rows, cols, swizzled, out);
+                    0, stream, false, codes, scales, rows, cols, swizzled,
+                    wide, out);
 }
 
 cudaError_t launch_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales,
@@ -151,14 +153,15 @@ cudaError_t launch_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales,
   const unsigned grid = dq_grid(units, dev);
   const int64_t stride = scale_bytes(rows, cols / 16, swizzled);
   uint16_t* out = static_cast<uint16_t*>(y);
+  const int wide = (reinterpret_cast<uintptr_t>(y) & 31u) == 0;
   if (units + (int64_t)grid * DQ_THREADS < (1ll << 32))
     return launch_pdl(dequant_nvfp4_kernel<uint32_t>, dim3(grid),
                       dim3(DQ_THREADS), 0, stream, false, codes, scales, S,
                       per_batch, (uint32_t)rows, (uint32_t)total_rows,
-                      (uint32_t)cols, swizzled, stride, out);
+                      (uint32_t)cols, swizzled, stride, wide, out);
   return launch_pdl(dequant_nvfp4_kernel<int64_t>, dim3(grid), dim3(DQ_THREADS),
                     0, stream, false, codes, scales, S, per_batch, rows,
-                    total_rows, cols, swizzled, stride, out);
+                    total_rows, cols, swizzled, stride, wide, out);
 }
 
 }  // namespace mxq
