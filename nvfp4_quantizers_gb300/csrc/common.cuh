@@ -214,6 +214,17 @@ __device__ __forceinline__ void st_v8(void* p, uint4 a, uint4 b) {
 // 32-byte alignment of the buffer), else as two 16-byte stores.
 __device__ __forceinline__ void st_32B(void* p, uint4 a, uint4 b, bool wide);
 
+// 32-byte non-allocating load (sm_100 family); p must be 32-byte aligned.
+__device__ __forceinline__ void ld_stream_v8(const void* p, uint4& a,
+                                             uint4& b) {
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, "
+      "[%8];"
+      : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y),
+        "=r"(b.z), "=r"(b.w)
+      : "l"(p));
+}
+
 __device__ __forceinline__ void st_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p),
                "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)

@@ -45,6 +45,7 @@ struct RowOut {
   int64_t col_tiles;    // swizzled: ceil(nblocks / 4)
   int64_t nblocks;      // H / 16
   int swizzled;
+  int wide;             // rows 32-byte aligned: one 32-byte load per block
 };
 
 // 16 bf16 values of one block (two 16-byte chunks).
@@ -76,10 +77,14 @@ __device__ __forceinline__ uint32_t warp_max(uint32_t a) {
 }
 
 __device__ __forceinline__ void load_block(Blk& v, const uint16_t* row,
-                                           int64_t b, bool valid) {
+                                           int64_t b, bool valid, bool wide) {
   if (valid) {
-    v.a = ld_stream_v4(row + b * 16);
-    v.b = ld_stream_v4(row + b * 16 + 8);
+    if (wide) {
+      ld_stream_v8(row + b * 16, v.a, v.b);
+    } else {
+      v.a = ld_stream_v4(row + b * 16);
+      v.b = ld_stream_v4(row + b * 16 + 8);
+    }
   } else {
     v.a = make_uint4(0, 0, 0, 0);
     v.b = v.a;
@@ -155,7 +160,7 @@ __device__ __forceinline__ void encode_row_warps(
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int64_t b = blk0 + r * 32 + lane;
-    load_block(v[r], row, b, load && b < o.nblocks);
+    load_block(v[r], row, b, load && b < o.nblocks, o.wide);
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
                        const int32_t* __restrict__ row_index, int64_t T_src,
                        uint8_t* __restrict__ codes,
                        uint8_t* __restrict__ scales, float* __restrict__ S_out,
-                       int swizzled) {
+                       int swizzled, int wide) {
   constexpr int ROWS = CTA_WARPS / WPR;
   __shared__ uint32_t red[CTA_WARPS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -209,7 +214,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
     load = src >= 0 && src < T_src;       // other indices: a zero row
   }
   RowOut o{codes + t * (H >> 1), scales, t, ((H >> 4) + 3) >> 2, H >> 4,
-           swizzled};
+           swizzled, wide};
   float S;
   encode_row_warps<R, WPR>(load ? x + src * ldx : x, load, real, 0.0f, false,
                            o, slot, wpart, lane, red, &S);
@@ -225,7 +230,8 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
                             const int32_t* __restrict__ row_index,
                             int64_t T_src, uint8_t* __restrict__ codes,
                             uint8_t* __restrict__ scales,
-                            float* __restrict__ S_out, int swizzled) {
+                            float* __restrict__ S_out, int swizzled,
+                            int wide) {
   __shared__ uint32_t red[CTA_WARPS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = blockIdx.x;
@@ -239,13 +245,13 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
   const uint16_t* row = load ? x + src * ldx : x;
   pdl_wait();
   RowOut o{codes + t * (H >> 1), scales, t, ((H >> 4) + 3) >> 2, H >> 4,
-           swizzled};
+           swizzled, wide};
   const int64_t span = CTA_WARPS * 32;
   uint32_t a = 0;
   for (int64_t b0 = 0; b0 < o.nblocks; b0 += span) {
     const int64_t b = b0 + threadIdx.x;
     Blk v;
-    load_block(v, row, b, load && b < o.nblocks);
+    load_block(v, row, b, load && b < o.nblocks, o.wide);
     a = max(a, block_absmax(v));
   }
   a = warp_max(a);
@@ -258,7 +264,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
     if (b0 + warp * 32 >= o.nblocks) continue;         // warp-uniform
     const int64_t b = b0 + threadIdx.x;
     Blk v;
-    load_block(v, row, b, load && b < o.nblocks);
+    load_block(v, row, b, load && b < o.nblocks, o.wide);
     uint32_t lo, hi, sb;
     encode_block(v, block_absmax(v), S, six_s, lo, hi, sb);
     store_block(o, b, real, lo, hi, sb, lane);
@@ -313,6 +319,7 @@ struct GroupParams {
   uint32_t* ws;                       // [64 + g] amax words
   uint32_t* counter;                  // this launch's task counter
   uint32_t* done;                     // finished amax tasks per group
+  int wide;                           // all parts 32-byte aligned
   int swizzled;
 };
 
@@ -450,7 +457,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
       if (r == 0 && wpart == 0 && lane == 0) p.group_scales[g] = S;
       RowOut o{p.codes + (g * p.R + r) * (p.K >> 1),
                p.scales + g * p.scale_stride, r, ((p.K >> 4) + 3) >> 2,
-               p.K >> 4, p.swizzled};
+               p.K >> 4, p.swizzled, p.wide};
       float S_used;
       encode_row_warps<R, WPR>(row, real, real, S, true, o, slot, wpart, lane,
                                red, &S_used);
@@ -486,18 +493,21 @@ cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
                                    int swizzled, cudaStream_t stream) {
   const int64_t T_pad = swizzled ? (T + 127) / 128 * 128 : T;
   const uint16_t* xs = static_cast<const uint16_t*>(x);
+  // every block starts a multiple of 32 bytes from x when ldx % 16 == 0
+  const int wide = (reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ldx % 16 == 0;
   const RowShape sh = pick_shape(H);
   if (sh.R == 0) {
     return launch_pdl(nvfp4_token_long_kernel, dim3((unsigned)T_pad),
                       dim3(CTA_WARPS * 32), 0, stream, false, xs, T, H, ldx,
-                      row_index, T_src, codes, scales, token_scales, swizzled);
+                      row_index, T_src, codes, scales, token_scales, swizzled,
+                      wide);
   }
   const int rows_per_cta = CTA_WARPS / sh.WPR;
   const unsigned grid = (unsigned)((T_pad + rows_per_cta - 1) / rows_per_cta);
 #define MXQ_TOKEN_LAUNCH(R_, W_)                                          \
   launch_pdl(nvfp4_token_kernel<R_, W_>, dim3(grid), dim3(CTA_WARPS * 32), \
              0, stream, false, xs, T, T_pad, H, ldx, row_index, T_src,     \
-             codes, scales, token_scales, swizzled)
+             codes, scales, token_scales, swizzled, wide)
   if (sh.R == 1) return MXQ_TOKEN_LAUNCH(1, 1);
   if (sh.R == 2) return MXQ_TOKEN_LAUNCH(2, 1);
   if (sh.WPR == 1) return MXQ_TOKEN_LAUNCH(4, 1);
@@ -574,6 +584,9 @@ cudaError_t launch_nvfp4_weight_shared(
   p.S_in = group_scales_in;
   p.ws = ws;
   p.swizzled = swizzled;
+  p.wide = 1;
+  for (int64_t i = 0; i < num_groups * num_parts; ++i)
+    if (reinterpret_cast<uintptr_t>(parts[i]) & 31u) p.wide = 0;
 
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
