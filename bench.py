@@ -557,9 +557,10 @@ def load_traffic(kernel_name):
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)[kernel_name]
-        with open(os.path.join(ROOT, d["source"]), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != d["source_sha256"]:
-                return None
+        for src, digest in d["sources_sha256"].items():
+            with open(os.path.join(ROOT, src), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
         return int(d["dram_bytes_per_launch"])
     except Exception:
         return None
