@@ -46,6 +46,7 @@ struct RowOut {
   int64_t nblocks;      // H / 16
   int swizzled;
   int wide;             // rows 32-byte aligned: one 32-byte load per block
+  uint8_t* stage;       // non-NULL: block scales go to this shared row
 };
 
 // 16 bf16 values of one block (two 16-byte chunks).
@@ -124,6 +125,10 @@ __device__ __forceinline__ void store_block(const RowOut& o, int64_t b,
                                             bool write_codes, uint32_t lo,
                                             uint32_t hi, uint32_t sb, int lane) {
   if (write_codes && b < o.nblocks) st_v2(o.codes_row + b * 8, lo, hi);
+  if (o.stage) {                          // uniform over the CTA
+    if (b < 4 * o.col_tiles) o.stage[b] = (uint8_t)sb;
+    return;
+  }
   // lanes 4i .. 4i+3 hold four consecutive block scales: two shuffles
   // assemble them, lowest block in the lowest byte, in lane 4i
   const uint32_t pair = sb | (__shfl_down_sync(FULL, sb, 1) << 8);
@@ -191,6 +196,11 @@ __device__ __forceinline__ void encode_row_warps(
 // ---------------------------------------------------------------------------
 // Per-token activations.
 // ---------------------------------------------------------------------------
+// With swizzled scales and 4 or 8 rows per CTA, a CTA takes rows of one
+// 128-row scale tile that share swizzled segments (rows k + 32q, or
+// 2k + d + 32q for 8 rows), stages their block scales in shared memory and
+// writes each column tile's segment with one 16- or 32-byte store instead
+// of one 4-byte store per row.
 template <int R, int WPR>
 __global__ void __launch_bounds__(CTA_WARPS * 32)
     nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t T_pad,
@@ -198,27 +208,63 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
                        const int32_t* __restrict__ row_index, int64_t T_src,
                        uint8_t* __restrict__ codes,
                        uint8_t* __restrict__ scales, float* __restrict__ S_out,
-                       int swizzled, int wide) {
+                       int swizzled, int wide, int sc_wide) {
   constexpr int ROWS = CTA_WARPS / WPR;
+  constexpr bool kStageable = ROWS == 4 || ROWS == 8;
   __shared__ uint32_t red[CTA_WARPS];
+  __shared__ __align__(16) uint8_t s_sc[kStageable ? ROWS : 1]
+                                       [kStageable ? 1024 / ROWS : 4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slot = warp / WPR, wpart = warp % WPR;
-  const int64_t t = (int64_t)blockIdx.x * ROWS + slot;
+  const bool staged = kStageable && swizzled;
+  constexpr int64_t P = 128 / ROWS;               // CTAs per 128-row tile
+  const int64_t rt = blockIdx.x / P, k = blockIdx.x % P;
+  const int64_t t =
+      !staged ? (int64_t)blockIdx.x * ROWS + slot
+              : rt * 128 + (ROWS == 8 ? 2 * k + (slot & 1) + 32 * (slot >> 1)
+                                      : k + 32 * slot);
+  const int64_t col_tiles = ((H >> 4) + 3) >> 2;
   pdl_wait();
-  if (t >= T_pad) return;                 // uniform over the row's warps
-  const bool real = t < T;
-  int64_t src = t;
-  bool load = real;
-  if (row_index && real) {                // gather: row t <- x[row_index[t]]
-    src = row_index[t];
-    load = src >= 0 && src < T_src;       // other indices: a zero row
+  if (t < T_pad) {                        // uniform over the row's warps
+    const bool real = t < T;
+    int64_t src = t;
+    bool load = real;
+    if (row_index && real) {              // gather: row t <- x[row_index[t]]
+      src = row_index[t];
+      load = src >= 0 && src < T_src;     // other indices: a zero row
+    }
+    RowOut o{codes + t * (H >> 1), scales, t, col_tiles, H >> 4,
+             swizzled, wide, staged ? s_sc[slot] : nullptr};
+    float S;
+    encode_row_warps<R, WPR>(load ? x + src * ldx : x, load, real, 0.0f,
+                             false, o, slot, wpart, lane, red, &S);
+    if (real && wpart == 0 && lane == 0) S_out[t] = S;
   }
-  RowOut o{codes + t * (H >> 1), scales, t, ((H >> 4) + 3) >> 2, H >> 4,
-           swizzled, wide};
-  float S;
-  encode_row_warps<R, WPR>(load ? x + src * ldx : x, load, real, 0.0f, false,
-                           o, slot, wpart, lane, red, &S);
-  if (real && wpart == 0 && lane == 0) S_out[t] = S;
+  if (staged) {
+    // T_pad is a multiple of 128 here, so every row of the CTA exists.
+    __syncthreads();
+    uint8_t* tile0 = scales + rt * col_tiles * 512;
+    for (int64_t ct = threadIdx.x; ct < col_tiles; ct += CTA_WARPS * 32) {
+      const int64_t c4 = ct * 4;
+      if (ROWS == 4) {
+        const uint4 v = make_uint4(*reinterpret_cast<const uint32_t*>(&s_sc[0][c4]),
+                                   *reinterpret_cast<const uint32_t*>(&s_sc[1 % ROWS][c4]),
+                                   *reinterpret_cast<const uint32_t*>(&s_sc[2 % ROWS][c4]),
+                                   *reinterpret_cast<const uint32_t*>(&s_sc[3 % ROWS][c4]));
+        st_v4(tile0 + ct * 512 + k * 16, v);
+      } else {
+        const uint4 a = make_uint4(*reinterpret_cast<const uint32_t*>(&s_sc[0][c4]),
+                                   *reinterpret_cast<const uint32_t*>(&s_sc[2 % ROWS][c4]),
+                                   *reinterpret_cast<const uint32_t*>(&s_sc[4 % ROWS][c4]),
+                                   *reinterpret_cast<const uint32_t*>(&s_sc[6 % ROWS][c4]));
+        const uint4 b = make_uint4(*reinterpret_cast<const uint32_t*>(&s_sc[1 % ROWS][c4]),
+                                   *reinterpret_cast<const uint32_t*>(&s_sc[3 % ROWS][c4]),
+                                   *reinterpret_cast<const uint32_t*>(&s_sc[5 % ROWS][c4]),
+                                   *reinterpret_cast<const uint32_t*>(&s_sc[7 % ROWS][c4]));
+        st_32B(tile0 + ct * 512 + k * 32, a, b, sc_wide);
+      }
+    }
+  }
   pdl_launch_dependents();
 }
 
@@ -245,7 +291,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
   const uint16_t* row = load ? x + src * ldx : x;
   pdl_wait();
   RowOut o{codes + t * (H >> 1), scales, t, ((H >> 4) + 3) >> 2, H >> 4,
-           swizzled, wide};
+           swizzled, wide, nullptr};
   const int64_t span = CTA_WARPS * 32;
   uint32_t a = 0;
   for (int64_t b0 = 0; b0 < o.nblocks; b0 += span) {
@@ -457,7 +503,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
       if (r == 0 && wpart == 0 && lane == 0) p.group_scales[g] = S;
       RowOut o{p.codes + (g * p.R + r) * (p.K >> 1),
                p.scales + g * p.scale_stride, r, ((p.K >> 4) + 3) >> 2,
-               p.K >> 4, p.swizzled, p.wide};
+               p.K >> 4, p.swizzled, p.wide, nullptr};
       float S_used;
       encode_row_warps<R, WPR>(row, real, real, S, true, o, slot, wpart, lane,
                                red, &S_used);
@@ -495,6 +541,7 @@ cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
   const uint16_t* xs = static_cast<const uint16_t*>(x);
   // every block starts a multiple of 32 bytes from x when ldx % 16 == 0
   const int wide = (reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ldx % 16 == 0;
+  const int sc_wide = (reinterpret_cast<uintptr_t>(scales) & 31u) == 0;
   const RowShape sh = pick_shape(H);
   if (sh.R == 0) {
     return launch_pdl(nvfp4_token_long_kernel, dim3((unsigned)T_pad),
@@ -507,7 +554,7 @@ cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
 #define MXQ_TOKEN_LAUNCH(R_, W_)                                          \
   launch_pdl(nvfp4_token_kernel<R_, W_>, dim3(grid), dim3(CTA_WARPS * 32), \
              0, stream, false, xs, T, T_pad, H, ldx, row_index, T_src,     \
-             codes, scales, token_scales, swizzled, wide)
+             codes, scales, token_scales, swizzled, wide, sc_wide)
   if (sh.R == 1) return MXQ_TOKEN_LAUNCH(1, 1);
   if (sh.R == 2) return MXQ_TOKEN_LAUNCH(2, 1);
   if (sh.WPR == 1) return MXQ_TOKEN_LAUNCH(4, 1);
