@@ -366,6 +366,7 @@ struct GroupParams {
   uint32_t* counter;                  // this launch's task counter
   uint32_t* done;                     // finished amax tasks per group
   int wide;                           // all parts 32-byte aligned
+  int sc_wide;                        // scale matrices 32-byte aligned
   int swizzled;
 };
 
@@ -397,6 +398,11 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
   __shared__ uint32_t red[CTA_WARPS];
   __shared__ int s_abort;
   __shared__ int64_t s_task[2];
+  // Encode tasks of 8 rows with swizzled scales: the rows 2k + d + 32q of
+  // one 128-row tile, whose block scales fill whole 32-byte sectors of the
+  // swizzled tiles; staged here, written as one 32-byte store per tile.
+  constexpr bool kStage8 = ROWS * kRowSetsPerTask == 8;
+  __shared__ __align__(16) uint8_t s_sc[kStage8 ? 8 : 1][kStage8 ? 256 : 4];
   __shared__ float s_S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slot = warp / WPR, wpart = warp % WPR;
@@ -432,19 +438,40 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
       // ---- amax of 64 KiB of group gl ----
       uint32_t a = 0;
       const int64_t q0 = idx * kTaskChunks;
+      // The task's chunks usually lie in one part: then one base pointer
+      // and 32-byte loads (pairs of chunks); otherwise a part lookup per
+      // 16-byte chunk.
+      int pi = 0;
+      while (pi + 1 < p.num_parts && q0 >= p.part_chunk0[pi + 1]) ++pi;
+      const bool one_part = p.wide && q0 + kTaskChunks <= p.part_chunk0[pi + 1];
+      if (one_part && !s_abort) {
+        const uint16_t* base = tab.part[gl][pi] + (q0 - p.part_chunk0[pi]) * 8;
 #pragma unroll
-      for (int rr = 0; rr < (int)(kTaskChunks / (CTA_WARPS * 32 * 8)); ++rr) {
-        uint4 v[8];
+        for (int rr = 0; rr < (int)(kTaskChunks / (CTA_WARPS * 32 * 8)); ++rr) {
+          uint4 v[8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int64_t q = q0 + (int64_t)(rr * 8 + jj) * (CTA_WARPS * 32) +
-                            threadIdx.x;
-          v[jj] = (q < group_chunks && !s_abort)
-                      ? ld_stream_v4(chunk_ptr(tab, p, gl, q))
-                      : make_uint4(0, 0, 0, 0);
+          for (int jj = 0; jj < 4; ++jj)
+            ld_stream_v8(base + ((int64_t)(rr * 4 + jj) * (CTA_WARPS * 32) +
+                                 threadIdx.x) * 16,
+                         v[2 * jj], v[2 * jj + 1]);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) a = max(a, chunk_absmax(v[jj]));
         }
+      } else {
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) a = max(a, chunk_absmax(v[jj]));
+        for (int rr = 0; rr < (int)(kTaskChunks / (CTA_WARPS * 32 * 8)); ++rr) {
+          uint4 v[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int64_t q = q0 + (int64_t)(rr * 8 + jj) * (CTA_WARPS * 32) +
+                              threadIdx.x;
+            v[jj] = (q < group_chunks && !s_abort)
+                        ? ld_stream_v4(chunk_ptr(tab, p, gl, q))
+                        : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) a = max(a, chunk_absmax(v[jj]));
+        }
       }
       const uint32_t m = warp_max(a);
       if (lane == 0) red[warp] = m;
@@ -490,8 +517,12 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
     }
     __syncthreads();
     const float S = s_S;
+    const bool staged = kStage8 && p.swizzled && (p.K >> 4) <= 256;
     for (int rs = 0; rs < kRowSetsPerTask; ++rs) {
-    const int64_t r = (idx * kRowSetsPerTask + rs) * ROWS + slot;
+    const int s8 = rs * ROWS + slot;
+    const int64_t r = staged ? (idx >> 4) * 128 + 2 * (idx & 15) + (s8 & 1) +
+                                   32 * (s8 >> 1)
+                             : (idx * kRowSetsPerTask + rs) * ROWS + slot;
     if (r < p.R_pad && !s_abort) {                      // uniform over the row
       const bool real = r < p.R;
       const uint16_t* row = nullptr;
@@ -503,11 +534,33 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
       if (r == 0 && wpart == 0 && lane == 0) p.group_scales[g] = S;
       RowOut o{p.codes + (g * p.R + r) * (p.K >> 1),
                p.scales + g * p.scale_stride, r, ((p.K >> 4) + 3) >> 2,
-               p.K >> 4, p.swizzled, p.wide, nullptr};
+               p.K >> 4, p.swizzled, p.wide,
+               staged ? s_sc[s8 % (kStage8 ? 8 : 1)] : nullptr};
       float S_used;
       encode_row_warps<R, WPR>(row, real, real, S, true, o, slot, wpart, lane,
                                red, &S_used);
     }
+    }
+    if (staged) {
+      __syncthreads();
+      // R_pad is a multiple of 128 here: all 8 rows exist
+      const int64_t col_tiles = ((p.K >> 4) + 3) >> 2;
+      uint8_t* tile0 = p.scales + g * p.scale_stride +
+                       (idx >> 4) * col_tiles * 512 + (idx & 15) * 32;
+      for (int64_t ct = threadIdx.x; ct < col_tiles; ct += CTA_WARPS * 32) {
+        const int64_t c4 = ct * 4;
+        const uint4 a = make_uint4(
+            *reinterpret_cast<const uint32_t*>(&s_sc[0][c4]),
+            *reinterpret_cast<const uint32_t*>(&s_sc[2 % (kStage8 ? 8 : 1)][c4]),
+            *reinterpret_cast<const uint32_t*>(&s_sc[4 % (kStage8 ? 8 : 1)][c4]),
+            *reinterpret_cast<const uint32_t*>(&s_sc[6 % (kStage8 ? 8 : 1)][c4]));
+        const uint4 b = make_uint4(
+            *reinterpret_cast<const uint32_t*>(&s_sc[1 % (kStage8 ? 8 : 1)][c4]),
+            *reinterpret_cast<const uint32_t*>(&s_sc[3 % (kStage8 ? 8 : 1)][c4]),
+            *reinterpret_cast<const uint32_t*>(&s_sc[5 % (kStage8 ? 8 : 1)][c4]),
+            *reinterpret_cast<const uint32_t*>(&s_sc[7 % (kStage8 ? 8 : 1)][c4]));
+        st_32B(tile0 + ct * 512, a, b, p.sc_wide);
+      }
     }
     __syncthreads();                  // s_S and red are reused by the next task
   }
@@ -631,6 +684,8 @@ cudaError_t launch_nvfp4_weight_shared(
   p.S_in = group_scales_in;
   p.ws = ws;
   p.swizzled = swizzled;
+  p.sc_wide = (reinterpret_cast<uintptr_t>(scales) & 31u) == 0 &&
+              p.scale_stride % 32 == 0;
   p.wide = 1;
   for (int64_t i = 0; i < num_groups * num_parts; ++i)
     if (reinterpret_cast<uintptr_t>(parts[i]) & 31u) p.wide = 0;
