@@ -259,24 +259,47 @@ def run_gpu(args):
         chk(L.dequantize_mxfp8(o_old["cc"].data_ptr(), o_old["cs"].data_ptr(), K, M,
                                lay, y_col.data_ptr(), s), "dq col")
         mark(3)
-        chk(L.nvfp4_quantize_per_token(x1.data_ptr(), M, K, K, o_new["tc"].data_ptr(),
-                                       o_new["ts"].data_ptr(), o_new["tS"].data_ptr(),
-                                       lay, s1), "per-token")
-        mark(4)
-        chk(L.dequantize_nvfp4(o_old["tc"].data_ptr(), o_old["ts"].data_ptr(),
-                               o_old["tS"].data_ptr(), q.S_PER_ROW, 1, M, K, lay,
-                               y_tok.data_ptr(), s1), "dq tokens")
-        mark(5)
-        chk(L.nvfp4_quantize_weight_shared(
-            PAIRS, 2, ctypes.cast(tab, ctypes.c_void_p),
-            ctypes.cast(rows_tab, ctypes.c_void_p), K, o_new["wc"].data_ptr(),
-            o_new["ws"].data_ptr(), o_new["wS"].data_ptr(), None, lay,
-            wsp.data_ptr(), wsp.numel(), s2), "weights")
-        mark(6)
-        chk(L.dequantize_nvfp4(o_old["wc"].data_ptr(), o_old["ws"].data_ptr(),
-                               o_old["wS"].data_ptr(), q.S_PER_BATCH, PAIRS,
-                               2 * PART_ROWS, K, lay, y_w.data_ptr(), s2),
-            "dq weights")
+        def token_q():
+            chk(L.nvfp4_quantize_per_token(
+                x1.data_ptr(), M, K, K, o_new["tc"].data_ptr(),
+                o_new["ts"].data_ptr(), o_new["tS"].data_ptr(), lay, s1),
+                "per-token")
+
+        def token_dq():
+            chk(L.dequantize_nvfp4(o_old["tc"].data_ptr(), o_old["ts"].data_ptr(),
+                                   o_old["tS"].data_ptr(), q.S_PER_ROW, 1, M, K,
+                                   lay, y_tok.data_ptr(), s1), "dq tokens")
+
+        def weights_q():
+            chk(L.nvfp4_quantize_weight_shared(
+                PAIRS, 2, ctypes.cast(tab, ctypes.c_void_p),
+                ctypes.cast(rows_tab, ctypes.c_void_p), K,
+                o_new["wc"].data_ptr(), o_new["ws"].data_ptr(),
+                o_new["wS"].data_ptr(), None, lay, wsp.data_ptr(), wsp.numel(),
+                s2), "weights")
+
+        def weights_dq():
+            chk(L.dequantize_nvfp4(o_old["wc"].data_ptr(), o_old["ws"].data_ptr(),
+                                   o_old["wS"].data_ptr(), q.S_PER_BATCH, PAIRS,
+                                   2 * PART_ROWS, K, lay, y_w.data_ptr(), s2),
+                "dq weights")
+        if concurrent:
+            # Each side chain dequantizes the previous step's codes first and
+            # quantizes this step's input last, so the step ends on the
+            # kernels that leave the least dirty data in L2 for the next
+            # step's rowcol kernel.
+            token_dq()
+            token_q()
+            weights_dq()
+            weights_q()
+        else:
+            token_q()
+            mark(4)
+            token_dq()
+            mark(5)
+            weights_q()
+            mark(6)
+            weights_dq()
         if concurrent:
             ev_join[0].record(side[0])
             ev_join[1].record(side[1])
