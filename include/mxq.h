@@ -85,6 +85,15 @@ int64_t mxq_scale_bytes(int64_t rows, int64_t cols, int scale_layout);
  * (MXQ_ERR_CUDA); MXQ_OK if neither is set.  Synchronizes the device. */
 mxq_status mxq_get_last_error(void);
 
+/* Self-test of the device-side failure detection (the pages have no
+ * counterpart; it exists so that tests can check the path without making
+ * the GPU fault or hang).  Launches one CTA whose bounded mbarrier wait --
+ * the same wait the kernels use -- waits on a barrier nothing completes;
+ * after 20 ms it gives up and records the error word, so the next
+ * mxq_get_last_error returns MXQ_ERR_TIMEOUT and the context stays usable.
+ * Returns MXQ_ERR_CUDA if the launch fails. */
+mxq_status mxq_selftest_wait_timeout(void* stream);
+
 /* Host-side fault injection for tests of the error paths: mode 0 = off,
  * 1 = every entry point fails its launch with MXQ_ERR_CUDA without
  * launching, 2 = argument checks fail with MXQ_ERR_ARG.  Also read once

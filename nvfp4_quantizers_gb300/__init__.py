@@ -13,6 +13,6 @@ from ._lib import (  # noqa: F401
     gemm_nvfp4_grouped, get_last_error, lib, moe_gate_up_swiglu,
     mxfp8_quantize_rowcol, nvfp4_quantize_per_token,
     nvfp4_quantize_per_token_gather, nvfp4_quantize_weight_shared,
-    scale_bytes, set_fault_inject, status_string)
+    scale_bytes, selftest_wait_timeout, set_fault_inject, status_string)
 
 __version__ = "0.1.0"

@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.mxq_scale_bytes.argtypes = [_i64, _i64, _int]
         L.mxq_get_last_error.restype = _int
         L.mxq_get_last_error.argtypes = []
+        L.mxq_selftest_wait_timeout.restype = _int
+        L.mxq_selftest_wait_timeout.argtypes = [_p]
         L.mxq_set_fault_inject.restype = None
         L.mxq_set_fault_inject.argtypes = [_int]
         L.mxfp8_quantize_rowcol.restype = _int
@@ -118,6 +120,16 @@ def get_last_error() -> int:
     """Synchronizes the device; returns the status of bounded device waits
     (MXQ_ERR_TIMEOUT) or of the CUDA runtime (MXQ_ERR_CUDA)."""
     return int(lib().mxq_get_last_error())
+
+
+def selftest_wait_timeout(device=None) -> None:
+    """Launch the failure-detection self-test kernel (a bounded device wait
+    that runs out after 20 ms); the next get_last_error() reports
+    MXQ_ERR_TIMEOUT (C: mxq_selftest_wait_timeout)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) \
+        if device is None else torch.device(device)
+    _check(lib().mxq_selftest_wait_timeout(_stream(dev)),
+           "mxq_selftest_wait_timeout")
 
 
 def set_fault_inject(mode: int) -> None:

@@ -199,6 +199,11 @@ mxq_status mxq_get_last_error(void) {
   return MXQ_OK;
 }
 
+mxq_status mxq_selftest_wait_timeout(void* stream) {
+  return from_cuda(launch_wait_selftest(20ull * 1000 * 1000,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 void mxq_set_fault_inject(int mode) {
   g_fault_mode.store(mode < 0 ? 0 : mode, std::memory_order_relaxed);
 }

@@ -300,22 +300,23 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Bounded wait on an mbarrier phase.  Gives up after ~1 s (or at once if
-// *abort is already set), ORs 1 into the device error word *err, sets
-// *abort so that every other wait of the CTA returns at once, and returns
-// false.  Callers keep executing their loop (skipping work) so that every
-// CTA-wide barrier is still reached by all threads.
+// Bounded wait on an mbarrier phase.  Gives up after limit_ns (~1 s by
+// default; or at once if *abort is already set), ORs 1 into the device
+// error word *err, sets *abort so that every other wait of the CTA returns
+// at once, and returns false.  Callers keep executing their loop (skipping
+// work) so that every CTA-wide barrier is still reached by all threads.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int* abort,
-                                          unsigned int* err) {
+                                          unsigned int* err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = global_timer_ns();
   while (true) {
     if (*abort) return false;
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       atomicOr(err, 1u);
       *abort = 1;
       return false;

@@ -32,6 +32,8 @@ cudaError_t make_tmap_2d_f32(CUtensorMap* map, const void* base,
 // mxfp8.cu
 // Reads (and clears when set) the error word of the bounded device waits.
 cudaError_t mxfp8_take_wait_error(unsigned int* word);
+// One CTA whose bounded mbarrier wait runs out after limit_ns.
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_mxfp8_rowcol(const void* x, int64_t M, int64_t K,
                                 int64_t ldx, uint8_t* row_codes,
                                 uint8_t* row_scales, uint8_t* col_codes,

@@ -297,7 +297,29 @@ __global__ void __launch_bounds__(THREADS, 2)
   pdl_launch_dependents();
 }
 
+// Failure-detection self-test: thread 0 waits on an mbarrier that nothing
+// will ever complete, through the same bounded wait the kernels use, with a
+// short limit; the wait gives up, records the error word and returns.
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    mbar_wait(smem_addr(&bar), 0, &abort, &g_mxfp8_wait_error, limit_ns);
+  __syncthreads();
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cudaGetLastError();
+}
 
 size_t mxfp8_rowcol_smem_bytes() { return sizeof(Smem) + 1024; }
 
