@@ -430,6 +430,8 @@ def run_gpu(args):
         "wall_s_timed_region": round(wall, 3),
     }
     out["gemm"] = run_gemm(q, W, dev, stream)
+    if not args.no_shapes:
+        out["shapes"] = run_shapes(q, W, dev, stream)
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args)
     print(json.dumps(out), flush=True)
@@ -553,6 +555,134 @@ def run_gemm(q, W, dev, stream, reps=20):
            "forward_us": round((ms_gq + ms_sw) * 1e3, 2),
            "padded_rows": Mp2, "output": "bf16 h [rows x 768]"})
     out["peaks_kind"] = peaks["kind"]
+    return out
+
+
+def _time_reps(fn, stream, reps, flush_w, flush_r, warmup=3):
+    """Per-launch device times (ms) of `fn` on `stream`: the L2 is flushed
+    before every rep (a write of one buffer larger than L2, then a read of
+    another, so the timed launch starts with clean lines that hold none of
+    its data), outside the events that bracket the launch."""
+    import torch
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+        for _ in range(reps):
+            flush_w.fill_(1)
+            flush_r.sum()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def _shape_line(ms_list, nbytes, elems, peak):
+    ms = sorted(ms_list)
+    med = statistics.median(ms)
+    p10 = ms[int(0.1 * (len(ms) - 1))]
+    p90 = ms[int(round(0.9 * (len(ms) - 1)))]
+    gbs = nbytes / med / 1e6
+    return {"us": round(med * 1e3, 2), "us_p10": round(p10 * 1e3, 2),
+            "us_p90": round(p90 * 1e3, 2), "GB/s": round(gbs, 1),
+            "GB/s_p10_p90": [round(nbytes / p90 / 1e6, 1),
+                             round(nbytes / p10 / 1e6, 1)],
+            "Gelem/s": round(elems / med / 1e6, 2),
+            "frac": round(gbs / peak, 3), "bytes": int(nbytes)}
+
+
+def run_shapes(q, W, dev, stream, reps=20):
+    """Each quantizer and dequantizer alone at the full sizes of the
+    workloads it is specified on, L2 flushed before every launch: MXFP8
+    rowwise + columnwise of the four 8192 x 4096 input classes and of the
+    linear layer's input [2048 x 2048] and weight [8192 x 2048]; NVFP4
+    per-token on the ragged batch of 64 sequences (lengths in [128, 4096],
+    hidden 2048); NVFP4 shared-scale weights of a 128-expert MoE layer
+    (gate/up pairs [2 x 768 x 2048] and down [2048 x 768]); and the
+    dequantizations of each."""
+    import torch
+    peak = measured_peak()[0]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    out = {}
+
+    def dev16(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def mx(name, bits):
+        x = dev16(bits)
+        m, k = x.shape
+        n = m * k
+        r = q.mxfp8_quantize_rowcol(x)
+        out[f"mxfp8_rowcol_{name}"] = _shape_line(
+            _time_reps(lambda: q.mxfp8_quantize_rowcol(x), stream, reps,
+                       flush_w, flush_r),
+            2 * n + 2 * (n + n // 32), n, peak)
+        return r
+
+    r = None
+    for cls, gen in (("random", W.mxfp8_random), ("boundary", W.mxfp8_boundary),
+                     ("zeros", W.mxfp8_zeros), ("maxes", W.mxfp8_maxes)):
+        r = mx(f"8192x4096_{cls}", gen(8192, 4096))
+    n = 8192 * 4096
+    for nm, cod, sc in (("row", r.row_codes, r.row_scales),
+                        ("col", r.col_codes_t, r.col_scales_t)):
+        out[f"dequantize_mxfp8_{nm}_8192x4096"] = _shape_line(
+            _time_reps(lambda: q.dequantize_mxfp8(cod, sc), stream, reps,
+                       flush_w, flush_r),
+            n + n // 32 + 2 * n, n, peak)
+    del r
+    mx("2048x2048_linear_input", W.linear_input())
+    mx("8192x2048_linear_weight", W.linear_weight())
+
+    # NVFP4 per-token, ragged batch flattened
+    H = 2048
+    lengths = W.ragged_lengths()
+    x = dev16(W.ragged_tokens(lengths, H))
+    T = x.shape[0]
+    tq = q.nvfp4_quantize_per_token(x)
+    tb = T * (2 * H + H // 2 + H // 16 + 4)
+    out[f"nvfp4_per_token_ragged_{T}x{H}"] = dict(_shape_line(
+        _time_reps(lambda: q.nvfp4_quantize_per_token(x), stream, reps,
+                   flush_w, flush_r), tb, T * H, peak),
+        sequences=int(len(lengths)))
+    out[f"dequantize_nvfp4_ragged_{T}x{H}"] = _shape_line(
+        _time_reps(lambda: q.dequantize_nvfp4(tq.codes, tq.block_scales,
+                                              tq.scales),
+                   stream, reps, flush_w, flush_r), tb, T * H, peak)
+    del x, tq
+
+    # NVFP4 weights of a 128-expert MoE layer
+    E, F = 128, 768
+    experts = W.moe_layer(E, H, F)
+    gate_up = [[dev16(g), dev16(u)] for g, u, d in experts]
+    down = [[dev16(d)] for g, u, d in experts]
+    del experts
+    for nm, groups, rows, cols in (("gate_up", gate_up, 2 * F, H),
+                                   ("down", down, H, F)):
+        ws = torch.empty(max(int(q.lib().nvfp4_quantize_weight_shared_workspace_size(E)), 256),
+                         dtype=torch.uint8, device=dev)
+        wq = q.nvfp4_quantize_weight_shared(groups, workspace=ws)
+        ne = E * rows * cols
+        wb = ne * 2 + ne // 2 + ne // 16 + 4 * E
+        out[f"nvfp4_weight_{nm}_{E}x{rows}x{cols}"] = _shape_line(
+            _time_reps(lambda: q.nvfp4_quantize_weight_shared(groups,
+                                                              workspace=ws),
+                       stream, reps, flush_w, flush_r), wb, ne, peak)
+        out[f"dequantize_nvfp4_{nm}_{E}x{rows}x{cols}"] = _shape_line(
+            _time_reps(lambda: q.dequantize_nvfp4(wq.codes, wq.block_scales,
+                                                  wq.scales),
+                       stream, reps, flush_w, flush_r), wb, ne, peak)
+        del wq
+    del gate_up, down, flush_w, flush_r
+    torch.cuda.empty_cache()
+    out["timing"] = (f"median of {reps} launches (p10/p90 beside it), each "
+                     "after an L2 flush; GB/s = algorithmic bytes / time")
     return out
 
 
@@ -752,6 +882,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=0,
                     help="rows of X per reference step (0: sized to ~1 min)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-shapes", action="store_true",
+                    help="skip the per-kernel lines at every workload's size")
     ap.add_argument("--serial", action="store_true",
                     help="run the step's three chains on one stream")
     args = ap.parse_args()

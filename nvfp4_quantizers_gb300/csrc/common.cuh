@@ -215,6 +215,35 @@ __device__ __forceinline__ void st_v8(void* p, uint4 a, uint4 b) {
 __device__ __forceinline__ void st_32B(void* p, uint4 a, uint4 b, bool wide);
 
 // 32-byte non-allocating load (sm_100 family); p must be 32-byte aligned.
+// L2 cache policy that marks the lines an access touches as the first to
+// evict (data read for the last time).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;"
+               : "=l"(pol));
+  return pol;
+}
+
+// 16- and 32-byte streaming loads under an L2 cache policy.
+__device__ __forceinline__ uint4 ld_last_v4(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, "
+      "[%4], %5;"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void ld_last_v8(const void* p, uint4& a, uint4& b,
+                                           uint64_t pol) {
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
+      : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y),
+        "=r"(b.z), "=r"(b.w)
+      : "l"(p), "l"(pol));
+}
+
 __device__ __forceinline__ void ld_stream_v8(const void* p, uint4& a,
                                              uint4& b) {
   asm volatile(
@@ -316,6 +345,42 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   while (true) {
     if (*abort) return false;
     if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) {
+      atomicOr(err, 1u);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about hint_ns pass, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar,
+                                                   uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for warps that have nothing else to do meanwhile: the same
+// bounds, but the waiting thread sleeps in the barrier (up to 100 us per
+// try) instead of spinning, leaving the issue slots to the warps that work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity,
+                                                volatile int* abort,
+                                                unsigned int* err,
+                                                uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (*abort) return false;
+    if (mbar_try_wait_hint(bar, parity, 100000u)) return true;
     if (global_timer_ns() - t0 > limit_ns) {
       atomicOr(err, 1u);
       *abort = 1;

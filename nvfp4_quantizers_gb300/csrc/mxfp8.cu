@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int64_t m0 = (int64_t)tm * BM, k0 = (int64_t)tk * BK;
     const int rows_valid = (int)imin<int64_t>(BM, p.M - m0);
     const int cols_valid = (int)imin<int64_t>(BK, p.K - k0);
-    const bool ok = mbar_wait(smem_addr(&s.full[stage]), phase, &s.abort,
+    const bool ok = mbar_wait_sleep(smem_addr(&s.full[stage]), phase, &s.abort,
                              &g_mxfp8_wait_error);
     const uint16_t* tile = s.tile[stage];
 

@@ -77,9 +77,19 @@ __device__ __forceinline__ uint32_t warp_max(uint32_t a) {
   return a;
 }
 
+// pol != 0: the rows are read for the last time (the weight quantizer's
+// second pass): their lines are marked first to evict in L2.
 __device__ __forceinline__ void load_block(Blk& v, const uint16_t* row,
-                                           int64_t b, bool valid, bool wide) {
-  if (valid) {
+                                           int64_t b, bool valid, bool wide,
+                                           uint64_t pol = 0) {
+  if (valid && pol) {
+    if (wide) {
+      ld_last_v8(row + b * 16, v.a, v.b, pol);
+    } else {
+      v.a = ld_last_v4(row + b * 16, pol);
+      v.b = ld_last_v4(row + b * 16 + 8, pol);
+    }
+  } else if (valid) {
     if (wide) {
       ld_stream_v8(row + b * 16, v.a, v.b);
     } else {
@@ -157,7 +167,7 @@ template <int R, int WPR>
 __device__ __forceinline__ void encode_row_warps(
     const uint16_t* row, bool load, bool write, float S_given, bool use_given,
     const RowOut& o, int row_slot, int wpart, int lane, uint32_t* red,
-    float* S_used) {
+    float* S_used, uint64_t pol = 0) {
   const int64_t blk0 = (int64_t)wpart * R * 32;
   Blk v[R];
   uint32_t am[R];
@@ -165,7 +175,7 @@ __device__ __forceinline__ void encode_row_warps(
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int64_t b = blk0 + r * 32 + lane;
-    load_block(v[r], row, b, load && b < o.nblocks, o.wide);
+    load_block(v[r], row, b, load && b < o.nblocks, o.wide, pol);
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -321,26 +331,31 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 
 // ---------------------------------------------------------------------------
 // Weight groups: one persistent kernel working through a task list.  Per
-// group g there are nA amax tasks (32 KiB of the group each) and nE encode
-// tasks (ROWS rows each); an encode task needs its group's S, i.e. every
-// amax task of the group.  The list holds all amax tasks, then all encode
-// tasks; CTAs take tasks in list order from an atomic counter, so an encode
-// task only ever waits (bounded) for amax tasks that running CTAs already
-// hold, and the data read by the amax tasks is still in L2 when the encode
-// tasks read it again.  (Interleaving the next group's amax tasks with the
-// encode tasks, to overlap HBM-bound and ALU-bound work, measured slower:
-// the encode tasks then wait for amax tasks handed out just before them.)
+// group g there are nA amax tasks (64 KiB of the group each) and nE encode
+// tasks (2 x ROWS rows each); an encode task needs its group's S, i.e.
+// every amax task of the group.  Groups are taken in windows of about
+// 32 MB of input, and the list runs A(0) A(1) E(0) A(2) E(1) ... E(last):
+// the amax tasks of a window, then those of the next window, then the
+// encode tasks of the first one.  CTAs take tasks in list order from an
+// atomic counter, so an encode task only ever waits (bounded) for amax
+// tasks that running CTAs already hold, and by the time it is handed out a
+// window of amax tasks and one of encode tasks separate it from its
+// group's; the two windows in flight (about 64 MB) stay in the 126 MB L2,
+// so the encode tasks read their rows back from L2 however many groups a
+// call holds (those reads mark the lines first to evict, so lines still
+// waiting for their second read outlive the ones read twice).
 //
 // Workspace: [1 + launch] the task counter of each launch; [64 + g] the
 // amax of group g (float bits, merged with atomicMax); [64 + G + g] the
-// number of group g's amax tasks that have merged their maximum (atomicAdd
-// after a fence).  Plain single-shot atomics: a compare-and-swap loop on
+// number of group g's amax tasks that have merged their maximum (a release
+// add after the maximum).  Plain single-shot atomics: a compare-and-swap loop on
 // one word per group serialises the hundreds of CTAs that finish together.
 // ---------------------------------------------------------------------------
 constexpr int kMaxGroupsPerLaunch = 256;
 constexpr int64_t kTaskChunks = 4096;         // 16-byte chunks per amax task
 constexpr int kRowSetsPerTask = 2;            // encode task: 2 x ROWS rows
 constexpr int kWsHeaderWords = 64;            // [1 + launch] = task counters
+constexpr int64_t kWindowBytes = 32ll << 20;  // input bytes per window
 
 // Error word of the bounded waits of this translation unit.
 __device__ unsigned int g_nvfp4_wait_error = 0;
@@ -357,6 +372,7 @@ struct GroupParams {
   int64_t g0;                         // global index of local group 0
   int ng;                             // groups in this launch
   int64_t nA, nE;                     // amax / encode tasks per group
+  int64_t win;                        // groups per window (>= 1)
   uint8_t* codes;                     // group g at g * R * K/2
   uint8_t* scales;                    // group g at g * scale_stride
   int64_t scale_stride;
@@ -379,15 +395,63 @@ __device__ __forceinline__ const uint16_t* chunk_ptr(const GroupTable& tab,
 }
 
 // Task t of the list -> (is_amax, local group, index within the group).
-// Task t of the list -> (is_amax, local group, index within the group).
+// With S given there are only encode tasks, group-major.  Otherwise the
+// list is A(0), then for w = 0, 1, ...: A(w+1) (if window w+1 exists) and
+// E(w); A(w) holds nA tasks per group of window w, E(w) nE per group, and
+// every window but the last holds `win` groups.
 __device__ __forceinline__ void task_of(const GroupParams& p, int64_t t,
                                         bool* is_a, int* gl, int64_t* idx) {
-  const int64_t na_all = p.S_in ? 0 : (int64_t)p.ng * p.nA;
-  *is_a = t < na_all;
-  if (!*is_a) t -= na_all;
-  const int64_t per = *is_a ? p.nA : p.nE;
-  *gl = (int)(t / per);
-  *idx = t - (int64_t)*gl * per;
+  if (p.S_in) {
+    *is_a = false;
+    *gl = (int)(t / p.nE);
+    *idx = t - (int64_t)*gl * p.nE;
+    return;
+  }
+  const int64_t W = p.win;
+  const int64_t nw = (p.ng + W - 1) / W;
+  const int64_t last = p.ng - (nw - 1) * W;        // groups of window nw-1
+  int64_t w = 0;                                   // window of the segment
+  int64_t g0 = 0, per = p.nA;                      // segment's first group
+  bool a = true;
+  const int64_t a0 = (nw == 1 ? last : W) * p.nA;
+  if (t >= a0) {
+    t -= a0;
+    // pairs (A(w+1), E(w)) with both windows full: w = 0 .. nw-3
+    const int64_t pair = W * (p.nA + p.nE);
+    const int64_t nfull = nw >= 3 ? nw - 2 : 0;
+    w = t / pair;
+    if (w > nfull) w = nfull;
+    t -= w * pair;
+    if (w + 1 < nw) {
+      const int64_t sa = (w + 1 == nw - 1 ? last : W) * p.nA;
+      if (t < sa) {
+        g0 = (w + 1) * W;
+      } else {
+        t -= sa;
+        const int64_t se = W * p.nE;               // window w < nw-1: full
+        a = false;
+        per = p.nE;
+        if (t < se) {
+          g0 = w * W;
+        } else {
+          t -= se;
+          g0 = (w + 1) * W;                        // final E(nw-1)
+        }
+      }
+    } else {
+      a = false;                                   // nw == 1: E(0)
+      per = p.nE;
+    }
+  }
+  *is_a = a;
+  const int64_t k = t / per;
+  *gl = (int)(g0 + k);
+  *idx = t - k * per;
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v)
+               : "memory");
 }
 
 template <int R, int WPR>
@@ -418,6 +482,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
   if (!p.S_in && threadIdx.x == 0) s_task[0] = (int64_t)atomicAdd(p.counter, 1u);
   __syncthreads();
   int buf = 0;
+  const uint64_t pol_last = l2_policy_evict_first();
   while (true) {
     int64_t t;
     if (p.S_in) {
@@ -480,8 +545,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
         uint32_t mm = red[0];
         for (int w = 1; w < CTA_WARPS; ++w) mm = max(mm, red[w]);
         if (mm) atomicMax(&amax[p.g0 + gl], mm << 16);
-        __threadfence();              // the maximum lands before the count
-        atomicAdd(&p.done[p.g0 + gl], 1u);
+        red_release_add(&p.done[p.g0 + gl], 1u);   // after the maximum
       }
       __syncthreads();
       continue;
@@ -538,7 +602,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
                staged ? s_sc[s8 % (kStage8 ? 8 : 1)] : nullptr};
       float S_used;
       encode_row_warps<R, WPR>(row, real, real, S, true, o, slot, wpart, lane,
-                               red, &S_used);
+                               red, &S_used, p.S_in ? 0 : pol_last);
     }
     }
     if (staged) {
@@ -676,6 +740,8 @@ cudaError_t launch_nvfp4_weight_shared(
   p.nA = (p.part_chunk0[num_parts] + kTaskChunks - 1) / kTaskChunks;
   const int64_t rows_per_task = kRowSetsPerTask * (CTA_WARPS / sh.WPR);
   p.nE = (p.R_pad + rows_per_task - 1) / rows_per_task;
+  p.win = kWindowBytes / (p.R * K * 2);
+  if (p.win < 1) p.win = 1;
   p.done = ws ? ws + kWsHeaderWords + num_groups : nullptr;
   p.codes = codes;
   p.scales = scales;

@@ -329,6 +329,7 @@ def check_weight_groups(q, groups_bits, lay, S_in=None):
     r = q.nvfp4_quantize_weight_shared(groups, S_dev, lay)
     y = q.dequantize_nvfp4(r.codes, r.block_scales, r.scales, lay)
     torch.cuda.synchronize()
+    assert q.get_last_error() == q.MXQ_OK       # no bounded wait gave up
     codes, bs, S, yb = host_u8(r.codes), host_u8(r.block_scales), \
         r.scales.cpu().numpy(), host_bits(y)
     for g, parts in enumerate(groups_bits):
@@ -379,6 +380,53 @@ def test_weight_ragged_parts(mxq, lay):
     check_weight_groups(mxq, groups, lay)
 
 
+@pytest.mark.parametrize("lay", LAYOUTS)
+def test_weight_odd_scale_rows(mxq, lay):
+    """Parts of 99 and 60 rows with K = 48: 477 block scales per group, so
+    the linear scale matrices of consecutive groups are not 4-byte aligned
+    (byte stores), and the swizzled ones have a padding column."""
+    rng = np.random.default_rng(13)
+    groups = [[W.to_bf16_bits(rng.standard_normal((99, 48)) * s),
+               W.to_bf16_bits(rng.standard_normal((60, 48)) * 3 * s)]
+              for s in (1e-2, 1.0, 7.0, 0.3)]
+    check_weight_groups(mxq, groups, lay)
+
+
+@pytest.mark.parametrize("lay", LAYOUTS)
+def test_weight_wide_rows_and_slices(mxq, lay):
+    """K = 1552 (97 blocks per row: 16 KiB units start and end inside rows,
+    and a partial 4-column scale tile), parts of 300 and 200 rows (units
+    straddle the part boundary), three groups at three scales."""
+    rng = np.random.default_rng(11)
+    groups = [[W.to_bf16_bits(rng.standard_normal((300, 1552)) * s),
+               W.to_bf16_bits(rng.standard_normal((200, 1552)) * 0.5 * s)]
+              for s in (2e-3, 1.0, 50.0)]
+    check_weight_groups(mxq, groups, lay)
+
+
+def test_weight_windows(mxq):
+    """Five gate/up pairs of [1024 x 4096] (16 MiB each): the unit list
+    spans three windows of groups (2, 2, 1).  Every group scale is checked,
+    and the groups at the start of the first and of the last window byte
+    for byte."""
+    rng = np.random.default_rng(12)
+    groups_bits = [[W.to_bf16_bits(rng.standard_normal((1024, 4096)) * s),
+                    W.to_bf16_bits(rng.standard_normal((1024, 4096)) * 2 * s)]
+                   for s in (0.01, 0.1, 1.0, 3.0, 0.02)]
+    groups = [[dev_bf16(x) for x in g] for g in groups_bits]
+    r = mxq.nvfp4_quantize_weight_shared(groups)
+    torch.cuda.synchronize()
+    assert mxq.get_last_error() == mxq.MXQ_OK
+    S = r.scales.cpu().numpy()
+    for e, (a, b) in enumerate(groups_bits):
+        assert S[e] == O.nvfp4_tensor_scale(max(O.bf16_amax(a), O.bf16_amax(b)))
+    for e in (0, 4):
+        oc, osc, oS = O.nvfp4_quantize_group(groups_bits[e])
+        assert_bytes_equal(host_u8(r.codes[e]), oc, f"group {e} codes")
+        assert_bytes_equal(host_u8(r.block_scales[e]), O.scale_swizzle(osc),
+                           f"group {e} scales")
+
+
 def test_weight_full_moe_layer_sampled(mxq):
     """128 Qwen3-30B-A3B-shaped experts at full size: gate/up fused pairs
     [1536 x 2048] under one scale each, down [2048 x 768] under its own.
@@ -391,6 +439,7 @@ def test_weight_full_moe_layer_sampled(mxq):
     dn = mxq.nvfp4_quantize_weight_shared([[dev_bf16(d)] for g, u, d in experts])
     ygu = mxq.dequantize_nvfp4(gu.codes, gu.block_scales, gu.scales)
     torch.cuda.synchronize()
+    assert mxq.get_last_error() == mxq.MXQ_OK
     for e, (g, u, d) in enumerate(experts):
         a_gu = max(O.bf16_amax(g), O.bf16_amax(u))
         assert gu.scales[e].item() == O.nvfp4_tensor_scale(a_gu)

@@ -14,6 +14,8 @@ The four input classes follow the quantizer-alignment section of that page
 from __future__ import annotations
 
 import hashlib
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import torch
@@ -203,18 +205,25 @@ def ragged_lengths(n_seq=64, lo=128, hi=4096, seed=0) -> np.ndarray:
 def ragged_tokens(lengths, H=2048, seed=0, outlier_token_frac=0.02,
                   outlier_channels=4, outlier_mul=100.0) -> np.ndarray:
     """Flattened [sum(lengths) x H] bf16 activations: t(4) values; in a
-    fraction of tokens a few random channels are multiplied by 100."""
+    fraction of tokens a few random channels are multiplied by 100.  Every
+    sequence draws from its own generator, so the sequences are made on a
+    thread pool with the same result as one after the other."""
+    lengths = np.asarray(lengths, np.int64)
     out = np.empty((int(np.sum(lengths)), H), np.uint16)
-    row = 0
-    for s, L in enumerate(np.asarray(lengths, np.int64)):
+    starts = np.concatenate([[0], np.cumsum(lengths)])
+
+    def one(s):
+        L = int(lengths[s])
         rng = _rng(seed, 9, s)
-        v = rng.standard_t(4, size=(int(L), H)).astype(np.float32)
-        hit = np.nonzero(rng.random(int(L)) < outlier_token_frac)[0]
+        v = rng.standard_t(4, size=(L, H)).astype(np.float32)
+        hit = np.nonzero(rng.random(L) < outlier_token_frac)[0]
         for t in hit:
             ch = rng.choice(H, outlier_channels, replace=False)
             v[t, ch] *= outlier_mul
-        out[row:row + L] = to_bf16_bits(v)
-        row += int(L)
+        out[starts[s]:starts[s] + L] = to_bf16_bits(v)
+
+    with ThreadPoolExecutor(min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(one, range(len(lengths))))
     return out
 
 
@@ -260,6 +269,14 @@ def moe_expert(e: int, hidden=2048, ffn=768, seed=0, outlier_frac=1e-4,
             w.reshape(-1)[idx] *= outlier_mul
         out.append(to_bf16_bits(w))
     return tuple(out)
+
+
+def moe_layer(n_experts=128, hidden=2048, ffn=768, seed=0):
+    """moe_expert for experts 0 .. n_experts-1 (each from its own generator),
+    made on a thread pool."""
+    with ThreadPoolExecutor(min(16, os.cpu_count() or 1)) as ex:
+        return list(ex.map(lambda e: moe_expert(e, hidden, ffn, seed),
+                           range(n_experts)))
 
 
 # --------------------------------------------------------------------------
