@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 // ---------------------------------------------------------------------------
 // Weight groups: one persistent kernel working through a task list.  Per
 // group g there are nA amax tasks (64 KiB of the group each) and nE encode
-// tasks (2 x ROWS rows each); an encode task needs its group's S, i.e.
+// tasks (2 or 4 sets of ROWS rows); an encode task needs its group's S, i.e.
 // every amax task of the group.  Groups are taken in windows of about
 // 32 MB of input, and the list runs A(0) A(1) E(0) A(2) E(1) ... E(last):
 // the amax tasks of a window, then those of the next window, then the
@@ -353,7 +353,15 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 // ---------------------------------------------------------------------------
 constexpr int kMaxGroupsPerLaunch = 256;
 constexpr int64_t kTaskChunks = 4096;         // 16-byte chunks per amax task
-constexpr int kRowSetsPerTask = 2;            // encode task: 2 x ROWS rows
+// Encode task: RowSets(R, WPR) sets of ROWS rows.  Rows of at most 1024
+// values (R <= 2 blocks per lane) take 4 sets, 32 rows (short rows would
+// otherwise make small tasks whose fixed cost dominates: 128 down
+// projections [2048 x 768], 210 -> 190 us); longer rows take 2 (4 sets
+// measured slower at 2048 values, and with WPR = 2 the 8 rows of 2 sets
+// fill whole swizzled scale sectors).
+__host__ __device__ constexpr int RowSets(int r, int wpr) {
+  return (wpr == 1 && r <= 2) ? 4 : 2;
+}
 constexpr int kWsHeaderWords = 64;            // [1 + launch] = task counters
 constexpr int64_t kWindowBytes = 32ll << 20;  // input bytes per window
 
@@ -465,6 +473,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
   // Encode tasks of 8 rows with swizzled scales: the rows 2k + d + 32q of
   // one 128-row tile, whose block scales fill whole 32-byte sectors of the
   // swizzled tiles; staged here, written as one 32-byte store per tile.
+  constexpr int kRowSetsPerTask = RowSets(R, WPR);
   constexpr bool kStage8 = ROWS * kRowSetsPerTask == 8;
   __shared__ __align__(16) uint8_t s_sc[kStage8 ? 8 : 1][kStage8 ? 256 : 4];
   __shared__ float s_S;
@@ -738,7 +747,7 @@ cudaError_t launch_nvfp4_weight_shared(
   p.R_pad = swizzled ? (p.R + 127) / 128 * 128 : p.R;
   p.K = K;
   p.nA = (p.part_chunk0[num_parts] + kTaskChunks - 1) / kTaskChunks;
-  const int64_t rows_per_task = kRowSetsPerTask * (CTA_WARPS / sh.WPR);
+  const int64_t rows_per_task = RowSets(sh.R, sh.WPR) * (CTA_WARPS / sh.WPR);
   p.nE = (p.R_pad + rows_per_task - 1) / rows_per_task;
   p.win = kWindowBytes / (p.R * K * 2);
   if (p.win < 1) p.win = 1;
