@@ -95,6 +95,14 @@ def lib():
             L.oracle_scale_swizzle.argtypes = [_p, _i64, _i64, _p]
             L.oracle_scale_unswizzle.restype = ctypes.c_int
             L.oracle_scale_unswizzle.argtypes = [_p, _i64, _i64, _p]
+            L.oracle_fp8blk_scale.restype = ctypes.c_float
+            L.oracle_fp8blk_scale.argtypes = [ctypes.c_float]
+            L.oracle_fp8blk_quantize.restype = ctypes.c_int
+            L.oracle_fp8blk_quantize.argtypes = [_p, _i64, _i64, _i64, _i64,
+                                                 _i64, _p, _p]
+            L.oracle_fp8blk_dequantize.restype = ctypes.c_int
+            L.oracle_fp8blk_dequantize.argtypes = [_p, _p, _i64, _i64, _i64,
+                                                   _i64, _p]
             _lib = L
     return _lib
 
@@ -414,3 +422,51 @@ def moe_gate_up_swiglu(a_codes, a_scales, a_S, offsets, w_codes, w_scales,
     C = gemm_nvfp4_grouped(a_codes, a_scales, a_S, offsets, w_codes,
                            w_scales, w_S)
     return silu(C[:, :F]) * C[:, F:]
+
+
+# --------------------------------------------------------------------------
+# FP8 E4M3 with FP32 block scales: the DeepSeek-V3-style recipe named in the
+# introduction of "Miles: end-to-end MXFP8 and per-token NVFP4 RL" (weights
+# in 128x128 blocks, activations in 1x128 tiles, scales computed online) and
+# its backward conversion (MXFP8 recipe section: dequantize, then requantize
+# in the backward orientation).  Arithmetic in mxq_oracle.c.
+# --------------------------------------------------------------------------
+def fp8_block_scale(amax: float) -> float:
+    """S = amax / 448 in binary32 (a decode scale)."""
+    return float(lib().oracle_fp8blk_scale(float(amax)))
+
+
+def fp8_block_quantize(x: np.ndarray, block_rows: int = 1,
+                       block_cols: int = 128):
+    """E4M3 codes u8 [R, C] and FP32 scales [R/block_rows, C/block_cols] of
+    x [R, C] (bf16 bits): 1x128 tiles (block_rows = 1) or 128x128 blocks."""
+    x = _bf16(x)
+    R, C = x.shape
+    codes = np.empty((R, C), np.uint8)
+    scales = np.empty((R // block_rows, C // block_cols), np.float32)
+    _check(lib().oracle_fp8blk_quantize(_ptr(x), R, C, C, block_rows,
+                                        block_cols, _ptr(codes), _ptr(scales)),
+           "fp8 block quantize")
+    return codes, scales
+
+
+def fp8_block_dequantize(codes: np.ndarray, scales: np.ndarray,
+                         block_rows: int = 1, block_cols: int = 128) -> np.ndarray:
+    """bf16 bits of E4M3(code) * S, S the code's block scale."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.float32)
+    R, C = codes.shape
+    y = np.empty((R, C), np.uint16)
+    _check(lib().oracle_fp8blk_dequantize(_ptr(codes), _ptr(scales), R, C,
+                                          block_rows, block_cols, _ptr(y)),
+           "fp8 block dequantize")
+    return y
+
+
+def fp8_block_requantize_transpose(codes: np.ndarray, scales: np.ndarray):
+    """The backward-orientation conversion of 1x128-tile FP8 activations
+    X [M, K]: dequantize to bf16, then quantize the transpose X^T [K, M]
+    in 1x128 tiles (128x1 blocks of X).  Returns (codes_t [K, M], scales_t
+    [K, M/128])."""
+    y = fp8_block_dequantize(codes, scales, 1, 128)
+    return fp8_block_quantize(np.ascontiguousarray(y.T), 1, 128)

@@ -425,3 +425,72 @@ int oracle_scale_unswizzle(const uint8_t* swz, int64_t R, int64_t C,
         }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* FP8 E4M3 with one FP32 scale per block: the DeepSeek-V3-style recipe of  */
+/* "Miles: end-to-end MXFP8 and per-token NVFP4 RL", introduction (weights  */
+/* in 128x128 blocks, activations in 1x128 tiles, scales computed online    */
+/* per tile or block) and MXFP8 recipe section (that recipe stores forward  */
+/* activations in 1x128 tiles and, before the backward GEMM, dequantizes    */
+/* and requantizes them in the backward orientation).  The pages give no    */
+/* formula for the scale; the reading used here is the one the NVFP4        */
+/* second level uses, with 448 (the E4M3 maximum) as the code range:        */
+/*   a = max |x| over the block (exact),                                     */
+/*   S = fl(a / 448)              (a decode scale: value = code * S),        */
+/*   enc = fl(1 / S), FLT_MAX-clamped; 0 when S = 0,                         */
+/*   code = RNE_E4M3(fl(x * enc)), saturating at 448, sign kept;             */
+/*   dequant y = RNE_bf16(fl(E4M3(code) * S)).                               */
+/* Blocks are br x bc (1 x 128 tiles or 128 x 128 blocks); R % br == 0 and  */
+/* C % bc == 0.  codes [R x C]; scales [R/br x C/bc] row-major.             */
+/* ------------------------------------------------------------------------ */
+float oracle_fp8blk_scale(float amax) {
+    const float e4m3_max = 448.0f;
+    return amax / e4m3_max;
+}
+
+int oracle_fp8blk_quantize(const uint16_t* x, int64_t R, int64_t C,
+                           int64_t ldx, int64_t br, int64_t bc,
+                           uint8_t* codes, float* scales) {
+    if (R < 0 || C < 0 || br < 1 || bc < 1 || R % br || C % bc || ldx < C)
+        return 1;
+    build_tables();
+    const int64_t nbc = C / bc;
+    for (int64_t bi = 0; bi < R / br; ++bi)
+        for (int64_t bj = 0; bj < nbc; ++bj) {
+            float a = 0.0f;
+            for (int64_t r = bi * br; r < (bi + 1) * br; ++r)
+                for (int64_t c = bj * bc; c < (bj + 1) * bc; ++c) {
+                    float v = fabsf((float)bf16_decode(x[r * ldx + c]));
+                    if (v > a) a = v;
+                }
+            float s = oracle_fp8blk_scale(a);
+            float enc;
+            if (s == 0.0f) {
+                enc = 0.0f;
+            } else {
+                enc = 1.0f / s;
+                if (enc > FLT_MAX) enc = FLT_MAX;
+            }
+            scales[bi * nbc + bj] = s;
+            for (int64_t r = bi * br; r < (bi + 1) * br; ++r)
+                for (int64_t c = bj * bc; c < (bj + 1) * bc; ++c) {
+                    float v = (float)bf16_decode(x[r * ldx + c]) * enc;
+                    codes[r * C + c] = rne_e4m3((double)v);
+                }
+        }
+    return 0;
+}
+
+int oracle_fp8blk_dequantize(const uint8_t* codes, const float* scales,
+                             int64_t R, int64_t C, int64_t br, int64_t bc,
+                             uint16_t* y) {
+    if (R < 0 || C < 0 || br < 1 || bc < 1 || R % br || C % bc) return 1;
+    const int64_t nbc = C / bc;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            float s = scales[(r / br) * nbc + c / bc];
+            float v = (float)e4m3_decode(codes[r * C + c]) * s;
+            y[r * C + c] = rne_bf16_from_f32(v);
+        }
+    return 0;
+}

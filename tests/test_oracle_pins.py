@@ -629,3 +629,134 @@ def test_moe_swiglu_structure(orc):
                                 wS_small)
     assert 0.01 < np.median(np.abs(h1[:, 2:])) < 100
     assert not np.allclose(h1, h2, rtol=1e-3)
+
+
+# --------------------------------------------------------------------------
+# FP8 with FP32 block scales (DeepSeek-V3-style recipe, introduction of
+# "Miles: end-to-end MXFP8 and per-token NVFP4 RL": 128x128 weight blocks,
+# 1x128 activation tiles, online scales; MXFP8 recipe section: the backward
+# conversion dequantizes and requantizes the 1x128 tiles).
+# --------------------------------------------------------------------------
+def _fp8blk_power_of_two_rows(rng, R, C):
+    """Rows whose 1x128 tiles have amax exactly 448 * 2^j (one element per
+    tile at +-448 * 2^j, the rest uniform below it)."""
+    x = np.empty((R, C), np.float32)
+    for r in range(R):
+        for t in range(C // 128):
+            j = int(rng.integers(-12, 12))
+            v = rng.uniform(-448, 448, 128) * 2.0 ** j
+            v[rng.integers(128)] = (448.0 if rng.random() < 0.5 else -448.0) * 2.0 ** j
+            x[r, t * 128:(t + 1) * 128] = v
+    return W.to_bf16_bits(x)
+
+
+def test_fp8blk_power_of_two_scale_matches_torch_cast(orc):
+    """amax = 448 * 2^j gives S = 2^j exactly, so x * fl(1/S) is exact and
+    the codes are torch's E4M3 cast of x * 2^-j (all within +-448)."""
+    rng = np.random.default_rng(31)
+    x = _fp8blk_power_of_two_rows(rng, 8, 512)
+    codes, S = orc.fp8_block_quantize(x, 1)
+    xf = W.bits_to_f32(x).astype(np.float64)
+    amax = np.abs(xf).reshape(8, 4, 128).max(axis=2)
+    j = np.log2(amax / 448.0)
+    assert np.array_equal(j, np.round(j))
+    assert np.array_equal(S.astype(np.float64), 2.0 ** j)
+    scaled = xf / np.repeat(2.0 ** j, 128, axis=1)
+    assert np.abs(scaled).max() <= 448.0
+    ref = torch.from_numpy(scaled).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+
+
+def test_fp8blk_block_max_gets_the_format_max(orc):
+    """In every non-zero block the element of largest magnitude encodes to
+    +-448 (0x7E / 0xFE): a * fl(1/fl(a/448)) is within a few ulp of 448,
+    far inside 448's rounding interval [432, 448].  A scale stored the other
+    way round (encode instead of decode) or a wrong block extent breaks it."""
+    rng = np.random.default_rng(32)
+    x = W.to_bf16_bits(rng.standard_t(3, size=(256, 384)).astype(np.float32)
+                       * 10.0 ** rng.uniform(-30, 30, size=(256, 1)).astype(np.float32))
+    xf = np.abs(W.bits_to_f32(x))
+    for br in (1, 128):
+        codes, S = orc.fp8_block_quantize(x, br)
+        blk = xf.reshape(256 // br, br, 3, 128).transpose(0, 2, 1, 3).reshape(
+            256 // br, 3, -1)
+        cb = codes.reshape(256 // br, br, 3, 128).transpose(0, 2, 1, 3).reshape(
+            256 // br, 3, -1)
+        arg = blk.argmax(axis=2)
+        top = np.take_along_axis(cb, arg[..., None], axis=2)[..., 0]
+        assert np.all((top & 0x7F) == 0x7E)
+        assert np.all(S > 0)
+        assert np.array_equal(S, (blk.max(axis=2) / np.float32(448)).astype(np.float32))
+
+
+def test_fp8blk_zero_block_and_signs(orc):
+    x = np.zeros((2, 256), np.uint16)
+    x[1, :128] = 0x8000                       # -0 everywhere in one tile
+    x[1, 200] = W.to_bf16_bits(np.array([3.0], np.float32))[0]
+    codes, S = orc.fp8_block_quantize(x, 1)
+    assert S[0, 0] == 0 and S[0, 1] == 0 and S[1, 0] == 0
+    assert np.all(codes[0] == 0) and np.all(codes[1, :128] == 0x80)
+    assert S[1, 1] == np.float32(3.0) / np.float32(448.0)
+    assert codes[1, 200] == 0x7E
+    y = orc.fp8_block_dequantize(codes, S, 1)
+    assert np.all(y[0] == 0) and np.all(y[1, :128] == 0x8000)
+
+
+def test_fp8blk_round_trip_within_half_a_step(orc):
+    """dequant(quant(x)) is within half an E4M3 step of x (relative 2^-4 in
+    the normal range, 2^-10 * S absolute in the subnormal range) plus the
+    bf16 rounding of the result (relative 2^-8)."""
+    rng = np.random.default_rng(33)
+    x = W.to_bf16_bits(rng.standard_normal((128, 512)).astype(np.float32))
+    xf = W.bits_to_f32(x).astype(np.float64)
+    for br in (1, 128):
+        codes, S = orc.fp8_block_quantize(x, br)
+        y = W.bits_to_f32(orc.fp8_block_dequantize(codes, S, br)).astype(np.float64)
+        s = np.repeat(np.repeat(S.astype(np.float64), br, axis=0), 128, axis=1)
+        bound = np.abs(xf) * (2.0 ** -4 + 2.0 ** -8) * (1 + 1e-6) + s * 2.0 ** -10 * (1 + 2.0 ** -8)
+        assert np.all(np.abs(y - xf) <= bound)
+
+
+def test_fp8blk_block_geometry_brute_force(orc):
+    """Raising one element changes the scale of exactly the block that holds
+    it: 1x128 tiles run along rows, 128x128 blocks tile the matrix."""
+    rng = np.random.default_rng(34)
+    base = W.to_bf16_bits(rng.uniform(-1, 1, (256, 256)).astype(np.float32))
+    for br in (1, 128):
+        _, S0 = orc.fp8_block_quantize(base, br)
+        for (r, c) in ((0, 0), (5, 130), (200, 127), (255, 255)):
+            x = base.copy()
+            x[r, c] = W.to_bf16_bits(np.array([1000.0], np.float32))[0]
+            _, S1 = orc.fp8_block_quantize(x, br)
+            changed = np.argwhere(S1 != S0)
+            assert changed.tolist() == [[r // br, c // 128]]
+
+
+def test_fp8blk_backward_conversion(orc):
+    """Requantizing 1x128 tiles in the backward orientation is exact when the
+    forward dequantization is (x built from E4M3 values times 2^j, so
+    dequant(quant(x)) == x): then it equals quantizing x^T directly.  On
+    generic data it is not: the dequantize-then-requantize path adds error
+    on top of the direct 128x1 quantization (MXFP8 recipe section)."""
+    rng = np.random.default_rng(35)
+    e4 = np.array([orc.decode_e4m3(c) for c in range(0x7F)])
+    M, K = 256, 256
+    v = rng.choice(e4, size=(M, K)) * rng.choice([-1.0, 1.0], size=(M, K))
+    j = rng.integers(-8, 8, size=(M, K // 128))
+    v[:, ::128] = 448.0                       # every tile's amax is 448 * 2^j
+    x = W.to_bf16_bits((v * np.repeat(2.0 ** j, 128, axis=1)).astype(np.float32))
+    codes, S = orc.fp8_block_quantize(x, 1)
+    assert np.array_equal(orc.fp8_block_dequantize(codes, S, 1), x)
+    ct, st = orc.fp8_block_requantize_transpose(codes, S)
+    dt, sd = orc.fp8_block_quantize(np.ascontiguousarray(x.T), 1)
+    assert np.array_equal(ct, dt) and np.array_equal(st, sd)
+    # generic data: the conversion differs from the direct quantization
+    g = W.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    codes, S = orc.fp8_block_quantize(g, 1)
+    ct, st = orc.fp8_block_requantize_transpose(codes, S)
+    dt, sd = orc.fp8_block_quantize(np.ascontiguousarray(g.T), 1)
+    assert (ct != dt).any()
+    gf = W.bits_to_f32(np.ascontiguousarray(g.T)).astype(np.float64)
+    err_conv = np.abs(W.bits_to_f32(orc.fp8_block_dequantize(ct, st, 1)) - gf).mean()
+    err_direct = np.abs(W.bits_to_f32(orc.fp8_block_dequantize(dt, sd, 1)) - gf).mean()
+    assert err_conv > err_direct
