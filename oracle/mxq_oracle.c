@@ -464,6 +464,10 @@ int oracle_fp8blk_quantize(const uint16_t* x, int64_t R, int64_t C,
                     if (v > a) a = v;
                 }
             float s = oracle_fp8blk_scale(a);
+            /* Stored before enc is derived: gcc -O2 otherwise concludes
+             * from "1/s > FLT_MAX" that s is 0 and stores 0 for a
+             * subnormal s (whose reciprocal overflows). */
+            scales[bi * nbc + bj] = s;
             float enc;
             if (s == 0.0f) {
                 enc = 0.0f;
@@ -471,7 +475,6 @@ int oracle_fp8blk_quantize(const uint16_t* x, int64_t R, int64_t C,
                 enc = 1.0f / s;
                 if (enc > FLT_MAX) enc = FLT_MAX;
             }
-            scales[bi * nbc + bj] = s;
             for (int64_t r = bi * br; r < (bi + 1) * br; ++r)
                 for (int64_t c = bj * bc; c < (bj + 1) * bc; ++c) {
                     float v = (float)bf16_decode(x[r * ldx + c]) * enc;

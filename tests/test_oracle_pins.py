@@ -760,3 +760,23 @@ def test_fp8blk_backward_conversion(orc):
     err_conv = np.abs(W.bits_to_f32(orc.fp8_block_dequantize(ct, st, 1)) - gf).mean()
     err_direct = np.abs(W.bits_to_f32(orc.fp8_block_dequantize(dt, sd, 1)) - gf).mean()
     assert err_conv > err_direct
+
+
+def test_fp8blk_subnormal_scale(orc):
+    """A block whose amax is ~1e-37 has a subnormal S = fl(amax / 448) (no
+    flush to zero) whose reciprocal overflows, so enc = FLT_MAX: S must be
+    numpy's binary32 quotient and the codes torch's E4M3 cast of
+    fl(x * FLT_MAX)."""
+    rng = np.random.default_rng(36)
+    v = (rng.uniform(-1, 1, (3, 256)) * 1e-37).astype(np.float32)
+    x = W.to_bf16_bits(v)
+    codes, S = orc.fp8_block_quantize(x, 1)
+    amax = np.abs(W.bits_to_f32(x)).reshape(3, 2, 128).max(axis=2)
+    ref = (amax.astype(np.float32) / np.float32(448.0)).astype(np.float32)
+    assert np.all(ref < np.finfo(np.float32).tiny) and np.all(ref > 0)
+    assert np.array_equal(S.view(np.uint32), ref.view(np.uint32))
+    xf = W.bits_to_f32(x).astype(np.float32)
+    prod = (xf * np.float32(np.finfo(np.float32).max)).astype(np.float64)
+    exp = torch.from_numpy(np.clip(prod, -448, 448).astype(np.float32)).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, exp)
