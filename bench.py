@@ -602,7 +602,9 @@ def run_shapes(q, W, dev, stream, reps=20):
     linear layer's input [2048 x 2048] and weight [8192 x 2048]; NVFP4
     per-token on the ragged batch of 64 sequences (lengths in [128, 4096],
     hidden 2048); NVFP4 shared-scale weights of a 128-expert MoE layer
-    (gate/up pairs [2 x 768 x 2048] and down [2048 x 768]); and the
+    (gate/up pairs [2 x 768 x 2048] and down [2048 x 768]); FP8 with FP32
+    block scales (1x128 tiles of the activation, 128x128 blocks of the
+    linear weight, the tiles' backward-orientation conversion); and the
     dequantizations of each."""
     import torch
     peak = measured_peak()[0]
@@ -679,7 +681,38 @@ def run_shapes(q, W, dev, stream, reps=20):
                                                   wq.scales),
                        stream, reps, flush_w, flush_r), wb, ne, peak)
         del wq
-    del gate_up, down, flush_w, flush_r
+    del gate_up, down
+
+    # FP8 with FP32 block scales: 1x128 tiles of X [8192 x 4096], 128x128
+    # blocks of the linear weight [8192 x 2048], the dequantizations and the
+    # backward-orientation conversion of the tiles
+    x = dev16(W.mxfp8_random(8192, 4096))
+    n = x.numel()
+    fq = q.fp8_block_quantize(x, 1)
+    out["fp8_block_1x128_8192x4096"] = _shape_line(
+        _time_reps(lambda: q.fp8_block_quantize(x, 1), stream, reps,
+                   flush_w, flush_r), 3 * n + 4 * (n // 128), n, peak)
+    out["fp8_block_dequantize_1x128_8192x4096"] = _shape_line(
+        _time_reps(lambda: q.fp8_block_dequantize(fq.codes, fq.scales, 1),
+                   stream, reps, flush_w, flush_r), 3 * n + 4 * (n // 128), n,
+        peak)
+    out["fp8_block_requantize_transpose_8192x4096"] = _shape_line(
+        _time_reps(lambda: q.fp8_block_requantize_transpose(fq.codes,
+                                                            fq.scales),
+                   stream, reps, flush_w, flush_r), 2 * n + 8 * (n // 128), n,
+        peak)
+    del x, fq
+    w = dev16(W.linear_weight())
+    n = w.numel()
+    wq = q.fp8_block_quantize(w, 128)
+    out["fp8_block_128x128_8192x2048"] = _shape_line(
+        _time_reps(lambda: q.fp8_block_quantize(w, 128), stream, reps,
+                   flush_w, flush_r), 3 * n + 4 * (n // 16384), n, peak)
+    out["fp8_block_dequantize_128x128_8192x2048"] = _shape_line(
+        _time_reps(lambda: q.fp8_block_dequantize(wq.codes, wq.scales, 128),
+                   stream, reps, flush_w, flush_r), 3 * n + 4 * (n // 16384),
+        n, peak)
+    del w, wq, flush_w, flush_r
     torch.cuda.empty_cache()
     out["timing"] = (f"median of {reps} launches (p10/p90 beside it), each "
                      "after an L2 flush; GB/s = algorithmic bytes / time")

@@ -297,6 +297,45 @@ mxq_status dequantize_nvfp4(const uint8_t* codes, const uint8_t* block_scales,
                             void* y, void* stream);
 
 /* --------------------------------------------------------------------- */
+/* FP8 E4M3 with one FP32 scale per block (the DeepSeek-V3-style recipe). */
+/*                                                                       */
+/* [MILES] introduction: that recipe scales weights in 128x128 blocks and */
+/* activations in 1x128 tiles, one FP32 scale per tile or block computed  */
+/* online.  [MILES] MXFP8 recipe section: it stores forward activations   */
+/* in 1x128 tiles and converts them to the backward orientation by        */
+/* dequantizing and requantizing before the backward GEMM.                */
+/*   S = amax / 448 (FP32 decode scale), enc = 1 / S (0 when S = 0,       */
+/*   FLT_MAX-clamped), code = RNE_E4M3(x * enc) saturating at +-448,      */
+/*   dequant y = RNE_bf16(E4M3(code) * S); binary32 throughout.           */
+/*                                                                       */
+/* fp8_block_quantize: x bf16 [rows x cols], row stride ldx elements      */
+/* (ldx >= cols, ldx % 8 == 0).  block_rows = 1: 1x128 tiles along rows;  */
+/* block_rows = 128: 128x128 blocks (rows % 128 == 0).  cols % 128 == 0.  */
+/* codes u8 [rows x cols]; scales f32 [rows/block_rows x cols/128],       */
+/* row-major.  All pointers 16-byte aligned.                              */
+/* --------------------------------------------------------------------- */
+mxq_status fp8_block_quantize(const void* x, int64_t rows, int64_t cols,
+                              int64_t ldx, int block_rows, uint8_t* codes,
+                              float* scales, void* stream);
+
+/* fp8_block_dequantize: bf16 y [rows x cols] from codes [rows x cols] and */
+/* scales [rows/block_rows x cols/128]; same shape rules.                 */
+mxq_status fp8_block_dequantize(const uint8_t* codes, const float* scales,
+                                int64_t rows, int64_t cols, int block_rows,
+                                void* y, void* stream);
+
+/* fp8_block_requantize_transpose: the backward-orientation conversion of  */
+/* 1x128-tile activations X [rows x cols] (codes, scales as produced by    */
+/* fp8_block_quantize with block_rows = 1): X is dequantized to bf16       */
+/* exactly as fp8_block_dequantize does and its transpose X^T [cols x rows] */
+/* is quantized in 1x128 tiles: codes_t u8 [cols x rows], scales_t f32     */
+/* [cols x rows/128].  rows % 128 == 0, cols % 128 == 0.                   */
+mxq_status fp8_block_requantize_transpose(const uint8_t* codes,
+                                          const float* scales, int64_t rows,
+                                          int64_t cols, uint8_t* codes_t,
+                                          float* scales_t, void* stream);
+
+/* --------------------------------------------------------------------- */
 /* Block-scaled GEMM consumers (5th-generation tensor cores).             */
 /*                                                                       */
 /* [MILES] MXFP8 recipe section: forward, weight-gradient and data-       */

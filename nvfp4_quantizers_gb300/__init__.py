@@ -8,8 +8,10 @@ it has not been built (``nvfp4_quantizers_gb300.build.build()``).
 from ._lib import (  # noqa: F401
     MXQ_ERR_ALIGN, MXQ_ERR_ARG, MXQ_ERR_CUDA, MXQ_ERR_LAYOUT, MXQ_ERR_NULL,
     MXQ_ERR_SHAPE, MXQ_ERR_TIMEOUT, MXQ_ERR_WORKSPACE, MXQ_OK, SCALE_LINEAR,
-    SCALE_SWIZZLED, S_PER_BATCH, S_PER_ROW, Mxfp8Quantized, MxqError,
-    Nvfp4Quantized, dequantize_mxfp8, dequantize_nvfp4, gemm_mxfp8,
+    SCALE_SWIZZLED, S_PER_BATCH, S_PER_ROW, Fp8BlockQuantized,
+    Mxfp8Quantized, MxqError, Nvfp4Quantized, dequantize_mxfp8,
+    dequantize_nvfp4, fp8_block_dequantize, fp8_block_quantize,
+    fp8_block_requantize_transpose, gemm_mxfp8,
     gemm_nvfp4_grouped, get_last_error, lib, moe_gate_up_swiglu,
     mxfp8_quantize_rowcol, nvfp4_quantize_per_token,
     nvfp4_quantize_per_token_gather, nvfp4_quantize_weight_shared,

@@ -101,6 +101,14 @@ def lib() -> ctypes.CDLL:
         L.dequantize_nvfp4.restype = _int
         L.dequantize_nvfp4.argtypes = [_p, _p, _p, _int, _i64, _i64, _i64,
                                        _int, _p, _p]
+        L.fp8_block_quantize.restype = _int
+        L.fp8_block_quantize.argtypes = [_p, _i64, _i64, _i64, _int, _p, _p,
+                                         _p]
+        L.fp8_block_dequantize.restype = _int
+        L.fp8_block_dequantize.argtypes = [_p, _p, _i64, _i64, _int, _p, _p]
+        L.fp8_block_requantize_transpose.restype = _int
+        L.fp8_block_requantize_transpose.argtypes = [_p, _p, _i64, _i64, _p,
+                                                     _p, _p]
         _lib = L
         return L
 
@@ -403,3 +411,63 @@ def moe_gate_up_swiglu(a_codes: torch.Tensor, a_scales: torch.Tensor,
         w_scales.data_ptr(), w_group_scales.data_ptr(), F, K, h.data_ptr(), F,
         _stream(a_codes.device)), "mxq_moe_gate_up_swiglu_nvfp4")
     return h
+
+
+# --------------------------------------------------------------------------
+# FP8 E4M3 with one FP32 scale per block (1x128 activation tiles, 128x128
+# weight blocks) and the backward-orientation conversion of 1x128 tiles.
+# --------------------------------------------------------------------------
+class Fp8BlockQuantized(NamedTuple):
+    codes: torch.Tensor                 # u8 [rows, cols]
+    scales: torch.Tensor                # f32 [rows / block_rows, cols / 128]
+    block_rows: int
+
+
+def fp8_block_quantize(x: torch.Tensor, block_rows: int = 1) -> Fp8BlockQuantized:
+    """E4M3 codes with one FP32 scale per 1x128 tile (block_rows = 1) or per
+    128x128 block (block_rows = 128) (C: fp8_block_quantize)."""
+    _bf16_2d(x, "x")
+    rows, cols = x.shape
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((max(rows // block_rows, 0), cols // 128),
+                         dtype=torch.float32, device=x.device)
+    _check(lib().fp8_block_quantize(x.data_ptr(), rows, cols, x.stride(0),
+                                    block_rows, codes.data_ptr(),
+                                    scales.data_ptr(), _stream(x.device)),
+           "fp8_block_quantize")
+    return Fp8BlockQuantized(codes, scales, block_rows)
+
+
+def fp8_block_dequantize(codes: torch.Tensor, scales: torch.Tensor,
+                         block_rows: int = 1) -> torch.Tensor:
+    """bf16 [rows, cols] = E4M3(code) * S (C: fp8_block_dequantize)."""
+    if codes.dtype != torch.uint8 or codes.dim() != 2 or not codes.is_contiguous():
+        raise ValueError("codes must be a contiguous uint8 [rows, cols] tensor")
+    if scales.dtype != torch.float32 or not scales.is_contiguous():
+        raise ValueError("scales must be a contiguous float32 tensor")
+    rows, cols = codes.shape
+    y = torch.empty((rows, cols), dtype=torch.bfloat16, device=codes.device)
+    _check(lib().fp8_block_dequantize(codes.data_ptr(), scales.data_ptr(),
+                                      rows, cols, block_rows, y.data_ptr(),
+                                      _stream(codes.device)),
+           "fp8_block_dequantize")
+    return y
+
+
+def fp8_block_requantize_transpose(codes: torch.Tensor, scales: torch.Tensor
+                                   ) -> Fp8BlockQuantized:
+    """1x128 tiles of X^T from the 1x128 tiles of X [rows, cols], through
+    X's bf16 dequantization (C: fp8_block_requantize_transpose)."""
+    if codes.dtype != torch.uint8 or codes.dim() != 2 or not codes.is_contiguous():
+        raise ValueError("codes must be a contiguous uint8 [rows, cols] tensor")
+    if scales.dtype != torch.float32 or not scales.is_contiguous():
+        raise ValueError("scales must be a contiguous float32 tensor")
+    rows, cols = codes.shape
+    codes_t = torch.empty((cols, rows), dtype=torch.uint8, device=codes.device)
+    scales_t = torch.empty((cols, rows // 128), dtype=torch.float32,
+                           device=codes.device)
+    _check(lib().fp8_block_requantize_transpose(
+        codes.data_ptr(), scales.data_ptr(), rows, cols, codes_t.data_ptr(),
+        scales_t.data_ptr(), _stream(codes.device)),
+        "fp8_block_requantize_transpose")
+    return Fp8BlockQuantized(codes_t, scales_t, 1)

@@ -369,6 +369,61 @@ mxq_status dequantize_nvfp4(const uint8_t* codes, const uint8_t* block_scales,
       scale_layout == MXQ_SCALE_SWIZZLED, y, static_cast<cudaStream_t>(stream)));
 }
 
+mxq_status fp8_block_quantize(const void* x, int64_t rows, int64_t cols,
+                              int64_t ldx, int block_rows, uint8_t* codes,
+                              float* scales, void* stream) {
+  const int fm = fault_mode();
+  if (fm == 2) return MXQ_ERR_ARG;
+  if (block_rows != 1 && block_rows != 128) return MXQ_ERR_ARG;
+  if (rows < 0 || cols < 0 || ldx < cols) return MXQ_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return MXQ_OK;
+  if (!x || !codes || !scales) return MXQ_ERR_NULL;
+  if (cols % 128 != 0 || rows % block_rows != 0) return MXQ_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || ldx % 8 != 0)
+    return MXQ_ERR_ALIGN;
+  if (fm == 1) return MXQ_ERR_CUDA;
+  return from_cuda(launch_fp8blk_quantize(x, rows, cols, ldx, block_rows,
+                                          codes, scales,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+mxq_status fp8_block_dequantize(const uint8_t* codes, const float* scales,
+                                int64_t rows, int64_t cols, int block_rows,
+                                void* y, void* stream) {
+  const int fm = fault_mode();
+  if (fm == 2) return MXQ_ERR_ARG;
+  if (block_rows != 1 && block_rows != 128) return MXQ_ERR_ARG;
+  if (rows < 0 || cols < 0) return MXQ_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return MXQ_OK;
+  if (!codes || !scales || !y) return MXQ_ERR_NULL;
+  if (cols % 128 != 0 || rows % block_rows != 0) return MXQ_ERR_SHAPE;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(y))
+    return MXQ_ERR_ALIGN;
+  if (fm == 1) return MXQ_ERR_CUDA;
+  return from_cuda(launch_fp8blk_dequantize(codes, scales, rows, cols,
+                                            block_rows, y,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+mxq_status fp8_block_requantize_transpose(const uint8_t* codes,
+                                          const float* scales, int64_t rows,
+                                          int64_t cols, uint8_t* codes_t,
+                                          float* scales_t, void* stream) {
+  const int fm = fault_mode();
+  if (fm == 2) return MXQ_ERR_ARG;
+  if (rows < 0 || cols < 0) return MXQ_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return MXQ_OK;
+  if (!codes || !scales || !codes_t || !scales_t) return MXQ_ERR_NULL;
+  if (rows % 128 != 0 || cols % 128 != 0) return MXQ_ERR_SHAPE;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(codes_t) ||
+      !aligned16(scales_t))
+    return MXQ_ERR_ALIGN;
+  if (fm == 1) return MXQ_ERR_CUDA;
+  return from_cuda(launch_fp8blk_requant_t(codes, scales, rows, cols, codes_t,
+                                           scales_t,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 mxq_status mxq_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
                           const uint8_t* bt_codes, const uint8_t* bt_scales,
                           int64_t M, int64_t N, int64_t K, float* C,

@@ -1,0 +1,309 @@
+// fp8block.cu -- FP8 E4M3 with one FP32 scale per block: 1x128 activation
+// tiles, 128x128 weight blocks, their dequantization to bf16, and the
+// backward-orientation conversion of 1x128-tile activations.
+//
+// "Miles: end-to-end MXFP8 and per-token NVFP4 RL", introduction: the
+// DeepSeek-V3-style block-scaled FP8 recipe scales weights in 128x128
+// blocks and activations in 1x128 tiles, one FP32 scale per tile or block
+// computed online.  MXFP8 recipe section: that recipe stores forward
+// activations in 1x128 tiles and, before the backward GEMM, converts them
+// to the backward orientation by dequantizing and requantizing.
+//
+// Arithmetic (IEEE binary32, round-to-nearest-even, no FTZ, no FMA):
+//   S    = amax / 448          (a decode scale: value = code * S)
+//   enc  = 1 / S               (0 when S = 0, clamped to FLT_MAX)
+//   code = E4M3_RNE(x * enc)   (saturating at +-448, sign kept)
+//   y    = bf16_RNE(E4M3(code) * S)
+// The conversion dequantizes a 128 x 128 tile of X [M x K] to bf16 exactly
+// as the dequantizer does, transposes it in shared memory and quantizes
+// each column (128 consecutive rows of X) as one 1x128 tile of X^T.
+//
+// Design (sm_103a): HBM-streaming.  Tiles: 8 lanes per 1x128 tile, 32
+// bytes of bf16 per lane in one load, amax by three shuffles, 16 codes per
+// lane in one 16-byte store.  Blocks: one CTA per 128x128 block in a
+// grid-stride loop, 64 values per thread held in registers across the
+// block reduction.  Dequantizer: one 16-code unit per thread per step, one
+// 32-byte store.
+#include <float.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace mxq {
+
+namespace {
+
+constexpr int FB_THREADS = 256;
+constexpr unsigned FULL = 0xffffffffu;
+
+// S and enc of a block whose amax (bf16 bit pattern) is a.
+__device__ __forceinline__ void fb_scales(uint32_t a, float& S, float& enc) {
+  S = __fdiv_rn(__uint_as_float(a << 16), 448.0f);
+  enc = 0.0f;
+  if (S != 0.0f) enc = fminf(__frcp_rn(S), FLT_MAX);
+}
+
+// max |x| (bf16 bits) of 16 packed bf16 values.
+__device__ __forceinline__ uint32_t absmax16(const uint4& a, const uint4& b) {
+  const uint32_t m =
+      bf16x2_maxabs(bf16x2_maxabs(bf16x2_maxabs(a.x, a.y),
+                                  bf16x2_maxabs(a.z, a.w)),
+                    bf16x2_maxabs(bf16x2_maxabs(b.x, b.y),
+                                  bf16x2_maxabs(b.z, b.w)));
+  return bf16x2_hmax(m & 0x7FFF7FFFu);
+}
+
+// 16 bf16 values -> 16 E4M3 codes (element 0 in the lowest byte).
+__device__ __forceinline__ uint4 encode16(const uint4& a, const uint4& b,
+                                          float enc) {
+  return make_uint4(
+      bf16x2_scale_e4m3x2(a.x, enc, enc) |
+          (bf16x2_scale_e4m3x2(a.y, enc, enc) << 16),
+      bf16x2_scale_e4m3x2(a.z, enc, enc) |
+          (bf16x2_scale_e4m3x2(a.w, enc, enc) << 16),
+      bf16x2_scale_e4m3x2(b.x, enc, enc) |
+          (bf16x2_scale_e4m3x2(b.y, enc, enc) << 16),
+      bf16x2_scale_e4m3x2(b.z, enc, enc) |
+          (bf16x2_scale_e4m3x2(b.w, enc, enc) << 16));
+}
+
+__device__ __forceinline__ void load16(const uint16_t* p, bool wide, uint4& a,
+                                       uint4& b) {
+  if (wide) {
+    ld_stream_v8(p, a, b);
+  } else {
+    a = ld_stream_v4(p);
+    b = ld_stream_v4(p + 8);
+  }
+}
+
+// 1x128 tiles along the rows of x [rows x cols]: lanes 8s .. 8s+7 of a warp
+// take tile 4w + s, 16 values each.
+__global__ void __launch_bounds__(FB_THREADS)
+    fp8blk_tile_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                       int64_t cols, int64_t ldx, uint8_t* __restrict__ codes,
+                       float* __restrict__ scales, int wide) {
+  const int64_t per_row = cols >> 7;
+  const int64_t ntiles = rows * per_row;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane >> 3, part = lane & 7;
+  const int64_t warp_id =
+      ((int64_t)blockIdx.x * FB_THREADS + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * FB_THREADS) >> 5;
+  pdl_wait();
+  for (int64_t t0 = warp_id * 4; t0 < ntiles; t0 += nwarps * 4) {
+    const int64_t t = t0 + sub;
+    const bool valid = t < ntiles;
+    const int64_t r = valid ? t / per_row : 0;
+    const int64_t c = valid ? (t - r * per_row) * 128 + part * 16 : 0;
+    uint4 a = make_uint4(0, 0, 0, 0), b = a;
+    if (valid) load16(x + r * ldx + c, wide, a, b);
+    uint32_t m = absmax16(a, b);
+    m = max(m, __shfl_xor_sync(FULL, m, 1));
+    m = max(m, __shfl_xor_sync(FULL, m, 2));
+    m = max(m, __shfl_xor_sync(FULL, m, 4));
+    float S, enc;
+    fb_scales(m, S, enc);
+    if (valid) {
+      st_v4(codes + r * cols + c, encode16(a, b, enc));
+      if (part == 0) scales[t] = S;
+    }
+  }
+  pdl_launch_dependents();
+}
+
+// 128x128 blocks: thread t holds row t % 128 of the block, columns
+// (t / 128) * 64 .. + 63.
+__global__ void __launch_bounds__(FB_THREADS)
+    fp8blk_block_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                        int64_t cols, int64_t ldx, uint8_t* __restrict__ codes,
+                        float* __restrict__ scales, int wide) {
+  __shared__ uint32_t red[FB_THREADS / 32];
+  const int64_t nbc = cols >> 7;
+  const int64_t nblk = (rows >> 7) * nbc;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rr = threadIdx.x & 127, cc = (threadIdx.x >> 7) * 64;
+  pdl_wait();
+  for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+    const int64_t bi = blk / nbc, bj = blk - bi * nbc;
+    const uint16_t* p = x + (bi * 128 + rr) * ldx + bj * 128 + cc;
+    uint4 v[8];
+    uint32_t m = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      load16(p + k * 16, wide, v[2 * k], v[2 * k + 1]);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m = max(m, absmax16(v[2 * k], v[2 * k + 1]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(FULL, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    uint32_t a = red[0];
+#pragma unroll
+    for (int w = 1; w < FB_THREADS / 32; ++w) a = max(a, red[w]);
+    __syncthreads();                    // red is rewritten by the next block
+    float S, enc;
+    fb_scales(a, S, enc);
+    uint8_t* q = codes + (bi * 128 + rr) * cols + bj * 128 + cc;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      st_v4(q + k * 16, encode16(v[2 * k], v[2 * k + 1], enc));
+    if (threadIdx.x == 0) scales[blk] = S;
+  }
+  pdl_launch_dependents();
+}
+
+// 16 E4M3 codes times S -> 16 bf16 (two 16-byte halves).
+__device__ __forceinline__ void decode16(const uint4& c, float S, uint4& lo,
+                                         uint4& hi) {
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+  uint32_t w[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    float a, b;
+    e4m3x2_to_f32((cw[h >> 1] >> ((h & 1) * 16)) & 0xFFFFu, a, b);
+    fmul2(a, b, S, S, a, b);
+    w[h] = f32x2_to_bf16x2(a, b);
+  }
+  lo = make_uint4(w[0], w[1], w[2], w[3]);
+  hi = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Dequantize codes [rows x cols] with scales per block of brows x 128
+// (brows_log2 = 0 or 7).
+__global__ void __launch_bounds__(FB_THREADS)
+    fp8blk_dequant_kernel(const uint8_t* __restrict__ codes,
+                          const float* __restrict__ scales, int64_t rows,
+                          int64_t cols, int brows_log2, int wide,
+                          uint16_t* __restrict__ y) {
+  const int64_t c16 = cols >> 4, nbc = cols >> 7;
+  const int64_t n16 = rows * c16;
+  pdl_wait();
+  for (int64_t i = (int64_t)blockIdx.x * FB_THREADS + threadIdx.x; i < n16;
+       i += (int64_t)gridDim.x * FB_THREADS) {
+    const uint4 c = ld_stream_v4(codes + i * 16);
+    const int64_t r = i / c16;
+    const int64_t col = (i - r * c16) * 16;
+    const float S = scales[(r >> brows_log2) * nbc + (col >> 7)];
+    uint4 lo, hi;
+    decode16(c, S, lo, hi);
+    st_32B(y + i * 16, lo, hi, wide);
+  }
+  pdl_launch_dependents();
+}
+
+// Backward-orientation conversion: tile (ti, tj) of X [M x K] is dequantized
+// into shared memory transposed (column-major bf16, row pitch 136), then
+// each of its 128 columns is quantized as one 1x128 tile of X^T.
+constexpr int kPitch = 136;
+
+__global__ void __launch_bounds__(FB_THREADS)
+    fp8blk_requant_t_kernel(const uint8_t* __restrict__ codes,
+                            const float* __restrict__ scales, int64_t M,
+                            int64_t K, uint8_t* __restrict__ codes_t,
+                            float* __restrict__ scales_t) {
+  __shared__ __align__(16) uint16_t sm[128 * kPitch];
+  const int64_t nti = M >> 7, ntj = K >> 7;
+  const int64_t ntiles = nti * ntj;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rr = threadIdx.x & 127, cc = (threadIdx.x >> 7) * 64;
+  pdl_wait();
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t ti = tile / ntj, tj = tile - ti * ntj;
+    const int64_t r0 = ti * 128, c0 = tj * 128;
+    // dequantize row r0 + rr, columns c0 + cc .. + 63, into sm[col][row]
+    const float S = scales[(r0 + rr) * ntj + tj];
+    const uint8_t* src = codes + (r0 + rr) * K + c0 + cc;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint4 lo, hi;
+      decode16(ld_stream_v4(src + k * 16), S, lo, hi);
+      const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int col = cc + k * 16 + 2 * e;
+        sm[col * kPitch + rr] = (uint16_t)(w[e] & 0xFFFFu);
+        sm[(col + 1) * kPitch + rr] = (uint16_t)(w[e] >> 16);
+      }
+    }
+    __syncthreads();
+    // quantize: warp w takes columns 16w .. 16w + 15; a lane holds rows
+    // 4 lane .. 4 lane + 3 of the column
+    for (int q = 0; q < 16; ++q) {
+      const int col = warp * 16 + q;
+      const uint2 v = *reinterpret_cast<const uint2*>(&sm[col * kPitch + 4 * lane]);
+      uint32_t m = bf16x2_hmax(bf16x2_maxabs(v.x, v.y) & 0x7FFF7FFFu);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(FULL, m, o));
+      float S2, enc;
+      fb_scales(m, S2, enc);
+      const uint32_t word = bf16x2_scale_e4m3x2(v.x, enc, enc) |
+                            (bf16x2_scale_e4m3x2(v.y, enc, enc) << 16);
+      *reinterpret_cast<uint32_t*>(codes_t + (c0 + col) * M + r0 + 4 * lane) =
+          word;
+      if (lane == 0) scales_t[(c0 + col) * nti + ti] = S2;
+    }
+    __syncthreads();                    // sm is rewritten by the next tile
+  }
+  pdl_launch_dependents();
+}
+
+unsigned fb_grid(int64_t work, int64_t per_cta, int dev, int ctas_per_sm) {
+  int64_t g = (work + per_cta - 1) / per_cta;
+  const int64_t cap = (int64_t)sm_count(dev) * ctas_per_sm;
+  return (unsigned)(g < 1 ? 1 : (g > cap ? cap : g));
+}
+
+}  // namespace
+
+cudaError_t launch_fp8blk_quantize(const void* x, int64_t rows, int64_t cols,
+                                   int64_t ldx, int block_rows,
+                                   uint8_t* codes, float* scales,
+                                   cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const uint16_t* xs = static_cast<const uint16_t*>(x);
+  // every 16-value segment starts a multiple of 32 bytes from x
+  const int wide = (reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ldx % 16 == 0;
+  if (block_rows == 1) {
+    const int64_t ntiles = rows * (cols >> 7);
+    const unsigned grid = fb_grid(ntiles, (FB_THREADS / 32) * 4, dev, 8);
+    return launch_pdl(fp8blk_tile_kernel, dim3(grid), dim3(FB_THREADS), 0,
+                      stream, false, xs, rows, cols, ldx, codes, scales, wide);
+  }
+  const int64_t nblk = (rows >> 7) * (cols >> 7);
+  const unsigned grid = fb_grid(nblk, 1, dev, 4);
+  return launch_pdl(fp8blk_block_kernel, dim3(grid), dim3(FB_THREADS), 0,
+                    stream, false, xs, rows, cols, ldx, codes, scales, wide);
+}
+
+cudaError_t launch_fp8blk_dequantize(const uint8_t* codes, const float* scales,
+                                     int64_t rows, int64_t cols,
+                                     int block_rows, void* y,
+                                     cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const int64_t n16 = rows * (cols >> 4);
+  const unsigned grid = fb_grid(n16, FB_THREADS, dev, 4);
+  const int wide = (reinterpret_cast<uintptr_t>(y) & 31u) == 0;
+  return launch_pdl(fp8blk_dequant_kernel, dim3(grid), dim3(FB_THREADS), 0,
+                    stream, false, codes, scales, rows, cols,
+                    block_rows == 1 ? 0 : 7, wide, static_cast<uint16_t*>(y));
+}
+
+cudaError_t launch_fp8blk_requant_t(const uint8_t* codes, const float* scales,
+                                    int64_t M, int64_t K, uint8_t* codes_t,
+                                    float* scales_t, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const int64_t ntiles = (M >> 7) * (K >> 7);
+  const unsigned grid = fb_grid(ntiles, 1, dev, 4);
+  return launch_pdl(fp8blk_requant_t_kernel, dim3(grid), dim3(FB_THREADS), 0,
+                    stream, false, codes, scales, M, K, codes_t, scales_t);
+}
+
+}  // namespace mxq

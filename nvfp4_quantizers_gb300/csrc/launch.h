@@ -51,11 +51,11 @@ cudaError_t launch_nvfp4_per_token(const void* x, int64_t T, int64_t H,
 
 constexpr int kMaxParts = 4;
 
-// Workspace of the shared-scale weight quantizer: a 256-byte header (grid
-// barrier counter) followed by one 32-bit amax word per group.
+// Workspace of the shared-scale weight quantizer: a 256-byte header (task
+// counters) followed by an amax word and a progress word per group.
 size_t nvfp4_weight_ws_bytes(int64_t num_groups);
 // Reads (and clears when set) the error word of the weight kernel's
-// bounded grid barrier.
+// bounded waits.
 cudaError_t nvfp4_take_wait_error(unsigned int* word);
 
 cudaError_t launch_nvfp4_weight_shared(
@@ -120,5 +120,19 @@ inline int64_t scale_bytes(int64_t rows, int64_t cols, int swizzled) {
   if (!swizzled) return rows * cols;
   return ((rows + 127) / 128) * 128 * ((cols + 3) / 4) * 4;
 }
+
+// fp8block.cu
+// block_rows 1 (1x128 tiles) or 128 (128x128 blocks).
+cudaError_t launch_fp8blk_quantize(const void* x, int64_t rows, int64_t cols,
+                                   int64_t ldx, int block_rows,
+                                   uint8_t* codes, float* scales,
+                                   cudaStream_t stream);
+cudaError_t launch_fp8blk_dequantize(const uint8_t* codes, const float* scales,
+                                     int64_t rows, int64_t cols,
+                                     int block_rows, void* y,
+                                     cudaStream_t stream);
+cudaError_t launch_fp8blk_requant_t(const uint8_t* codes, const float* scales,
+                                    int64_t M, int64_t K, uint8_t* codes_t,
+                                    float* scales_t, cudaStream_t stream);
 
 }  // namespace mxq

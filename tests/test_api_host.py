@@ -132,6 +132,31 @@ def test_moe_entry_point_argument_errors(L):
     assert f(FAKE, FAKE, FAKE, O, 0, FAKE, FAKE, FAKE, 128, 256, FAKE, 128, None) == q.MXQ_OK
 
 
+def test_fp8_block_argument_errors(L):
+    import nvfp4_quantizers_gb300 as q
+    f = L.fp8_block_quantize
+    assert f(FAKE, 64, 256, 256, 2, FAKE, FAKE, None) == q.MXQ_ERR_ARG
+    assert f(FAKE, 64, 200, 200, 1, FAKE, FAKE, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, 100, 256, 256, 128, FAKE, FAKE, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, 64, 256, 128, 1, FAKE, FAKE, None) == q.MXQ_ERR_SHAPE
+    assert f(None, 64, 256, 256, 1, FAKE, FAKE, None) == q.MXQ_ERR_NULL
+    assert f(FAKE + 2, 64, 256, 256, 1, FAKE, FAKE, None) == q.MXQ_ERR_ALIGN
+    assert f(FAKE, 64, 256, 260, 1, FAKE, FAKE, None) == q.MXQ_ERR_ALIGN
+    assert f(FAKE, 0, 256, 256, 1, None, None, None) == q.MXQ_OK
+    d = L.fp8_block_dequantize
+    assert d(FAKE, FAKE, 64, 256, 3, FAKE, None) == q.MXQ_ERR_ARG
+    assert d(FAKE, FAKE, 64, 192, 1, FAKE, None) == q.MXQ_ERR_SHAPE
+    assert d(FAKE, FAKE, 64, 256, 128, FAKE, None) == q.MXQ_ERR_SHAPE
+    assert d(FAKE, None, 64, 256, 1, FAKE, None) == q.MXQ_ERR_NULL
+    assert d(FAKE, FAKE, 64, 256, 1, FAKE + 8, None) == q.MXQ_ERR_ALIGN
+    t = L.fp8_block_requantize_transpose
+    assert t(FAKE, FAKE, 64, 256, FAKE, FAKE, None) == q.MXQ_ERR_SHAPE
+    assert t(FAKE, FAKE, 128, 200, FAKE, FAKE, None) == q.MXQ_ERR_SHAPE
+    assert t(FAKE, FAKE, 128, 256, None, FAKE, None) == q.MXQ_ERR_NULL
+    assert t(FAKE, FAKE, 128, 256, FAKE, FAKE + 4, None) == q.MXQ_ERR_ALIGN
+    assert t(FAKE, FAKE, 0, 256, None, None, None) == q.MXQ_OK
+
+
 def test_fault_injection_returns_errors_without_launching(L):
     import nvfp4_quantizers_gb300 as q
     try:
