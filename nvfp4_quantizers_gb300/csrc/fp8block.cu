@@ -19,11 +19,13 @@
 // each column (128 consecutive rows of X) as one 1x128 tile of X^T.
 //
 // Design (sm_103a): HBM-streaming.  Tiles: 8 lanes per 1x128 tile, 32
-// bytes of bf16 per lane in one load, amax by three shuffles, 16 codes per
-// lane in one 16-byte store.  Blocks: one CTA per 128x128 block in a
-// grid-stride loop, 64 values per thread held in registers across the
-// block reduction.  Dequantizer: one 16-code unit per thread per step, one
-// 32-byte store.
+// bytes of bf16 per lane in one load (two tiles per lane in flight), amax
+// by three shuffles, 16 codes per lane in one 16-byte store.  Blocks: one
+// CTA per 128x128 block in a grid-stride loop, 64 values per thread held
+// in registers across the block reduction.  Dequantizer: one 16-code unit
+// per thread per step, one 32-byte store.  Conversion: all of a thread's
+// code loads issued before it decodes, and four columns quantized per
+// step so their reductions overlap.
 #include <float.h>
 
 #include "common.cuh"
@@ -91,22 +93,34 @@ __global__ void __launch_bounds__(FB_THREADS)
       ((int64_t)blockIdx.x * FB_THREADS + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * FB_THREADS) >> 5;
   pdl_wait();
-  for (int64_t t0 = warp_id * 4; t0 < ntiles; t0 += nwarps * 4) {
-    const int64_t t = t0 + sub;
-    const bool valid = t < ntiles;
-    const int64_t r = valid ? t / per_row : 0;
-    const int64_t c = valid ? (t - r * per_row) * 128 + part * 16 : 0;
-    uint4 a = make_uint4(0, 0, 0, 0), b = a;
-    if (valid) load16(x + r * ldx + c, wide, a, b);
-    uint32_t m = absmax16(a, b);
-    m = max(m, __shfl_xor_sync(FULL, m, 1));
-    m = max(m, __shfl_xor_sync(FULL, m, 2));
-    m = max(m, __shfl_xor_sync(FULL, m, 4));
-    float S, enc;
-    fb_scales(m, S, enc);
-    if (valid) {
-      st_v4(codes + r * cols + c, encode16(a, b, enc));
-      if (part == 0) scales[t] = S;
+  // two tiles per lane per step (tiles t0 + sub and t0 + 4 nwarps + sub),
+  // both loads issued before either is used
+  for (int64_t t0 = warp_id * 4; t0 < ntiles; t0 += nwarps * 8) {
+    int64_t t[2], r[2], c[2];
+    bool valid[2];
+    uint4 a[2], b[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      t[h] = t0 + h * nwarps * 4 + sub;
+      valid[h] = t[h] < ntiles;
+      r[h] = valid[h] ? t[h] / per_row : 0;
+      c[h] = valid[h] ? (t[h] - r[h] * per_row) * 128 + part * 16 : 0;
+      a[h] = make_uint4(0, 0, 0, 0);
+      b[h] = a[h];
+      if (valid[h]) load16(x + r[h] * ldx + c[h], wide, a[h], b[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t m = absmax16(a[h], b[h]);
+      m = max(m, __shfl_xor_sync(FULL, m, 1));
+      m = max(m, __shfl_xor_sync(FULL, m, 2));
+      m = max(m, __shfl_xor_sync(FULL, m, 4));
+      float S, enc;
+      fb_scales(m, S, enc);
+      if (valid[h]) {
+        st_v4(codes + r[h] * cols + c[h], encode16(a[h], b[h], enc));
+        if (part == 0) scales[t[h]] = S;
+      }
     }
   }
   pdl_launch_dependents();
@@ -195,7 +209,11 @@ __global__ void __launch_bounds__(FB_THREADS)
 
 // Backward-orientation conversion: tile (ti, tj) of X [M x K] is dequantized
 // into shared memory transposed (column-major bf16, row pitch 136), then
-// each of its 128 columns is quantized as one 1x128 tile of X^T.
+// each of its 128 columns is quantized as one 1x128 tile of X^T: a warp
+// takes 16 columns, four at a time, a lane 4 rows of each, so every code
+// store is 128 contiguous bytes per warp.  (A thread per column, with no
+// cross-lane reduction, measured slower: its 16-byte stores land in 32
+// different rows of X^T.)
 constexpr int kPitch = 136;
 
 __global__ void __launch_bounds__(FB_THREADS)
@@ -215,10 +233,13 @@ __global__ void __launch_bounds__(FB_THREADS)
     // dequantize row r0 + rr, columns c0 + cc .. + 63, into sm[col][row]
     const float S = scales[(r0 + rr) * ntj + tj];
     const uint8_t* src = codes + (r0 + rr) * K + c0 + cc;
+    uint4 cv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) cv[k] = ld_stream_v4(src + k * 16);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       uint4 lo, hi;
-      decode16(ld_stream_v4(src + k * 16), S, lo, hi);
+      decode16(cv[k], S, lo, hi);
       const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -228,21 +249,30 @@ __global__ void __launch_bounds__(FB_THREADS)
       }
     }
     __syncthreads();
-    // quantize: warp w takes columns 16w .. 16w + 15; a lane holds rows
-    // 4 lane .. 4 lane + 3 of the column
-    for (int q = 0; q < 16; ++q) {
-      const int col = warp * 16 + q;
-      const uint2 v = *reinterpret_cast<const uint2*>(&sm[col * kPitch + 4 * lane]);
-      uint32_t m = bf16x2_hmax(bf16x2_maxabs(v.x, v.y) & 0x7FFF7FFFu);
+    for (int q0 = 0; q0 < 16; q0 += 4) {       // 4 independent columns
+      uint2 v[4];
+      uint32_t m[4];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(FULL, m, o));
-      float S2, enc;
-      fb_scales(m, S2, enc);
-      const uint32_t word = bf16x2_scale_e4m3x2(v.x, enc, enc) |
-                            (bf16x2_scale_e4m3x2(v.y, enc, enc) << 16);
-      *reinterpret_cast<uint32_t*>(codes_t + (c0 + col) * M + r0 + 4 * lane) =
-          word;
-      if (lane == 0) scales_t[(c0 + col) * nti + ti] = S2;
+      for (int j = 0; j < 4; ++j) {
+        const int col = warp * 16 + q0 + j;
+        v[j] = *reinterpret_cast<const uint2*>(&sm[col * kPitch + 4 * lane]);
+        m[j] = bf16x2_hmax(bf16x2_maxabs(v[j].x, v[j].y) & 0x7FFF7FFFu);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m[j] = max(m[j], __shfl_xor_sync(FULL, m[j], o));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int col = warp * 16 + q0 + j;
+        float S2, enc;
+        fb_scales(m[j], S2, enc);
+        const uint32_t word = bf16x2_scale_e4m3x2(v[j].x, enc, enc) |
+                              (bf16x2_scale_e4m3x2(v[j].y, enc, enc) << 16);
+        *reinterpret_cast<uint32_t*>(codes_t + (c0 + col) * M + r0 + 4 * lane) =
+            word;
+        if (lane == 0) scales_t[(c0 + col) * nti + ti] = S2;
+      }
     }
     __syncthreads();                    // sm is rewritten by the next tile
   }
@@ -269,7 +299,7 @@ cudaError_t launch_fp8blk_quantize(const void* x, int64_t rows, int64_t cols,
   const int wide = (reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ldx % 16 == 0;
   if (block_rows == 1) {
     const int64_t ntiles = rows * (cols >> 7);
-    const unsigned grid = fb_grid(ntiles, (FB_THREADS / 32) * 4, dev, 8);
+    const unsigned grid = fb_grid(ntiles, (FB_THREADS / 32) * 8, dev, 8);
     return launch_pdl(fp8blk_tile_kernel, dim3(grid), dim3(FB_THREADS), 0,
                       stream, false, xs, rows, cols, ldx, codes, scales, wide);
   }
@@ -301,7 +331,7 @@ cudaError_t launch_fp8blk_requant_t(const uint8_t* codes, const float* scales,
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   const int64_t ntiles = (M >> 7) * (K >> 7);
-  const unsigned grid = fb_grid(ntiles, 1, dev, 4);
+  const unsigned grid = fb_grid(ntiles, 1, dev, 6);
   return launch_pdl(fp8blk_requant_t_kernel, dim3(grid), dim3(FB_THREADS), 0,
                     stream, false, codes, scales, M, K, codes_t, scales_t);
 }
