@@ -103,6 +103,16 @@ def lib():
             L.oracle_fp8blk_dequantize.restype = ctypes.c_int
             L.oracle_fp8blk_dequantize.argtypes = [_p, _p, _i64, _i64, _i64,
                                                    _i64, _p]
+            L.oracle_philox4x64.restype = None
+            L.oracle_philox4x64.argtypes = [_p, _p, _p]
+            L.oracle_rht_signs.restype = ctypes.c_uint32
+            L.oracle_rht_signs.argtypes = [ctypes.c_uint64]
+            L.oracle_rht16.restype = None
+            L.oracle_rht16.argtypes = [_p, ctypes.c_uint32, _p]
+            L.oracle_nvfp4_rht_sr_rows.restype = ctypes.c_int
+            L.oracle_nvfp4_rht_sr_rows.argtypes = [_p, _i64, _i64, _i64,
+                                                   ctypes.c_uint64, ctypes.c_int,
+                                                   _p, _p, _p]
             _lib = L
     return _lib
 
@@ -470,3 +480,51 @@ def fp8_block_requantize_transpose(codes: np.ndarray, scales: np.ndarray):
     [K, M/128])."""
     y = fp8_block_dequantize(codes, scales, 1, 128)
     return fp8_block_quantize(np.ascontiguousarray(y.T), 1, 128)
+
+
+# --------------------------------------------------------------------------
+# NVFP4 with the original pretraining recipe's stabilizers (NVFP4 recipe
+# section of "Miles: end-to-end MXFP8 and per-token NVFP4 RL": stochastic
+# rounding for unbiased quantized gradients, Random Hadamard Transforms to
+# disperse block outliers).  Readings and arithmetic in mxq_oracle.c.
+# --------------------------------------------------------------------------
+RHT = 1
+SR = 2
+
+
+def philox4x64(counter, key) -> np.ndarray:
+    """Philox4x64-10 (Salmon et al., SC 2011) of a 4-word counter and a
+    2-word key."""
+    c = np.ascontiguousarray(counter, np.uint64)
+    k = np.ascontiguousarray(key, np.uint64)
+    out = np.empty(4, np.uint64)
+    lib().oracle_philox4x64(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def rht_signs(seed: int) -> int:
+    """The 16 RHT sign bits of a seed (bit i set: s_i = -1)."""
+    return int(lib().oracle_rht_signs(ctypes.c_uint64(seed)))
+
+
+def rht16(x: np.ndarray, signs: int) -> np.ndarray:
+    """(1/4) H16 (s * x) for one block of 16 binary32 values."""
+    x = np.ascontiguousarray(x, np.float32)
+    y = np.empty(16, np.float32)
+    lib().oracle_rht16(_ptr(x), signs, _ptr(y))
+    return y
+
+
+def nvfp4_quantize_rht_sr(x: np.ndarray, seed: int, flags: int):
+    """Per-token NVFP4 of x [R, C] (bf16 bits) with the optional RHT
+    (flags & RHT) and stochastic rounding (flags & SR).  Returns (codes
+    u8 [R, C/2], block scales u8 [R, C/16] logical, S f32 [R])."""
+    x = _bf16(x)
+    R, C = x.shape
+    codes = np.empty((R, C // 2), np.uint8)
+    scales = np.empty((R, C // 16), np.uint8)
+    S = np.empty(R, np.float32)
+    _check(lib().oracle_nvfp4_rht_sr_rows(_ptr(x), R, C, C, ctypes.c_uint64(seed),
+                                          flags, _ptr(codes), _ptr(scales),
+                                          _ptr(S)), "nvfp4 rht/sr")
+    return codes, scales, S

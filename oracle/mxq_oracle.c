@@ -56,6 +56,7 @@
 #include <float.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #if !defined(FLT_EVAL_METHOD) || FLT_EVAL_METHOD != 0
@@ -495,5 +496,167 @@ int oracle_fp8blk_dequantize(const uint8_t* codes, const float* scales,
             float v = (float)e4m3_decode(codes[r * C + c]) * s;
             y[r * C + c] = rne_bf16_from_f32(v);
         }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4 with the stabilizers of the original NVFP4 pretraining recipe     */
+/* ("Miles: end-to-end MXFP8 and per-token NVFP4 RL", NVFP4 recipe         */
+/* section: that recipe adds stochastic rounding, applied to gradients to  */
+/* make the quantized values unbiased, and Random Hadamard Transforms,     */
+/* which disperse block-level outliers of weight-gradient GEMM inputs).    */
+/* The pages give no formulas; the readings used here:                     */
+/*  - random bits: Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel    */
+/*    random numbers: as easy as 1, 2, 3", SC 2011), a counter-based        */
+/*    generator, so every element's bits depend only on (seed, position);  */
+/*  - RHT: each 16-value block x (along the row) becomes                   */
+/*    y = (1/4) H16 (s * x), H16 the Sylvester Hadamard matrix, s the 16   */
+/*    signs given by the low 16 bits of word 0 of Philox(counter 0, key    */
+/*    (seed, 1)) (bit i set -> s_i = -1); evaluated in binary32 as the     */
+/*    four butterfly stages h = 1, 2, 4, 8 ((a, b) -> (a + b, a - b) on    */
+/*    elements i, i + h with i & h == 0), then times 1/4 (exact);          */
+/*  - the per-token FP32 scale and the E4M3 block scales follow Algorithm  */
+/*    2 on the (transformed) binary32 values;                              */
+/*  - SR: element (r, c) takes u = (w >> 8) * 2^-24, w the 32-bit word     */
+/*    c % 8 of Philox(counter (r, c / 8, 0, 0), key (seed, 2)) (word j is  */
+/*    the low half of output j / 2 for even j, the high half for odd j);   */
+/*    |v| = |fl(y * enc)| saturated at 6 rounds up to the next E2M1        */
+/*    magnitude iff u < (|v| - lo) / (hi - lo), lo <= |v| < hi the         */
+/*    bracketing magnitudes (that ratio is exact in binary32: hi - lo is a */
+/*    power of two and |v| - lo is exact); values on the grid stay; sign   */
+/*    kept.                                                                */
+/* ------------------------------------------------------------------------ */
+static uint64_t mulhi64(uint64_t a, uint64_t b, uint64_t* lo) {
+    /* 64 x 64 -> 128 bits from four 32 x 32 products */
+    uint64_t a0 = a & 0xffffffffu, a1 = a >> 32;
+    uint64_t b0 = b & 0xffffffffu, b1 = b >> 32;
+    uint64_t p00 = a0 * b0, p01 = a0 * b1, p10 = a1 * b0, p11 = a1 * b1;
+    uint64_t mid = (p00 >> 32) + (p01 & 0xffffffffu) + (p10 & 0xffffffffu);
+    *lo = (mid << 32) | (p00 & 0xffffffffu);
+    return p11 + (p01 >> 32) + (p10 >> 32) + (mid >> 32);
+}
+
+void oracle_philox4x64(const uint64_t ctr_in[4], const uint64_t key_in[2],
+                       uint64_t out[4]) {
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t c[4] = {ctr_in[0], ctr_in[1], ctr_in[2], ctr_in[3]};
+    uint64_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        uint64_t lo0, lo1;
+        uint64_t hi0 = mulhi64(M0, c[0], &lo0);
+        uint64_t hi1 = mulhi64(M1, c[2], &lo1);
+        uint64_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+        c[0] = n0; c[1] = lo1; c[2] = n2; c[3] = lo0;
+        k0 += W0;
+        k1 += W1;
+    }
+    for (int i = 0; i < 4; ++i) out[i] = c[i];
+}
+
+static uint32_t philox_word(uint64_t seed, uint64_t stream, uint64_t c0,
+                            uint64_t c1, int j) {
+    const uint64_t ctr[4] = {c0, c1, 0, 0}, key[2] = {seed, stream};
+    uint64_t out[4];
+    oracle_philox4x64(ctr, key, out);
+    uint64_t w = out[j / 2];
+    return (uint32_t)((j & 1) ? (w >> 32) : (w & 0xffffffffu));
+}
+
+/* The 16 RHT signs of a seed, bit i set -> s_i = -1. */
+uint32_t oracle_rht_signs(uint64_t seed) {
+    return philox_word(seed, 1, 0, 0, 0) & 0xffffu;
+}
+
+/* y = (1/4) H16 (s * x) in binary32, butterfly order as stated above. */
+void oracle_rht16(const float* x, uint32_t signs, float* y) {
+    float v[16];
+    for (int i = 0; i < 16; ++i) v[i] = ((signs >> i) & 1) ? -x[i] : x[i];
+    for (int h = 1; h < 16; h <<= 1)
+        for (int i = 0; i < 16; ++i)
+            if ((i & h) == 0) {
+                float a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+    for (int i = 0; i < 16; ++i) y[i] = v[i] * 0.25f;
+}
+
+/* E2M1 code of v with stochastic rounding by u in [0, 1). */
+static uint8_t sr_e2m1(float v, float u) {
+    int neg = signbit(v) ? 1 : 0;
+    float a = fabsf(v);
+    if (a > 6.0f) a = 6.0f;
+    int lo = 0;                                  /* largest magnitude <= a */
+    for (int c = 0; c <= 7; ++c)
+        if (T_E2M1[c] <= (double)a) lo = c;
+    int code = lo;
+    if ((double)a != T_E2M1[lo]) {
+        float frac = (a - (float)T_E2M1[lo]) /
+                     ((float)T_E2M1[lo + 1] - (float)T_E2M1[lo]);
+        if (u < frac) code = lo + 1;
+    }
+    return (uint8_t)(code | (neg << 3));
+}
+
+/* Per-token NVFP4 of x [R x C] (C % 16 == 0) with the optional RHT (flags
+ * bit 0) and SR (bit 1).  codes [R x C/2] packed, low nibble = lower
+ * index; scales [R x C/16] logical; S [R]. */
+int oracle_nvfp4_rht_sr_rows(const uint16_t* x, int64_t R, int64_t C,
+                             int64_t ldx, uint64_t seed, int flags,
+                             uint8_t* codes, uint8_t* scales, float* S_out) {
+    if (R < 0 || C < 0 || C % 16 || ldx < C) return 1;
+    build_tables();
+    const uint32_t signs = oracle_rht_signs(seed);
+    const int64_t nb = C / 16;
+    float* y = (float*)malloc(sizeof(float) * (size_t)(C > 0 ? C : 1));
+    if (!y) return 2;
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            float xb[16];
+            for (int i = 0; i < 16; ++i)
+                xb[i] = (float)bf16_decode(x[r * ldx + b * 16 + i]);
+            if (flags & 1) oracle_rht16(xb, signs, &y[b * 16]);
+            else memcpy(&y[b * 16], xb, sizeof(xb));
+        }
+        float at = 0.0f;
+        for (int64_t c = 0; c < C; ++c)
+            if (fabsf(y[c]) > at) at = fabsf(y[c]);
+        const float S = at / 2688.0f;
+        S_out[r] = S;
+        for (int64_t b = 0; b < nb; ++b) {
+            float ab = 0.0f;
+            for (int i = 0; i < 16; ++i)
+                if (fabsf(y[b * 16 + i]) > ab) ab = fabsf(y[b * 16 + i]);
+            uint8_t sb = 0x00;
+            if (S != 0.0f) sb = rne_e4m3((double)(ab / (6.0f * S)));
+            scales[r * nb + b] = sb;
+            float d = (float)T_E4M3[sb] * S;
+            float enc;
+            if (d == 0.0f) {
+                enc = 0.0f;
+            } else {
+                enc = 1.0f / d;
+                if (enc > FLT_MAX) enc = FLT_MAX;
+            }
+            uint8_t q[16];
+            for (int i = 0; i < 16; ++i) {
+                float v = y[b * 16 + i] * enc;
+                if (flags & 2) {
+                    const int64_t c = b * 16 + i;
+                    const uint32_t w = philox_word(seed, 2, (uint64_t)r,
+                                                   (uint64_t)(c / 8), (int)(c % 8));
+                    const float u = (float)(w >> 8) * 0x1p-24f;
+                    q[i] = sr_e2m1(v, u);
+                } else {
+                    q[i] = rne_e2m1((double)v);
+                }
+            }
+            for (int i = 0; i < 8; ++i)
+                codes[r * (C / 2) + b * 8 + i] =
+                    (uint8_t)(q[2 * i] | (q[2 * i + 1] << 4));
+        }
+    }
+    free(y);
     return 0;
 }

@@ -780,3 +780,100 @@ def test_fp8blk_subnormal_scale(orc):
     exp = torch.from_numpy(np.clip(prod, -448, 448).astype(np.float32)).to(
         torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(codes, exp)
+
+
+# --------------------------------------------------------------------------
+# NVFP4 with the pretraining recipe's stabilizers (NVFP4 recipe section:
+# stochastic rounding for unbiased quantized gradients, Random Hadamard
+# Transforms to disperse block outliers).
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("key,counter", [((0, 0), (0, 0, 0, 0)),
+                                         ((0x0123456789abcdef, 0xfedcba9876543210), (5, 0, 0, 0)),
+                                         ((2**64 - 1, 2**64 - 1), (2**64 - 2, 7, 9, 2**64 - 1))])
+def test_philox4x64_matches_numpy(orc, key, counter):
+    """The oracle's Philox4x64-10 against numpy's own implementation of the
+    same published generator (numpy steps the counter once before each
+    block of four outputs)."""
+    bg = np.random.Philox(counter=np.array(counter, np.uint64),
+                          key=np.array(key, np.uint64))
+    raw = bg.random_raw(8)
+    c = list(counter)
+    for blk in range(2):
+        # counter + 1 with carry across the four 64-bit words
+        i = 0
+        while True:
+            c[i] = (c[i] + 1) % 2 ** 64
+            if c[i] != 0 or i == 3:
+                break
+            i += 1
+        assert np.array_equal(orc.philox4x64(c, key), raw[4 * blk:4 * blk + 4])
+
+
+def _sylvester16():
+    H = np.array([[1.0]])
+    for _ in range(4):
+        H = np.kron(np.array([[1.0, 1.0], [1.0, -1.0]]), H)
+    return H
+
+
+def test_rht16_is_the_sylvester_transform(orc):
+    """On small integers every butterfly sum is exact, so the binary32
+    transform equals (1/4) H16 (s * x) in float64, H16 built by Kronecker
+    products; (1/4) H16 is orthonormal, so applying it twice with all signs
+    + returns x."""
+    rng = np.random.default_rng(51)
+    H = _sylvester16()
+    assert np.allclose(H @ H.T / 16, np.eye(16))
+    for seed in (0, 1, 12345):
+        s = np.array([-1.0 if (orc.rht_signs(seed) >> i) & 1 else 1.0
+                      for i in range(16)])
+        for _ in range(20):
+            x = rng.integers(-8, 9, 16).astype(np.float32)
+            y = orc.rht16(x, orc.rht_signs(seed))
+            assert np.array_equal(y.astype(np.float64), H @ (s * x) / 4)
+    x = rng.integers(-8, 9, 16).astype(np.float32)
+    assert np.array_equal(orc.rht16(orc.rht16(x, 0), 0), x)
+
+
+def test_rht_sr_reduce_to_per_token(orc):
+    """Without RHT and SR the path is the per-token quantizer; with RHT on
+    inputs whose transforms are bf16 values, it is the per-token quantizer
+    of the transformed rows."""
+    x = W.ragged_tokens([5, 3], H=256)
+    assert all(np.array_equal(a, b) for a, b in zip(
+        orc.nvfp4_quantize_rht_sr(x, 9, 0), orc.nvfp4_quantize_per_token(x)))
+    rng = np.random.default_rng(52)
+    xi = rng.integers(-8, 9, (6, 64)).astype(np.float32)
+    xb = W.to_bf16_bits(xi)
+    signs = orc.rht_signs(3)
+    y = np.stack([np.concatenate([orc.rht16(row[b * 16:(b + 1) * 16], signs)
+                                  for b in range(4)]) for row in xi])
+    yb = W.to_bf16_bits(y)
+    assert np.array_equal(W.bits_to_f32(yb), y)          # exact in bf16
+    got = orc.nvfp4_quantize_rht_sr(xb, 3, orc.RHT)
+    exp = orc.nvfp4_quantize_per_token(yb)
+    assert all(np.array_equal(a, b) for a, b in zip(got, exp))
+
+
+def test_sr_is_unbiased_and_keeps_grid_values(orc):
+    """A block whose maximum is 2688 has S = 1, block scale 448 and
+    enc = 1/448, so x = 1008 scales to exactly 2.25: stochastic rounding
+    gives 2 or 3 with mean 2.25 (4096 independent positions), while
+    x = 1344 (exactly 3.0) always gives 3."""
+    R = 4096
+    row = np.zeros(16, np.float32)
+    row[0] = 2688.0
+    row[1] = 1008.0
+    row[2] = 1344.0
+    x = W.to_bf16_bits(np.tile(row, (R, 1)))
+    codes, sc, S = orc.nvfp4_quantize_rht_sr(x, 77, orc.SR)
+    assert np.all(S == 1.0) and np.all(sc[:, 0] == 0x7E)
+    e2 = np.array([orc.decode_e2m1(c) for c in range(16)])
+    v1 = e2[codes[:, 0] >> 4]
+    v2 = e2[codes[:, 1] & 0xF]
+    assert set(np.unique(v1)) == {2.0, 3.0}
+    assert abs(v1.mean() - 2.25) < 0.03
+    assert np.all(v2 == 3.0)
+    again = orc.nvfp4_quantize_rht_sr(x, 77, orc.SR)[0]
+    other = orc.nvfp4_quantize_rht_sr(x, 78, orc.SR)[0]
+    assert np.array_equal(codes, again) and not np.array_equal(codes, other)
