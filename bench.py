@@ -601,7 +601,8 @@ def run_shapes(q, W, dev, stream, reps=20):
     rowwise + columnwise of the four 8192 x 4096 input classes and of the
     linear layer's input [2048 x 2048] and weight [8192 x 2048]; NVFP4
     per-token on the ragged batch of 64 sequences (lengths in [128, 4096],
-    hidden 2048); NVFP4 shared-scale weights of a 128-expert MoE layer
+    hidden 2048), also with the pretraining recipe's Hadamard transform and
+    stochastic rounding; NVFP4 shared-scale weights of a 128-expert MoE layer
     (gate/up pairs [2 x 768 x 2048] and down [2048 x 768]); FP8 with FP32
     block scales (1x128 tiles of the activation, 128x128 blocks of the
     linear weight, the tiles' backward-orientation conversion); and the
@@ -657,6 +658,11 @@ def run_shapes(q, W, dev, stream, reps=20):
         _time_reps(lambda: q.dequantize_nvfp4(tq.codes, tq.block_scales,
                                               tq.scales),
                    stream, reps, flush_w, flush_r), tb, T * H, peak)
+    # the pretraining recipe's stabilizers on the same batch
+    for nm, fl in (("rht", q.NVFP4_RHT), ("rht_sr", q.NVFP4_RHT | q.NVFP4_SR)):
+        out[f"nvfp4_per_token_{nm}_ragged_{T}x{H}"] = _shape_line(
+            _time_reps(lambda: q.nvfp4_quantize_per_token_rht_sr(x, 2026, fl),
+                       stream, reps, flush_w, flush_r), tb, T * H, peak)
     del x, tq
 
     # NVFP4 weights of a 128-expert MoE layer

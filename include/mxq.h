@@ -297,6 +297,39 @@ mxq_status dequantize_nvfp4(const uint8_t* codes, const uint8_t* block_scales,
                             void* y, void* stream);
 
 /* --------------------------------------------------------------------- */
+/* NVFP4 per-token quantize with the stabilizers of the original NVFP4    */
+/* pretraining recipe.                                                    */
+/*                                                                       */
+/* [MILES] NVFP4 recipe section: that recipe uses stochastic rounding      */
+/* (SR, applied to gradients so the quantized values are unbiased) and    */
+/* Random Hadamard Transforms (RHT, dispersing block-level outliers of    */
+/* weight-gradient GEMM inputs); the RL recipe leaves both out.           */
+/*                                                                       */
+/* Same outputs and layouts as nvfp4_quantize_per_token.  flags:          */
+/*   MXQ_NVFP4_RHT: each 16-value block x becomes (1/4) H16 (s * x)        */
+/*     before quantization (H16 the Sylvester Hadamard matrix, s 16 signs  */
+/*     drawn from the seed); S and the block scales are those of the      */
+/*     transformed values, and dequantization returns transformed values  */
+/*     (the inverse transform belongs to the consumer, where H cancels    */
+/*     between two operands transformed with the same signs).             */
+/*   MXQ_NVFP4_SR: E2M1 codes by stochastic rounding: |x * enc| rounds up  */
+/*     to the next E2M1 magnitude with probability equal to its distance  */
+/*     from the one below, over their spacing.                            */
+/* Random bits: Philox4x64-10 keyed by seed, so the result depends only   */
+/* on (seed, input); flags = 0 gives nvfp4_quantize_per_token's bytes.    */
+/* H % 16 == 0, ldx % 8 == 0.                                             */
+/* --------------------------------------------------------------------- */
+#define MXQ_NVFP4_RHT 1
+#define MXQ_NVFP4_SR  2
+mxq_status nvfp4_quantize_per_token_rht_sr(const void* x, int64_t T,
+                                           int64_t H, int64_t ldx,
+                                           uint64_t seed, int flags,
+                                           uint8_t* codes,
+                                           uint8_t* block_scales,
+                                           float* token_scales,
+                                           int scale_layout, void* stream);
+
+/* --------------------------------------------------------------------- */
 /* FP8 E4M3 with one FP32 scale per block (the DeepSeek-V3-style recipe). */
 /*                                                                       */
 /* [MILES] introduction: that recipe scales weights in 128x128 blocks and */

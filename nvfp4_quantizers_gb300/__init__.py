@@ -14,7 +14,8 @@ from ._lib import (  # noqa: F401
     fp8_block_requantize_transpose, gemm_mxfp8,
     gemm_nvfp4_grouped, get_last_error, lib, moe_gate_up_swiglu,
     mxfp8_quantize_rowcol, nvfp4_quantize_per_token,
-    nvfp4_quantize_per_token_gather, nvfp4_quantize_weight_shared,
+    NVFP4_RHT, NVFP4_SR, nvfp4_quantize_per_token_gather,
+    nvfp4_quantize_per_token_rht_sr, nvfp4_quantize_weight_shared,
     scale_bytes, selftest_wait_timeout, set_fault_inject, status_string)
 
 __version__ = "0.1.0"

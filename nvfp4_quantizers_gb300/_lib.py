@@ -101,6 +101,9 @@ def lib() -> ctypes.CDLL:
         L.dequantize_nvfp4.restype = _int
         L.dequantize_nvfp4.argtypes = [_p, _p, _p, _int, _i64, _i64, _i64,
                                        _int, _p, _p]
+        L.nvfp4_quantize_per_token_rht_sr.restype = _int
+        L.nvfp4_quantize_per_token_rht_sr.argtypes = [
+            _p, _i64, _i64, _i64, ctypes.c_uint64, _int, _p, _p, _p, _int, _p]
         L.fp8_block_quantize.restype = _int
         L.fp8_block_quantize.argtypes = [_p, _i64, _i64, _i64, _int, _p, _p,
                                          _p]
@@ -250,6 +253,31 @@ def nvfp4_quantize_per_token_gather(x: torch.Tensor, row_index: torch.Tensor,
         x.data_ptr(), T_src, H, x.stride(0), row_index.data_ptr(), T,
         codes.data_ptr(), bs.data_ptr(), S.data_ptr(), lay, _stream(dev)),
         "nvfp4_quantize_per_token_gather")
+    return Nvfp4Quantized(codes, bs, S, lay)
+
+
+NVFP4_RHT = 1
+NVFP4_SR = 2
+
+
+def nvfp4_quantize_per_token_rht_sr(x: torch.Tensor, seed: int, flags: int,
+                                    scale_layout="swizzled") -> Nvfp4Quantized:
+    """Per-token NVFP4 with the pretraining recipe's stabilizers: a 16-value
+    Random Hadamard Transform (flags & NVFP4_RHT) and stochastic rounding
+    (flags & NVFP4_SR), random bits from Philox4x64-10 keyed by seed
+    (C: nvfp4_quantize_per_token_rht_sr)."""
+    x = _bf16_2d(x, "x")
+    lay = _layout(scale_layout)
+    T, H = x.shape
+    dev = x.device
+    codes = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
+    bs = torch.empty((scale_bytes(T, H // 16, lay),), dtype=torch.uint8,
+                     device=dev)
+    S = torch.empty((T,), dtype=torch.float32, device=dev)
+    _check(lib().nvfp4_quantize_per_token_rht_sr(
+        x.data_ptr(), T, H, x.stride(0), ctypes.c_uint64(seed), flags,
+        codes.data_ptr(), bs.data_ptr(), S.data_ptr(), lay, _stream(dev)),
+        "nvfp4_quantize_per_token_rht_sr")
     return Nvfp4Quantized(codes, bs, S, lay)
 
 

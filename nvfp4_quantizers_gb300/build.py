@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmxq.so")
 SOURCES = ["api.cu", "mxfp8.cu", "nvfp4.cu", "dequant.cu", "noalloc.cu",
-           "gemm.cu", "fp8block.cu"]
+           "gemm.cu", "fp8block.cu", "nvfp4_rht.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [

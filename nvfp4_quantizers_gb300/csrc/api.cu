@@ -369,6 +369,30 @@ mxq_status dequantize_nvfp4(const uint8_t* codes, const uint8_t* block_scales,
       scale_layout == MXQ_SCALE_SWIZZLED, y, static_cast<cudaStream_t>(stream)));
 }
 
+mxq_status nvfp4_quantize_per_token_rht_sr(const void* x, int64_t T,
+                                           int64_t H, int64_t ldx,
+                                           uint64_t seed, int flags,
+                                           uint8_t* codes,
+                                           uint8_t* block_scales,
+                                           float* token_scales,
+                                           int scale_layout, void* stream) {
+  const int fm = fault_mode();
+  if (fm == 2) return MXQ_ERR_ARG;
+  if (!valid_layout(scale_layout)) return MXQ_ERR_LAYOUT;
+  if (flags < 0 || flags > (MXQ_NVFP4_RHT | MXQ_NVFP4_SR)) return MXQ_ERR_ARG;
+  if (T < 0 || H < 0 || ldx < H) return MXQ_ERR_SHAPE;
+  if (T == 0 || H == 0) return MXQ_OK;
+  if (!x || !codes || !block_scales || !token_scales) return MXQ_ERR_NULL;
+  if (H % 16 != 0) return MXQ_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(block_scales) ||
+      !aligned16(token_scales) || ldx % 8 != 0)
+    return MXQ_ERR_ALIGN;
+  if (fm == 1) return MXQ_ERR_CUDA;
+  return from_cuda(launch_nvfp4_rht_sr(
+      x, T, H, ldx, seed, flags, codes, block_scales, token_scales,
+      scale_layout == MXQ_SCALE_SWIZZLED, static_cast<cudaStream_t>(stream)));
+}
+
 mxq_status fp8_block_quantize(const void* x, int64_t rows, int64_t cols,
                               int64_t ldx, int block_rows, uint8_t* codes,
                               float* scales, void* stream) {

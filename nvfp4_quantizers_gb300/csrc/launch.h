@@ -121,6 +121,14 @@ inline int64_t scale_bytes(int64_t rows, int64_t cols, int swizzled) {
   return ((rows + 127) / 128) * 128 * ((cols + 3) / 4) * 4;
 }
 
+// nvfp4_rht.cu
+// flags: bit 0 Random Hadamard Transform, bit 1 stochastic rounding.
+cudaError_t launch_nvfp4_rht_sr(const void* x, int64_t T, int64_t H,
+                                int64_t ldx, uint64_t seed, int flags,
+                                uint8_t* codes, uint8_t* scales,
+                                float* token_scales, int swizzled,
+                                cudaStream_t stream);
+
 // fp8block.cu
 // block_rows 1 (1x128 tiles) or 128 (128x128 blocks).
 cudaError_t launch_fp8blk_quantize(const void* x, int64_t rows, int64_t cols,

@@ -1,0 +1,264 @@
+// nvfp4_rht.cu -- per-token NVFP4 with the stabilizers of the original NVFP4
+// pretraining recipe: a 16-value Random Hadamard Transform before
+// quantization and stochastic rounding of the E2M1 codes.
+//
+// "Miles: end-to-end MXFP8 and per-token NVFP4 RL", NVFP4 recipe section:
+// the pretraining recipe uses stochastic rounding (applied to gradients, so
+// that the quantized values are unbiased) and Random Hadamard Transforms
+// (which disperse block-level outliers, especially of weight-gradient GEMM
+// inputs); the RL recipe itself leaves both out.
+//
+// Readings (the pages give no formulas):
+//   random bits  Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random
+//                numbers: as easy as 1, 2, 3", SC 2011): every element's bits
+//                depend only on (seed, position)
+//   RHT          y = (1/4) H16 (s * x) per 16-value block along the row, H16
+//                the Sylvester Hadamard matrix, s the signs given by the low
+//                16 bits of word 0 of Philox(counter 0, key (seed, 1)) (bit i
+//                set: s_i = -1); binary32 butterflies h = 1, 2, 4, 8
+//                ((a, b) -> (a + b, a - b)), then times 1/4 (exact)
+//   scales       the per-token S and the E4M3 block scales of the per-token
+//                quantizer, computed on the transformed binary32 values
+//   SR           element (r, c): u = (w >> 8) 2^-24, w the 32-bit word c % 8
+//                of Philox(counter (r, c / 8, 0, 0), key (seed, 2)); |v|
+//                (saturated at 6) rounds up to the next E2M1 magnitude iff
+//                u < (|v| - lo) / (hi - lo); sign kept
+//
+// Design (sm_103a): one warp per row (grid-stride), a lane per 16-value
+// block.  Pass 1 loads, transforms and reduces the row's amax; pass 2
+// reloads (from L1/L2), transforms again and encodes, so no row is held in
+// registers whatever its length.
+#include <float.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace mxq {
+
+namespace {
+
+constexpr int RS_THREADS = 256;
+constexpr unsigned FULL = 0xffffffffu;
+
+// Philox4x64-10: one 4-word block from a 4-word counter and a 2-word key.
+__device__ __forceinline__ void philox4x64(uint64_t c0, uint64_t c1,
+                                           uint64_t c2, uint64_t c3,
+                                           uint64_t k0, uint64_t k1,
+                                           uint64_t out[4]) {
+  const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+  const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
+    const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+    const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+    k0 += W0;
+    k1 += W1;
+  }
+  out[0] = c0;
+  out[1] = c1;
+  out[2] = c2;
+  out[3] = c3;
+}
+
+// The 16 binary32 values of a block from its bf16 words, sign-flipped,
+// butterflied and scaled by 1/4 when rht.
+__device__ __forceinline__ void block_values(const uint4& a, const uint4& b,
+                                             bool rht, uint32_t signs,
+                                             float (&v)[16]) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = bf16lo_to_f32(w[i]);
+    v[2 * i + 1] = bf16hi_to_f32(w[i]);
+  }
+  if (!rht) return;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    v[i] = __uint_as_float(__float_as_uint(v[i]) ^ (((signs >> i) & 1u) << 31));
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if ((i & h) == 0) {
+        const float x0 = v[i], x1 = v[i + h];
+        v[i] = __fadd_rn(x0, x1);
+        v[i + h] = __fsub_rn(x0, x1);
+      }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+}
+
+__device__ __forceinline__ float block_amax(const float (&v)[16]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+  return m;
+}
+
+// E2M1 code of v by stochastic rounding with u in [0, 1): the grid spacing
+// is 0.5 below 2, 1 below 4 and 2 below 6, so (|v| - lo) / (hi - lo) is
+// exact in binary32.
+__device__ __forceinline__ uint32_t sr_e2m1(float v, float u) {
+  const uint32_t neg = __float_as_uint(v) >> 31;
+  const float a = fminf(fabsf(v), 6.0f);
+  uint32_t idx;
+  float frac;
+  if (a < 2.0f) {
+    const float lo = floorf(a * 2.0f);            // 0..3 half-steps
+    idx = (uint32_t)lo;
+    frac = a * 2.0f - lo;
+  } else if (a < 4.0f) {
+    const float lo = floorf(a);                   // 2 or 3
+    idx = (uint32_t)lo + 2u;
+    frac = a - lo;
+  } else if (a < 6.0f) {
+    idx = 6u;                                     // 4
+    frac = (a - 4.0f) * 0.5f;
+  } else {
+    idx = 7u;                                     // 6
+    frac = 0.0f;
+  }
+  if (u < frac) ++idx;
+  return idx | (neg << 3);
+}
+
+__global__ void __launch_bounds__(RS_THREADS)
+    nvfp4_rht_sr_kernel(const uint16_t* __restrict__ x, int64_t T,
+                        int64_t T_pad, int64_t H, int64_t ldx, uint64_t seed,
+                        int flags, uint8_t* __restrict__ codes,
+                        uint8_t* __restrict__ scales, float* __restrict__ S_out,
+                        int swizzled) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = ((int64_t)blockIdx.x * RS_THREADS + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * RS_THREADS) >> 5;
+  const bool rht = (flags & 1) != 0, sr = (flags & 2) != 0;
+  const int64_t nb = H >> 4;
+  const int64_t col_tiles = (nb + 3) >> 2;
+  const int64_t iters = (nb + 31) >> 5;           // warp-uniform
+  uint32_t signs = 0;
+  if (rht) {
+    uint64_t o[4];
+    philox4x64(0, 0, 0, 0, seed, 1, o);
+    signs = (uint32_t)(o[0] & 0xffffu);
+  }
+  pdl_wait();
+  for (int64_t row = warp_id; row < T_pad; row += nwarps) {
+    const bool real = row < T;
+    const uint16_t* xr = x + (real ? row : 0) * ldx;
+    // ---- pass 1: the row's amax over the (transformed) values ----
+    float am = 0.0f;
+    for (int64_t j = 0; j < iters; ++j) {
+      const int64_t b = j * 32 + lane;
+      if (real && b < nb) {
+        const uint4 a0 = *reinterpret_cast<const uint4*>(xr + b * 16);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(xr + b * 16 + 8);
+        float v[16];
+        block_values(a0, a1, rht, signs, v);
+        am = fmaxf(am, block_amax(v));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(FULL, am, o));
+    const float S = __fdiv_rn(am, kNvfp4ScaleDenom);
+    const float six_s = __fmul_rn(6.0f, S);
+    if (real && lane == 0) S_out[row] = S;
+    // ---- pass 2: block scales and codes ----
+    for (int64_t j = 0; j < iters; ++j) {
+      const int64_t b = j * 32 + lane;
+      const bool valid = b < nb;
+      float v[16];
+      if (real && valid) {
+        const uint4 a0 = *reinterpret_cast<const uint4*>(xr + b * 16);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(xr + b * 16 + 8);
+        block_values(a0, a1, rht, signs, v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+      }
+      uint32_t sb = 0;
+      if (S != 0.0f)
+        sb = cvt_e4m3x2(__fdiv_rn(block_amax(v), six_s), 0.0f) & 0xFFu;
+      const float d = __fmul_rn(e4m3_to_f32(sb), S);
+      float enc = 0.0f;
+      if (d != 0.0f) enc = fminf(__frcp_rn(d), FLT_MAX);
+      float q[16];
+#pragma unroll
+      for (int i = 0; i < 16; i += 2)
+        fmul2(v[i], v[i + 1], enc, enc, q[i], q[i + 1]);
+      uint32_t lo, hi;
+      if (!sr) {
+        lo = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[0]));
+        hi = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[8]));
+      } else {
+        uint32_t c[16];
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          uint64_t o[4];
+          philox4x64((uint64_t)row, (uint64_t)(b * 2 + g), 0, 0, seed, 2, o);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t wd = o[k >> 1];
+            const uint32_t w = (uint32_t)((k & 1) ? (wd >> 32) : wd);
+            const float u = __uint2float_rn(w >> 8) * 0x1p-24f;
+            c[g * 8 + k] = sr_e2m1(q[g * 8 + k], u);
+          }
+        }
+        lo = hi = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          lo |= c[k] << (4 * k);
+          hi |= c[8 + k] << (4 * k);
+        }
+      }
+      if (real && valid) st_v2(codes + row * (H >> 1) + b * 8, lo, hi);
+      // lanes 4i .. 4i+3 hold four consecutive blocks: one 32-bit word
+      const uint32_t pair = sb | (__shfl_down_sync(FULL, sb, 1) << 8);
+      const uint32_t word = pair | (__shfl_down_sync(FULL, pair, 2) << 16);
+      if ((lane & 3) == 0) {
+        if (swizzled) {
+          if (b < 4 * col_tiles)
+            *reinterpret_cast<uint32_t*>(scales + swz_offset(row, b, col_tiles)) =
+                word;
+        } else if (real) {
+          if ((nb & 3) == 0) {
+            if (b < nb)
+              *reinterpret_cast<uint32_t*>(scales + row * nb + b) = word;
+          } else {
+            for (int k = 0; k < 4; ++k)
+              if (b + k < nb) scales[row * nb + b + k] = (uint8_t)(word >> (8 * k));
+          }
+        }
+      }
+    }
+  }
+  pdl_launch_dependents();
+}
+
+}  // namespace
+
+cudaError_t launch_nvfp4_rht_sr(const void* x, int64_t T, int64_t H,
+                                int64_t ldx, uint64_t seed, int flags,
+                                uint8_t* codes, uint8_t* scales,
+                                float* token_scales, int swizzled,
+                                cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const int64_t T_pad = swizzled ? (T + 127) / 128 * 128 : T;
+  const int64_t per_cta = RS_THREADS / 32;
+  int64_t grid = (T_pad + per_cta - 1) / per_cta;
+  const int64_t cap = (int64_t)sm_count(dev) * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  return launch_pdl(nvfp4_rht_sr_kernel, dim3((unsigned)grid),
+                    dim3(RS_THREADS), 0, stream, false,
+                    static_cast<const uint16_t*>(x), T, T_pad, H, ldx, seed,
+                    flags, codes, scales, token_scales, swizzled);
+}
+
+}  // namespace mxq

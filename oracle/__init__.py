@@ -112,7 +112,7 @@ def lib():
             L.oracle_nvfp4_rht_sr_rows.restype = ctypes.c_int
             L.oracle_nvfp4_rht_sr_rows.argtypes = [_p, _i64, _i64, _i64,
                                                    ctypes.c_uint64, ctypes.c_int,
-                                                   _p, _p, _p]
+                                                   _i64, _p, _p, _p]
             _lib = L
     return _lib
 
@@ -515,16 +515,19 @@ def rht16(x: np.ndarray, signs: int) -> np.ndarray:
     return y
 
 
-def nvfp4_quantize_rht_sr(x: np.ndarray, seed: int, flags: int):
+def nvfp4_quantize_rht_sr(x: np.ndarray, seed: int, flags: int,
+                          row0: int = 0):
     """Per-token NVFP4 of x [R, C] (bf16 bits) with the optional RHT
-    (flags & RHT) and stochastic rounding (flags & SR).  Returns (codes
-    u8 [R, C/2], block scales u8 [R, C/16] logical, S f32 [R])."""
+    (flags & RHT) and stochastic rounding (flags & SR); x holds rows
+    row0 .. row0 + R - 1 of the tensor.  Returns (codes u8 [R, C/2], block
+    scales u8 [R, C/16] logical, S f32 [R])."""
     x = _bf16(x)
     R, C = x.shape
     codes = np.empty((R, C // 2), np.uint8)
     scales = np.empty((R, C // 16), np.uint8)
     S = np.empty(R, np.float32)
     _check(lib().oracle_nvfp4_rht_sr_rows(_ptr(x), R, C, C, ctypes.c_uint64(seed),
-                                          flags, _ptr(codes), _ptr(scales),
-                                          _ptr(S)), "nvfp4 rht/sr")
+                                          flags, row0, _ptr(codes),
+                                          _ptr(scales), _ptr(S)),
+           "nvfp4 rht/sr")
     return codes, scales, S

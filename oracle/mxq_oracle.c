@@ -600,11 +600,13 @@ static uint8_t sr_e2m1(float v, float u) {
 }
 
 /* Per-token NVFP4 of x [R x C] (C % 16 == 0) with the optional RHT (flags
- * bit 0) and SR (bit 1).  codes [R x C/2] packed, low nibble = lower
+ * bit 0) and SR (bit 1); row r of x is row row0 + r of the tensor (the SR
+ * counters use that index).  codes [R x C/2] packed, low nibble = lower
  * index; scales [R x C/16] logical; S [R]. */
 int oracle_nvfp4_rht_sr_rows(const uint16_t* x, int64_t R, int64_t C,
                              int64_t ldx, uint64_t seed, int flags,
-                             uint8_t* codes, uint8_t* scales, float* S_out) {
+                             int64_t row0, uint8_t* codes, uint8_t* scales,
+                             float* S_out) {
     if (R < 0 || C < 0 || C % 16 || ldx < C) return 1;
     build_tables();
     const uint32_t signs = oracle_rht_signs(seed);
@@ -644,7 +646,7 @@ int oracle_nvfp4_rht_sr_rows(const uint16_t* x, int64_t R, int64_t C,
                 float v = y[b * 16 + i] * enc;
                 if (flags & 2) {
                     const int64_t c = b * 16 + i;
-                    const uint32_t w = philox_word(seed, 2, (uint64_t)r,
+                    const uint32_t w = philox_word(seed, 2, (uint64_t)(row0 + r),
                                                    (uint64_t)(c / 8), (int)(c % 8));
                     const float u = (float)(w >> 8) * 0x1p-24f;
                     q[i] = sr_e2m1(v, u);

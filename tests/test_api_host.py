@@ -132,6 +132,19 @@ def test_moe_entry_point_argument_errors(L):
     assert f(FAKE, FAKE, FAKE, O, 0, FAKE, FAKE, FAKE, 128, 256, FAKE, 128, None) == q.MXQ_OK
 
 
+def test_rht_sr_argument_errors(L):
+    import nvfp4_quantizers_gb300 as q
+    f = L.nvfp4_quantize_per_token_rht_sr
+    assert f(FAKE, 8, 64, 64, 1, 4, FAKE, FAKE, FAKE, 1, None) == q.MXQ_ERR_ARG
+    assert f(FAKE, 8, 64, 64, 1, -1, FAKE, FAKE, FAKE, 1, None) == q.MXQ_ERR_ARG
+    assert f(FAKE, 8, 40, 40, 1, 3, FAKE, FAKE, FAKE, 1, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, 8, 64, 32, 1, 3, FAKE, FAKE, FAKE, 1, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, 8, 64, 64, 1, 3, FAKE, None, FAKE, 1, None) == q.MXQ_ERR_NULL
+    assert f(FAKE, 8, 64, 68, 1, 3, FAKE, FAKE, FAKE, 1, None) == q.MXQ_ERR_ALIGN
+    assert f(FAKE, 8, 64, 64, 1, 3, FAKE, FAKE, FAKE, 5, None) == q.MXQ_ERR_LAYOUT
+    assert f(FAKE, 0, 64, 64, 1, 3, None, None, None, 1, None) == q.MXQ_OK
+
+
 def test_fp8_block_argument_errors(L):
     import nvfp4_quantizers_gb300 as q
     f = L.fp8_block_quantize
