@@ -25,9 +25,9 @@
 //                u < (|v| - lo) / (hi - lo); sign kept
 //
 // Design (sm_103a): one warp per row (grid-stride), a lane per 16-value
-// block.  Pass 1 loads, transforms and reduces the row's amax; pass 2
-// reloads (from L1/L2), transforms again and encodes, so no row is held in
-// registers whatever its length.
+// block.  Pass 1 loads (up to four blocks per lane at once), transforms and
+// reduces the row's amax; pass 2 reloads (from L1/L2), transforms again and
+// encodes, so no row is held in registers whatever its length.
 #include <float.h>
 
 #include "common.cuh"
@@ -38,6 +38,7 @@ namespace mxq {
 namespace {
 
 constexpr int RS_THREADS = 256;
+constexpr int kChunk = 4;           // blocks per lane loaded together
 constexpr unsigned FULL = 0xffffffffu;
 
 // Philox4x64-10: one 4-word block from a 4-word counter and a 2-word key.
@@ -127,7 +128,7 @@ __device__ __forceinline__ uint32_t sr_e2m1(float v, float u) {
   return idx | (neg << 3);
 }
 
-__global__ void __launch_bounds__(RS_THREADS)
+__global__ void __launch_bounds__(RS_THREADS, 2)
     nvfp4_rht_sr_kernel(const uint16_t* __restrict__ x, int64_t T,
                         int64_t T_pad, int64_t H, int64_t ldx, uint64_t seed,
                         int flags, uint8_t* __restrict__ codes,
@@ -150,15 +151,26 @@ __global__ void __launch_bounds__(RS_THREADS)
   for (int64_t row = warp_id; row < T_pad; row += nwarps) {
     const bool real = row < T;
     const uint16_t* xr = x + (real ? row : 0) * ldx;
-    // ---- pass 1: the row's amax over the (transformed) values ----
+    // ---- pass 1: the row's amax over the (transformed) values; up to
+    // four of a lane's blocks loaded before any is transformed ----
     float am = 0.0f;
-    for (int64_t j = 0; j < iters; ++j) {
-      const int64_t b = j * 32 + lane;
-      if (real && b < nb) {
-        const uint4 a0 = *reinterpret_cast<const uint4*>(xr + b * 16);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(xr + b * 16 + 8);
+    for (int64_t j0 = 0; j0 < iters; j0 += kChunk) {
+      uint4 raw[2 * kChunk];
+#pragma unroll
+      for (int k = 0; k < kChunk; ++k) {
+        const int64_t b = (j0 + k) * 32 + lane;
+        if (real && j0 + k < iters && b < nb) {
+          raw[2 * k] = *reinterpret_cast<const uint4*>(xr + b * 16);
+          raw[2 * k + 1] = *reinterpret_cast<const uint4*>(xr + b * 16 + 8);
+        } else {
+          raw[2 * k] = make_uint4(0, 0, 0, 0);
+          raw[2 * k + 1] = raw[2 * k];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kChunk; ++k) {
         float v[16];
-        block_values(a0, a1, rht, signs, v);
+        block_values(raw[2 * k], raw[2 * k + 1], rht, signs, v);
         am = fmaxf(am, block_amax(v));
       }
     }
