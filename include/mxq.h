@@ -389,6 +389,22 @@ mxq_status mxq_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
                           int64_t M, int64_t N, int64_t K, float* C,
                           int64_t ldc, void* stream);
 
+/* mxq_gemm_bf16_mxfp8: the dequantized-backward GEMM ([MILES] backward-  */
+/* mode section: BF16 backward GEMMs on BF16 dequantizations of the exact  */
+/* forward operands) without a bf16 copy of the quantized operand in HBM:  */
+/*   C[m, n] = sum_k A[m, k] * Bq[k, n],                                  */
+/* A bf16 [M x K] (row stride lda elements, lda >= K, lda % 8 == 0), B    */
+/* given as B^T [N x K]: MXFP8 codes (bt_codes, row stride K) and swizzled */
+/* E8M0 scales (bt_scales, 1x32 blocks along K) -- the columnwise copy of */
+/* a [K x N] forward tensor; Bq = E4M3(code) * 2^(s - 127), exact in bf16. */
+/* The bf16 values of B are formed in shared memory only.  fp32            */
+/* accumulation, fp32 C [M x N] (ldc >= N, ldc % 4 == 0).                  */
+/* M % 128 == 0, N % 128 == 0, K % 64 == 0.                               */
+mxq_status mxq_gemm_bf16_mxfp8(const void* a, int64_t lda,
+                               const uint8_t* bt_codes,
+                               const uint8_t* bt_scales, int64_t M, int64_t N,
+                               int64_t K, float* C, int64_t ldc, void* stream);
+
 /* mxq_gemm_nvfp4_grouped: expert-grouped NVFP4 GEMM.  A holds the routed  */
 /* activations of all groups, grouped contiguously: rows                  */
 /* group_offsets[g] .. group_offsets[g+1] (HOST array of num_groups + 1    */

@@ -11,7 +11,7 @@ from ._lib import (  # noqa: F401
     SCALE_SWIZZLED, S_PER_BATCH, S_PER_ROW, Fp8BlockQuantized,
     Mxfp8Quantized, MxqError, Nvfp4Quantized, dequantize_mxfp8,
     dequantize_nvfp4, fp8_block_dequantize, fp8_block_quantize,
-    fp8_block_requantize_transpose, gemm_mxfp8,
+    fp8_block_requantize_transpose, gemm_bf16_mxfp8, gemm_mxfp8,
     gemm_nvfp4_grouped, get_last_error, lib, moe_gate_up_swiglu,
     mxfp8_quantize_rowcol, nvfp4_quantize_per_token,
     NVFP4_RHT, NVFP4_SR, nvfp4_quantize_per_token_gather,

@@ -101,6 +101,9 @@ def lib() -> ctypes.CDLL:
         L.dequantize_nvfp4.restype = _int
         L.dequantize_nvfp4.argtypes = [_p, _p, _p, _int, _i64, _i64, _i64,
                                        _int, _p, _p]
+        L.mxq_gemm_bf16_mxfp8.restype = _int
+        L.mxq_gemm_bf16_mxfp8.argtypes = [_p, _i64, _p, _p, _i64, _i64, _i64,
+                                          _p, _i64, _p]
         L.nvfp4_quantize_per_token_rht_sr.restype = _int
         L.nvfp4_quantize_per_token_rht_sr.argtypes = [
             _p, _i64, _i64, _i64, ctypes.c_uint64, _int, _p, _p, _p, _int, _p]
@@ -393,6 +396,25 @@ def gemm_mxfp8(a_codes: torch.Tensor, a_scales: torch.Tensor,
                                 bt_codes.data_ptr(), bt_scales.data_ptr(), M, N,
                                 K, C.data_ptr(), N, _stream(a_codes.device)),
            "mxq_gemm_mxfp8")
+    return C
+
+
+def gemm_bf16_mxfp8(a: torch.Tensor, bt_codes: torch.Tensor,
+                    bt_scales: torch.Tensor) -> torch.Tensor:
+    """fp32 C [M, N] = A (bf16 [M, K]) times the dequantization of an MXFP8
+    operand given as B^T [N, K] (codes + swizzled E8M0 scales), its bf16
+    values formed in shared memory only (C: mxq_gemm_bf16_mxfp8)."""
+    _bf16_2d(a, "a")
+    M, K = a.shape
+    N = bt_codes.shape[0]
+    if bt_codes.dtype != torch.uint8 or tuple(bt_codes.shape) != (N, K) or \
+            not bt_codes.is_contiguous():
+        raise ValueError("bt_codes must be a contiguous uint8 [N, K] tensor")
+    C = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    _check(lib().mxq_gemm_bf16_mxfp8(a.data_ptr(), a.stride(0),
+                                     bt_codes.data_ptr(), bt_scales.data_ptr(),
+                                     M, N, K, C.data_ptr(), N,
+                                     _stream(a.device)), "mxq_gemm_bf16_mxfp8")
     return C
 
 

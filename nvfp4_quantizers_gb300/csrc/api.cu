@@ -155,6 +155,23 @@ cudaError_t make_tmap_2d_bytes(CUtensorMap* map, const void* base,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_tmap_2d_bytes_plain(CUtensorMap* map, const void* base,
+                                     uint64_t inner, uint64_t outer,
+                                     uint64_t outer_stride_bytes,
+                                     uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {outer_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace mxq
 
 using namespace mxq;
@@ -469,6 +486,28 @@ mxq_status mxq_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
   return from_cuda(launch_gemm_mxfp8(a_codes, a_scales, bt_codes, bt_scales, M,
                                      N, K, C, ldc,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+mxq_status mxq_gemm_bf16_mxfp8(const void* a, int64_t lda,
+                               const uint8_t* bt_codes,
+                               const uint8_t* bt_scales, int64_t M, int64_t N,
+                               int64_t K, float* C, int64_t ldc, void* stream) {
+  const int fm = fault_mode();
+  if (fm == 2) return MXQ_ERR_ARG;
+  if (M < 0 || N < 0 || K < 0 || lda < K || ldc < N) return MXQ_ERR_SHAPE;
+  if (M == 0 || N == 0) return MXQ_OK;
+  if (!a || !bt_codes || !bt_scales || !C) return MXQ_ERR_NULL;
+  if (M % 128 != 0 || N % 128 != 0 || K % 64 != 0 || K == 0)
+    return MXQ_ERR_SHAPE;
+  if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31))
+    return MXQ_ERR_SHAPE;
+  if (!aligned16(a) || !aligned16(bt_codes) || !aligned16(bt_scales) ||
+      !aligned16(C) || lda % 8 != 0 || ldc % 4 != 0)
+    return MXQ_ERR_ALIGN;
+  if (fm == 1) return MXQ_ERR_CUDA;
+  return from_cuda(launch_gemm_bf16_mxfp8(a, lda, bt_codes, bt_scales, M, N, K,
+                                          C, ldc,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 mxq_status mxq_gemm_nvfp4_grouped(

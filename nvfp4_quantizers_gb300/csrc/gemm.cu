@@ -871,4 +871,334 @@ cudaError_t launch_moe_gate_up_swiglu(
                         tiles_m * p.tiles_n, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Dequantized-backward GEMM: bf16 A times an MXFP8 operand whose bf16
+// values are formed in shared memory and never written to HBM.
+//
+// "Miles: end-to-end MXFP8 and per-token NVFP4 RL", backward-mode section:
+// in dequantized-backward mode the backward GEMMs run in BF16 on BF16
+// dequantizations of the exact forward low-precision operands.  Here
+//   C[m, n] = sum_k A[m, k] * Bq[k, n],   A bf16 [M x K] (e.g. dY),
+// Bq given as B^T [N x K]: MXFP8 codes with 1x32 E8M0 scales along K (the
+// columnwise copy of a forward operand), Bq[k, n] = E4M3(code) * 2^(s-127),
+// exact in bf16.  fp32 accumulation in tensor memory, fp32 C.
+//
+// Design: persistent, one CTA per SM, 128 x 128 output tiles, 11 warps.
+// Warp 0 lane 0 streams K-stages of 64 values into a 3-deep ring: the A
+// tile (bf16, 128-byte rows, 128-byte swizzle) and the B^T code tile
+// (128 rows x 64 bytes, unswizzled) by 2-D TMA.  Warps 7-10 (one thread
+// per B row) turn the codes into bf16 in the stage's B buffer, in the
+// 128-byte-swizzled K-major layout the tensor core reads, then fence the
+// writes to the async proxy and count themselves on the stage's
+// "converted" barrier.  Warp 2 waits for both and hands the stage to warp
+// 1, whose lane 0 issues four kind::f16 MMAs (K = 16 each) and commits;
+// warps 3-6 take the accumulator to registers, release it and store C in
+// 32 x 32 fp32 boxes by TMA.  Every wait is bounded.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int DQ_M = 128, DQ_N = 128;
+constexpr int DQ_KE = 64;                 // K values per stage
+constexpr int DQ_STAGES = 3;
+constexpr int DQ_THREADS = 32 * 11;
+constexpr uint32_t kDqTmemCols = 128;
+
+struct alignas(1024) DqSmem {
+  uint8_t a[DQ_STAGES][DQ_M * 128];       // bf16, 128-byte swizzled rows
+  uint8_t b[DQ_STAGES][DQ_N * 128];       // bf16 from the codes, same layout
+  uint8_t braw[DQ_STAGES][DQ_N * DQ_KE];  // E4M3 codes, 64-byte rows
+  uint8_t cst[4][32 * 128];               // epilogue staging boxes
+  alignas(8) uint64_t full[DQ_STAGES];
+  alignas(8) uint64_t conv[DQ_STAGES];
+  alignas(8) uint64_t empty[DQ_STAGES];
+  alignas(8) uint64_t acc_full;
+  alignas(8) uint64_t acc_empty;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct DqParams {
+  int64_t M, N, K;
+  int64_t k_stages;
+  int64_t tiles_n, n_tiles;
+  const uint8_t* b_sf;                    // swizzled E8M0 of B^T [N x K/32]
+  int64_t b_sf_ct;                        // scale column tiles, ceil(K/128)
+};
+
+// Instruction descriptor of a dense kind::f16 MMA with bf16 A and B (both
+// K-major), fp32 accumulator, M = DQ_M, N = DQ_N.
+__device__ __forceinline__ uint32_t idesc_bf16() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(DQ_N >> 3) << 17) |
+         ((uint32_t)(DQ_M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma_f16(uint32_t d, uint64_t adesc,
+                                           uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(DQ_THREADS, 1)
+    gemm_bf16_dq_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_b,
+                        const __grid_constant__ CUtensorMap tmap_c,
+                        const __grid_constant__ DqParams p) {
+  extern __shared__ uint8_t dsmem_raw[];
+  DqSmem& s = *reinterpret_cast<DqSmem*>(
+      (reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == 0) tmem_alloc(smem_addr(&s.tmem_base), kDqTmemCols);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < DQ_STAGES; ++i) {
+      mbar_init(smem_addr(&s.full[i]), 1);
+      mbar_init(smem_addr(&s.conv[i]), 4);          // converter warps
+      mbar_init(smem_addr(&s.empty[i]), 1);
+    }
+    mbar_init(smem_addr(&s.acc_full), 1);
+    mbar_init(smem_addr(&s.acc_empty), 4);          // epilogue warps
+    s.abort = 0;
+    fence_barrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  pdl_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- producer ----------------
+      int64_t it = 0;
+      for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
+        const int64_t m0 = (t / p.tiles_n) * DQ_M;
+        const int64_t n0 = (t % p.tiles_n) * DQ_N;
+        for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
+          const int st = (int)(it % DQ_STAGES);
+          const uint32_t ph = (uint32_t)((it / DQ_STAGES) & 1);
+          if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1, &s.abort,
+                         &g_gemm_wait_error))
+            break;
+          const uint32_t full = smem_addr(&s.full[st]);
+          mbar_arrive_expect_tx(full, DQ_M * 128 + DQ_N * DQ_KE);
+          tma_load_2d(smem_addr(s.a[st]), &tmap_a, (int32_t)(kt * DQ_KE),
+                      (int32_t)m0, full);
+          tma_load_2d(smem_addr(s.braw[st]), &tmap_b, (int32_t)(kt * DQ_KE),
+                      (int32_t)n0, full);
+        }
+        if (s.abort) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    int64_t it = 0;
+    bool aborted = false;
+    for (int64_t t = blockIdx.x; t < p.n_tiles && !aborted; t += gridDim.x) {
+      for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
+        __syncwarp();
+        if (stage_handoff(false)) {
+          aborted = true;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const int st = (int)(it % DQ_STAGES);
+          const uint32_t a_addr = smem_addr(s.a[st]);
+          const uint32_t b_addr = smem_addr(s.b[st]);
+          // four MMAs of K = 16 bf16 values (32 bytes of each row)
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t ad = smem_desc(a_addr + j * 32, 16, 1024, 2);
+            const uint64_t bd = smem_desc(b_addr + j * 32, 16, 1024, 2);
+            tc_mma_f16(tmem, ad, bd, idesc_bf16(),
+                       (kt > 0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_addr(&s.empty[st]));
+          if (kt == p.k_stages - 1) tc_commit(smem_addr(&s.acc_full));
+        }
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------- waiter ----------------
+    int64_t it = 0;
+    int local = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++local) {
+      if (lane == 0)
+        ok = mbar_wait(smem_addr(&s.acc_empty), (uint32_t)((local & 1) ^ 1),
+                       &s.abort, &g_gemm_wait_error);
+      for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
+        const int st = (int)(it % DQ_STAGES);
+        const uint32_t ph = (uint32_t)((it / DQ_STAGES) & 1);
+        if (lane == 0 && ok)
+          ok = mbar_wait(smem_addr(&s.full[st]), ph, &s.abort,
+                         &g_gemm_wait_error) &&
+               mbar_wait(smem_addr(&s.conv[st]), ph, &s.abort,
+                         &g_gemm_wait_error);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        if (stage_handoff(!ok)) {
+          ok = false;
+          break;
+        }
+      }
+    }
+  } else if (warp >= 7) {
+    // ---------------- converters: warps 7-10, one thread per B row -------
+    const int n = threadIdx.x - 7 * 32;               // 0 .. 127
+    int64_t it = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+      const int64_t n0 = (t % p.tiles_n) * DQ_N;
+      for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
+        const int st = (int)(it % DQ_STAGES);
+        const uint32_t ph = (uint32_t)((it / DQ_STAGES) & 1);
+        if (lane == 0)
+          ok = mbar_wait(smem_addr(&s.full[st]), ph, &s.abort,
+                         &g_gemm_wait_error);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        // the row's 64 codes, chunk order rotated by n / 2 so that the 8
+        // lanes of a shared-memory phase read 8 different bank groups
+        uint4 cv[4];
+        const uint8_t* raw = s.braw[st] + n * DQ_KE;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int cc = (c + (n >> 1)) & 3;
+          const uint4 v = *reinterpret_cast<const uint4*>(raw + cc * 16);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (cc == j) cv[j] = v;
+        }
+        // E8M0 scales of the row's two 32-value blocks of this stage
+        const int64_t kb = kt * 2;
+        const float s0 = e8m0_scale(p.b_sf[swz_offset(n0 + n, kb, p.b_sf_ct)]);
+        const float s1 = e8m0_scale(p.b_sf[swz_offset(n0 + n, kb + 1, p.b_sf_ct)]);
+        uint8_t* row = s.b[st] + n * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float sc = c < 2 ? s0 : s1;
+          const uint32_t cw[4] = {cv[c].x, cv[c].y, cv[c].z, cv[c].w};
+          uint32_t w[8];
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            float x0, x1;
+            e4m3x2_to_f32((cw[h >> 1] >> ((h & 1) * 16)) & 0xFFFFu, x0, x1);
+            fmul2(x0, x1, sc, sc, x0, x1);
+            w[h] = f32x2_to_bf16x2(x0, x1);
+          }
+          // 16-byte chunks 2c and 2c+1 of the row, 128-byte swizzle
+          const int q0 = (2 * c) ^ (n & 7), q1 = (2 * c + 1) ^ (n & 7);
+          *reinterpret_cast<uint4*>(row + q0 * 16) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(row + q1 * 16) =
+              make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&s.conv[st]));
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 3-6 ----------------
+    const int q = warp & 3;                           // tensor-memory quarter
+    uint8_t* box = s.cst[warp - 3];
+    int local = 0;
+    for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++local) {
+      const bool ok = __all_sync(
+          0xffffffffu,
+          mbar_wait(smem_addr(&s.acc_full), (uint32_t)(local & 1), &s.abort,
+                    &g_gemm_wait_error));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t r[128];
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tc_ld_32x32_async(lane_base + (uint32_t)(c * 32), r + c * 32);
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&s.acc_empty));
+      const int64_t m0 = (t / p.tiles_n) * DQ_M;
+      const int64_t n0 = (t % p.tiles_n) * DQ_N;
+      uint8_t* rowp = box + lane * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (lane == 0) bulk_wait_read_0();              // the box's last store
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float4 v;
+          v.x = __uint_as_float(r[c * 32 + 4 * j]);
+          v.y = __uint_as_float(r[c * 32 + 4 * j + 1]);
+          v.z = __uint_as_float(r[c * 32 + 4 * j + 2]);
+          v.w = __uint_as_float(r[c * 32 + 4 * j + 3]);
+          *reinterpret_cast<float4*>(rowp + ((j ^ (lane & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmap_c, smem_addr(box), (int32_t)(n0 + c * 32),
+                       (int32_t)(m0 + q * 32));
+          bulk_commit();
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kDqTmemCols);
+  pdl_launch_dependents();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_bf16_mxfp8(const void* a, int64_t lda,
+                                   const uint8_t* bt_codes,
+                                   const uint8_t* bt_scales, int64_t M,
+                                   int64_t N, int64_t K, float* C, int64_t ldc,
+                                   cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  CUtensorMap ta, tb, tc;
+  err = make_tmap_2d_bf16(&ta, a, (uint64_t)K, (uint64_t)M, (uint64_t)lda * 2,
+                          DQ_KE, DQ_M, true);
+  if (err != cudaSuccess) return err;
+  err = make_tmap_2d_bytes_plain(&tb, bt_codes, (uint64_t)K, (uint64_t)N,
+                                 (uint64_t)K, DQ_KE, DQ_N);
+  if (err != cudaSuccess) return err;
+  err = make_tmap_c(&tc, C, M, N, ldc);
+  if (err != cudaSuccess) return err;
+  DqParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.k_stages = K / DQ_KE;
+  p.tiles_n = N / DQ_N;
+  p.n_tiles = (M / DQ_M) * p.tiles_n;
+  p.b_sf = bt_scales;
+  p.b_sf_ct = (K / 32 + 3) / 4;
+  const size_t smem = sizeof(DqSmem) + 1024;
+  static int configured[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    err = cudaFuncSetAttribute(gemm_bf16_dq_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+    if (err != cudaSuccess) return err;
+    configured[dev] = 1;
+  }
+  const int64_t grid = imin<int64_t>(p.n_tiles, sm_count(dev));
+  return launch_pdl(gemm_bf16_dq_kernel, dim3((unsigned)grid),
+                    dim3(DQ_THREADS), smem, stream, false, ta, tb, tc, p);
+}
+
 }  // namespace mxq

@@ -23,6 +23,11 @@ cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base,
                               uint64_t inner, uint64_t outer,
                               uint64_t outer_stride_bytes, uint32_t box_inner,
                               uint32_t box_outer, bool swizzle128);
+// byte matrix, no swizzle.
+cudaError_t make_tmap_2d_bytes_plain(CUtensorMap* map, const void* base,
+                                     uint64_t inner, uint64_t outer,
+                                     uint64_t outer_stride_bytes,
+                                     uint32_t box_inner, uint32_t box_outer);
 // fp32 matrix, 128-byte swizzle (box_inner * 4 <= 128).
 cudaError_t make_tmap_2d_f32(CUtensorMap* map, const void* base,
                              uint64_t inner, uint64_t outer,
@@ -98,6 +103,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
 
 // gemm.cu
 cudaError_t gemm_take_wait_error(unsigned int* word);
+// C [M x N] fp32 = A bf16 [M x K] (row stride lda) x dequant(B), B^T
+// [N x K] given as MXFP8 codes + swizzled E8M0 scales.
+cudaError_t launch_gemm_bf16_mxfp8(const void* a, int64_t lda,
+                                   const uint8_t* bt_codes,
+                                   const uint8_t* bt_scales, int64_t M,
+                                   int64_t N, int64_t K, float* C, int64_t ldc,
+                                   cudaStream_t stream);
 cudaError_t launch_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
                               const uint8_t* bt_codes,
                               const uint8_t* bt_scales, int64_t M, int64_t N,

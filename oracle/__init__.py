@@ -531,3 +531,21 @@ def nvfp4_quantize_rht_sr(x: np.ndarray, seed: int, flags: int,
                                           _ptr(scales), _ptr(S)),
            "nvfp4 rht/sr")
     return codes, scales, S
+
+
+def gemm_bf16_mxfp8(a: np.ndarray, bt_codes: np.ndarray,
+                    bt_scales: np.ndarray) -> np.ndarray:
+    """The dequantized-backward GEMM (backward-mode section of "Miles:
+    end-to-end MXFP8 and per-token NVFP4 RL": BF16 GEMMs on BF16
+    dequantizations of the exact forward operands): float64
+    A [M, K] (bf16 bits) @ dequant(B^T [N, K])^T, the dequantization
+    exact (E4M3 x 2^k lands on the bf16 grid)."""
+    a64 = W_bits_to_f64(a)
+    b64 = W_bits_to_f64(mxfp8_dequantize(bt_codes, bt_scales))
+    return a64 @ b64.T
+
+
+def W_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float64 values (exact)."""
+    u = np.ascontiguousarray(bits, np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)

@@ -170,6 +170,18 @@ def test_fp8_block_argument_errors(L):
     assert t(FAKE, FAKE, 0, 256, None, None, None) == q.MXQ_OK
 
 
+def test_bf16_mxfp8_gemm_argument_errors(L):
+    import nvfp4_quantizers_gb300 as q
+    f = L.mxq_gemm_bf16_mxfp8
+    assert f(FAKE, 128, FAKE, FAKE, 100, 128, 128, FAKE, 128, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, 128, FAKE, FAKE, 128, 128, 96, FAKE, 128, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, 64, FAKE, FAKE, 128, 128, 128, FAKE, 128, None) == q.MXQ_ERR_SHAPE
+    assert f(FAKE, 128, None, FAKE, 128, 128, 128, FAKE, 128, None) == q.MXQ_ERR_NULL
+    assert f(FAKE, 132, FAKE, FAKE, 128, 128, 128, FAKE, 128, None) == q.MXQ_ERR_ALIGN
+    assert f(FAKE + 8, 128, FAKE, FAKE, 128, 128, 128, FAKE, 128, None) == q.MXQ_ERR_ALIGN
+    assert f(FAKE, 128, FAKE, FAKE, 0, 128, 128, FAKE, 128, None) == q.MXQ_OK
+
+
 def test_fault_injection_returns_errors_without_launching(L):
     import nvfp4_quantizers_gb300 as q
     try:

@@ -1,0 +1,65 @@
+"""GPU parity of the dequantized-backward GEMM without a bf16 copy of the
+quantized operand ("Miles: end-to-end MXFP8 and per-token NVFP4 RL",
+backward-mode section: BF16 backward GEMMs consume BF16 dequantizations of
+the exact forward operands).  The MXFP8 operand is made by the oracle
+(codes and scales of B's columnwise copy), so the GEMM's inputs do not come
+from the GPU quantizer; the product is compared with the float64 oracle by
+relative Frobenius error (fp32 accumulation: about 1e-6; the bar is 1e-4,
+inside the 1e-3 of the GEMM contract)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from gpu_util import dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mxq():
+    if not torch.cuda.is_available():
+        pytest.fail("the GPU tests need a CUDA device")
+    from nvfp4_quantizers_gb300 import build
+    build.build()
+    import nvfp4_quantizers_gb300 as q
+    q.lib()
+    return q
+
+
+def rel_fro(c, ref):
+    return np.linalg.norm(c - ref) / max(np.linalg.norm(ref), 1e-300)
+
+
+def _case(q, M, K, N, seed, rows=None):
+    rng = np.random.default_rng(seed)
+    A = W.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    Bw = W.to_bf16_bits((0.02 * rng.standard_normal((K, N)) *
+                         10.0 ** rng.uniform(-3, 3, (1, N))).astype(np.float32))
+    bc, bs = O.mxfp8_quantize_colwise(Bw)          # B^T [N x K], logical scales
+    C = q.gemm_bf16_mxfp8(dev_bf16(A), torch.from_numpy(bc).cuda(),
+                          torch.from_numpy(O.scale_swizzle(bs)).cuda())
+    torch.cuda.synchronize()
+    assert q.get_last_error() == q.MXQ_OK
+    got = C.cpu().numpy().astype(np.float64)
+    sel = np.arange(M) if rows is None else rows
+    ref = O.gemm_bf16_mxfp8(A[sel], bc, bs)
+    err = rel_fro(got[sel], ref)
+    assert err <= 1e-4, err
+    return err
+
+
+@pytest.mark.parametrize("M,K,N", [(128, 64, 128), (128, 128, 256),
+                                   (384, 512, 512), (256, 1024, 384)])
+def test_small(mxq, M, K, N):
+    _case(mxq, M, K, N, seed=M + K + N)
+
+
+def test_linear_dgrad_shape(mxq):
+    """The linear layer (2048, 2048) -> 8192 of the memory section, data
+    gradient: dX [2048 x 2048] = dY [2048 x 8192] x W, W's columnwise copy
+    as B^T [2048 x 8192]; 64 sampled rows against the oracle."""
+    rows = np.union1d(np.random.default_rng(3).choice(2048, 62, replace=False),
+                      [0, 2047])
+    _case(mxq, 2048, 8192, 2048, seed=9, rows=rows)

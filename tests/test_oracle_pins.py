@@ -877,3 +877,20 @@ def test_sr_is_unbiased_and_keeps_grid_values(orc):
     again = orc.nvfp4_quantize_rht_sr(x, 77, orc.SR)[0]
     other = orc.nvfp4_quantize_rht_sr(x, 78, orc.SR)[0]
     assert np.array_equal(codes, again) and not np.array_equal(codes, other)
+
+
+def test_gemm_bf16_mxfp8_closed_form(orc):
+    """One non-zero code in B^T: column n of C is column k of A times that
+    code's value E4M3(c) * 2^(s - 127); everything else is zero."""
+    rng = np.random.default_rng(61)
+    A = W.to_bf16_bits(rng.standard_normal((4, 64)).astype(np.float32))
+    codes = np.zeros((3, 64), np.uint8)
+    scales = np.full((3, 2), 127, np.uint8)
+    codes[1, 40] = 0x46                      # E4M3 1.75 * 2 = 3.5
+    scales[1, 1] = 127 + 5                   # block 1 of row 1: 2^5
+    C = orc.gemm_bf16_mxfp8(A, codes, scales)
+    af = W.bits_to_f32(A).astype(np.float64)
+    assert orc.decode_e4m3(0x46) == 3.5
+    exp = np.zeros((4, 3))
+    exp[:, 1] = af[:, 40] * 3.5 * 32
+    assert np.array_equal(C, exp)
