@@ -446,7 +446,7 @@ def tensor_peaks():
         kind = "measured bf16 x nominal ratio"
     except Exception:
         bf16, kind = 1900.0, "fallback bf16 x nominal ratio"
-    return {"fp8": 2 * bf16, "fp4": 6 * bf16, "kind": kind}
+    return {"bf16": bf16, "fp8": 2 * bf16, "fp4": 6 * bf16, "kind": kind}
 
 
 def gemm_roofline(us, flops, nbytes, tensor_peak_tflops):
@@ -554,6 +554,30 @@ def run_gemm(q, W, dev, stream, reps=20):
                nb_gq / ms_gq / 1e6 / measured_peak()[0], 3),
            "forward_us": round((ms_gq + ms_sw) * 1e3, 2),
            "padded_rows": Mp2, "output": "bf16 h [rows x 768]"})
+    # Dequantized-backward data gradient of the linear layer (2048, 2048) ->
+    # 8192: dX [2048 x 2048] = dY [2048 x 8192] x W, W's columnwise MXFP8
+    # copy dequantized in shared memory; beside it the path that writes the
+    # bf16 dequantization to HBM and runs cuBLAS on it.
+    dY = torch.from_numpy(W.gemm_tokens(2048, 8192).view(np.int16)).view(
+        torch.bfloat16).to(dev)
+    wq = q.mxfp8_quantize_rowcol(torch.from_numpy(W.linear_weight().view(
+        np.int16)).view(torch.bfloat16).to(dev), rowwise=False, colwise=True)
+
+    def t_dq():
+        return q.gemm_bf16_mxfp8(dY, wq.col_codes_t, wq.col_scales_t)
+
+    def t_mat():
+        wt = q.dequantize_mxfp8(wq.col_codes_t, wq.col_scales_t)
+        return torch.matmul(dY, wt.t())
+    ms_dq = _time_fn(t_dq, stream, reps)
+    ms_mat = _time_fn(t_mat, stream, reps)
+    fl = 2.0 * 2048 * 2048 * 8192
+    nb = 2048 * 8192 * 2 + 2048 * 8192 * (1 + 1 / 32) + 2048 * 2048 * 4
+    out["bf16_x_mxfp8_dgrad_2048x8192x2048"] = dict(
+        gemm_roofline(ms_dq * 1e3, fl, nb, peaks["bf16"]),
+        **{"materialized_us": round(ms_mat * 1e3, 2),
+           "materialized": "dequantize to bf16 in HBM, then cuBLAS bf16",
+           "peak_bf16": round(peaks["bf16"], 1)})
     out["peaks_kind"] = peaks["kind"]
     return out
 

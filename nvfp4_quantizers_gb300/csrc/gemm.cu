@@ -884,9 +884,12 @@ cudaError_t launch_moe_gate_up_swiglu(
 // exact in bf16.  fp32 accumulation in tensor memory, fp32 C.
 //
 // Design: persistent, one CTA per SM, 128 x 128 output tiles, 11 warps.
-// Warp 0 lane 0 streams K-stages of 64 values into a 3-deep ring: the A
+// Warp 0 lane 0 streams K-stages of 64 values into a 5-deep ring: the A
 // tile (bf16, 128-byte rows, 128-byte swizzle) and the B^T code tile
-// (128 rows x 64 bytes, unswizzled) by 2-D TMA.  Warps 7-10 (one thread
+// (128 rows x 64 bytes, unswizzled) by 2-D TMA, and the 512-byte scale
+// tile holding the stage's E8M0 columns by a bulk copy (reading the
+// scales from global memory in the converters stalled every stage on
+// their latency: 218 us for the linear layer's data gradient).  Warps 7-10 (one thread
 // per B row) turn the codes into bf16 in the stage's B buffer, in the
 // 128-byte-swizzled K-major layout the tensor core reads, then fence the
 // writes to the async proxy and count themselves on the stage's
@@ -899,7 +902,7 @@ namespace {
 
 constexpr int DQ_M = 128, DQ_N = 128;
 constexpr int DQ_KE = 64;                 // K values per stage
-constexpr int DQ_STAGES = 3;
+constexpr int DQ_STAGES = 5;
 constexpr int DQ_THREADS = 32 * 11;
 constexpr uint32_t kDqTmemCols = 128;
 
@@ -907,7 +910,12 @@ struct alignas(1024) DqSmem {
   uint8_t a[DQ_STAGES][DQ_M * 128];       // bf16, 128-byte swizzled rows
   uint8_t b[DQ_STAGES][DQ_N * 128];       // bf16 from the codes, same layout
   uint8_t braw[DQ_STAGES][DQ_N * DQ_KE];  // E4M3 codes, 64-byte rows
-  uint8_t cst[4][32 * 128];               // epilogue staging boxes
+  // the 512-byte swizzled E8M0 tile (128 rows x 4 blocks of 32) holding
+  // the stage's two scale columns
+  alignas(16) uint8_t bsf[DQ_STAGES][512];
+  // epilogue staging boxes: 1024-byte aligned, as the 128-byte swizzle of
+  // the C tensor map is laid out from 1024-byte boundaries
+  alignas(1024) uint8_t cst[4][32 * 128];
   alignas(8) uint64_t full[DQ_STAGES];
   alignas(8) uint64_t conv[DQ_STAGES];
   alignas(8) uint64_t empty[DQ_STAGES];
@@ -984,11 +992,14 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
                          &g_gemm_wait_error))
             break;
           const uint32_t full = smem_addr(&s.full[st]);
-          mbar_arrive_expect_tx(full, DQ_M * 128 + DQ_N * DQ_KE);
+          mbar_arrive_expect_tx(full, DQ_M * 128 + DQ_N * DQ_KE + 512);
           tma_load_2d(smem_addr(s.a[st]), &tmap_a, (int32_t)(kt * DQ_KE),
                       (int32_t)m0, full);
           tma_load_2d(smem_addr(s.braw[st]), &tmap_b, (int32_t)(kt * DQ_KE),
                       (int32_t)n0, full);
+          bulk_g2s(smem_addr(s.bsf[st]),
+                   p.b_sf + ((n0 / 128) * p.b_sf_ct + kt / 2) * 512, 512u,
+                   full);
         }
         if (s.abort) break;
       }
@@ -1052,7 +1063,6 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     int64_t it = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-      const int64_t n0 = (t % p.tiles_n) * DQ_N;
       for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
         const int st = (int)(it % DQ_STAGES);
         const uint32_t ph = (uint32_t)((it / DQ_STAGES) & 1);
@@ -1073,10 +1083,13 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           for (int j = 0; j < 4; ++j)
             if (cc == j) cv[j] = v;
         }
-        // E8M0 scales of the row's two 32-value blocks of this stage
-        const int64_t kb = kt * 2;
-        const float s0 = e8m0_scale(p.b_sf[swz_offset(n0 + n, kb, p.b_sf_ct)]);
-        const float s1 = e8m0_scale(p.b_sf[swz_offset(n0 + n, kb + 1, p.b_sf_ct)]);
+        // E8M0 scales of the row's two 32-value blocks of this stage, from
+        // the staged swizzled tile: row n at (n % 32) * 16 + (n / 32) * 4,
+        // block column 2 (kt % 2) and 2 (kt % 2) + 1
+        const uint8_t* sft = s.bsf[st] + (n & 31) * 16 + (n >> 5) * 4 +
+                             2 * (int)(kt & 1);
+        const float s0 = e8m0_scale(sft[0]);
+        const float s1 = e8m0_scale(sft[1]);
         uint8_t* row = s.b[st] + n * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
