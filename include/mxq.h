@@ -269,7 +269,8 @@ mxq_status nvfp4_quantize_weight_shared_noalloc(
 /*                                                                       */
 /* y = bf16_RNE( fp32( E4M3(code) * 2^(scale - 127) ) ), blocks of 32      */
 /* along each row.  Exact for codes produced from bf16 data, except that  */
-/* a block of bf16-max magnitude overflows to +-inf (2^128).              */
+/* a block of bf16-max magnitude overflows to +-inf (2^128).  The E8M0   */
+/* NaN byte 0xFF and the E4M3 NaN codes 0x7F / 0xFF decode to NaN.        */
 /* codes u8 [rows x cols]; scales logical [rows x cols/32] in              */
 /* scale_layout; y bf16 [rows x cols].  Dequantize the columnwise copy by */
 /* passing (col_codes_t, col_scales_t, K, M): the result is X^T.          */

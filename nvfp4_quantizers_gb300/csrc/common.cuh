@@ -171,10 +171,12 @@ __device__ __forceinline__ float e8m0_inv_scale(uint32_t s) {
   return __uint_as_float((254u - s) << 23);
 }
 
-// 2^k for the E8M0 byte s in [0, 254] (2^-127 is the f32 subnormal
-// 0x00400000).
+// 2^(s - 127) for the E8M0 byte s in [0, 254] (2^-127 is the f32
+// subnormal 0x00400000); NaN for 0xFF.
 __device__ __forceinline__ float e8m0_scale(uint32_t s) {
-  return s == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(s << 23);
+  return s == 0     ? __uint_as_float(0x00400000u)
+         : s == 255 ? __uint_as_float(0x7FC00000u)   // E8M0 NaN
+                    : __uint_as_float(s << 23);
 }
 
 // ---------------------------------------------------------------------------

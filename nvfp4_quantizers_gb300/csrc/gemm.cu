@@ -883,27 +883,30 @@ cudaError_t launch_moe_gate_up_swiglu(
 // columnwise copy of a forward operand), Bq[k, n] = E4M3(code) * 2^(s-127),
 // exact in bf16.  fp32 accumulation in tensor memory, fp32 C.
 //
-// Design: persistent, one CTA per SM, 128 x 128 output tiles, 11 warps.
+// Design: persistent, one CTA per SM, 128 x 128 output tiles, 23 warps.
 // Warp 0 lane 0 streams K-stages of 64 values into a 5-deep ring: the A
 // tile (bf16, 128-byte rows, 128-byte swizzle) and the B^T code tile
 // (128 rows x 64 bytes, unswizzled) by 2-D TMA, and the 512-byte scale
-// tile holding the stage's E8M0 columns by a bulk copy (reading the
-// scales from global memory in the converters stalled every stage on
-// their latency: 218 us for the linear layer's data gradient).  Warps 7-10 (one thread
-// per B row) turn the codes into bf16 in the stage's B buffer, in the
-// 128-byte-swizzled K-major layout the tensor core reads, then fence the
-// writes to the async proxy and count themselves on the stage's
-// "converted" barrier.  Warp 2 waits for both and hands the stage to warp
-// 1, whose lane 0 issues four kind::f16 MMAs (K = 16 each) and commits;
-// warps 3-6 take the accumulator to registers, release it and store C in
-// 32 x 32 fp32 boxes by TMA.  Every wait is bounded.
+// tile holding the stage's E8M0 columns by a bulk copy.  Warps 7-22, in
+// two groups of 8 for the even and the odd stages (two threads per B row,
+// 32 values each), turn the codes into bf16 in the
+// stage's B buffer, in the 128-byte-swizzled K-major layout the tensor
+// core reads, then fence the writes to the async proxy and count
+// themselves on the stage's "converted" barrier.  The bf16 values come
+// from integer bit moves and packed bf16 multiplies by powers of two, in
+// an order free of shared-memory bank conflicts on both the code reads
+// and the bf16 writes.  Warp 2 waits for both barriers and hands the stage
+// to warp 1, whose lane 0 issues four kind::f16 MMAs (K = 16 each) and
+// commits; warps 3-6 take the accumulator 32 columns at a time to
+// registers, release it after the last, and store C in 32 x 32 fp32 boxes
+// by TMA.  Every wait is bounded.
 // ---------------------------------------------------------------------------
 namespace {
 
 constexpr int DQ_M = 128, DQ_N = 128;
 constexpr int DQ_KE = 64;                 // K values per stage
 constexpr int DQ_STAGES = 5;
-constexpr int DQ_THREADS = 32 * 11;
+constexpr int DQ_THREADS = 32 * 23;
 constexpr uint32_t kDqTmemCols = 128;
 
 struct alignas(1024) DqSmem {
@@ -950,6 +953,85 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d, uint64_t adesc,
       : "memory");
 }
 
+// Sixteen E4M3 codes with one E8M0 scale s -> sixteen bf16
+// RNE_bf16(E4M3(c) * 2^(s - 127)), packed in pairs (element 0 low), without
+// the conversion pipe.  A code's sign moved to bit 15 and its other seven
+// bits moved up by four form the bf16 E4M3(c) * 2^-120 exactly (the E4M3
+// exponent lands in the low four bits of the bf16 exponent field, the
+// mantissa in the top three mantissa bits; subnormal codes land on bf16
+// subnormals of the same scale).  One or two packed bf16 multiplies by
+// powers of two then give the scaled value with one rounding: 2^(s - 7)
+// when that is a bf16 (s <= 134), else 2^120 (exact) then 2^(s - 127).
+// The product has at most four significant bits, so its binary32 value is
+// exact whenever finite and rounding it once to bf16 equals the binary32
+// multiply followed by the bf16 conversion; overflow gives inf on both
+// routes.  The E8M0 NaN byte 0xFF multiplies by a bf16 NaN; chunks holding
+// an E4M3 NaN code (S.1111.111) take the conversion instructions instead.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ void e4m3x16_scale_bf16(const uint4 v, uint32_t sb,
+                                                   uint32_t (&w)[8]) {
+  const uint32_t cw[4] = {v.x, v.y, v.z, v.w};
+  uint32_t nan = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    nan |= ((cw[i] & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+  if (__builtin_expect(nan != 0, 0)) {
+    const float sc = e8m0_scale(sb);
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      float x0, x1;
+      e4m3x2_to_f32((cw[h >> 1] >> ((h & 1) * 16)) & 0xFFFFu, x0, x1);
+      fmul2(x0, x1, sc, sc, x0, x1);
+      w[h] = f32x2_to_bf16x2(x0, x1);
+    }
+    return;
+  }
+  const bool one = sb <= 134u;
+  const uint32_t f1 = (one ? sb + 120u : 247u) << 7;
+  const uint32_t f2 = one ? (127u << 7) : sb < 255u ? sb << 7 : 0x7FC0u;
+  const uint32_t f1x2 = f1 | (f1 << 16), f2x2 = f2 | (f2 << 16);
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    // codes 2h, 2h + 1 into the low bytes of the two 16-bit halves, each
+    // high byte filled with copies of its code's sign bit (the permute's
+    // sign-replicating selectors); shifted up by four, the mask keeps the
+    // sign at bit 15 and the seven other code bits at bits 4-10
+    uint32_t t;
+    if ((h & 1) == 0)
+      asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(cw[h >> 1]), "n"(0x9180));
+    else
+      asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(cw[h >> 1]), "n"(0xB3A2));
+    w[h] = (t << 4) & 0x87F087F0u;
+  }
+  if (one) {
+#pragma unroll
+    for (int h = 0; h < 8; ++h) w[h] = bf16x2_mul(w[h], f1x2);
+  } else {
+#pragma unroll
+    for (int h = 0; h < 8; ++h) w[h] = bf16x2_mul(bf16x2_mul(w[h], f1x2), f2x2);
+  }
+}
+
+// Position in the stage ring, advanced once per K-stage: slot, phase
+// parity of the slot's barriers, and the stage's parity.
+struct RingPos {
+  int st = 0;
+  uint32_t ph = 0;
+  int par = 0;
+  __device__ __forceinline__ void next() {
+    par ^= 1;
+    if (++st == DQ_STAGES) {
+      st = 0;
+      ph ^= 1;
+    }
+  }
+};
+
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     gemm_bf16_dq_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b,
@@ -964,7 +1046,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < DQ_STAGES; ++i) {
       mbar_init(smem_addr(&s.full[i]), 1);
-      mbar_init(smem_addr(&s.conv[i]), 4);          // converter warps
+      mbar_init(smem_addr(&s.conv[i]), 8);          // converter warps
       mbar_init(smem_addr(&s.empty[i]), 1);
     }
     mbar_init(smem_addr(&s.acc_full), 1);
@@ -981,15 +1063,15 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- producer ----------------
-      int64_t it = 0;
+      RingPos rp;
       for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
         const int64_t m0 = (t / p.tiles_n) * DQ_M;
         const int64_t n0 = (t % p.tiles_n) * DQ_N;
-        for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
-          const int st = (int)(it % DQ_STAGES);
-          const uint32_t ph = (uint32_t)((it / DQ_STAGES) & 1);
-          if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1, &s.abort,
-                         &g_gemm_wait_error))
+        for (int64_t kt = 0; kt < p.k_stages; ++kt, rp.next()) {
+          const int st = rp.st;
+          const uint32_t ph = rp.ph;
+          if (!mbar_wait_sleep(smem_addr(&s.empty[st]), ph ^ 1, &s.abort,
+                               &g_gemm_wait_error))
             break;
           const uint32_t full = smem_addr(&s.full[st]);
           mbar_arrive_expect_tx(full, DQ_M * 128 + DQ_N * DQ_KE + 512);
@@ -1006,10 +1088,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    int64_t it = 0;
+    RingPos rp;
     bool aborted = false;
     for (int64_t t = blockIdx.x; t < p.n_tiles && !aborted; t += gridDim.x) {
-      for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
+      for (int64_t kt = 0; kt < p.k_stages; ++kt, rp.next()) {
         __syncwarp();
         if (stage_handoff(false)) {
           aborted = true;
@@ -1017,7 +1099,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         }
         if (lane == 0) {
           tc_fence_after();
-          const int st = (int)(it % DQ_STAGES);
+          const int st = rp.st;
           const uint32_t a_addr = smem_addr(s.a[st]);
           const uint32_t b_addr = smem_addr(s.b[st]);
           // four MMAs of K = 16 bf16 values (32 bytes of each row)
@@ -1034,21 +1116,22 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     }
   } else if (warp == 2) {
     // ---------------- waiter ----------------
-    int64_t it = 0;
+    RingPos rp;
     int local = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++local) {
       if (lane == 0)
-        ok = mbar_wait(smem_addr(&s.acc_empty), (uint32_t)((local & 1) ^ 1),
-                       &s.abort, &g_gemm_wait_error);
-      for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
-        const int st = (int)(it % DQ_STAGES);
-        const uint32_t ph = (uint32_t)((it / DQ_STAGES) & 1);
+        ok = mbar_wait_sleep(smem_addr(&s.acc_empty),
+                             (uint32_t)((local & 1) ^ 1), &s.abort,
+                             &g_gemm_wait_error);
+      for (int64_t kt = 0; kt < p.k_stages; ++kt, rp.next()) {
+        const int st = rp.st;
+        const uint32_t ph = rp.ph;
         if (lane == 0 && ok)
-          ok = mbar_wait(smem_addr(&s.full[st]), ph, &s.abort,
-                         &g_gemm_wait_error) &&
-               mbar_wait(smem_addr(&s.conv[st]), ph, &s.abort,
-                         &g_gemm_wait_error);
+          ok = mbar_wait_sleep(smem_addr(&s.full[st]), ph, &s.abort,
+                               &g_gemm_wait_error) &&
+               mbar_wait_sleep(smem_addr(&s.conv[st]), ph, &s.abort,
+                               &g_gemm_wait_error);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         __syncwarp();
         if (stage_handoff(!ok)) {
@@ -1058,53 +1141,48 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       }
     }
   } else if (warp >= 7) {
-    // ---------------- converters: warps 7-10, one thread per B row -------
-    const int n = threadIdx.x - 7 * 32;               // 0 .. 127
-    int64_t it = 0;
+    // ---------------- converters: warps 7-22 ----------------
+    // Two groups of 8 warps take the even and the odd stages, so two
+    // stages are converted at once.  In a group, two threads per B row:
+    // thread ct: row n = ct % 128, half hc = ct / 128.  It converts the
+    // code chunks 2 hh and 2 hh + 1 of its row (32 values, one E8M0 block),
+    // hh = hc ^ p(n), in the order c ^ g(n): with p(n) = 1 for n % 8 in
+    // {0, 1, 4, 5} and g(n) = 1 for n % 8 in {2, 3, 4, 5}, the 8 lanes of
+    // every shared-memory phase read 8 different bank groups of the code
+    // tile (64-byte rows) and write 8 different bank groups of the
+    // swizzled bf16 tile (chunk j of row n at j ^ (n % 8)).
+    const int grp = (warp - 7) >> 3;                  // stage parity
+    const int ct = threadIdx.x - 7 * 32 - grp * 256;  // 0 .. 255
+    const int n = ct & 127;
+    const int hh = (ct >> 7) ^ ((0x33 >> (n & 7)) & 1);
+    const int g = (0x3C >> (n & 7)) & 1;
+    RingPos rp;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-      for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
-        const int st = (int)(it % DQ_STAGES);
-        const uint32_t ph = (uint32_t)((it / DQ_STAGES) & 1);
+      for (int64_t kt = 0; kt < p.k_stages; ++kt, rp.next()) {
+        if (rp.par != grp) continue;
+        const int st = rp.st;
+        const uint32_t ph = rp.ph;
         if (lane == 0)
-          ok = mbar_wait(smem_addr(&s.full[st]), ph, &s.abort,
-                         &g_gemm_wait_error);
+          ok = mbar_wait_sleep(smem_addr(&s.full[st]), ph, &s.abort,
+                               &g_gemm_wait_error);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        // the row's 64 codes, chunk order rotated by n / 2 so that the 8
-        // lanes of a shared-memory phase read 8 different bank groups
-        uint4 cv[4];
-        const uint8_t* raw = s.braw[st] + n * DQ_KE;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int cc = (c + (n >> 1)) & 3;
-          const uint4 v = *reinterpret_cast<const uint4*>(raw + cc * 16);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (cc == j) cv[j] = v;
-        }
-        // E8M0 scales of the row's two 32-value blocks of this stage, from
+        // the E8M0 scale of the row's 32-value block hh of this stage, from
         // the staged swizzled tile: row n at (n % 32) * 16 + (n / 32) * 4,
-        // block column 2 (kt % 2) and 2 (kt % 2) + 1
-        const uint8_t* sft = s.bsf[st] + (n & 31) * 16 + (n >> 5) * 4 +
-                             2 * (int)(kt & 1);
-        const float s0 = e8m0_scale(sft[0]);
-        const float s1 = e8m0_scale(sft[1]);
+        // block column 2 (kt % 2) + hh
+        const uint32_t sb =
+            s.bsf[st][(n & 31) * 16 + (n >> 5) * 4 + 2 * (int)(kt & 1) + hh];
+        const uint8_t* raw = s.braw[st] + n * DQ_KE;
         uint8_t* row = s.b[st] + n * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float sc = c < 2 ? s0 : s1;
-          const uint32_t cw[4] = {cv[c].x, cv[c].y, cv[c].z, cv[c].w};
+        for (int c = 0; c < 2; ++c) {
+          const int cc = 2 * hh + (c ^ g);              // code chunk
+          const uint4 v = *reinterpret_cast<const uint4*>(raw + cc * 16);
           uint32_t w[8];
-#pragma unroll
-          for (int h = 0; h < 8; ++h) {
-            float x0, x1;
-            e4m3x2_to_f32((cw[h >> 1] >> ((h & 1) * 16)) & 0xFFFFu, x0, x1);
-            fmul2(x0, x1, sc, sc, x0, x1);
-            w[h] = f32x2_to_bf16x2(x0, x1);
-          }
-          // 16-byte chunks 2c and 2c+1 of the row, 128-byte swizzle
-          const int q0 = (2 * c) ^ (n & 7), q1 = (2 * c + 1) ^ (n & 7);
+          e4m3x16_scale_bf16(v, sb, w);
+          // bf16 chunks 2 cc and 2 cc + 1 of the row, 128-byte swizzle
+          const int q0 = (2 * cc) ^ (n & 7), q1 = (2 * cc + 1) ^ (n & 7);
           *reinterpret_cast<uint4*>(row + q0 * 16) =
               make_uint4(w[0], w[1], w[2], w[3]);
           *reinterpret_cast<uint4*>(row + q1 * 16) =
@@ -1117,39 +1195,43 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     }
   } else {
     // ---------------- epilogue: warps 3-6 ----------------
+    // 32 accumulator columns at a time (32 registers): each 32 x 32 box
+    // goes tensor memory -> registers -> swizzled staging -> TMA store; the
+    // accumulator is released once its last columns are in registers.
     const int q = warp & 3;                           // tensor-memory quarter
     uint8_t* box = s.cst[warp - 3];
+    uint8_t* rowp = box + lane * 128;
     int local = 0;
     for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++local) {
+      // a tile's whole main loop passes here: sleep, and leave the issue
+      // slots to the converter warps on the same schedulers
       const bool ok = __all_sync(
           0xffffffffu,
-          mbar_wait(smem_addr(&s.acc_full), (uint32_t)(local & 1), &s.abort,
-                    &g_gemm_wait_error));
+          mbar_wait_sleep(smem_addr(&s.acc_full), (uint32_t)(local & 1),
+                          &s.abort, &g_gemm_wait_error));
       if (!ok) break;
       tc_fence_after();
-      uint32_t r[128];
       const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tc_ld_32x32_async(lane_base + (uint32_t)(c * 32), r + c * 32);
-      tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&s.acc_empty));
       const int64_t m0 = (t / p.tiles_n) * DQ_M;
       const int64_t n0 = (t % p.tiles_n) * DQ_N;
-      uint8_t* rowp = box + lane * 128;
-#pragma unroll
       for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc_ld_32x32_async(lane_base + (uint32_t)(c * 32), r);
+        tc_wait_ld();
+        if (c == 3) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&s.acc_empty));
+        }
         if (lane == 0) bulk_wait_read_0();              // the box's last store
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           float4 v;
-          v.x = __uint_as_float(r[c * 32 + 4 * j]);
-          v.y = __uint_as_float(r[c * 32 + 4 * j + 1]);
-          v.z = __uint_as_float(r[c * 32 + 4 * j + 2]);
-          v.w = __uint_as_float(r[c * 32 + 4 * j + 3]);
+          v.x = __uint_as_float(r[4 * j]);
+          v.y = __uint_as_float(r[4 * j + 1]);
+          v.z = __uint_as_float(r[4 * j + 2]);
+          v.w = __uint_as_float(r[4 * j + 3]);
           *reinterpret_cast<float4*>(rowp + ((j ^ (lane & 7)) << 4)) = v;
         }
         fence_proxy_async_smem();

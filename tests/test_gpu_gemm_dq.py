@@ -63,3 +63,39 @@ def test_linear_dgrad_shape(mxq):
     rows = np.union1d(np.random.default_rng(3).choice(2048, 62, replace=False),
                       [0, 2047])
     _case(mxq, 2048, 8192, 2048, seed=9, rows=rows)
+
+
+def test_in_smem_dequantization_exact(mxq):
+    """A = I (bf16 ones on the diagonal): every C[m, n] is one product
+    1 x Bq[m, n] plus zeros, so C must equal the oracle's bf16
+    dequantization of B bit for bit -- a check of the operand the tensor
+    core read, value by value.  Every E4M3 code but the NaN pair, scales
+    from 2^-117 to 2^119 (bf16-normal products, no overflow), with rows
+    pinned on both sides of the one-multiply limit (exponent byte 134/135)
+    and at the ends of the range."""
+    M = K = 256
+    N = 384
+    rng = np.random.default_rng(21)
+    codes = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x00
+    codes[4, :254] = np.setdiff1d(np.arange(256), [0x7F, 0xFF]).astype(np.uint8)
+    scales = rng.integers(10, 247, (N, K // 32), dtype=np.uint8)
+    scales[0], scales[1], scales[2], scales[3] = 134, 135, 10, 246
+    # NaN sources: the E8M0 NaN byte on row 5, an E4M3 NaN code on row 6;
+    # with A = I every row of C sums over them, so columns 5 and 6 of C are
+    # NaN throughout
+    scales[5, 2] = 0xFF
+    codes[6, 77] = 0x7F
+    A = np.where(np.eye(M, K, dtype=bool), 0x3F80, 0).astype(np.uint16)
+    C = mxq.gemm_bf16_mxfp8(dev_bf16(A), torch.from_numpy(codes).cuda(),
+                            torch.from_numpy(O.scale_swizzle(scales)).cuda())
+    torch.cuda.synchronize()
+    assert mxq.get_last_error() == mxq.MXQ_OK
+    want = W.bits_to_f32(O.mxfp8_dequantize(codes, scales)).T
+    assert np.isnan(want[64:96, 5]).all() and np.isnan(want[77, 6])
+    got = C.cpu().numpy()
+    assert np.isnan(got[:, 5:7]).all()
+    got[:, 5:7] = want[:, 5:7] = 0
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, (len(bad), bad[:5], got[tuple(bad[0])],
+                           want[tuple(bad[0])])

@@ -75,6 +75,31 @@ def check_mxfp8(q, x_bits, lay, rowwise=True, colwise=True, dequant=True,
 
 
 @pytest.mark.parametrize("lay", LAYOUTS)
+def test_mxfp8_dequant_every_code_and_scale(mxq, lay):
+    """Dequantization of arbitrary bytes: all 256 codes (the E4M3 NaN pair
+    included) under every E8M0 byte 0..255 (0xFF = NaN), 2^-127 subnormal
+    and 2^127-overflow corners included.  Non-NaN outputs bit for bit, NaN
+    where the oracle has NaN."""
+    rows, cols = 256, 8192
+    codes = np.tile(np.arange(256, dtype=np.uint8), (rows, cols // 256))
+    codes = np.random.default_rng(31).permuted(codes, axis=1)
+    scales = np.tile(np.arange(256, dtype=np.uint8)[:, None], (1, cols // 32))
+    sdev = exp_scales(scales, lay)
+    y = mxq.dequantize_mxfp8(torch.from_numpy(codes).cuda(),
+                             torch.from_numpy(np.ascontiguousarray(sdev)).cuda(),
+                             lay)
+    torch.cuda.synchronize()
+    got = host_bits(y)
+    want = O.mxfp8_dequantize(codes, scales)
+    nan_g = (got & 0x7FFF) > 0x7F80
+    nan_w = (want & 0x7FFF) > 0x7F80
+    assert np.array_equal(nan_g, nan_w)
+    assert nan_w[255].all() and nan_w[:255][(codes[:255] & 0x7F) != 0x7F].sum() == 0
+    assert_bytes_equal(np.where(nan_g, 0, got), np.where(nan_w, 0, want),
+                       f"dequant of every code and scale [{lay}]")
+
+
+@pytest.mark.parametrize("lay", LAYOUTS)
 def test_mxfp8_small_case_rowwise(mxq, lay):
     """[256 x 512] N(0,1) with boundary / power-of-two / ulp-edge / zero /
     bf16-max rows; rowwise quantize + dequantize."""
