@@ -155,23 +155,6 @@ cudaError_t make_tmap_2d_bytes(CUtensorMap* map, const void* base,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t make_tmap_2d_bytes_plain(CUtensorMap* map, const void* base,
-                                     uint64_t inner, uint64_t outer,
-                                     uint64_t outer_stride_bytes,
-                                     uint32_t box_inner, uint32_t box_outer) {
-  EncodeTiledFn fn = encode_tiled_fn();
-  if (!fn) return cudaErrorNotSupported;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {outer_stride_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base),
-                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 }  // namespace mxq
 
 using namespace mxq;

@@ -883,39 +883,37 @@ cudaError_t launch_moe_gate_up_swiglu(
 // columnwise copy of a forward operand), Bq[k, n] = E4M3(code) * 2^(s-127),
 // exact in bf16.  fp32 accumulation in tensor memory, fp32 C.
 //
-// Design: persistent, one CTA per SM, 128 x 128 output tiles, 23 warps.
-// Warp 0 lane 0 streams K-stages of 64 values into a 5-deep ring: the A
-// tile (bf16, 128-byte rows, 128-byte swizzle) and the B^T code tile
-// (128 rows x 64 bytes, unswizzled) by 2-D TMA, and the 512-byte scale
-// tile holding the stage's E8M0 columns by a bulk copy.  Warps 7-22, in
-// two groups of 8 for the even and the odd stages (two threads per B row,
-// 32 values each), turn the codes into bf16 in the
-// stage's B buffer, in the 128-byte-swizzled K-major layout the tensor
-// core reads, then fence the writes to the async proxy and count
-// themselves on the stage's "converted" barrier.  The bf16 values come
-// from integer bit moves and packed bf16 multiplies by powers of two, in
-// an order free of shared-memory bank conflicts on both the code reads
-// and the bf16 writes.  Warp 2 waits for both barriers and hands the stage
-// to warp 1, whose lane 0 issues four kind::f16 MMAs (K = 16 each) and
-// commits; warps 3-6 take the accumulator 32 columns at a time to
-// registers, release it after the last, and store C in 32 x 32 fp32 boxes
-// by TMA.  Every wait is bounded.
+// Design: persistent, one CTA per SM, 256 x 128 output tiles computed as
+// two 128 x 128 accumulators that share one converted B tile (so each B
+// value is converted once per 256 rows of A), 23 warps, a 4-deep ring of
+// K-stages of 64 values.  Warp 0 lane 0 loads a stage's A tile (bf16, 256
+// rows of 128 bytes, 128-byte swizzle) by 2-D TMA.  Warps 7-22, in two
+// groups of 8 for the even and the odd stages (two threads per B row, 32
+// values each), read the B^T codes and E8M0 scales from global memory one
+// own stage ahead and, once the stage's slot is free, write the bf16
+// values into its B buffer in the 128-byte-swizzled K-major layout the
+// tensor core reads; then they fence the writes to the async proxy and
+// count themselves on the stage's "converted" barrier.  The bf16 values
+// come from integer bit moves and packed bf16 multiplies by powers of two,
+// in an order free of shared-memory bank conflicts.  Warp 2 waits for the
+// A tile and the conversion and hands the stage to warp 1, whose lane 0
+// issues eight kind::f16 MMAs (K = 16 each, four per accumulator) and
+// commits; warps 3-6 take the accumulators 32 columns at a time to
+// registers, release them after the last, and store C in 32 x 32 fp32
+// boxes by TMA.  Every wait is bounded.
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr int DQ_M = 128, DQ_N = 128;
+constexpr int DQ_M = 128, DQ_N = 128;     // one MMA / accumulator
+constexpr int DQ_MT = 2 * DQ_M;           // rows of A per tile
 constexpr int DQ_KE = 64;                 // K values per stage
-constexpr int DQ_STAGES = 5;
+constexpr int DQ_STAGES = 4;
 constexpr int DQ_THREADS = 32 * 23;
-constexpr uint32_t kDqTmemCols = 128;
+constexpr uint32_t kDqTmemCols = 256;     // two 128 x 128 fp32 accumulators
 
 struct alignas(1024) DqSmem {
-  uint8_t a[DQ_STAGES][DQ_M * 128];       // bf16, 128-byte swizzled rows
+  uint8_t a[DQ_STAGES][DQ_MT * 128];      // bf16, 128-byte swizzled rows
   uint8_t b[DQ_STAGES][DQ_N * 128];       // bf16 from the codes, same layout
-  uint8_t braw[DQ_STAGES][DQ_N * DQ_KE];  // E4M3 codes, 64-byte rows
-  // the 512-byte swizzled E8M0 tile (128 rows x 4 blocks of 32) holding
-  // the stage's two scale columns
-  alignas(16) uint8_t bsf[DQ_STAGES][512];
   // epilogue staging boxes: 1024-byte aligned, as the 128-byte swizzle of
   // the C tensor map is laid out from 1024-byte boundaries
   alignas(1024) uint8_t cst[4][32 * 128];
@@ -932,6 +930,7 @@ struct DqParams {
   int64_t M, N, K;
   int64_t k_stages;
   int64_t tiles_n, n_tiles;
+  const uint8_t* b_codes;                 // E4M3 codes of B^T [N x K]
   const uint8_t* b_sf;                    // swizzled E8M0 of B^T [N x K/32]
   int64_t b_sf_ct;                        // scale column tiles, ceil(K/128)
 };
@@ -1034,7 +1033,6 @@ struct RingPos {
 
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     gemm_bf16_dq_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                        const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_c,
                         const __grid_constant__ DqParams p) {
   extern __shared__ uint8_t dsmem_raw[];
@@ -1065,8 +1063,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       // ---------------- producer ----------------
       RingPos rp;
       for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
-        const int64_t m0 = (t / p.tiles_n) * DQ_M;
-        const int64_t n0 = (t % p.tiles_n) * DQ_N;
+        const int64_t m0 = (t / p.tiles_n) * DQ_MT;
         for (int64_t kt = 0; kt < p.k_stages; ++kt, rp.next()) {
           const int st = rp.st;
           const uint32_t ph = rp.ph;
@@ -1074,14 +1071,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
                                &g_gemm_wait_error))
             break;
           const uint32_t full = smem_addr(&s.full[st]);
-          mbar_arrive_expect_tx(full, DQ_M * 128 + DQ_N * DQ_KE + 512);
+          mbar_arrive_expect_tx(full, DQ_MT * 128);
+          // two boxes of 128 rows; rows past M (M % 256 == 128) read as 0
           tma_load_2d(smem_addr(s.a[st]), &tmap_a, (int32_t)(kt * DQ_KE),
                       (int32_t)m0, full);
-          tma_load_2d(smem_addr(s.braw[st]), &tmap_b, (int32_t)(kt * DQ_KE),
-                      (int32_t)n0, full);
-          bulk_g2s(smem_addr(s.bsf[st]),
-                   p.b_sf + ((n0 / 128) * p.b_sf_ct + kt / 2) * 512, 512u,
-                   full);
+          tma_load_2d(smem_addr(s.a[st]) + DQ_M * 128, &tmap_a,
+                      (int32_t)(kt * DQ_KE), (int32_t)(m0 + DQ_M), full);
         }
         if (s.abort) break;
       }
@@ -1102,12 +1097,18 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           const int st = rp.st;
           const uint32_t a_addr = smem_addr(s.a[st]);
           const uint32_t b_addr = smem_addr(s.b[st]);
-          // four MMAs of K = 16 bf16 values (32 bytes of each row)
+          // per K = 16 bf16 values (32 bytes of each row), one MMA per
+          // 128-row half of A into its accumulator (columns 128 h), both on
+          // the same converted B
           for (int j = 0; j < 4; ++j) {
-            const uint64_t ad = smem_desc(a_addr + j * 32, 16, 1024, 2);
             const uint64_t bd = smem_desc(b_addr + j * 32, 16, 1024, 2);
-            tc_mma_f16(tmem, ad, bd, idesc_bf16(),
-                       (kt > 0 || j > 0) ? 1u : 0u);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint64_t ad =
+                  smem_desc(a_addr + h * DQ_M * 128 + j * 32, 16, 1024, 2);
+              tc_mma_f16(tmem + (uint32_t)(h * DQ_N), ad, bd, idesc_bf16(),
+                         (kt > 0 || j > 0) ? 1u : 0u);
+            }
           }
           tc_commit(smem_addr(&s.empty[st]));
           if (kt == p.k_stages - 1) tc_commit(smem_addr(&s.acc_full));
@@ -1148,50 +1149,87 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     // code chunks 2 hh and 2 hh + 1 of its row (32 values, one E8M0 block),
     // hh = hc ^ p(n), in the order c ^ g(n): with p(n) = 1 for n % 8 in
     // {0, 1, 4, 5} and g(n) = 1 for n % 8 in {2, 3, 4, 5}, the 8 lanes of
-    // every shared-memory phase read 8 different bank groups of the code
-    // tile (64-byte rows) and write 8 different bank groups of the
-    // swizzled bf16 tile (chunk j of row n at j ^ (n % 8)).
+    // every shared-memory phase write 8 different bank groups of the
+    // swizzled bf16 tile (chunk j of row n at j ^ (n % 8)).  The codes and
+    // the scale byte come straight from global memory (L2), loaded one own
+    // stage ahead; a stage's conversion waits only for its slot to be
+    // released by the MMAs, not for the A tile.
     const int grp = (warp - 7) >> 3;                  // stage parity
     const int ct = threadIdx.x - 7 * 32 - grp * 256;  // 0 .. 255
     const int n = ct & 127;
     const int hh = (ct >> 7) ^ ((0x33 >> (n & 7)) & 1);
     const int g = (0x3C >> (n & 7)) & 1;
-    RingPos rp;
-    bool ok = true;
-    for (int64_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-      for (int64_t kt = 0; kt < p.k_stages; ++kt, rp.next()) {
-        if (rp.par != grp) continue;
-        const int st = rp.st;
-        const uint32_t ph = rp.ph;
-        if (lane == 0)
-          ok = mbar_wait_sleep(smem_addr(&s.full[st]), ph, &s.abort,
-                               &g_gemm_wait_error);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        // the E8M0 scale of the row's 32-value block hh of this stage, from
-        // the staged swizzled tile: row n at (n % 32) * 16 + (n / 32) * 4,
-        // block column 2 (kt % 2) + hh
-        const uint32_t sb =
-            s.bsf[st][(n & 31) * 16 + (n >> 5) * 4 + 2 * (int)(kt & 1) + hh];
-        const uint8_t* raw = s.braw[st] + n * DQ_KE;
-        uint8_t* row = s.b[st] + n * 128;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int cc = 2 * hh + (c ^ g);              // code chunk
-          const uint4 v = *reinterpret_cast<const uint4*>(raw + cc * 16);
-          uint32_t w[8];
-          e4m3x16_scale_bf16(v, sb, w);
-          // bf16 chunks 2 cc and 2 cc + 1 of the row, 128-byte swizzle
-          const int q0 = (2 * cc) ^ (n & 7), q1 = (2 * cc + 1) ^ (n & 7);
-          *reinterpret_cast<uint4*>(row + q0 * 16) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(row + q1 * 16) =
-              make_uint4(w[4], w[5], w[6], w[7]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&s.conv[st]));
+    const int sf_in_tile = (n & 31) * 16 + (n >> 5) * 4 + hh;
+    // (t, kt) advanced by d K-stages along this CTA's tile sequence
+    auto advance = [&](int64_t& t_, int64_t& kt_, int d) {
+      kt_ += d;
+      while (kt_ >= p.k_stages) {
+        kt_ -= p.k_stages;
+        t_ += gridDim.x;
       }
+    };
+    // the row's codes and its scales' tile row, set when the tile changes
+    // (loads run in tile order)
+    int64_t cur_t = -1;
+    const uint8_t* crow = nullptr;
+    const uint8_t* srow = nullptr;
+    auto load = [&](int64_t t_, int64_t kt_, uint4& c0, uint4& c1,
+                    uint32_t& sbv) {
+      if (t_ != cur_t) {
+        cur_t = t_;
+        const int64_t nrow = (t_ % p.tiles_n) * DQ_N + n;
+        crow = p.b_codes + nrow * p.K + hh * 32;
+        srow = p.b_sf + (nrow >> 7) * p.b_sf_ct * 512 + sf_in_tile;
+      }
+      const uint8_t* src = crow + kt_ * DQ_KE;
+      c0 = ld_stream_v4(src + g * 16);
+      c1 = ld_stream_v4(src + (g ^ 1) * 16);
+      // swizzled scale tile (nrow / 128, kt / 2): block column 2 (kt % 2) + hh
+      sbv = __ldg(srow + (kt_ >> 1) * 512 + 2 * (int)(kt_ & 1));
+    };
+    RingPos rp;
+    if (grp) rp.next();
+    int64_t t = blockIdx.x, kt = 0;
+    advance(t, kt, grp);
+    uint4 cv0 = make_uint4(0, 0, 0, 0), cv1 = cv0;
+    uint32_t sb = 0;
+    if (t < p.n_tiles) load(t, kt, cv0, cv1, sb);
+    while (t < p.n_tiles) {
+      const int st = rp.st;
+      bool ok = true;
+      if (lane == 0)
+        ok = mbar_wait_sleep(smem_addr(&s.empty[st]), rp.ph ^ 1, &s.abort,
+                             &g_gemm_wait_error);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      int64_t t2 = t, kt2 = kt;
+      advance(t2, kt2, 2);
+      uint4 nv0 = cv0, nv1 = cv1;
+      uint32_t nsb = sb;
+      if (t2 < p.n_tiles) load(t2, kt2, nv0, nv1, nsb);
+      uint8_t* row = s.b[st] + n * 128;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int cc = 2 * hh + (c ^ g);                // code chunk
+        uint32_t w[8];
+        e4m3x16_scale_bf16(c == 0 ? cv0 : cv1, sb, w);
+        // bf16 chunks 2 cc and 2 cc + 1 of the row, 128-byte swizzle
+        const int q0 = (2 * cc) ^ (n & 7), q1 = (2 * cc + 1) ^ (n & 7);
+        *reinterpret_cast<uint4*>(row + q0 * 16) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(row + q1 * 16) =
+            make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&s.conv[st]));
+      cv0 = nv0;
+      cv1 = nv1;
+      sb = nsb;
+      t = t2;
+      kt = kt2;
+      rp.next();
+      rp.next();
     }
   } else {
     // ---------------- epilogue: warps 3-6 ----------------
@@ -1212,13 +1250,16 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-      const int64_t m0 = (t / p.tiles_n) * DQ_M;
+      const int64_t m0 = (t / p.tiles_n) * DQ_MT;
       const int64_t n0 = (t % p.tiles_n) * DQ_N;
-      for (int c = 0; c < 4; ++c) {
+      // chunk c: accumulator h = c / 4 (rows m0 + 128 h + 32 q + lane),
+      // columns 32 (c % 4) ..; a half past M is not stored
+      const int nc = (m0 + DQ_M < p.M) ? 8 : 4;
+      for (int c = 0; c < 8; ++c) {
         uint32_t r[32];
         tc_ld_32x32_async(lane_base + (uint32_t)(c * 32), r);
         tc_wait_ld();
-        if (c == 3) {
+        if (c == 7) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&s.acc_empty));
@@ -1236,9 +1277,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmap_c, smem_addr(box), (int32_t)(n0 + c * 32),
-                       (int32_t)(m0 + q * 32));
+        if (lane == 0 && c < nc) {
+          tma_store_2d(&tmap_c, smem_addr(box), (int32_t)(n0 + (c & 3) * 32),
+                       (int32_t)(m0 + (c >> 2) * DQ_M + q * 32));
           bulk_commit();
         }
       }
@@ -1263,12 +1304,9 @@ cudaError_t launch_gemm_bf16_mxfp8(const void* a, int64_t lda,
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  CUtensorMap ta, tb, tc;
+  CUtensorMap ta, tc;
   err = make_tmap_2d_bf16(&ta, a, (uint64_t)K, (uint64_t)M, (uint64_t)lda * 2,
                           DQ_KE, DQ_M, true);
-  if (err != cudaSuccess) return err;
-  err = make_tmap_2d_bytes_plain(&tb, bt_codes, (uint64_t)K, (uint64_t)N,
-                                 (uint64_t)K, DQ_KE, DQ_N);
   if (err != cudaSuccess) return err;
   err = make_tmap_c(&tc, C, M, N, ldc);
   if (err != cudaSuccess) return err;
@@ -1278,7 +1316,8 @@ cudaError_t launch_gemm_bf16_mxfp8(const void* a, int64_t lda,
   p.K = K;
   p.k_stages = K / DQ_KE;
   p.tiles_n = N / DQ_N;
-  p.n_tiles = (M / DQ_M) * p.tiles_n;
+  p.n_tiles = ((M + DQ_MT - 1) / DQ_MT) * p.tiles_n;
+  p.b_codes = bt_codes;
   p.b_sf = bt_scales;
   p.b_sf_ct = (K / 32 + 3) / 4;
   const size_t smem = sizeof(DqSmem) + 1024;
@@ -1293,7 +1332,7 @@ cudaError_t launch_gemm_bf16_mxfp8(const void* a, int64_t lda,
   }
   const int64_t grid = imin<int64_t>(p.n_tiles, sm_count(dev));
   return launch_pdl(gemm_bf16_dq_kernel, dim3((unsigned)grid),
-                    dim3(DQ_THREADS), smem, stream, false, ta, tb, tc, p);
+                    dim3(DQ_THREADS), smem, stream, false, ta, tc, p);
 }
 
 }  // namespace mxq

@@ -23,11 +23,6 @@ cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base,
                               uint64_t inner, uint64_t outer,
                               uint64_t outer_stride_bytes, uint32_t box_inner,
                               uint32_t box_outer, bool swizzle128);
-// byte matrix, no swizzle.
-cudaError_t make_tmap_2d_bytes_plain(CUtensorMap* map, const void* base,
-                                     uint64_t inner, uint64_t outer,
-                                     uint64_t outer_stride_bytes,
-                                     uint32_t box_inner, uint32_t box_outer);
 // fp32 matrix, 128-byte swizzle (box_inner * 4 <= 128).
 cudaError_t make_tmap_2d_f32(CUtensorMap* map, const void* base,
                              uint64_t inner, uint64_t outer,
