@@ -24,8 +24,8 @@
 // CTA per 128x128 block in a grid-stride loop, 64 values per thread held
 // in registers across the block reduction.  Dequantizer: one 16-code unit
 // per thread per step, one 32-byte store.  Conversion: all of a thread's
-// code loads issued before it decodes, and four columns quantized per
-// step so their reductions overlap.
+// code loads issued before it decodes, and eight columns quantized per
+// step with one reduce-scatter for all of them.
 #include <float.h>
 
 #include "common.cuh"
@@ -208,70 +208,123 @@ __global__ void __launch_bounds__(FB_THREADS)
 }
 
 // Backward-orientation conversion: tile (ti, tj) of X [M x K] is dequantized
-// into shared memory transposed (column-major bf16, row pitch 136), then
-// each of its 128 columns is quantized as one 1x128 tile of X^T: a warp
-// takes 16 columns, four at a time, a lane 4 rows of each, so every code
-// store is 128 contiguous bytes per warp.  (A thread per column, with no
-// cross-lane reduction, measured slower: its 16-byte stores land in 32
-// different rows of X^T.)
+// into shared memory transposed (column-major bf16, column pitch 136
+// halfwords), then each of its 128 columns is quantized as one 1x128 tile
+// of X^T.
+//   Dequantize: a thread takes two adjacent rows and 32 columns and writes
+//   each column's pair of rows as one 32-bit word (consecutive lanes hold
+//   consecutive row pairs: no bank conflicts); its loads of the CTA's next
+//   tile are issued right after, so they are in flight while this tile is
+//   quantized.
+//   Quantize: a warp takes 16 columns, 8 at a time, a lane 4 rows of each,
+//   so every code store is 128 contiguous bytes per warp.  The 8 column
+//   maxima are reduced together by a reduce-scatter over the lanes (lane
+//   bits 4, 3, 2 select the half of the remaining columns a lane keeps: 4
+//   + 2 + 1 exchanges, then two for the last lane bits), which leaves the
+//   maximum of column (lane / 4) % 8 in lanes 4j .. 4j + 3; each lane then
+//   derives the scales of that one column (one IEEE divide and reciprocal
+//   per lane instead of per column and lane), and the encoders fetch the
+//   8 reciprocals by shuffle.  (A thread per column, with no cross-lane
+//   reduction, measured slower: its 16-byte stores land in 32 different
+//   rows of X^T.)
 constexpr int kPitch = 136;
+constexpr int kPitchW = kPitch / 2;       // 32-bit words per column
 
 __global__ void __launch_bounds__(FB_THREADS)
     fp8blk_requant_t_kernel(const uint8_t* __restrict__ codes,
                             const float* __restrict__ scales, int64_t M,
                             int64_t K, uint8_t* __restrict__ codes_t,
                             float* __restrict__ scales_t) {
-  __shared__ __align__(16) uint16_t sm[128 * kPitch];
+  __shared__ __align__(16) uint32_t sm[128 * kPitchW];
   const int64_t nti = M >> 7, ntj = K >> 7;
   const int64_t ntiles = nti * ntj;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rr = threadIdx.x & 127, cc = (threadIdx.x >> 7) * 64;
-  pdl_wait();
+  const int pr = threadIdx.x & 63;                  // row pair 2 pr, 2 pr + 1
+  const int cq = (threadIdx.x >> 6) * 32;           // 32-column quarter
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  const int mycol = (lane >> 2) & 7;                // column whose scales
+  pdl_wait();                                       // this lane derives
+  // the codes and scales of this thread's two rows of a tile; the next
+  // tile's are loaded while the current one is quantized
+  uint4 cv[4];
+  float S0 = 0.0f, S1 = 0.0f;
+  auto load_tile = [&](int64_t tile) {
+    const int64_t ti = tile / ntj, tj = tile - ti * ntj;
+    const int64_t ra = ti * 128 + 2 * pr;
+    S0 = scales[ra * ntj + tj];
+    S1 = scales[(ra + 1) * ntj + tj];
+    const uint8_t* src = codes + ra * K + tj * 128 + cq;
+    cv[0] = ld_stream_v4(src);
+    cv[1] = ld_stream_v4(src + 16);
+    cv[2] = ld_stream_v4(src + K);
+    cv[3] = ld_stream_v4(src + K + 16);
+  };
+  if ((int64_t)blockIdx.x < ntiles) load_tile(blockIdx.x);
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const int64_t ti = tile / ntj, tj = tile - ti * ntj;
     const int64_t r0 = ti * 128, c0 = tj * 128;
-    // dequantize row r0 + rr, columns c0 + cc .. + 63, into sm[col][row]
-    const float S = scales[(r0 + rr) * ntj + tj];
-    const uint8_t* src = codes + (r0 + rr) * K + c0 + cc;
-    uint4 cv[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) cv[k] = ld_stream_v4(src + k * 16);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint4 lo, hi;
-      decode16(cv[k], S, lo, hi);
-      const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    for (int k = 0; k < 2; ++k) {                   // 16-column halves
+      uint4 lo0, hi0, lo1, hi1;
+      decode16(cv[k], S0, lo0, hi0);
+      decode16(cv[2 + k], S1, lo1, hi1);
+      const uint32_t w0[8] = {lo0.x, lo0.y, lo0.z, lo0.w,
+                              hi0.x, hi0.y, hi0.z, hi0.w};
+      const uint32_t w1[8] = {lo1.x, lo1.y, lo1.z, lo1.w,
+                              hi1.x, hi1.y, hi1.z, hi1.w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const int col = cc + k * 16 + 2 * e;
-        sm[col * kPitch + rr] = (uint16_t)(w[e] & 0xFFFFu);
-        sm[(col + 1) * kPitch + rr] = (uint16_t)(w[e] >> 16);
+        const int col = cq + 16 * k + 2 * e;
+        // column col: (row 2 pr, row 2 pr + 1) = the low halves
+        sm[col * kPitchW + pr] = __byte_perm(w0[e], w1[e], 0x5410);
+        sm[(col + 1) * kPitchW + pr] = __byte_perm(w0[e], w1[e], 0x7632);
       }
     }
+    if (tile + gridDim.x < ntiles) load_tile(tile + gridDim.x);
     __syncthreads();
-    for (int q0 = 0; q0 < 16; q0 += 4) {       // 4 independent columns
-      uint2 v[4];
-      uint32_t m[4];
+#pragma unroll 1
+    for (int q0 = 0; q0 < 16; q0 += 8) {
+      const int cbase = warp * 16 + q0;
+      uint2 v[8];
+      uint32_t m[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int col = warp * 16 + q0 + j;
-        v[j] = *reinterpret_cast<const uint2*>(&sm[col * kPitch + 4 * lane]);
+      for (int j = 0; j < 8; ++j) {
+        v[j] = *reinterpret_cast<const uint2*>(
+            &sm[(cbase + j) * kPitchW + 2 * lane]);
         m[j] = bf16x2_hmax(bf16x2_maxabs(v[j].x, v[j].y) & 0x7FFF7FFFu);
       }
+      // reduce-scatter of the 8 column maxima (bf16 bit patterns of
+      // non-negative values order like the values)
+      uint32_t r4[4], r2[2], r1;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t send = b4 ? m[k] : m[k + 4];
+        const uint32_t keep = b4 ? m[k + 4] : m[k];
+        r4[k] = max(keep, __shfl_xor_sync(FULL, send, 16));
+      }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) m[j] = max(m[j], __shfl_xor_sync(FULL, m[j], o));
+      for (int k = 0; k < 2; ++k) {
+        const uint32_t send = b3 ? r4[k] : r4[k + 2];
+        const uint32_t keep = b3 ? r4[k + 2] : r4[k];
+        r2[k] = max(keep, __shfl_xor_sync(FULL, send, 8));
+      }
+      {
+        const uint32_t send = b2 ? r2[0] : r2[1];
+        const uint32_t keep = b2 ? r2[1] : r2[0];
+        r1 = max(keep, __shfl_xor_sync(FULL, send, 4));
+      }
+      r1 = max(r1, __shfl_xor_sync(FULL, r1, 2));
+      r1 = max(r1, __shfl_xor_sync(FULL, r1, 1));
+      float S2, enc;
+      fb_scales(r1, S2, enc);
+      if ((lane & 3) == 0) scales_t[(c0 + cbase + mycol) * nti + ti] = S2;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int col = warp * 16 + q0 + j;
-        float S2, enc;
-        fb_scales(m[j], S2, enc);
-        const uint32_t word = bf16x2_scale_e4m3x2(v[j].x, enc, enc) |
-                              (bf16x2_scale_e4m3x2(v[j].y, enc, enc) << 16);
-        *reinterpret_cast<uint32_t*>(codes_t + (c0 + col) * M + r0 + 4 * lane) =
-            word;
-        if (lane == 0) scales_t[(c0 + col) * nti + ti] = S2;
+      for (int j = 0; j < 8; ++j) {
+        const float ej = __shfl_sync(FULL, enc, 4 * j);
+        const uint32_t word = bf16x2_scale_e4m3x2(v[j].x, ej, ej) |
+                              (bf16x2_scale_e4m3x2(v[j].y, ej, ej) << 16);
+        *reinterpret_cast<uint32_t*>(codes_t + (c0 + cbase + j) * M + r0 +
+                                     4 * lane) = word;
       }
     }
     __syncthreads();                    // sm is rewritten by the next tile
@@ -331,7 +384,8 @@ cudaError_t launch_fp8blk_requant_t(const uint8_t* codes, const float* scales,
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   const int64_t ntiles = (M >> 7) * (K >> 7);
-  const unsigned grid = fb_grid(ntiles, 1, dev, 6);
+  // 4 resident CTAs per SM (63 registers x 256 threads)
+  const unsigned grid = fb_grid(ntiles, 1, dev, 4);
   return launch_pdl(fp8blk_requant_t_kernel, dim3(grid), dim3(FB_THREADS), 0,
                     stream, false, codes, scales, M, K, codes_t, scales_t);
 }
