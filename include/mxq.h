@@ -397,7 +397,9 @@ mxq_status mxq_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
 /* A bf16 [M x K] (row stride lda elements, lda >= K, lda % 8 == 0), B    */
 /* given as B^T [N x K]: MXFP8 codes (bt_codes, row stride K) and swizzled */
 /* E8M0 scales (bt_scales, 1x32 blocks along K) -- the columnwise copy of */
-/* a [K x N] forward tensor; Bq = E4M3(code) * 2^(s - 127), exact in bf16. */
+/* a [K x N] forward tensor; Bq = bf16_RNE(E4M3(code) * 2^(s - 127)),    */
+/* bit-identical to dequantize_mxfp8 (exact unless the product leaves     */
+/* bf16's normal range; the E8M0 byte 0xFF and E4M3 NaN codes give NaN).  */
 /* The bf16 values of B are formed in shared memory only.  fp32            */
 /* accumulation, fp32 C [M x N] (ldc >= N, ldc % 4 == 0).                  */
 /* M % 128 == 0, N % 128 == 0, K % 64 == 0.                               */
