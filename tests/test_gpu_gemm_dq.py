@@ -99,3 +99,36 @@ def test_in_smem_dequantization_exact(mxq):
     bad = np.argwhere(got != want)
     assert bad.size == 0, (len(bad), bad[:5], got[tuple(bad[0])],
                            want[tuple(bad[0])])
+
+
+def test_strided_a_and_wide_c(mxq):
+    """A as a column slice of a wider matrix (lda = K + 64) and C written
+    with ldc = N + 32 through the C ABI: the product lands in C's first N
+    columns, the 32 padding columns keep their sentinel."""
+    M, K, N = 256, 512, 256
+    rng = np.random.default_rng(17)
+    wide = W.to_bf16_bits(rng.standard_normal((M, K + 64)).astype(np.float32))
+    A = np.ascontiguousarray(wide[:, :K])
+    Bw = W.to_bf16_bits((0.05 * rng.standard_normal((K, N))).astype(np.float32))
+    bc, bs = O.mxfp8_quantize_colwise(Bw)
+    a_dev = dev_bf16(wide)[:, :K]
+    assert a_dev.stride(0) == K + 64
+    codes = torch.from_numpy(bc).cuda()
+    scales = torch.from_numpy(O.scale_swizzle(bs)).cuda()
+    ldc = N + 32
+    C = torch.full((M, ldc), -7.0, dtype=torch.float32, device="cuda")
+    st = mxq.lib().mxq_gemm_bf16_mxfp8(a_dev.data_ptr(), a_dev.stride(0),
+                                        codes.data_ptr(), scales.data_ptr(),
+                                        M, N, K, C.data_ptr(), ldc,
+                                        torch.cuda.current_stream().cuda_stream)
+    assert st == mxq.MXQ_OK
+    torch.cuda.synchronize()
+    assert mxq.get_last_error() == mxq.MXQ_OK
+    got = C.cpu().numpy()
+    assert np.all(got[:, N:] == -7.0)
+    ref = O.gemm_bf16_mxfp8(A, bc, bs)
+    assert rel_fro(got[:, :N].astype(np.float64), ref) <= 1e-4
+    # the binding passes the slice's row stride as lda
+    C2 = mxq.gemm_bf16_mxfp8(a_dev, codes, scales)
+    torch.cuda.synchronize()
+    assert np.array_equal(C2.cpu().numpy(), got[:, :N])
