@@ -128,7 +128,10 @@ __device__ __forceinline__ uint32_t sr_e2m1(float v, float u) {
   return idx | (neg << 3);
 }
 
-__global__ void __launch_bounds__(RS_THREADS, 2)
+// SR is a template parameter: without stochastic rounding the kernel needs
+// no Philox state and fits 4 CTAs per SM instead of 2.
+template <bool SR>
+__global__ void __launch_bounds__(RS_THREADS, SR ? 2 : 4)
     nvfp4_rht_sr_kernel(const uint16_t* __restrict__ x, int64_t T,
                         int64_t T_pad, int64_t H, int64_t ldx, uint64_t seed,
                         int flags, uint8_t* __restrict__ codes,
@@ -137,7 +140,8 @@ __global__ void __launch_bounds__(RS_THREADS, 2)
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = ((int64_t)blockIdx.x * RS_THREADS + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * RS_THREADS) >> 5;
-  const bool rht = (flags & 1) != 0, sr = (flags & 2) != 0;
+  const bool rht = (flags & 1) != 0;
+  constexpr bool sr = SR;
   const int64_t nb = H >> 4;
   const int64_t col_tiles = (nb + 3) >> 2;
   const int64_t iters = (nb + 31) >> 5;           // warp-uniform
@@ -267,7 +271,12 @@ cudaError_t launch_nvfp4_rht_sr(const void* x, int64_t T, int64_t H,
   const int64_t cap = (int64_t)sm_count(dev) * 8;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  return launch_pdl(nvfp4_rht_sr_kernel, dim3((unsigned)grid),
+  if (flags & 2)
+    return launch_pdl(nvfp4_rht_sr_kernel<true>, dim3((unsigned)grid),
+                      dim3(RS_THREADS), 0, stream, false,
+                      static_cast<const uint16_t*>(x), T, T_pad, H, ldx, seed,
+                      flags, codes, scales, token_scales, swizzled);
+  return launch_pdl(nvfp4_rht_sr_kernel<false>, dim3((unsigned)grid),
                     dim3(RS_THREADS), 0, stream, false,
                     static_cast<const uint16_t*>(x), T, T_pad, H, ldx, seed,
                     flags, codes, scales, token_scales, swizzled);
