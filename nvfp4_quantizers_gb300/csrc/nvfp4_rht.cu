@@ -67,20 +67,24 @@ __device__ __forceinline__ void philox4x64(uint64_t c0, uint64_t c1,
 }
 
 // The 16 binary32 values of a block from its bf16 words, sign-flipped,
-// butterflied and scaled by 1/4 when rht.
+// butterflied and scaled by 1/4 when rht.  smask[i] holds the signs of
+// values 2i (bit 15) and 2i + 1 (bit 31): they are applied to the packed
+// bf16 words, as a sign flip commutes with the exact widening.
 __device__ __forceinline__ void block_values(const uint4& a, const uint4& b,
-                                             bool rht, uint32_t signs,
+                                             bool rht,
+                                             const uint32_t (&smask)[8],
                                              float (&v)[16]) {
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  if (rht) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] ^= smask[i];
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     v[2 * i] = bf16lo_to_f32(w[i]);
     v[2 * i + 1] = bf16hi_to_f32(w[i]);
   }
   if (!rht) return;
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    v[i] = __uint_as_float(__float_as_uint(v[i]) ^ (((signs >> i) & 1u) << 31));
 #pragma unroll
   for (int h = 1; h < 16; h <<= 1)
 #pragma unroll
@@ -151,6 +155,11 @@ __global__ void __launch_bounds__(RS_THREADS, SR ? 2 : 4)
     philox4x64(0, 0, 0, 0, seed, 1, o);
     signs = (uint32_t)(o[0] & 0xffffu);
   }
+  uint32_t smask[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    smask[i] = (((signs >> (2 * i)) & 1u) << 15) |
+               (((signs >> (2 * i + 1)) & 1u) << 31);
   pdl_wait();
   for (int64_t row = warp_id; row < T_pad; row += nwarps) {
     const bool real = row < T;
@@ -174,7 +183,7 @@ __global__ void __launch_bounds__(RS_THREADS, SR ? 2 : 4)
 #pragma unroll
       for (int k = 0; k < kChunk; ++k) {
         float v[16];
-        block_values(raw[2 * k], raw[2 * k + 1], rht, signs, v);
+        block_values(raw[2 * k], raw[2 * k + 1], rht, smask, v);
         am = fmaxf(am, block_amax(v));
       }
     }
@@ -191,7 +200,7 @@ __global__ void __launch_bounds__(RS_THREADS, SR ? 2 : 4)
       if (real && valid) {
         const uint4 a0 = *reinterpret_cast<const uint4*>(xr + b * 16);
         const uint4 a1 = *reinterpret_cast<const uint4*>(xr + b * 16 + 8);
-        block_values(a0, a1, rht, signs, v);
+        block_values(a0, a1, rht, smask, v);
       } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = 0.0f;
