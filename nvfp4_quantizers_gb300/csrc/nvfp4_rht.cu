@@ -67,9 +67,10 @@ __device__ __forceinline__ void philox4x64(uint64_t c0, uint64_t c1,
 }
 
 // The 16 binary32 values of a block from its bf16 words, sign-flipped,
-// butterflied and scaled by 1/4 when rht.  smask[i] holds the signs of
-// values 2i (bit 15) and 2i + 1 (bit 31): they are applied to the packed
-// bf16 words, as a sign flip commutes with the exact widening.
+// butterflied and, for QUARTER, scaled by 1/4 when rht.  smask[i] holds the
+// signs of values 2i (bit 15) and 2i + 1 (bit 31): they are applied to the
+// packed bf16 words, as a sign flip commutes with the exact widening.
+template <bool QUARTER = true>
 __device__ __forceinline__ void block_values(const uint4& a, const uint4& b,
                                              bool rht,
                                              const uint32_t (&smask)[8],
@@ -94,8 +95,10 @@ __device__ __forceinline__ void block_values(const uint4& a, const uint4& b,
         v[i] = __fadd_rn(x0, x1);
         v[i + h] = __fsub_rn(x0, x1);
       }
+  if (QUARTER) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+    for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+  }
 }
 
 __device__ __forceinline__ float block_amax(const float (&v)[16]) {
@@ -183,12 +186,15 @@ __global__ void __launch_bounds__(RS_THREADS, SR ? 2 : 4)
 #pragma unroll
       for (int k = 0; k < kChunk; ++k) {
         float v[16];
-        block_values(raw[2 * k], raw[2 * k + 1], rht, smask, v);
+        block_values<false>(raw[2 * k], raw[2 * k + 1], rht, smask, v);
         am = fmaxf(am, block_amax(v));
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(FULL, am, o));
+    // pass 1 leaves out the 1/4: rounding is monotone and symmetric, so the
+    // largest |fl(y / 4)| is fl(max |y| / 4), subnormals included
+    if (rht) am = __fmul_rn(am, 0.25f);
     const float S = __fdiv_rn(am, kNvfp4ScaleDenom);
     const float six_s = __fmul_rn(6.0f, S);
     if (real && lane == 0) S_out[row] = S;
