@@ -66,6 +66,28 @@ __device__ __forceinline__ void philox4x64(uint64_t c0, uint64_t c1,
   out[3] = c3;
 }
 
+// Two binary32 values in one 64-bit register pair, and packed add /
+// subtract of two such pairs (two IEEE operations each, round to nearest
+// even, no flush to zero).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t p, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // The 16 binary32 values of a block from its bf16 words, sign-flipped,
 // butterflied and, for QUARTER, scaled by 1/4 when rht.  smask[i] holds the
 // signs of values 2i (bit 15) and 2i + 1 (bit 31): they are applied to the
@@ -86,15 +108,30 @@ __device__ __forceinline__ void block_values(const uint4& a, const uint4& b,
     v[2 * i + 1] = bf16hi_to_f32(w[i]);
   }
   if (!rht) return;
+  // butterflies h = 1, 2, 4 on 64-bit pairs P[i] = (v[i], v[i + 8]): the
+  // partners i ^ h of both halves sit in the same lanes of P[i ^ h], so one
+  // packed add and one packed subtract do two butterflies; then h = 8
+  // inside each pair.  The same IEEE operations in the same order as the
+  // scalar stages.
+  uint64_t P[8];
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1)
+  for (int i = 0; i < 8; ++i) P[i] = pack_f32x2(v[i], v[i + 8]);
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+  for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
       if ((i & h) == 0) {
-        const float x0 = v[i], x1 = v[i + h];
-        v[i] = __fadd_rn(x0, x1);
-        v[i + h] = __fsub_rn(x0, x1);
+        const uint64_t a = P[i], b = P[i + h];
+        P[i] = add_f32x2(a, b);
+        P[i + h] = sub_f32x2(a, b);
       }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float x0, x1;
+    unpack_f32x2(P[i], x0, x1);
+    v[i] = __fadd_rn(x0, x1);
+    v[i + 8] = __fsub_rn(x0, x1);
+  }
   if (QUARTER) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
