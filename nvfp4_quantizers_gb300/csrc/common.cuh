@@ -402,6 +402,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 1-D bulk copy global -> shared of `bytes` bytes (both addresses 16-byte
+// aligned, bytes a multiple of 16), completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src,
+                                         uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Programmatic dependent launch.  Every kernel calls pdl_wait() before its
 // first global-memory access: it returns once the previous kernel on the
 // stream has completed and its writes are visible (and at once when the

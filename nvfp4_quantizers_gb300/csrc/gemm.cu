@@ -14,29 +14,30 @@
 //           sum_k a[r, k] w_e[n, k], where a and w are E2M1 x E4M3 block
 //           values and the two FP32 scales are applied in the epilogue.
 //
-// Design (persistent, one CTA per SM, 128 x 128 output tiles, 7 warps):
-//  * warp 0 lane 0 streams K-stages into a 4-deep shared-memory ring: the
-//    A and B code tiles by 2-D TMA with the 128-byte swizzle (one 128-byte
-//    row per matrix row), and the matching 512-byte scale tiles, which the
-//    quantizers already store in the 128x4 layout the tensor core reads, by
-//    1-D bulk copies; completion on mbarriers.
+// Design (persistent, one CTA per SM, 128 x 256 fp32 output tiles, 11
+// warps, one accumulator):
+//  * warp 0 lane 0 streams K-stages of 128 bytes per row into a 3-deep
+//    shared-memory ring: the A (128 rows) and B (256 rows) code tiles by
+//    2-D TMA with the 128-byte swizzle, and the matching 512-byte scale
+//    tiles, which the quantizers already store in the 128x4 layout the
+//    tensor core reads, by one 1-D bulk copy per 128-row block; completion
+//    on mbarriers.  Every CTA loads its own operands (no clusters).
 //  * warp 2 polls the stage and accumulator barriers and hands each ready
 //    stage to warp 1 through a named barrier, so that the MMA-issuing
 //    thread never waits on shared memory between MMAs;
 //  * warp 1 lane 0 copies each stage's scale tiles into tensor memory
 //    (tcgen05.cp 32x128b.warpx4) and issues the block-scaled MMAs
 //    (tcgen05.mma kind::mxf8f6f4 block_scale, or kind::mxf4nvf4 with
-//    4 E4M3 scales per 64 values); the fp32 accumulator lives in tensor
-//    memory, double-buffered so that the epilogue of one tile overlaps the
-//    MMAs of the next; tcgen05.commit frees each stage when its MMAs are
-//    done and hands each finished accumulator to the epilogue.
-//  * warps 3-6 read the accumulator with tcgen05.ld (each warp its 32-lane
-//    quarter = 32 rows), scale (NVFP4), store fp32 C and release the
-//    accumulator buffer.
+//    4 E4M3 scales per 64 values, N = 256); the 128 x 256 fp32 accumulator
+//    lives in tensor memory; tcgen05.commit frees each stage when its MMAs
+//    are done and hands each finished accumulator to the epilogue.
+//  * warps 3-10 (4 lane quarters x 2 column halves) take the accumulator
+//    into registers (128 values per thread) and release it at once, so the
+//    next tile's MMAs overlap the scaling (NVFP4: S_tok x S_w) and the
+//    stores; C leaves through 32 x 32 fp32 TMA stores from
+//    128-byte-swizzled staging boxes (whole 128-byte rows per global write).
 // Every wait is bounded; on timeout the kernel records the error word and
 // skips the remaining work (still freeing its tensor memory).
-//  * C leaves through 32 x 32 fp32 TMA stores from 128-byte-swizzled
-//    staging boxes (whole 128-byte rows per global write).
 #include "common.cuh"
 #include "launch.h"
 
@@ -170,49 +171,6 @@ __device__ __forceinline__ void tc_ld_32x32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src,
-                                         uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
-      "[%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// 2-D TMA load delivered to the same shared-memory offset (and completing
-// on the same mbarrier offset) in every CTA of the cluster named in mask.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst,
-                                               const CUtensorMap* map,
-                                               int32_t x, int32_t y,
-                                               uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_"
-      "tx::bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar),
-      "h"(mask)
-      : "memory");
-}
-// Arrive on the mbarrier at this offset in every CTA of mask once all
-// previously issued tcgen05 operations of this thread have completed.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
-      "multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA in the cluster.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::
-          : "memory");
-}
 
 // Stage handoff between the waiter warp and the MMA warp: both warps
 // (converged) meet at named barrier 1; the result is the OR of the abort
@@ -321,10 +279,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int64_t tile,
   return t;
 }
 
-// Persistent: cluster c of CL CTAs handles tile groups u = c, c + grid/CL,
-// ...; CTA rank r of the cluster takes tile u * CL + r.  The CL tiles of a
-// group share their A rows (tiles_n is a multiple of CL), so with CL = 2
-// each CTA loads half of the A stage and multicasts it to both.
+// Persistent: CTA b handles tiles b, b + grid, b + 2 grid, ...
 //
 // One 128 x 256 fp32 accumulator in tensor memory.  The eight epilogue
 // warps copy it to registers (128 values per thread) and hand it back to
@@ -336,7 +291,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int64_t tile,
 // B stage holds 128 gate rows and the 128 matching up rows, so one tile
 // gives 128 output columns h = silu(s g) * (s u), s = S_tok x S_w, bf16
 // (binary32 with a fast exponential and divide before the bf16 rounding).
-template <int CL, int EPI>
+template <int EPI>
 __global__ void __launch_bounds__(GTHREADS, 1)
     gemm_block_scaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
                              const __grid_constant__ CUtensorMap tmap_b,
@@ -351,8 +306,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < GSTAGES; ++i) {
       mbar_init(smem_addr(&s.full[i]), 1);
-      // freed by the MMA commits of every CTA that writes this slot
-      mbar_init(smem_addr(&s.empty[i]), CL);
+      mbar_init(smem_addr(&s.empty[i]), 1);   // freed by the MMA commit
     }
     mbar_init(smem_addr(&s.acc_full), 1);
     mbar_init(smem_addr(&s.acc_empty), kEpiWarps);
@@ -362,14 +316,9 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // The peer's multicast loads and commits target this CTA's barriers:
-  // they must be initialised cluster-wide before anyone issues one.
-  if (CL > 1) cluster_sync();
   const uint32_t tmem = s.tmem_base;
-  const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
-  const uint16_t cmask = (uint16_t)((1u << CL) - 1u);
-  const int64_t n_units = p.n_tiles / CL;
-  const int64_t unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
+  const int64_t n_units = p.n_tiles;
+  const int64_t unit0 = blockIdx.x, unit_step = gridDim.x;
   pdl_wait();
 
   const int n_sf = p.kind == 1 ? 4 : 1;  // scale tiles per stage and row block
@@ -380,7 +329,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       int64_t it = 0;
       int grp_cursor = 0;
       for (int64_t u = unit0; u < n_units; u += unit_step) {
-        const Tile t = decode_tile(p, u * CL + crank, &grp_cursor);
+        const Tile t = decode_tile(p, u, &grp_cursor);
         // B row blocks of this tile that exist (the last column tile may
         // hold only 128 columns); rows past them are never stored.
         const int nrb = (EPI == 1 || t.n0 + 128 < p.N) ? 2 : 1;
@@ -394,15 +343,8 @@ __global__ void __launch_bounds__(GTHREADS, 1)
             break;
           const uint32_t full = smem_addr(&s.full[st]);
           mbar_arrive_expect_tx(full, stage_bytes);
-          if (CL == 1) {
-            tma_load_2d(smem_addr(s.a[st]), &tmap_a, (int32_t)(kt * GKB),
-                        (int32_t)t.m0, full);
-          } else {
-            // rows [crank * 64, crank * 64 + 64) of the A stage, to both CTAs
-            tma_load_2d_mc(smem_addr(s.a[st]) + crank * (GM / CL) * GKB,
-                           &tmap_a, (int32_t)(kt * GKB),
-                           (int32_t)(t.m0 + crank * (GM / CL)), full, cmask);
-          }
+          tma_load_2d(smem_addr(s.a[st]), &tmap_a, (int32_t)(kt * GKB),
+                      (int32_t)t.m0, full);
           const int64_t brow = t.grp * p.b_rows_group_stride + t.n0;
           if (EPI == 0) {
             tma_load_2d(smem_addr(s.b[st]), &tmap_b, (int32_t)(kt * GKB),
@@ -431,15 +373,6 @@ __global__ void __launch_bounds__(GTHREADS, 1)
           }
         }
         if (s.abort) break;
-      }
-      if (CL > 1) {
-        // Wait until both CTAs' MMAs have released every slot, so that no
-        // commit from the peer is still headed for this CTA's barriers
-        // when it exits.
-        for (int64_t j = it > GSTAGES ? it - GSTAGES : 0; j < it; ++j)
-          mbar_wait(smem_addr(&s.empty[j % GSTAGES]),
-                    (uint32_t)((j / GSTAGES) & 1), &s.abort,
-                    &g_gemm_wait_error);
       }
     }
   } else if (warp == 1) {
@@ -495,10 +428,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
                           sf_col + j * 4, sf_col + 16 + j * 8, acc);
             }
           }
-          if (CL == 1)
-            tc_commit(smem_addr(&s.empty[st]));
-          else
-            tc_commit_mc(smem_addr(&s.empty[st]), cmask);
+          tc_commit(smem_addr(&s.empty[st]));
           if (kt == p.k_stages - 1) tc_commit(smem_addr(&s.acc_full));
         }
       }
@@ -572,7 +502,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&s.acc_empty));
 
-      const Tile t = decode_tile(p, u * CL + crank, &grp_cursor);
+      const Tile t = decode_tile(p, u, &grp_cursor);
       float rs = 1.0f;
       if (p.kind == 1)
         rs = __fmul_rn(p.s_tok[t.m0 + q * 32 + lane], p.s_w[t.grp]);
@@ -650,7 +580,6 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (CL > 1) cluster_sync();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
   pdl_launch_dependents();
 }
@@ -677,58 +606,7 @@ struct AOperand {
   int64_t row_bytes, rows;
 };
 
-template <int CL, int EPI>
-cudaError_t launch_gemm_cl(const AOperand& a, const CUtensorMap& tb,
-                           const CUtensorMap& tc, const GemmParams& pp,
-                           int dev, cudaStream_t stream) {
-  auto kern = gemm_block_scaled_kernel<CL, EPI>;
-  const size_t smem = gemm_smem_bytes();
-  static int configured[64] = {};
-  static int max_clusters[64] = {};
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(GTHREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = CL;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = CL > 1 ? 2 : 1;
-  if (!configured[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    int n = sm_count(dev) / CL;
-    if (CL > 1) {
-      // clusters that fit on the GPU at once (GPCs may leave SMs unpaired)
-      cfg.gridDim = dim3((unsigned)(n * CL));
-      int fit = 0;
-      if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess &&
-          fit > 0)
-        n = imin(n, fit);
-      else
-        cudaGetLastError();
-    }
-    max_clusters[dev] = n;
-    configured[dev] = 1;
-  }
-  CUtensorMap ta;
-  cudaError_t err = make_tmap_2d_u8(&ta, a.base, (uint64_t)a.row_bytes,
-                                    (uint64_t)a.rows, (uint64_t)a.row_bytes,
-                                    (uint32_t)(GM / CL));
-  if (err != cudaSuccess) return err;
-  const int64_t units = imin<int64_t>(pp.n_tiles / CL, max_clusters[dev]);
-  cfg.gridDim = dim3((unsigned)(units * CL));
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, pp);
-}
-
-// Tiles of one row block are paired across a 2-CTA cluster when the
-// column-tile count is even; otherwise one CTA per cluster.
+// One CTA per SM (or per tile when there are fewer tiles).
 template <int EPI>
 cudaError_t launch_gemm(const AOperand& a, const CUtensorMap& tb,
                         const CUtensorMap& tc, const GemmParams& p,
@@ -736,11 +614,25 @@ cudaError_t launch_gemm(const AOperand& a, const CUtensorMap& tb,
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   GemmParams pp = p;
   pp.n_tiles = tiles;
-  if (p.tiles_n % 2 == 0)
-    return launch_gemm_cl<2, EPI>(a, tb, tc, pp, dev, stream);
-  return launch_gemm_cl<1, EPI>(a, tb, tc, pp, dev, stream);
+  auto kern = gemm_block_scaled_kernel<EPI>;
+  const size_t smem = gemm_smem_bytes();
+  static int configured[64] = {};
+  if (!configured[dev]) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+    if (err != cudaSuccess) return err;
+    configured[dev] = 1;
+  }
+  CUtensorMap ta;
+  err = make_tmap_2d_u8(&ta, a.base, (uint64_t)a.row_bytes, (uint64_t)a.rows,
+                        (uint64_t)a.row_bytes, (uint32_t)GM);
+  if (err != cudaSuccess) return err;
+  const int64_t grid = imin<int64_t>(tiles, sm_count(dev));
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(GTHREADS), smem, stream,
+                    false, ta, tb, tc, pp);
 }
 
 // Grouped NVFP4 parameters shared by the plain and the SwiGLU GEMM.
