@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import concurrent.futures as cf
+import ctypes
 import json
 import os
 import statistics
@@ -42,18 +43,25 @@ METRIC = ("quantize GB/s and % of GB300 HBM peak (bytes in + codes/scales "
           "out), bit-exact")
 UNIT = "GB/s"
 M, K = 8192, 4096
-PAIRS = 4                       # X viewed as 4 gate/up pairs
-PART_ROWS = M // (2 * PAIRS)    # 1024 rows per part
+# For the weight quantizer X is viewed as [16384 x 2048] (the MoE layer's
+# hidden size as K): 8 gate/up pairs of two [1024 x 2048] parts, each pair
+# under one FP32 scale.
+WK = 2048
+PAIRS = 8
+PART_ROWS = M * K // WK // (2 * PAIRS)    # 1024 rows per part
 WORKLOAD = ("MXFP8 rowwise+columnwise quantize (one pass) + both MXFP8 "
             "dequantizes + NVFP4 per-token quantize/dequantize + NVFP4 "
             "shared-scale weight quantize/dequantize of an activation "
-            "[8192 x 4096] bf16, N(0,1) with 0.1% entries x100")
+            "[8192 x 4096] bf16, N(0,1) with 0.1% entries x100 (as weights: "
+            "8 gate/up pairs of [1024 x 2048] parts)")
 
 
 # --------------------------------------------------------------------------
 # Algorithmic bytes per operation.
 # --------------------------------------------------------------------------
 def op_bytes():
+    """Algorithmic bytes of each of the step's operations, in the order the
+    per-kernel pass runs them."""
     n = M * K
     return {
         "mxfp8_quantize_rowcol": n * 2 + 2 * (n + n // 32),
@@ -193,8 +201,8 @@ def run_gpu(args):
             "tc": torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
             "ts": torch.empty(q.scale_bytes(M, K // 16), dtype=torch.uint8, device=dev),
             "tS": torch.empty(M, dtype=torch.float32, device=dev),
-            "wc": torch.empty((PAIRS, 2 * PART_ROWS, K // 2), dtype=torch.uint8, device=dev),
-            "ws": torch.empty((PAIRS, q.scale_bytes(2 * PART_ROWS, K // 16)), dtype=torch.uint8, device=dev),
+            "wc": torch.empty((PAIRS, 2 * PART_ROWS, WK // 2), dtype=torch.uint8, device=dev),
+            "ws": torch.empty((PAIRS, q.scale_bytes(2 * PART_ROWS, WK // 16)), dtype=torch.uint8, device=dev),
             "wS": torch.empty(PAIRS, dtype=torch.float32, device=dev),
         }
 
@@ -202,14 +210,13 @@ def run_gpu(args):
     y_row = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
     y_col = torch.empty((K, M), dtype=torch.bfloat16, device=dev)
     y_tok = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
-    y_w = torch.empty((PAIRS, 2 * PART_ROWS, K), dtype=torch.bfloat16, device=dev)
+    y_w = torch.empty((PAIRS, 2 * PART_ROWS, WK), dtype=torch.bfloat16, device=dev)
     L = q.lib()
     ws_bytes = int(L.nvfp4_quantize_weight_shared_workspace_size(PAIRS))
     wsp = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    import ctypes
     parts_tabs = []
     for xi in X:
-        flat = xi.view(2 * PAIRS, PART_ROWS, K)
+        flat = xi.view(2 * PAIRS, PART_ROWS, WK)
         parts_tabs.append((ctypes.c_void_p * (2 * PAIRS))(
             *[flat[i].data_ptr() for i in range(2 * PAIRS)]))
     rows_tab = (ctypes.c_int64 * 2)(PART_ROWS, PART_ROWS)
@@ -229,102 +236,144 @@ def run_gpu(args):
             raise RuntimeError(f"{what}: {q.status_string(st)}")
 
     names = list(op_bytes().keys())
-    ev = None
+    SIDE = {"nvfp4_quantize_per_token": 0, "dequantize_nvfp4_tokens": 0,
+            "nvfp4_quantize_weight_shared": 1, "dequantize_nvfp4_weights": 1}
 
-    def step(i, record=None, only=None, concurrent=False):
-        o_new, o_old = outs[i % 2], outs[(i + 1) % 2]
-        s1, s2 = (s_side[0], s_side[1]) if concurrent else (s, s)
-        x0, x1, x2 = X[i % 3], X[(i + 1) % 3], X[(i + 2) % 3]
-        tab = parts_tabs[(i + 2) % 3]
+    def phase_table(ph):
+        """The step's operations for buffer phase ph (outputs alternate over
+        2 sets, inputs over 3): name -> (C function, arguments on the main
+        stream, arguments on the operation's side stream).  Built once, so
+        that a step costs the host only its launches."""
+        o_new, o_old = outs[ph % 2], outs[(ph + 1) % 2]
+        x0, x1 = X[ph % 3], X[(ph + 1) % 3]
+        tab = parts_tabs[(ph + 2) % 3]
+        t = {}
 
-        def mark(j):
-            if record is None:
-                return
-            if only is None:
-                record[j].record(stream)
-            elif j in only:
-                record[only.index(j)].record(stream)
-        mark(0)
-        chk(L.mxfp8_quantize_rowcol(x0.data_ptr(), M, K, K, o_new["rc"].data_ptr(),
-                                    o_new["rs"].data_ptr(), o_new["cc"].data_ptr(),
-                                    o_new["cs"].data_ptr(), lay, s), "rowcol")
-        mark(1)
-        if concurrent:
-            ev_fork.record(stream)
-            side[0].wait_event(ev_fork)
-            side[1].wait_event(ev_fork)
-        chk(L.dequantize_mxfp8(o_old["rc"].data_ptr(), o_old["rs"].data_ptr(), M, K,
-                               lay, y_row.data_ptr(), s), "dq row")
-        mark(2)
-        chk(L.dequantize_mxfp8(o_old["cc"].data_ptr(), o_old["cs"].data_ptr(), K, M,
-                               lay, y_col.data_ptr(), s), "dq col")
-        mark(3)
-        def token_q():
-            chk(L.nvfp4_quantize_per_token(
-                x1.data_ptr(), M, K, K, o_new["tc"].data_ptr(),
-                o_new["ts"].data_ptr(), o_new["tS"].data_ptr(), lay, s1),
-                "per-token")
+        def add(nm, fn, mk):
+            side_s = s_side[SIDE[nm]] if nm in SIDE else s
+            t[nm] = (fn, mk(s), mk(side_s))
+        add("mxfp8_quantize_rowcol", L.mxfp8_quantize_rowcol, lambda st: (
+            x0.data_ptr(), M, K, K, o_new["rc"].data_ptr(),
+            o_new["rs"].data_ptr(), o_new["cc"].data_ptr(),
+            o_new["cs"].data_ptr(), lay, st))
+        add("dequantize_mxfp8_row", L.dequantize_mxfp8, lambda st: (
+            o_old["rc"].data_ptr(), o_old["rs"].data_ptr(), M, K, lay,
+            y_row.data_ptr(), st))
+        add("dequantize_mxfp8_col", L.dequantize_mxfp8, lambda st: (
+            o_old["cc"].data_ptr(), o_old["cs"].data_ptr(), K, M, lay,
+            y_col.data_ptr(), st))
+        add("nvfp4_quantize_per_token", L.nvfp4_quantize_per_token,
+            lambda st: (x1.data_ptr(), M, K, K, o_new["tc"].data_ptr(),
+                        o_new["ts"].data_ptr(), o_new["tS"].data_ptr(), lay,
+                        st))
+        add("dequantize_nvfp4_tokens", L.dequantize_nvfp4, lambda st: (
+            o_old["tc"].data_ptr(), o_old["ts"].data_ptr(),
+            o_old["tS"].data_ptr(), q.S_PER_ROW, 1, M, K, lay,
+            y_tok.data_ptr(), st))
+        add("nvfp4_quantize_weight_shared", L.nvfp4_quantize_weight_shared,
+            lambda st: (PAIRS, 2, ctypes.cast(tab, ctypes.c_void_p),
+                        ctypes.cast(rows_tab, ctypes.c_void_p), WK,
+                        o_new["wc"].data_ptr(), o_new["ws"].data_ptr(),
+                        o_new["wS"].data_ptr(), None, lay, wsp.data_ptr(),
+                        wsp.numel(), st))
+        add("dequantize_nvfp4_weights", L.dequantize_nvfp4, lambda st: (
+            o_old["wc"].data_ptr(), o_old["ws"].data_ptr(),
+            o_old["wS"].data_ptr(), q.S_PER_BATCH, PAIRS, 2 * PART_ROWS, WK,
+            lay, y_w.data_ptr(), st))
+        return t
 
-        def token_dq():
-            chk(L.dequantize_nvfp4(o_old["tc"].data_ptr(), o_old["ts"].data_ptr(),
-                                   o_old["tS"].data_ptr(), q.S_PER_ROW, 1, M, K,
-                                   lay, y_tok.data_ptr(), s1), "dq tokens")
+    tables = [phase_table(ph) for ph in range(6)]
 
-        def weights_q():
-            chk(L.nvfp4_quantize_weight_shared(
-                PAIRS, 2, ctypes.cast(tab, ctypes.c_void_p),
-                ctypes.cast(rows_tab, ctypes.c_void_p), K,
-                o_new["wc"].data_ptr(), o_new["ws"].data_ptr(),
-                o_new["wS"].data_ptr(), None, lay, wsp.data_ptr(), wsp.numel(),
-                s2), "weights")
+    def launch(fn, a, nm):
+        st = fn(*a)
+        if st != 0:
+            raise RuntimeError(f"{nm}: {q.status_string(st)}")
 
-        def weights_dq():
-            chk(L.dequantize_nvfp4(o_old["wc"].data_ptr(), o_old["ws"].data_ptr(),
-                                   o_old["wS"].data_ptr(), q.S_PER_BATCH, PAIRS,
-                                   2 * PART_ROWS, K, lay, y_w.data_ptr(), s2),
-                "dq weights")
-        if concurrent:
-            # Each side chain dequantizes the previous step's codes first and
-            # quantizes this step's input last, so the step ends on the
-            # kernels that leave the least dirty data in L2 for the next
-            # step's rowcol kernel.
-            token_dq()
-            token_q()
-            weights_dq()
-            weights_q()
-        else:
-            token_q()
-            mark(4)
-            token_dq()
-            mark(5)
-            weights_q()
-            mark(6)
-            weights_dq()
-        if concurrent:
-            ev_join[0].record(side[0])
-            ev_join[1].record(side[1])
-            stream.wait_event(ev_join[0])
-            stream.wait_event(ev_join[1])
-        mark(7)
+    def step_serial(i, record):
+        """All operations on the main stream; record[j] .. record[j + 1]
+        brackets operation j (the per-kernel pass)."""
+        t = tables[i % 6]
+        for j, nm in enumerate(names):
+            record[j].record(stream)
+            fn, a, _ = t[nm]
+            launch(fn, a, nm)
+        record[len(names)].record(stream)
+
+    # Concurrent order after the first operation: the MXFP8 dequantizations
+    # (main stream), then each side chain dequantizing the previous step's
+    # codes before quantizing this step's input, so that the step ends on
+    # the kernels that leave the least dirty data in L2 for the next step.
+    ORDER = ("dequantize_mxfp8_row", "dequantize_mxfp8_col",
+             "mxfp8_quantize_rowcol", "dequantize_nvfp4_tokens",
+             "nvfp4_quantize_per_token", "dequantize_nvfp4_weights",
+             "nvfp4_quantize_weight_shared")
+
+    def step(i, first, bracket=None):
+        """One step: operation `first` alone on the main stream (between the
+        events of `bracket`, when given), then the rest as three concurrent
+        chains (the MXFP8 dequantizations on the main stream, the per-token
+        and the weight chain on side streams) that join before the next
+        step."""
+        t = tables[i % 6]
+        fn, a, _ = t[first]
+        if bracket is not None:
+            bracket[0].record(stream)
+        launch(fn, a, first)
+        if bracket is not None:
+            bracket[1].record(stream)
+        ev_fork.record(stream)
+        side[0].wait_event(ev_fork)
+        side[1].wait_event(ev_fork)
+        for nm in ORDER:
+            if nm != first:
+                fn, _, a = t[nm]
+                launch(fn, a, nm)
+        ev_join[0].record(side[0])
+        ev_join[1].record(side[1])
+        stream.wait_event(ev_join[0])
+        stream.wait_event(ev_join[1])
 
     # Our kernels per step: rowcol 1, dequant 2 + 1 + 1, per-token 1,
-    # weights 1 (one cooperative kernel per call of up to 256 groups).
+    # weights 1 (one kernel per call of up to 256 groups).
     launches_per_step = 1 + 2 + 1 + 1 + 1 + 1
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            step(i, concurrent=not args.serial)
+            if args.serial:
+                step_serial(i, [torch.cuda.Event() for _ in range(8)])
+            else:
+                step(i, "mxfp8_quantize_rowcol")
     torch.cuda.synchronize(dev)
+
+    # Per-kernel breakdown: a pass with events between all kernels, one
+    # stream (events between kernels cost the launch overlap, so this pass
+    # is not used for the headline number).  The kernel with the largest
+    # share is the roofline line's kernel.
+    nb = min(args.steps, 200)
+    recs8 = [[torch.cuda.Event(enable_timing=True) for _ in range(8)]
+             for _ in range(nb)]
+    th0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(nb):
+            step_serial(args.warmup + i, recs8[i])
+    host_serial_ms = (time.perf_counter() - th0) * 1e3 / nb
+    torch.cuda.synchronize(dev)
+    per_kernel_ms = {}
+    for j, nm in enumerate(names):
+        per_kernel_ms[nm] = statistics.mean(
+            recs8[i][j].elapsed_time(recs8[i][j + 1]) for i in range(nb))
+    dom = max(names, key=lambda nm: per_kernel_ms[nm])
     if world > 1:
         dist.barrier()
 
-    # Timed region: K steps.  Only the dominant quantizer kernel
-    # (mxfp8_quantize_rowcol) is bracketed by events inside a step, so the
-    # other kernels keep their programmatic-dependent-launch overlap.
+    # Timed region: K steps.  The dominant kernel runs first in each step,
+    # alone on the main stream, between two events; the other kernels keep
+    # their programmatic-dependent-launch overlap.
     recs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
             for _ in range(args.steps)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    i0 = args.warmup + nb
     with ClockSampler(local) as clk:
         torch.cuda.synchronize(dev)
         if world > 1:
@@ -333,9 +382,13 @@ def run_gpu(args):
         with torch.cuda.stream(stream):
             start.record(stream)
             for i in range(args.steps):
-                step(args.warmup + i, recs[i], only=(0, 1),
-                     concurrent=not args.serial)
+                if args.serial:
+                    step_serial(i0 + i, [recs[i][0]] + [torch.cuda.Event()
+                                                        for _ in range(7)])
+                else:
+                    step(i0 + i, dom, recs[i])
             end.record(stream)
+        host_ms = (time.perf_counter() - t0) * 1e3 / args.steps
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
@@ -344,23 +397,11 @@ def run_gpu(args):
     ms_max = max_over_ranks(ms, dist if world > 1 else None, dev)
     ob = op_bytes()
     step_bytes = sum(ob.values())
-    dom = "mxfp8_quantize_rowcol"
-    dom_ms = statistics.mean(recs[i][0].elapsed_time(recs[i][1])
-                             for i in range(args.steps))
-    # Per-kernel breakdown: a separate pass with events between all kernels
-    # (events between kernels cost the launch overlap, so this pass is not
-    # used for the headline number).
-    nb = min(args.steps, 200)
-    recs8 = [[torch.cuda.Event(enable_timing=True) for _ in range(8)]
-             for _ in range(nb)]
-    with torch.cuda.stream(stream):
-        for i in range(nb):
-            step(args.warmup + args.steps + i, recs8[i])
-    torch.cuda.synchronize(dev)
-    per_kernel_ms = {}
-    for j, nm in enumerate(names):
-        per_kernel_ms[nm] = statistics.mean(
-            recs8[i][j].elapsed_time(recs8[i][j + 1]) for i in range(nb))
+    if args.serial:
+        dom_ms = per_kernel_ms[dom]
+    else:
+        dom_ms = statistics.mean(recs[i][0].elapsed_time(recs[i][1])
+                                 for i in range(args.steps))
     peak, peak_kind = measured_peak()
     value = weak_scaling_value(step_bytes, args.steps, world, ms_max)
 
@@ -401,18 +442,20 @@ def run_gpu(args):
         "config": {
             "workload": WORKLOAD,
             "M": M, "K": K, "scale_layout": "swizzled",
-            "weight_pairs": f"{PAIRS} x 2 x [{PART_ROWS} x {K}]",
+            "weight_pairs": f"{PAIRS} x 2 x [{PART_ROWS} x {WK}]",
             "l2": ("inputs larger than L2: 3 rotating input copies and 2 "
                    "rotating output sets, every kernel reads data last "
                    "touched >= one step (~680 MB) earlier"),
             "parallelism": f"weak: one independent replica per GPU x{world}",
             "streams": ("1 (serial)" if args.serial else
-                        "3: rowcol alone, then its dequantizations, the "
-                        "per-token chain and the weight chain concurrently"),
+                        "3: the dominant kernel alone, then the MXFP8 "
+                        "dequantizations, the per-token chain and the weight "
+                        "chain concurrently"),
         },
         "pct_hbm_peak": round(100 * value / world / peak, 1),
         "roofline": {
             "kernel": dom,
+            "chosen_by": "largest share of the per-kernel pass",
             "bound": "hbm",
             "achieved": round(dom_gbs, 1),
             "peak": peak,
@@ -428,6 +471,8 @@ def run_gpu(args):
         "clocks": clk.summary(),
         "e2e": e2e,
         "wall_s_timed_region": round(wall, 3),
+        "host_enqueue_ms_per_step": {"timed": round(host_ms, 4),
+                                     "per_kernel_pass": round(host_serial_ms, 4)},
     }
     out["gemm"] = run_gemm(q, W, dev, stream)
     if not args.no_shapes:
@@ -582,30 +627,44 @@ def run_gemm(q, W, dev, stream, reps=20):
     return out
 
 
-def _time_reps(fn, stream, reps, flush_w, flush_r, warmup=3):
-    """Per-launch device times (ms) of `fn` on `stream`: the L2 is flushed
-    before every rep (a write of one buffer larger than L2, then a read of
-    another, so the timed launch starts with clean lines that hold none of
-    its data), outside the events that bracket the launch."""
+def _sets_for(footprint, l2, lo=2, hi=32):
+    """Rotation depth: enough buffer sets (inputs + outputs of one launch
+    each) that a launch's data was last touched at least 4 x L2 bytes of
+    traffic earlier."""
+    n = -(-4 * l2 // max(int(footprint), 1))
+    return int(max(lo, min(hi, n)))
+
+
+def _time_rotating(calls, stream, rounds=9, min_launches=24, warmup=3):
+    """Per-launch device times (ms) of back-to-back launches that cycle over
+    `calls` (each launching the kernel on its own input and output buffers,
+    all on `stream`): every launch finds its inputs out of L2 and, as in a
+    steady stream of launches, absorbs the write-back of the dirty lines the
+    launch before it left in L2, so a kernel's own write-back is inside the
+    timed region.  Each round times n launches between two events (n a
+    multiple of len(calls)); returns the per-launch mean of every round."""
     import torch
+    per = len(calls)
+    n = per * max(1, -(-min_launches // per))
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, per)):
+            calls[i % per]()
+    torch.cuda.synchronize()
     evs = []
     with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            fn()
-        for _ in range(reps):
-            flush_w.fill_(1)
-            flush_r.sum()
+        for _ in range(rounds):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            fn()
+            for i in range(n):
+                calls[i % per]()
             e1.record(stream)
             evs.append((e0, e1))
     torch.cuda.synchronize()
-    return [a.elapsed_time(b) for a, b in evs]
+    return [a.elapsed_time(b) / n for a, b in evs]
 
 
-def _shape_line(ms_list, nbytes, elems, peak):
+def _shape_line(ms_list, nbytes, elems, peak, sets):
     ms = sorted(ms_list)
     med = statistics.median(ms)
     p10 = ms[int(0.1 * (len(ms) - 1))]
@@ -616,54 +675,202 @@ def _shape_line(ms_list, nbytes, elems, peak):
             "GB/s_p10_p90": [round(nbytes / p90 / 1e6, 1),
                              round(nbytes / p10 / 1e6, 1)],
             "Gelem/s": round(elems / med / 1e6, 2),
-            "frac": round(gbs / peak, 3), "bytes": int(nbytes)}
+            "frac": round(gbs / peak, 3), "bytes": int(nbytes),
+            "writeback_included": True, "rotating_sets": int(sets)}
 
 
-def run_shapes(q, W, dev, stream, reps=20):
+class _Ops:
+    """Launchers of single library calls on preallocated buffers, straight
+    through the C ABI (no allocation or Python marshalling per launch), for
+    back-to-back timing."""
+
+    def __init__(self, q, dev, stream):
+        import torch
+        self.torch = torch
+        self.q = q
+        self.L = q.lib()
+        self.dev = dev
+        self.s = ctypes.c_void_p(stream.cuda_stream)
+        self.lay = q.SCALE_SWIZZLED
+
+    def u8(self, n):
+        return self.torch.empty(int(n), dtype=self.torch.uint8, device=self.dev)
+
+    def chk(self, st, what):
+        if st != 0:
+            raise RuntimeError(f"{what}: {self.q.status_string(st)}")
+
+    def rowcol(self, x):
+        M, K = x.shape
+        q = self.q
+        rc, cc = self.u8(M * K), self.u8(M * K)
+        rs = self.u8(q.scale_bytes(M, K // 32))
+        cs = self.u8(q.scale_bytes(K, M // 32))
+        args = (x.data_ptr(), M, K, K, rc.data_ptr(), rs.data_ptr(),
+                cc.data_ptr(), cs.data_ptr(), self.lay, self.s)
+        keep = (x, rc, rs, cc, cs)
+
+        def call(keep=keep):
+            self.chk(self.L.mxfp8_quantize_rowcol(*args), "rowcol")
+        return call, (rc, rs, cc, cs)
+
+    def dq_mxfp8(self, codes, scales):
+        rows, cols = codes.shape
+        y = self.torch.empty((rows, cols), dtype=self.torch.bfloat16,
+                             device=self.dev)
+        args = (codes.data_ptr(), scales.data_ptr(), rows, cols, self.lay,
+                y.data_ptr(), self.s)
+        keep = (codes, scales, y)
+
+        def call(keep=keep):
+            self.chk(self.L.dequantize_mxfp8(*args), "dequantize_mxfp8")
+        return call
+
+    def per_token(self, x, rht_flags=None, seed=2026):
+        T, H = x.shape
+        q = self.q
+        c = self.u8(T * H // 2)
+        bs = self.u8(q.scale_bytes(T, H // 16))
+        S = self.torch.empty(T, dtype=self.torch.float32, device=self.dev)
+        keep = (x, c, bs, S)
+        if rht_flags is None:
+            args = (x.data_ptr(), T, H, H, c.data_ptr(), bs.data_ptr(),
+                    S.data_ptr(), self.lay, self.s)
+
+            def call(keep=keep):
+                self.chk(self.L.nvfp4_quantize_per_token(*args), "per-token")
+        else:
+            args = (x.data_ptr(), T, H, H, ctypes.c_uint64(seed), rht_flags,
+                    c.data_ptr(), bs.data_ptr(), S.data_ptr(), self.lay,
+                    self.s)
+
+            def call(keep=keep):
+                self.chk(self.L.nvfp4_quantize_per_token_rht_sr(*args),
+                         "per-token rht/sr")
+        return call, (c, bs, S)
+
+    def dq_nvfp4(self, codes, bs, S, mode, batch, rows, cols):
+        y = self.torch.empty(batch * rows * cols, dtype=self.torch.bfloat16,
+                             device=self.dev)
+        args = (codes.data_ptr(), bs.data_ptr(), S.data_ptr(), mode, batch,
+                rows, cols, self.lay, y.data_ptr(), self.s)
+        keep = (codes, bs, S, y)
+
+        def call(keep=keep):
+            self.chk(self.L.dequantize_nvfp4(*args), "dequantize_nvfp4")
+        return call
+
+    def weights(self, parts, G, P, part_rows, K):
+        """parts: G * P contiguous bf16 tensors (group-major)."""
+        q = self.q
+        R = sum(part_rows)
+        tab = (ctypes.c_void_p * (G * P))(*[t.data_ptr() for t in parts])
+        rows = (ctypes.c_int64 * P)(*part_rows)
+        c = self.u8(G * R * K // 2)
+        sbytes = q.scale_bytes(R, K // 16)
+        bs = self.u8(G * sbytes)
+        S = self.torch.empty(G, dtype=self.torch.float32, device=self.dev)
+        wsb = int(self.L.nvfp4_quantize_weight_shared_workspace_size(G))
+        ws = self.u8(max(wsb, 256))
+        args = (G, P, ctypes.cast(tab, ctypes.c_void_p),
+                ctypes.cast(rows, ctypes.c_void_p), K, c.data_ptr(),
+                bs.data_ptr(), S.data_ptr(), None, self.lay, ws.data_ptr(),
+                ws.numel(), self.s)
+        keep = (parts, tab, rows, c, bs, S, ws)
+
+        def call(keep=keep):
+            self.chk(self.L.nvfp4_quantize_weight_shared(*args), "weights")
+        return call, (c, bs, S)
+
+    def fp8blk(self, x, block_rows):
+        rows, cols = x.shape
+        c = self.u8(rows * cols)
+        sc = self.torch.empty((rows // block_rows) * (cols // 128),
+                              dtype=self.torch.float32, device=self.dev)
+        args = (x.data_ptr(), rows, cols, cols, block_rows, c.data_ptr(),
+                sc.data_ptr(), self.s)
+        keep = (x, c, sc)
+
+        def call(keep=keep):
+            self.chk(self.L.fp8_block_quantize(*args), "fp8 block")
+        return call, (c, sc)
+
+    def fp8blk_dq(self, codes, sc, rows, cols, block_rows):
+        y = self.torch.empty(rows * cols, dtype=self.torch.bfloat16,
+                             device=self.dev)
+        args = (codes.data_ptr(), sc.data_ptr(), rows, cols, block_rows,
+                y.data_ptr(), self.s)
+        keep = (codes, sc, y)
+
+        def call(keep=keep):
+            self.chk(self.L.fp8_block_dequantize(*args), "fp8 block dequant")
+        return call
+
+    def fp8blk_rt(self, codes, sc, rows, cols):
+        ct = self.u8(rows * cols)
+        st = self.torch.empty(cols * (rows // 128), dtype=self.torch.float32,
+                              device=self.dev)
+        args = (codes.data_ptr(), sc.data_ptr(), rows, cols, ct.data_ptr(),
+                st.data_ptr(), self.s)
+        keep = (codes, sc, ct, st)
+
+        def call(keep=keep):
+            self.chk(self.L.fp8_block_requantize_transpose(*args),
+                     "fp8 block requantize-transpose")
+        return call
+
+
+def run_shapes(q, W, dev, stream):
     """Each quantizer and dequantizer alone at the full sizes of the
-    workloads it is specified on, L2 flushed before every launch: MXFP8
-    rowwise + columnwise of the four 8192 x 4096 input classes and of the
-    linear layer's input [2048 x 2048] and weight [8192 x 2048]; NVFP4
-    per-token on the ragged batch of 64 sequences (lengths in [128, 4096],
-    hidden 2048), also with the pretraining recipe's Hadamard transform and
-    stochastic rounding; NVFP4 shared-scale weights of a 128-expert MoE layer
-    (gate/up pairs [2 x 768 x 2048] and down [2048 x 768]); FP8 with FP32
-    block scales (1x128 tiles of the activation, 128x128 blocks of the
-    linear weight, the tiles' backward-orientation conversion); and the
-    dequantizations of each."""
+    workloads it is specified on: MXFP8 rowwise + columnwise of the four
+    8192 x 4096 input classes and of the linear layer's input [2048 x 2048]
+    and weight [8192 x 2048]; NVFP4 per-token on the ragged batch of 64
+    sequences (lengths in [128, 4096], hidden 2048), also with the
+    pretraining recipe's Hadamard transform and stochastic rounding; NVFP4
+    shared-scale weights of a 128-expert MoE layer (gate/up pairs
+    [2 x 768 x 2048] and down [2048 x 768]); FP8 with FP32 block scales (1x128
+    tiles of the activation, 128x128 blocks of the linear weight, the tiles'
+    backward-orientation conversion); and the dequantizations of each.
+
+    Every line times back-to-back launches cycling over several sets of
+    input and output buffers (at least 4 x L2 of data per cycle), so each
+    launch reads its inputs from HBM and pays for its own write-back."""
     import torch
     peak = measured_peak()[0]
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    ops = _Ops(q, dev, stream)
     out = {}
 
     def dev16(bits):
         return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
 
-    def mx(name, bits):
+    def line(name, calls, nbytes, elems, **extra):
+        out[name] = dict(_shape_line(_time_rotating(calls, stream), nbytes,
+                                     elems, peak, len(calls)), **extra)
+
+    # MXFP8 rowwise + columnwise, then both dequantizations
+    def mx(name, bits, dequant=False):
         x = dev16(bits)
         m, k = x.shape
         n = m * k
-        r = q.mxfp8_quantize_rowcol(x)
-        out[f"mxfp8_rowcol_{name}"] = _shape_line(
-            _time_reps(lambda: q.mxfp8_quantize_rowcol(x), stream, reps,
-                       flush_w, flush_r),
-            2 * n + 2 * (n + n // 32), n, peak)
-        return r
+        b = 2 * n + 2 * (n + n // 32)
+        sets = _sets_for(b, l2)
+        built = [ops.rowcol(x if i == 0 else x.clone()) for i in range(sets)]
+        line(f"mxfp8_rowcol_{name}", [c for c, _ in built], b, n)
+        if dequant:
+            for nm, j in (("row", 0), ("col", 2)):
+                calls = []
+                for _, o in built:
+                    rows, cols = (m, k) if nm == "row" else (k, m)
+                    calls.append(ops.dq_mxfp8(o[j].view(rows, cols), o[j + 1]))
+                line(f"dequantize_mxfp8_{nm}_{m}x{k}", calls,
+                     n + n // 32 + 2 * n, n)
+        del built, x
+        torch.cuda.empty_cache()
 
-    r = None
     for cls, gen in (("random", W.mxfp8_random), ("boundary", W.mxfp8_boundary),
                      ("zeros", W.mxfp8_zeros), ("maxes", W.mxfp8_maxes)):
-        r = mx(f"8192x4096_{cls}", gen(8192, 4096))
-    n = 8192 * 4096
-    for nm, cod, sc in (("row", r.row_codes, r.row_scales),
-                        ("col", r.col_codes_t, r.col_scales_t)):
-        out[f"dequantize_mxfp8_{nm}_8192x4096"] = _shape_line(
-            _time_reps(lambda: q.dequantize_mxfp8(cod, sc), stream, reps,
-                       flush_w, flush_r),
-            n + n // 32 + 2 * n, n, peak)
-    del r
+        mx(f"8192x4096_{cls}", gen(8192, 4096), dequant=(cls == "random"))
     mx("2048x2048_linear_input", W.linear_input())
     mx("8192x2048_linear_weight", W.linear_weight())
 
@@ -672,80 +879,80 @@ def run_shapes(q, W, dev, stream, reps=20):
     lengths = W.ragged_lengths()
     x = dev16(W.ragged_tokens(lengths, H))
     T = x.shape[0]
-    tq = q.nvfp4_quantize_per_token(x)
     tb = T * (2 * H + H // 2 + H // 16 + 4)
-    out[f"nvfp4_per_token_ragged_{T}x{H}"] = dict(_shape_line(
-        _time_reps(lambda: q.nvfp4_quantize_per_token(x), stream, reps,
-                   flush_w, flush_r), tb, T * H, peak),
-        sequences=int(len(lengths)))
-    out[f"dequantize_nvfp4_ragged_{T}x{H}"] = _shape_line(
-        _time_reps(lambda: q.dequantize_nvfp4(tq.codes, tq.block_scales,
-                                              tq.scales),
-                   stream, reps, flush_w, flush_r), tb, T * H, peak)
+    sets = _sets_for(tb, l2)
+    xs = [x] + [x.clone() for _ in range(sets - 1)]
+    built = [ops.per_token(xi) for xi in xs]
+    line(f"nvfp4_per_token_ragged_{T}x{H}", [c for c, _ in built], tb, T * H,
+         sequences=int(len(lengths)))
+    line(f"dequantize_nvfp4_ragged_{T}x{H}",
+         [ops.dq_nvfp4(c, bs, S, q.S_PER_ROW, 1, T, H)
+          for _, (c, bs, S) in built], tb, T * H)
+    del built
     # the pretraining recipe's stabilizers on the same batch
     for nm, fl in (("rht", q.NVFP4_RHT), ("rht_sr", q.NVFP4_RHT | q.NVFP4_SR)):
-        out[f"nvfp4_per_token_{nm}_ragged_{T}x{H}"] = _shape_line(
-            _time_reps(lambda: q.nvfp4_quantize_per_token_rht_sr(x, 2026, fl),
-                       stream, reps, flush_w, flush_r), tb, T * H, peak)
-    del x, tq
+        built = [ops.per_token(xi, rht_flags=fl) for xi in xs]
+        line(f"nvfp4_per_token_{nm}_ragged_{T}x{H}", [c for c, _ in built],
+             tb, T * H)
+        del built
+    del x, xs
+    torch.cuda.empty_cache()
 
     # NVFP4 weights of a 128-expert MoE layer
     E, F = 128, 768
     experts = W.moe_layer(E, H, F)
-    gate_up = [[dev16(g), dev16(u)] for g, u, d in experts]
-    down = [[dev16(d)] for g, u, d in experts]
-    del experts
-    for nm, groups, rows, cols in (("gate_up", gate_up, 2 * F, H),
-                                   ("down", down, H, F)):
-        ws = torch.empty(max(int(q.lib().nvfp4_quantize_weight_shared_workspace_size(E)), 256),
-                         dtype=torch.uint8, device=dev)
-        wq = q.nvfp4_quantize_weight_shared(groups, workspace=ws)
+    for nm, rows_p, cols in (("gate_up", [F, F], H), ("down", [H], F)):
+        if nm == "gate_up":
+            host = [p for g, u, d in experts for p in (g, u)]
+        else:
+            host = [d for g, u, d in experts]
+        P = len(rows_p)
+        rows = sum(rows_p)
         ne = E * rows * cols
         wb = ne * 2 + ne // 2 + ne // 16 + 4 * E
-        out[f"nvfp4_weight_{nm}_{E}x{rows}x{cols}"] = _shape_line(
-            _time_reps(lambda: q.nvfp4_quantize_weight_shared(groups,
-                                                              workspace=ws),
-                       stream, reps, flush_w, flush_r), wb, ne, peak)
-        out[f"dequantize_nvfp4_{nm}_{E}x{rows}x{cols}"] = _shape_line(
-            _time_reps(lambda: q.dequantize_nvfp4(wq.codes, wq.block_scales,
-                                                  wq.scales),
-                       stream, reps, flush_w, flush_r), wb, ne, peak)
-        del wq
-    del gate_up, down
+        sets = _sets_for(wb, l2)
+        base = [dev16(h) for h in host]
+        del host
+        built = []
+        for i in range(sets):
+            parts = base if i == 0 else [t.clone() for t in base]
+            built.append(ops.weights(parts, E, P, rows_p, cols))
+        line(f"nvfp4_weight_{nm}_{E}x{rows}x{cols}", [c for c, _ in built],
+             wb, ne)
+        line(f"dequantize_nvfp4_{nm}_{E}x{rows}x{cols}",
+             [ops.dq_nvfp4(c, bs, S, q.S_PER_BATCH, E, rows, cols)
+              for _, (c, bs, S) in built], wb, ne)
+        del built, base
+        torch.cuda.empty_cache()
+    del experts
 
     # FP8 with FP32 block scales: 1x128 tiles of X [8192 x 4096], 128x128
     # blocks of the linear weight [8192 x 2048], the dequantizations and the
     # backward-orientation conversion of the tiles
-    x = dev16(W.mxfp8_random(8192, 4096))
-    n = x.numel()
-    fq = q.fp8_block_quantize(x, 1)
-    out["fp8_block_1x128_8192x4096"] = _shape_line(
-        _time_reps(lambda: q.fp8_block_quantize(x, 1), stream, reps,
-                   flush_w, flush_r), 3 * n + 4 * (n // 128), n, peak)
-    out["fp8_block_dequantize_1x128_8192x4096"] = _shape_line(
-        _time_reps(lambda: q.fp8_block_dequantize(fq.codes, fq.scales, 1),
-                   stream, reps, flush_w, flush_r), 3 * n + 4 * (n // 128), n,
-        peak)
-    out["fp8_block_requantize_transpose_8192x4096"] = _shape_line(
-        _time_reps(lambda: q.fp8_block_requantize_transpose(fq.codes,
-                                                            fq.scales),
-                   stream, reps, flush_w, flush_r), 2 * n + 8 * (n // 128), n,
-        peak)
-    del x, fq
-    w = dev16(W.linear_weight())
-    n = w.numel()
-    wq = q.fp8_block_quantize(w, 128)
-    out["fp8_block_128x128_8192x2048"] = _shape_line(
-        _time_reps(lambda: q.fp8_block_quantize(w, 128), stream, reps,
-                   flush_w, flush_r), 3 * n + 4 * (n // 16384), n, peak)
-    out["fp8_block_dequantize_128x128_8192x2048"] = _shape_line(
-        _time_reps(lambda: q.fp8_block_dequantize(wq.codes, wq.scales, 128),
-                   stream, reps, flush_w, flush_r), 3 * n + 4 * (n // 16384),
-        n, peak)
-    del w, wq, flush_w, flush_r
-    torch.cuda.empty_cache()
-    out["timing"] = (f"median of {reps} launches (p10/p90 beside it), each "
-                     "after an L2 flush; GB/s = algorithmic bytes / time")
+    for nm, bits, br in (("1x128_8192x4096", W.mxfp8_random(8192, 4096), 1),
+                         ("128x128_8192x2048", W.linear_weight(), 128)):
+        x = dev16(bits)
+        rows, cols = x.shape
+        n = x.numel()
+        b = 3 * n + 4 * (n // (128 * br))
+        sets = _sets_for(b, l2)
+        built = [ops.fp8blk(x if i == 0 else x.clone(), br) for i in range(sets)]
+        line(f"fp8_block_{nm}", [c for c, _ in built], b, n)
+        line(f"fp8_block_dequantize_{nm}",
+             [ops.fp8blk_dq(c, sc, rows, cols, br) for _, (c, sc) in built],
+             b, n)
+        if br == 1:
+            line("fp8_block_requantize_transpose_8192x4096",
+                 [ops.fp8blk_rt(c, sc, rows, cols) for _, (c, sc) in built],
+                 2 * n + 8 * (n // 128), n)
+        del built, x
+        torch.cuda.empty_cache()
+    out["timing"] = ("median over 9 rounds of the per-launch mean of >= 24 "
+                     "back-to-back launches cycling over `rotating_sets` "
+                     "buffer sets (>= 4 x L2 of data per cycle): inputs come "
+                     "from HBM and each launch absorbs the write-back of the "
+                     "previous launch's dirty lines; p10/p90 over the rounds; "
+                     "GB/s = algorithmic bytes / time")
     return out
 
 
@@ -801,7 +1008,7 @@ def run_e2e(q, dev, x_bits, args):
         q.dequantize_mxfp8(r.col_codes_t, r.col_scales_t)
         t = q.nvfp4_quantize_per_token(x)
         q.dequantize_nvfp4(t.codes, t.block_scales, t.scales)
-        parts = x.view(2 * PAIRS, PART_ROWS, K)
+        parts = x.view(2 * PAIRS, PART_ROWS, WK)
         w = q.nvfp4_quantize_weight_shared(
             [[parts[2 * g], parts[2 * g + 1]] for g in range(PAIRS)])
         q.dequantize_nvfp4(w.codes, w.block_scales, w.scales)
@@ -869,9 +1076,30 @@ def oracle_timed(rows_total, threads):
     return sum(op_bytes().values()) * frac / dt / 1e9, dt
 
 
-def cpu_baseline(args, min_s=10.0, max_passes=40):
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+def cpu_baseline(args, min_s=10.0, max_passes=40, single_min_s=5.0):
     """The oracle over `cpu_rows` rows of X, repeated until at least min_s
-    seconds of CPU work have run (at most max_passes passes)."""
+    seconds of CPU work have run (at most max_passes passes), on all host
+    cores; then on one thread, over 32-row slices until single_min_s
+    seconds have run."""
     import oracle as O
     import workloads as W
     O.lib()
@@ -887,12 +1115,24 @@ def cpu_baseline(args, min_s=10.0, max_passes=40):
             total += time.perf_counter() - t0
             passes += 1
     v = sum(op_bytes().values()) * (rows / M) * passes / total / 1e9
+    # one thread: whole 32-row slices, as many as fit in single_min_s
+    n1, t1 = 0, 0.0
+    while n1 == 0 or (t1 < single_min_s and n1 < len(slices)):
+        t0 = time.perf_counter()
+        oracle_sample_step(slices[n1 % len(slices)])
+        t1 += time.perf_counter() - t0
+        n1 += 1
+    v1 = sum(op_bytes().values()) * (32 * n1 / M) / t1 / 1e9
     return {"value": round(v, 4), "unit": UNIT, "cores": cores,
-            "kind": "oracle",
-            "sample": (f"{passes} passes of the step's 8 operations over "
+            "kind": "oracle", "cpu_model": cpu_model(),
+            "sample": (f"{passes} passes of the step's 7 operations over "
                        f"{rows} of the 8192 rows of X ({rows * K} elements "
                        f"per pass), 32-row slices over {cores} threads, "
-                       f"{total:.1f} s")}
+                       f"{total:.1f} s"),
+            "single_thread": {
+                "value": round(v1, 5), "unit": UNIT, "cores": 1,
+                "sample": (f"{n1} slices of 32 rows of X through the step's "
+                           f"7 operations on one thread, {t1:.1f} s")}}
 
 
 def run_reference(args):
@@ -928,11 +1168,137 @@ def run_reference(args):
                    "sample_rows": rows},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT,
                          "cores": cores, "kind": "oracle",
+                         "cpu_model": cpu_model(),
                          "sample": f"{rows} of 8192 rows per step"},
         "e2e": {"value": round(value, 4), "unit": UNIT,
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
+
+
+PROFILE_WORKLOADS = (
+    "rowcol_8192x4096", "rowcol_8192x2048", "dequant_mxfp8_8192x4096",
+    "per_token_ragged", "dequant_nvfp4_ragged", "rht_ragged",
+    "weight_gate_up_128", "weight_down_128", "weight_step_8pairs",
+    "dequant_nvfp4_gate_up_128", "fp8_block_1x128", "fp8_block_128x128",
+    "fp8_block_requant_t", "gemm_mxfp8", "gemm_nvfp4_grouped",
+    "moe_gate_up_swiglu", "gemm_bf16_dq")
+
+
+def run_profile(args):
+    """One workload's kernel alone, launched `--launches` times after one
+    warm-up launch, on one set of buffers (a few GB at most): the harness
+    the ncu captures run, so that a capture holds no other workload."""
+    import torch
+    import nvfp4_quantizers_gb300 as q
+    import workloads as W
+    from nvfp4_quantizers_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    ops = _Ops(q, dev, stream)
+
+    def dev16(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    name = args.profile
+    H, E, F = 2048, 128, 768
+    if name.startswith("rowcol"):
+        x = dev16(W.mxfp8_random(8192, 4096) if name.endswith("4096")
+                  else W.linear_weight())
+        call, _ = ops.rowcol(x)
+    elif name == "dequant_mxfp8_8192x4096":
+        _, o = ops.rowcol(dev16(W.mxfp8_random(8192, 4096)))
+        _()
+        call = ops.dq_mxfp8(o[0].view(8192, 4096), o[1])
+    elif name in ("per_token_ragged", "dequant_nvfp4_ragged", "rht_ragged"):
+        x = dev16(W.ragged_tokens(W.ragged_lengths(), H))
+        T = x.shape[0]
+        call, o = ops.per_token(x, rht_flags=q.NVFP4_RHT
+                                if name == "rht_ragged" else None)
+        if name == "dequant_nvfp4_ragged":
+            call()
+            call = ops.dq_nvfp4(o[0], o[1], o[2], q.S_PER_ROW, 1, T, H)
+    elif name.startswith(("weight_", "dequant_nvfp4_gate_up")):
+        if name == "weight_step_8pairs":
+            xs = dev16(W.mxfp8_random(8192, 4096)).view(16, 1024, 2048)
+            call, o = ops.weights([xs[i] for i in range(16)], 8, 2,
+                                  [1024, 1024], 2048)
+        else:
+            experts = W.moe_layer(E, H, F)
+            if "down" in name:
+                parts, rows_p, K = [dev16(d) for g, u, d in experts], [H], F
+            else:
+                parts = [dev16(t) for g, u, d in experts for t in (g, u)]
+                rows_p, K = [F, F], H
+            del experts
+            call, o = ops.weights(parts, E, len(rows_p), rows_p, K)
+            if name.startswith("dequant"):
+                call()
+                call = ops.dq_nvfp4(o[0], o[1], o[2], q.S_PER_BATCH, E,
+                                    sum(rows_p), K)
+    elif name.startswith("fp8_block"):
+        br = 128 if name == "fp8_block_128x128" else 1
+        x = dev16(W.linear_weight() if br == 128 else
+                  W.mxfp8_random(8192, 4096))
+        call, o = ops.fp8blk(x, br)
+        if name == "fp8_block_requant_t":
+            call()
+            call = ops.fp8blk_rt(o[0], o[1], 8192, 4096)
+    elif name.startswith(("gemm", "moe")):
+        gemm_calls = _gemm_workloads(q, W, dev)
+        call = gemm_calls[name]
+    else:
+        raise SystemExit(f"unknown workload {name}; one of {PROFILE_WORKLOADS}")
+    with torch.cuda.stream(stream):
+        call()
+        torch.cuda.synchronize()
+        for _ in range(args.launches):
+            call()
+    torch.cuda.synchronize()
+    st = q.get_last_error()
+    print(json.dumps({"profile": name, "launches": args.launches,
+                      "status": q.status_string(st)}))
+    if st != 0:
+        raise SystemExit(1)
+
+
+def _gemm_workloads(q, W, dev):
+    """Launchers of the GEMM consumers on their benchmark workloads (the
+    Python API allocates C per call)."""
+    import torch
+
+    def dev16(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    out = {}
+    A, B = W.gemm_mxfp8_inputs(2048, 2048, 8192)
+    qa = q.mxfp8_quantize_rowcol(dev16(A), rowwise=True, colwise=False)
+    qb = q.mxfp8_quantize_rowcol(dev16(B), rowwise=False, colwise=True)
+    out["gemm_mxfp8"] = lambda: q.gemm_mxfp8(qa.row_codes, qa.row_scales,
+                                             qb.col_codes_t, qb.col_scales_t)
+    E, H, F = 128, 2048, 768
+    tokens = W.gemm_tokens(4096, H)
+    route = W.topk_routing(4096, E, 8)
+    idx, offs, _ = W.expert_gather_index(route, E)
+    tg = q.nvfp4_quantize_per_token_gather(dev16(tokens),
+                                           torch.from_numpy(idx).to(dev))
+    wts = dev16(np.stack([np.concatenate(W.moe_expert(e, hidden=H, ffn=F)[:2])
+                          for e in range(E)]))
+    tw = q.nvfp4_quantize_weight_shared([[wts[e]] for e in range(E)])
+    del wts
+    out["gemm_nvfp4_grouped"] = lambda: q.gemm_nvfp4_grouped(
+        tg.codes, tg.block_scales, tg.scales, offs, tw.codes, tw.block_scales,
+        tw.scales)
+    out["moe_gate_up_swiglu"] = lambda: q.moe_gate_up_swiglu(
+        tg.codes, tg.block_scales, tg.scales, offs, tw.codes, tw.block_scales,
+        tw.scales)
+    dY = dev16(W.gemm_tokens(2048, 8192))
+    wq = q.mxfp8_quantize_rowcol(dev16(W.linear_weight()), rowwise=False,
+                                 colwise=True)
+    out["gemm_bf16_dq"] = lambda: q.gemm_bf16_mxfp8(dY, wq.col_codes_t,
+                                                    wq.col_scales_t)
+    return out
 
 
 def main():
@@ -949,9 +1315,16 @@ def main():
                     help="skip the per-kernel lines at every workload's size")
     ap.add_argument("--serial", action="store_true",
                     help="run the step's three chains on one stream")
+    ap.add_argument("--profile", default=None, choices=PROFILE_WORKLOADS,
+                    help="launch only this workload's kernel (for ncu)")
+    ap.add_argument("--launches", type=int, default=3,
+                    help="launches after one warm-up launch, with --profile")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
