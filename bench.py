@@ -760,8 +760,9 @@ class _Ops:
             self.chk(self.L.dequantize_nvfp4(*args), "dequantize_nvfp4")
         return call
 
-    def weights(self, parts, G, P, part_rows, K):
-        """parts: G * P contiguous bf16 tensors (group-major)."""
+    def weights(self, parts, G, P, part_rows, K, S_in=None):
+        """parts: G * P contiguous bf16 tensors (group-major); S_in: the
+        group scales to use (float32 [G] on the device) or None."""
         q = self.q
         R = sum(part_rows)
         tab = (ctypes.c_void_p * (G * P))(*[t.data_ptr() for t in parts])
@@ -774,9 +775,10 @@ class _Ops:
         ws = self.u8(max(wsb, 256))
         args = (G, P, ctypes.cast(tab, ctypes.c_void_p),
                 ctypes.cast(rows, ctypes.c_void_p), K, c.data_ptr(),
-                bs.data_ptr(), S.data_ptr(), None, self.lay, ws.data_ptr(),
-                ws.numel(), self.s)
-        keep = (parts, tab, rows, c, bs, S, ws)
+                bs.data_ptr(), S.data_ptr(),
+                None if S_in is None else S_in.data_ptr(), self.lay,
+                ws.data_ptr(), ws.numel(), self.s)
+        keep = (parts, tab, rows, c, bs, S, ws, S_in)
 
         def call(keep=keep):
             self.chk(self.L.nvfp4_quantize_weight_shared(*args), "weights")
@@ -1180,6 +1182,7 @@ PROFILE_WORKLOADS = (
     "rowcol_8192x4096", "rowcol_8192x2048", "dequant_mxfp8_8192x4096",
     "per_token_ragged", "dequant_nvfp4_ragged", "rht_ragged",
     "weight_gate_up_128", "weight_down_128", "weight_step_8pairs",
+    "weight_gate_up_128_given_scale",
     "dequant_nvfp4_gate_up_128", "fp8_block_1x128", "fp8_block_128x128",
     "fp8_block_requant_t", "gemm_mxfp8", "gemm_nvfp4_grouped",
     "moe_gate_up_swiglu", "gemm_bf16_dq")
@@ -1234,6 +1237,10 @@ def run_profile(args):
                 rows_p, K = [F, F], H
             del experts
             call, o = ops.weights(parts, E, len(rows_p), rows_p, K)
+            if name.endswith("given_scale"):
+                call()
+                call, o = ops.weights(parts, E, len(rows_p), rows_p, K,
+                                      S_in=o[2])
             if name.startswith("dequant"):
                 call()
                 call = ops.dq_nvfp4(o[0], o[1], o[2], q.S_PER_BATCH, E,

@@ -27,6 +27,14 @@
  *  - Results are deterministic and bit-exact with respect to the algorithm
  *    stated at each entry point: the same input bytes always give the same
  *    output bytes, on any launch configuration.
+ *  - Bounded device waits: the kernels of the entry points marked
+ *    "[bounded waits]" wait on the GPU (for data copies in flight, for
+ *    other CTAs); every such wait gives up after about one second, skips
+ *    the rest of the kernel's work and records an error word.  The call
+ *    itself has already returned MXQ_OK by then, and its outputs are
+ *    incomplete: the failure is reported only by the next
+ *    mxq_get_last_error() (which synchronizes the device).  Callers that
+ *    must know check it after the work has completed.
  *
  * Scale layouts (argument `scale_layout`)
  * ---------------------------------------
@@ -127,6 +135,8 @@ void mxq_set_fault_inject(int mode);
 /* Either pair may be NULL (both pointers of the pair) to skip that copy;  */
 /* at least one pair must be given.  K % 32 == 0; M % 32 == 0 when the     */
 /* columnwise copy is requested.  M == 0 or K == 0 is a no-op.            */
+/* [bounded waits]: a device-side wait that gives up is reported by the   */
+/* next mxq_get_last_error(), not by this call's status.                  */
 /* --------------------------------------------------------------------- */
 mxq_status mxfp8_quantize_rowcol(const void* x, int64_t M, int64_t K,
                                  int64_t ldx, uint8_t* row_codes,
@@ -216,6 +226,8 @@ mxq_status nvfp4_quantize_per_token_gather(
 /* ws / ws_bytes  device workspace of at least                             */
 /*                nvfp4_quantize_weight_shared_workspace_size() bytes.     */
 /* K % 16 == 0; 1 <= num_parts <= 4.                                       */
+/* [bounded waits]: a device-side wait that gives up is reported by the   */
+/* next mxq_get_last_error(), not by this call's status.                  */
 /* --------------------------------------------------------------------- */
 size_t nvfp4_quantize_weight_shared_workspace_size(int64_t num_groups);
 
@@ -243,13 +255,19 @@ mxq_status nvfp4_quantize_weight_shared(
 /*    nvfp4_quantize_weight_shared_noalloc_max_groups() (4096); larger    */
 /*    requests are rejected with MXQ_ERR_SHAPE before anything runs.      */
 /*  - The first call on a device looks up the array's device address      */
-/*    (cudaGetSymbolAddress) with that device current; make that first    */
-/*    call before any stream capture on the device.                       */
+/*    (cudaGetSymbolAddress) with that device current, and a call that    */
+/*    finds the device's context replaced (cudaDeviceReset) looks it up   */
+/*    again; make the first call on a device, and the first after a       */
+/*    reset, before any stream capture on the device.                     */
+/*  - Honours the host-side fault injection of mxq_set_fault_inject like  */
+/*    every other entry point.                                            */
 /*  - Every call shares the array.  A call clears the words it uses on    */
 /*    its own stream before using them, so back-to-back calls on one      */
 /*    stream are correct; calls whose work overlaps on the GPU (unordered */
 /*    streams) race on the array.                                         */
 /*  - Calls no cudaMalloc, cudaFree or allocating routine.                */
+/* [bounded waits]: a device-side wait that gives up is reported by the   */
+/* next mxq_get_last_error(), not by this call's status.                  */
 /* --------------------------------------------------------------------- */
 int64_t nvfp4_quantize_weight_shared_noalloc_max_groups(void);
 
@@ -384,6 +402,8 @@ mxq_status fp8_block_requantize_transpose(const uint8_t* codes,
 /* col_scales_t), or the rowwise copy of an [N x K] weight.  Scales must   */
 /* be in MXQ_SCALE_SWIZZLED layout.  C is fp32 [M x N], row stride ldc    */
 /* (ldc >= N, ldc % 4 == 0).  M % 128 == 0, N % 128 == 0, K % 128 == 0.    */
+/* [bounded waits]: a device-side wait that gives up is reported by the   */
+/* next mxq_get_last_error(), not by this call's status.                  */
 /* --------------------------------------------------------------------- */
 mxq_status mxq_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
                           const uint8_t* bt_codes, const uint8_t* bt_scales,
@@ -403,6 +423,8 @@ mxq_status mxq_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
 /* The bf16 values of B are formed in shared memory only.  fp32            */
 /* accumulation, fp32 C [M x N] (ldc >= N, ldc % 4 == 0).                  */
 /* M % 128 == 0, N % 128 == 0, K % 64 == 0.                               */
+/* [bounded waits]: a device-side wait that gives up is reported by the   */
+/* next mxq_get_last_error(), not by this call's status.                  */
 mxq_status mxq_gemm_bf16_mxfp8(const void* a, int64_t lda,
                                const uint8_t* bt_codes,
                                const uint8_t* bt_scales, int64_t M, int64_t N,
@@ -422,6 +444,8 @@ mxq_status mxq_gemm_bf16_mxfp8(const void* a, int64_t lda,
 /*             sum_k (E2M1 x E4M3)(a[r, k]) * (E2M1 x E4M3)(w_g[n, k])     */
 /* with fp32 accumulation; C fp32 [M_total x N], row stride ldc.           */
 /* N % 128 == 0, K % 256 == 0, num_groups <= 256.                          */
+/* [bounded waits]: a device-side wait that gives up is reported by the   */
+/* next mxq_get_last_error(), not by this call's status.                  */
 /* --------------------------------------------------------------------- */
 mxq_status mxq_gemm_nvfp4_grouped(
     const uint8_t* a_codes, const uint8_t* a_scales, const float* a_token_scales,
@@ -456,6 +480,8 @@ mxq_status mxq_gemm_nvfp4_grouped(
 /* F % 128 == 0, K % 256 == 0, num_groups <= 256.                         */
 /* binary32 arithmetic before the bf16 rounding; silu uses a fast         */
 /* exponential and divide (relative error below 2^-20, far inside bf16).  */
+/* [bounded waits]: a device-side wait that gives up is reported by the   */
+/* next mxq_get_last_error(), not by this call's status.                  */
 /* --------------------------------------------------------------------- */
 mxq_status mxq_moe_gate_up_swiglu_nvfp4(
     const uint8_t* a_codes, const uint8_t* a_scales, const float* a_token_scales,

@@ -72,6 +72,8 @@ EncodeTiledFn encode_tiled_fn() {
 
 }  // namespace
 
+int host_fault_mode() { return fault_mode(); }
+
 int sm_count(int device) {
   if (device < 0 || device >= kMaxDevices) return 1;
   int n = g_sm_count[device];

@@ -13,6 +13,10 @@
 namespace mxq {
 
 // Host utilities (api.cu).
+// Host-side fault injection (mxq_set_fault_inject / MXQ_FAULT_INJECT):
+// 0 = off, 1 = fail every launch with MXQ_ERR_CUDA, 2 = reject every call
+// with MXQ_ERR_ARG.
+int host_fault_mode();
 int sm_count(int device);
 int64_t l2_bytes(int device);
 cudaError_t make_tmap_2d_bytes(CUtensorMap* map, const void* base,

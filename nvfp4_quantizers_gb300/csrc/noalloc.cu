@@ -11,20 +11,23 @@
 // library's own device memory instead.
 //
 //  * The scratch is a file-scope device array of 64 + 2 * kNoAllocMaxGroups
-//    32-bit words (32.25 KiB: a task counter, one amax word and one
+//    32-bit words (32.25 KiB: task counters, one amax word and one
 //    progress counter per group).  Every GPU that loads the library holds
 //    it until the process exits.
 //  * Host code cannot use the array's name as a device address (on the
 //    host it only stands in for the symbol).  The first call on a device
 //    looks the address up with cudaGetSymbolAddress, with that device
-//    current, and caches it; make that first call before any stream
-//    capture on the device.
+//    current, and caches it together with the identity of the device's
+//    current context; a call that finds another context (after a
+//    cudaDeviceReset, say) looks the address up again.  Make the first call
+//    on a device, and the first after a reset, before any stream capture.
 //  * All calls share the one array and it keeps the last call's contents:
 //    the words a call uses are cleared (cudaMemsetAsync on the call's
 //    stream) before its kernel runs.  Calls whose kernels overlap on
 //    the GPU (different streams, no ordering between them) race on the
 //    array; order them on one stream.
 //  * Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -38,7 +41,7 @@ namespace mxq {
 namespace {
 
 constexpr int64_t kNoAllocMaxGroups = 4096;
-// 256-byte header (task counter) + an amax word and a progress counter per
+// 256-byte header (task counters) + an amax word and a progress counter per
 // group.
 constexpr int64_t kNoAllocWords = 64 + 2 * kNoAllocMaxGroups;
 static __device__ __align__(256) uint32_t g_noalloc_amax[kNoAllocWords];
@@ -46,20 +49,57 @@ static __device__ __align__(256) uint32_t g_noalloc_amax[kNoAllocWords];
 constexpr int kMaxDev = 64;
 std::mutex g_mu;
 uint32_t* g_addr[kMaxDev] = {};
+unsigned long long g_ctx_id[kMaxDev] = {};
 
-// Device address of g_noalloc_amax on the current device (looked up once
-// per device).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 if it cannot be
+// read), from the driver entry points cuCtxGetCurrent and cuCtxGetId.
+unsigned long long current_ctx_id() {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000,
+                                         cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000,
+                                         cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_cur && get_id && get_cur(&ctx) == CUDA_SUCCESS && ctx &&
+      get_id(ctx, &id) == CUDA_SUCCESS)
+    return id;
+  return 0;
+}
+
+// Device address of g_noalloc_amax on the current device: looked up with
+// cudaGetSymbolAddress on the first call on the device, and again when the
+// device's context is no longer the one the cached address belongs to.
 cudaError_t noalloc_scratch(uint32_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  // 0 when no context is current yet (the lookup below creates it)
+  const unsigned long long ctx = current_ctx_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
+  if (!g_addr[dev] || ctx == 0 || ctx != g_ctx_id[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_amax);
     if (e != cudaSuccess) return e;
     g_addr[dev] = static_cast<uint32_t*>(p);
+    g_ctx_id[dev] = current_ctx_id();   // the context the lookup used
   }
   *out = g_addr[dev];
   return cudaSuccess;
@@ -86,6 +126,8 @@ mxq_status nvfp4_quantize_weight_shared_noalloc(
     const int64_t* part_rows, int64_t K, uint8_t* codes,
     uint8_t* block_scales, float* group_scales, const float* group_scales_in,
     int scale_layout, void* stream) {
+  const int fm = host_fault_mode();
+  if (fm == 2) return MXQ_ERR_ARG;
   if (scale_layout != MXQ_SCALE_LINEAR && scale_layout != MXQ_SCALE_SWIZZLED)
     return MXQ_ERR_LAYOUT;
   if (num_groups < 0 || K < 0) return MXQ_ERR_SHAPE;
@@ -109,6 +151,7 @@ mxq_status nvfp4_quantize_weight_shared_noalloc(
       !is_aligned16(group_scales) ||
       (group_scales_in && !is_aligned16(group_scales_in)))
     return MXQ_ERR_ALIGN;
+  if (fm == 1) return MXQ_ERR_CUDA;
   uint32_t* scratch = nullptr;
   if (noalloc_scratch(&scratch) != cudaSuccess) return MXQ_ERR_CUDA;
   cudaError_t e = launch_nvfp4_weight_shared(

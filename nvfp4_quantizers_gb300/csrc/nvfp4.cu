@@ -334,16 +334,18 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 // group g there are nA amax tasks (64 KiB of the group each) and nE encode
 // tasks (2 or 4 sets of ROWS rows); an encode task needs its group's S, i.e.
 // every amax task of the group.  Groups are taken in windows of about
-// 32 MB of input, and the list runs A(0) A(1) E(0) A(2) E(1) ... E(last):
+// 24 MB of input, and the list runs A(0) A(1) E(0) A(2) E(1) ... E(last):
 // the amax tasks of a window, then those of the next window, then the
-// encode tasks of the first one.  CTAs take tasks in list order from an
-// atomic counter, so an encode task only ever waits (bounded) for amax
-// tasks that running CTAs already hold, and by the time it is handed out a
-// window of amax tasks and one of encode tasks separate it from its
-// group's; the two windows in flight (about 64 MB) stay in the 126 MB L2,
-// so the encode tasks read their rows back from L2 however many groups a
-// call holds (those reads mark the lines first to evict, so lines still
-// waiting for their second read outlive the ones read twice).
+// encode tasks of the first one (task_of has the general form with the
+// amax tasks L windows ahead; L = 1 measured best: 24 MB windows 248 us,
+// 32 MB 261 us, 48 MB 287 us, 16 MB x L = 2 262 us for 128 gate/up pairs).
+// CTAs take tasks in list order from an atomic counter, so an encode task
+// only ever waits (bounded) for amax tasks that running CTAs already hold,
+// and by the time it is handed out a window of amax tasks and one of encode
+// tasks separate it from its group's; the two windows in flight stay in
+// the 126 MB L2, so the encode tasks read their rows back from L2 however
+// many groups a call holds (those reads mark the lines first to evict, so
+// lines still waiting for their second read outlive the ones read twice).
 //
 // Workspace: [1 + launch] the task counter of each launch; [64 + g] the
 // amax of group g (float bits, merged with atomicMax); [64 + G + g] the
@@ -363,7 +365,8 @@ __host__ __device__ constexpr int RowSets(int r, int wpr) {
   return (wpr == 1 && r <= 2) ? 4 : 2;
 }
 constexpr int kWsHeaderWords = 64;            // [1 + launch] = task counters
-constexpr int64_t kWindowBytes = 32ll << 20;  // input bytes per window
+constexpr int64_t kWindowBytes = 24ll << 20;  // input bytes per window
+constexpr int64_t kLeadWindows = 1;           // amax windows ahead, L
 
 // Error word of the bounded waits of this translation unit.
 __device__ unsigned int g_nvfp4_wait_error = 0;
@@ -381,6 +384,7 @@ struct GroupParams {
   int ng;                             // groups in this launch
   int64_t nA, nE;                     // amax / encode tasks per group
   int64_t win;                        // groups per window (>= 1)
+  int64_t lead;                       // windows of amax tasks ahead, L
   uint8_t* codes;                     // group g at g * R * K/2
   uint8_t* scales;                    // group g at g * scale_stride
   int64_t scale_stride;
@@ -404,9 +408,12 @@ __device__ __forceinline__ const uint16_t* chunk_ptr(const GroupTable& tab,
 
 // Task t of the list -> (is_amax, local group, index within the group).
 // With S given there are only encode tasks, group-major.  Otherwise the
-// list is A(0), then for w = 0, 1, ...: A(w+1) (if window w+1 exists) and
-// E(w); A(w) holds nA tasks per group of window w, E(w) nE per group, and
-// every window but the last holds `win` groups.
+// list is A(0) .. A(L-1), then for w = 0, 1, ...: A(w+L) (if window w+L
+// exists) and E(w); A(w) holds nA tasks per group of window w, E(w) nE per
+// group, and every window but the last holds `win` groups.  The amax tasks
+// of a group thus run L windows of amax work and L - 1 windows of encode
+// work before its encode tasks, which is the time its slowest amax task
+// has to become visible, while the L2 holds about L + 1 windows of input.
 __device__ __forceinline__ void task_of(const GroupParams& p, int64_t t,
                                         bool* is_a, int* gl, int64_t* idx) {
   if (p.S_in) {
@@ -415,46 +422,60 @@ __device__ __forceinline__ void task_of(const GroupParams& p, int64_t t,
     *idx = t - (int64_t)*gl * p.nE;
     return;
   }
+  // Closed form (no loop over windows: the decode is on every task's
+  // path).  Every window but the last is full (W groups): a = W nA amax
+  // and e = W nE encode tasks; the last has `last` groups.
   const int64_t W = p.win;
   const int64_t nw = (p.ng + W - 1) / W;
-  const int64_t last = p.ng - (nw - 1) * W;        // groups of window nw-1
-  int64_t w = 0;                                   // window of the segment
-  int64_t g0 = 0, per = p.nA;                      // segment's first group
-  bool a = true;
-  const int64_t a0 = (nw == 1 ? last : W) * p.nA;
-  if (t >= a0) {
-    t -= a0;
-    // pairs (A(w+1), E(w)) with both windows full: w = 0 .. nw-3
-    const int64_t pair = W * (p.nA + p.nE);
-    const int64_t nfull = nw >= 3 ? nw - 2 : 0;
-    w = t / pair;
-    if (w > nfull) w = nfull;
-    t -= w * pair;
-    if (w + 1 < nw) {
-      const int64_t sa = (w + 1 == nw - 1 ? last : W) * p.nA;
-      if (t < sa) {
-        g0 = (w + 1) * W;
-      } else {
-        t -= sa;
-        const int64_t se = W * p.nE;               // window w < nw-1: full
-        a = false;
-        per = p.nE;
-        if (t < se) {
-          g0 = w * W;
-        } else {
-          t -= se;
-          g0 = (w + 1) * W;                        // final E(nw-1)
-        }
-      }
-    } else {
-      a = false;                                   // nw == 1: E(0)
-      per = p.nE;
-    }
+  const int64_t last = p.ng - (nw - 1) * W;
+  const int64_t L = p.lead < nw ? p.lead : nw;
+  const int64_t a = W * p.nA, e = W * p.nE;
+  const int64_t a_last = last * p.nA, e_last = last * p.nE;
+  auto amax_task = [&](int64_t w, int64_t r) {
+    *is_a = true;
+    *gl = (int)(w * W + r / p.nA);
+    *idx = r % p.nA;
+  };
+  auto enc_task = [&](int64_t w, int64_t r) {
+    *is_a = false;
+    *gl = (int)(w * W + r / p.nE);
+    *idx = r % p.nE;
+  };
+  // 1. A(0) .. A(L-1)
+  if (L < nw) {
+    if (t < L * a) return amax_task(t / a, t % a);
+    t -= L * a;
+  } else {
+    if (t < (nw - 1) * a) return amax_task(t / a, t % a);
+    t -= (nw - 1) * a;
+    if (t < a_last) return amax_task(nw - 1, t);
+    t -= a_last;
   }
-  *is_a = a;
-  const int64_t k = t / per;
-  *gl = (int)(g0 + k);
-  *idx = t - k * per;
+  int64_t w_tail = 0;                              // first window of step 3
+  if (L < nw) {
+    // 2. pairs A(w+L) E(w), w = 0 .. nw-L-1; the last pair's A is the
+    //    last window
+    const int64_t full_pairs = nw - L - 1;
+    if (t < full_pairs * (a + e)) {
+      const int64_t w = t / (a + e), r = t % (a + e);
+      if (r < a) return amax_task(w + L, r);
+      return enc_task(w, r - a);
+    }
+    t -= full_pairs * (a + e);
+    if (t < a_last) return amax_task(nw - 1, t);
+    t -= a_last;
+    if (t < e) return enc_task(nw - L - 1, t);
+    t -= e;
+    w_tail = nw - L;
+  }
+  // 3. E(w) for the remaining windows, the last one possibly partial
+  const int64_t full_tail = (nw - 1) - w_tail;     // full windows before the last
+  if (t < full_tail * e) return enc_task(w_tail + t / e, t % e);
+  t -= full_tail * e;
+  if (t < e_last) return enc_task(nw - 1, t);
+  *is_a = false;                                   // past the list's end
+  *gl = 0;
+  *idx = 0;
 }
 
 __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
@@ -751,6 +772,7 @@ cudaError_t launch_nvfp4_weight_shared(
   p.nE = (p.R_pad + rows_per_task - 1) / rows_per_task;
   p.win = kWindowBytes / (p.R * K * 2);
   if (p.win < 1) p.win = 1;
+  p.lead = kLeadWindows;
   p.done = ws ? ws + kWsHeaderWords + num_groups : nullptr;
   p.codes = codes;
   p.scales = scales;

@@ -201,6 +201,36 @@ def test_fault_injection_returns_errors_without_launching(L):
         L.mxq_set_fault_inject(0)
 
 
+def test_noalloc_entry_point_honours_fault_injection(L):
+    import nvfp4_quantizers_gb300 as q
+    f = L.nvfp4_quantize_weight_shared_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_int, ctypes.c_void_p]
+    ptrs = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    rows = (ctypes.c_int64 * 2)(16, 16)
+    args = (1, 2, ctypes.cast(ptrs, ctypes.c_void_p),
+            ctypes.cast(rows, ctypes.c_void_p), 64, FAKE, FAKE, FAKE, None, 1,
+            None)
+    try:
+        L.mxq_set_fault_inject(2)
+        assert f(*args) == q.MXQ_ERR_ARG
+        L.mxq_set_fault_inject(1)
+        # valid arguments: reported as a failed launch, nothing issued
+        assert f(*args) == q.MXQ_ERR_CUDA
+    finally:
+        L.mxq_set_fault_inject(0)
+    # argument errors come before any device call
+    assert f(4097, 2, ctypes.cast(ptrs, ctypes.c_void_p),
+             ctypes.cast(rows, ctypes.c_void_p), 64, FAKE, FAKE, FAKE, None,
+             1, None) == q.MXQ_ERR_SHAPE
+    assert f(1, 2, ctypes.cast(ptrs, ctypes.c_void_p),
+             ctypes.cast(rows, ctypes.c_void_p), 64, FAKE + 8, FAKE, FAKE,
+             None, 1, None) == q.MXQ_ERR_ALIGN
+
+
 def test_python_binding_raises_on_error(L):
     import nvfp4_quantizers_gb300 as q
     with pytest.raises(q.MxqError) as ei:

@@ -166,11 +166,11 @@ def _bands(M, n, seed):
     return sorted(set(b.tolist()) | {0, M // 32 - 1})
 
 
-@pytest.mark.parametrize("cls", ["random", "boundary"])
+@pytest.mark.parametrize("cls", ["random", "boundary", "zeros", "maxes"])
 def test_mxfp8_full_size_sampled(mxq, cls):
     """The 8192 x 4096 activation at full size (the benchmark's launch
-    configuration): sampled 32-row bands compared with the oracle for both
-    copies and both dequantizations."""
+    configuration), for each of the four input classes: sampled 32-row bands
+    compared with the oracle for both copies and both dequantizations."""
     M, K = 8192, 4096
     x_bits = W.MXFP8_CLASSES[cls](M, K)
     x = dev_bf16(x_bits)
@@ -430,14 +430,14 @@ def test_weight_wide_rows_and_slices(mxq, lay):
 
 
 def test_weight_windows(mxq):
-    """Five gate/up pairs of [1024 x 4096] (16 MiB each): the unit list
-    spans three windows of groups (2, 2, 1).  Every group scale is checked,
-    and the groups at the start of the first and of the last window byte
-    for byte."""
+    """Three gate/up pairs of [2048 x 4096] (32 MiB each, larger than a
+    window): the task list spans three windows of one group each.  Every
+    group scale is checked, and the first and the last group byte for
+    byte."""
     rng = np.random.default_rng(12)
-    groups_bits = [[W.to_bf16_bits(rng.standard_normal((1024, 4096)) * s),
-                    W.to_bf16_bits(rng.standard_normal((1024, 4096)) * 2 * s)]
-                   for s in (0.01, 0.1, 1.0, 3.0, 0.02)]
+    groups_bits = [[W.to_bf16_bits(rng.standard_normal((2048, 4096)) * s),
+                    W.to_bf16_bits(rng.standard_normal((2048, 4096)) * 2 * s)]
+                   for s in (0.01, 1.0, 0.02)]
     groups = [[dev_bf16(x) for x in g] for g in groups_bits]
     r = mxq.nvfp4_quantize_weight_shared(groups)
     torch.cuda.synchronize()
@@ -445,7 +445,7 @@ def test_weight_windows(mxq):
     S = r.scales.cpu().numpy()
     for e, (a, b) in enumerate(groups_bits):
         assert S[e] == O.nvfp4_tensor_scale(max(O.bf16_amax(a), O.bf16_amax(b)))
-    for e in (0, 4):
+    for e in (0, 2):
         oc, osc, oS = O.nvfp4_quantize_group(groups_bits[e])
         assert_bytes_equal(host_u8(r.codes[e]), oc, f"group {e} codes")
         assert_bytes_equal(host_u8(r.block_scales[e]), O.scale_swizzle(osc),
@@ -456,13 +456,14 @@ def test_weight_full_moe_layer_sampled(mxq):
     """128 Qwen3-30B-A3B-shaped experts at full size: gate/up fused pairs
     [1536 x 2048] under one scale each, down [2048 x 768] under its own.
     Every group scale is checked; three experts are checked byte for byte
-    (codes, scales, dequant)."""
+    (codes, scales, and the dequantization of both)."""
     E = 128
     experts = [W.moe_expert(e) for e in range(E)]
     gu = mxq.nvfp4_quantize_weight_shared(
         [[dev_bf16(g), dev_bf16(u)] for g, u, d in experts])
     dn = mxq.nvfp4_quantize_weight_shared([[dev_bf16(d)] for g, u, d in experts])
     ygu = mxq.dequantize_nvfp4(gu.codes, gu.block_scales, gu.scales)
+    ydn = mxq.dequantize_nvfp4(dn.codes, dn.block_scales, dn.scales)
     torch.cuda.synchronize()
     assert mxq.get_last_error() == mxq.MXQ_OK
     for e, (g, u, d) in enumerate(experts):
@@ -482,3 +483,46 @@ def test_weight_full_moe_layer_sampled(mxq):
         assert_bytes_equal(host_u8(dn.codes[e]), oc, f"expert {e} down codes")
         assert_bytes_equal(host_u8(dn.block_scales[e]), O.scale_swizzle(osc),
                            f"expert {e} down scales")
+        assert_bytes_equal(host_bits(ydn[e]),
+                           O.nvfp4_dequantize(oc, osc, np.array([oS])),
+                           f"expert {e} down dequant")
+
+
+# --------------------------------------------------------------------------
+# Weight groups of many shapes: the MoE layer's gate/up pairs and down
+# projections, small and odd part sizes, rows whose block count is not a
+# multiple of 4, many groups, given scales right after computed ones.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("lay", LAYOUTS)
+@pytest.mark.parametrize("rows,K,G", [
+    ((768, 768), 2048, 3),      # gate/up pairs
+    ((2048,), 768, 5),          # down projections, 48 blocks per row
+    ((200, 56), 512, 7),        # ~256 KiB groups, parts of 200 and 56 rows
+    ((33,), 4096, 9),           # 33 rows of 4096: a partial scale tile
+    ((1000,), 1552, 2),         # 97 blocks per row: byte scale stores
+])
+def test_weight_group_shapes(mxq, lay, rows, K, G):
+    rng = np.random.default_rng(sum(rows) + K + G)
+    groups = [[W.to_bf16_bits(rng.standard_normal((r, K)) * s * (1 + i))
+               for i, r in enumerate(rows)]
+              for s in np.geomspace(1e-3, 40.0, G)]
+    check_weight_groups(mxq, groups, lay)
+
+
+def test_weight_many_groups(mxq):
+    """300 small groups (more than one launch's 256) and a zero group."""
+    rng = np.random.default_rng(21)
+    groups = [[W.to_bf16_bits(rng.standard_normal((32, 64)) * (g % 7 + 1))]
+              for g in range(300)]
+    groups[5] = [np.zeros((32, 64), np.uint16)]
+    check_weight_groups(mxq, groups, "swizzled")
+
+
+def test_weight_scale_in_after_amax(mxq):
+    """A call with group_scales_in right after an amax call on the same
+    workspace-sized groups: the given scales are used as they are."""
+    experts = [W.moe_expert(e, hidden=2048, ffn=768, seed=6) for e in range(3)]
+    gu = [[g, u] for g, u, d in experts]
+    r = check_weight_groups(mxq, gu, "swizzled")
+    S_in = (r.scales.cpu().numpy() * np.float32(1.5)).astype(np.float32)
+    check_weight_groups(mxq, gu, "swizzled", S_in=S_in)

@@ -45,7 +45,7 @@ def _dev(bits):
         .view(torch.bfloat16).cuda()
 
 
-def _call_noalloc(L, groups, scale_layout):
+def _call_noalloc(L, groups, scale_layout, S_in=None):
     import nvfp4_quantizers_gb300 as q
     G, P = len(groups), len(groups[0])
     K = groups[0][0].shape[1]
@@ -58,7 +58,8 @@ def _call_noalloc(L, groups, scale_layout):
     S = torch.full((G,), -1.0, dtype=torch.float32, device="cuda")
     st = L.nvfp4_quantize_weight_shared_noalloc(
         G, P, ctypes.cast(ptrs, _p), ctypes.cast(rows, _p), K,
-        codes.data_ptr(), scales.data_ptr(), S.data_ptr(), None,
+        codes.data_ptr(), scales.data_ptr(), S.data_ptr(),
+        None if S_in is None else S_in.data_ptr(),
         q._lib._layout(scale_layout),
         torch.cuda.current_stream().cuda_stream)
     assert st == q.MXQ_OK, q.status_string(st)
@@ -107,3 +108,47 @@ def test_noalloc_rejects_too_many_groups(L):
         cap + 1, 1, ctypes.cast(ptrs, _p), ctypes.cast(rows, _p), 16,
         0x10000, 0x10000, 0x10000, None, 1, None)
     assert st == q.MXQ_ERR_SHAPE
+
+
+def _compare(L, groups, S_in=None, scale_layout="swizzled"):
+    """The no-alloc call (twice) against the workspace entry point."""
+    import nvfp4_quantizers_gb300 as q
+    ref = q.nvfp4_quantize_weight_shared(groups, S_in, scale_layout)
+    for _ in range(2):
+        got = _call_noalloc(L, groups, scale_layout, S_in)
+        torch.cuda.synchronize()
+        assert torch.equal(got[0], ref.codes)
+        assert torch.equal(got[1], ref.block_scales)
+        assert torch.equal(got[2].view(torch.int32), ref.scales.view(torch.int32))
+    assert q.get_last_error() == q.MXQ_OK
+
+
+def test_noalloc_more_groups_than_one_launch(L):
+    """300 small groups: two launches, whose group words sit at different
+    offsets of the library's array."""
+    rng = np.random.default_rng(41)
+    groups = [[_dev(W.to_bf16_bits(rng.standard_normal((32, 64)) * (g % 5 + 1)))]
+              for g in range(300)]
+    _compare(L, groups)
+
+
+def test_noalloc_near_the_group_cap(L):
+    """4000 groups of [16 x 16]: the array's words up to near its end."""
+    rng = np.random.default_rng(42)
+    host = W.to_bf16_bits(rng.standard_normal((4000, 16, 16)))
+    x = _dev(host.reshape(4000 * 16, 16))
+    groups = [[x[16 * g:16 * g + 16]] for g in range(4000)]
+    _compare(L, groups)
+
+
+def test_noalloc_scales_given_after_an_amax_call(L):
+    """An amax call, then a call with group_scales_in: the array keeps the
+    first call's words, which the second must not use."""
+    import nvfp4_quantizers_gb300 as q
+    experts = [W.moe_expert(e, hidden=512, ffn=128, seed=43) for e in range(4)]
+    groups = [[_dev(g), _dev(u)] for g, u, _ in experts]
+    _compare(L, groups)
+    S_in = torch.tensor([0.5, 0.01, 2.0, 1e-4], dtype=torch.float32,
+                        device="cuda")
+    _compare(L, groups, S_in=S_in)
+
