@@ -573,16 +573,27 @@ def run_gemm(q, W, dev, stream, reps=20):
         torch.bfloat16).to(dev)
     idx_dev = torch.from_numpy(idx).to(dev)
 
-    def t_gq():
-        return q.nvfp4_quantize_per_token_gather(tok_dev, idx_dev)
-    ms_gq = _time_fn(t_gq, stream, reps)
-    tg = t_gq()
+    ops = _Ops(q, dev, stream)
+    call_gq, _ = ops.gather_quantize(tok_dev, idx_dev)
+    ms_gq = _time_fn(call_gq, stream, reps)
+    tg = q.nvfp4_quantize_per_token_gather(tok_dev, idx_dev)
 
     def t_sw():
         return q.moe_gate_up_swiglu(tg.codes, tg.block_scales, tg.scales,
                                     offs2, tw.codes, tw.block_scales,
                                     tw.scales)
     ms_sw = _time_fn(t_sw, stream, reps)
+    # the same forward with the gather in the GEMM's operand load: the
+    # unique tokens quantized once (linear block scales), each routed row
+    # gathered by the GEMM
+    call_q1, _ = ops.per_token(tok_dev, lay=q.SCALE_LINEAR)
+    ms_q1 = _time_fn(call_q1, stream, reps)
+    xq = q.nvfp4_quantize_per_token(tok_dev, "linear")
+
+    def t_swg():
+        return q.moe_gate_up_swiglu_gather(xq, idx_dev, offs2, tw.codes,
+                                           tw.block_scales, tw.scales)
+    ms_swg = _time_fn(t_swg, stream, reps)
     Mp2 = int(offs2[-1])
     # gather-quantize: the unique tokens read once, gathered codes, block
     # scales and token scales written
@@ -597,7 +608,13 @@ def run_gemm(q, W, dev, stream, reps=20):
            "gather_quantize_GB/s": round(nb_gq / ms_gq / 1e6, 1),
            "gather_quantize_hbm_frac": round(
                nb_gq / ms_gq / 1e6 / measured_peak()[0], 3),
-           "forward_us": round((ms_gq + ms_sw) * 1e3, 2),
+           "forward_us_materialized": round((ms_gq + ms_sw) * 1e3, 2),
+           "quantize_unique_tokens_us": round(ms_q1 * 1e3, 2),
+           "gather_in_gemm_us": round(ms_swg * 1e3, 2),
+           "forward_us": round((ms_q1 + ms_swg) * 1e3, 2),
+           "forward": ("per-token quantize of the 4096 unique tokens, then the "
+                       "gate/up GEMM gathering the routed rows in its operand "
+                       "load (no routed copy in HBM)"),
            "padded_rows": Mp2, "output": "bf16 h [rows x 768]"})
     # Dequantized-backward data gradient of the linear layer (2048, 2048) ->
     # 8192: dX [2048 x 2048] = dY [2048 x 8192] x W, W's columnwise MXFP8
@@ -726,16 +743,17 @@ class _Ops:
             self.chk(self.L.dequantize_mxfp8(*args), "dequantize_mxfp8")
         return call
 
-    def per_token(self, x, rht_flags=None, seed=2026):
+    def per_token(self, x, rht_flags=None, seed=2026, lay=None):
         T, H = x.shape
         q = self.q
+        lay = self.lay if lay is None else lay
         c = self.u8(T * H // 2)
-        bs = self.u8(q.scale_bytes(T, H // 16))
+        bs = self.u8(q.scale_bytes(T, H // 16, lay))
         S = self.torch.empty(T, dtype=self.torch.float32, device=self.dev)
         keep = (x, c, bs, S)
         if rht_flags is None:
             args = (x.data_ptr(), T, H, H, c.data_ptr(), bs.data_ptr(),
-                    S.data_ptr(), self.lay, self.s)
+                    S.data_ptr(), lay, self.s)
 
             def call(keep=keep):
                 self.chk(self.L.nvfp4_quantize_per_token(*args), "per-token")
@@ -747,6 +765,22 @@ class _Ops:
             def call(keep=keep):
                 self.chk(self.L.nvfp4_quantize_per_token_rht_sr(*args),
                          "per-token rht/sr")
+        return call, (c, bs, S)
+
+    def gather_quantize(self, x, idx):
+        """Per-token NVFP4 of the rows idx of x (the routed copy)."""
+        T_src, H = x.shape
+        T = idx.numel()
+        q = self.q
+        c = self.u8(T * H // 2)
+        bs = self.u8(q.scale_bytes(T, H // 16))
+        S = self.torch.empty(T, dtype=self.torch.float32, device=self.dev)
+        args = (x.data_ptr(), T_src, H, H, idx.data_ptr(), T, c.data_ptr(),
+                bs.data_ptr(), S.data_ptr(), self.lay, self.s)
+        keep = (x, idx, c, bs, S)
+
+        def call(keep=keep):
+            self.chk(self.L.nvfp4_quantize_per_token_gather(*args), "gather")
         return call, (c, bs, S)
 
     def dq_nvfp4(self, codes, bs, S, mode, batch, rows, cols):
@@ -1185,7 +1219,7 @@ PROFILE_WORKLOADS = (
     "weight_gate_up_128_given_scale",
     "dequant_nvfp4_gate_up_128", "fp8_block_1x128", "fp8_block_128x128",
     "fp8_block_requant_t", "gemm_mxfp8", "gemm_nvfp4_grouped",
-    "moe_gate_up_swiglu", "gemm_bf16_dq")
+    "moe_gate_up_swiglu", "moe_gate_up_swiglu_gather", "gemm_bf16_dq")
 
 
 def run_profile(args):
@@ -1300,6 +1334,10 @@ def _gemm_workloads(q, W, dev):
     out["moe_gate_up_swiglu"] = lambda: q.moe_gate_up_swiglu(
         tg.codes, tg.block_scales, tg.scales, offs, tw.codes, tw.block_scales,
         tw.scales)
+    xq = q.nvfp4_quantize_per_token(dev16(tokens), "linear")
+    idx_dev = torch.from_numpy(idx).to(dev)
+    out["moe_gate_up_swiglu_gather"] = lambda: q.moe_gate_up_swiglu_gather(
+        xq, idx_dev, offs, tw.codes, tw.block_scales, tw.scales)
     dY = dev16(W.gemm_tokens(2048, 8192))
     wq = q.mxfp8_quantize_rowcol(dev16(W.linear_weight()), rowwise=False,
                                  colwise=True)

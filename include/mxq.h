@@ -489,6 +489,44 @@ mxq_status mxq_moe_gate_up_swiglu_nvfp4(
     const uint8_t* w_scales, const float* w_group_scales, int64_t F, int64_t K,
     void* h, int64_t ldh, void* stream);
 
+/* --------------------------------------------------------------------- */
+/* The grouped NVFP4 GEMM and the MoE gate/up + SwiGLU GEMM with the      */
+/* routing gather in the GEMM's operand load.                             */
+/*                                                                       */
+/* [MILES] NVFP4 recipe section (SwiGLU MoE layers, gate and up fused     */
+/* into one GEMM under one FP32 weight scale) and experiments section     */
+/* (the per-token scale applied in the GEMM rather than as a separate     */
+/* operation).  Per-token quantization does not depend on the batch, so   */
+/* the unique tokens are quantized once (nvfp4_quantize_per_token with    */
+/* MXQ_SCALE_LINEAR) and the GEMM gathers each routed row's codes (TMA    */
+/* gather of four rows per instruction) and block scales as it loads A;   */
+/* no routed copy of the tokens is written.                               */
+/*                                                                       */
+/* x_codes        u8 [T_src x K/2], x_scales its LINEAR E4M3 block scales */
+/*                [T_src x K/16], x_token_scales f32 [T_src].              */
+/* row_index      int32 [group_offsets[num_groups]] (device): routed row r */
+/*                is token row_index[r]; an index outside [0, T_src) is a  */
+/*                padding row, whose outputs are +0.                       */
+/* Everything else, and every result byte, as mxq_gemm_nvfp4_grouped and */
+/* mxq_moe_gate_up_swiglu_nvfp4 on the gathered operand that             */
+/* nvfp4_quantize_per_token_gather writes.                                */
+/* [bounded waits]: a device-side wait that gives up is reported by the   */
+/* next mxq_get_last_error(), not by this call's status.                  */
+/* --------------------------------------------------------------------- */
+mxq_status mxq_gemm_nvfp4_grouped_gather(
+    const uint8_t* x_codes, const uint8_t* x_scales, const float* x_token_scales,
+    int64_t T_src, const int32_t* row_index, const int64_t* group_offsets,
+    int64_t num_groups, const uint8_t* w_codes, const uint8_t* w_scales,
+    const float* w_group_scales, int64_t N, int64_t K, float* C, int64_t ldc,
+    void* stream);
+
+mxq_status mxq_moe_gate_up_swiglu_nvfp4_gather(
+    const uint8_t* x_codes, const uint8_t* x_scales, const float* x_token_scales,
+    int64_t T_src, const int32_t* row_index, const int64_t* group_offsets,
+    int64_t num_groups, const uint8_t* w_codes, const uint8_t* w_scales,
+    const float* w_group_scales, int64_t F, int64_t K, void* h, int64_t ldh,
+    void* stream);
+
 #ifdef __cplusplus
 }
 #endif

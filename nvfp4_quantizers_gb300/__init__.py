@@ -12,7 +12,8 @@ from ._lib import (  # noqa: F401
     Mxfp8Quantized, MxqError, Nvfp4Quantized, dequantize_mxfp8,
     dequantize_nvfp4, fp8_block_dequantize, fp8_block_quantize,
     fp8_block_requantize_transpose, gemm_bf16_mxfp8, gemm_mxfp8,
-    gemm_nvfp4_grouped, get_last_error, lib, moe_gate_up_swiglu,
+    gemm_nvfp4_grouped, gemm_nvfp4_grouped_gather, get_last_error, lib,
+    moe_gate_up_swiglu, moe_gate_up_swiglu_gather,
     mxfp8_quantize_rowcol, nvfp4_quantize_per_token,
     NVFP4_RHT, NVFP4_SR, nvfp4_quantize_per_token_gather,
     nvfp4_quantize_per_token_rht_sr, nvfp4_quantize_weight_shared,

@@ -98,6 +98,12 @@ def lib() -> ctypes.CDLL:
         L.mxq_moe_gate_up_swiglu_nvfp4.restype = _int
         L.mxq_moe_gate_up_swiglu_nvfp4.argtypes = [
             _p, _p, _p, _p, _i64, _p, _p, _p, _i64, _i64, _p, _i64, _p]
+        L.mxq_gemm_nvfp4_grouped_gather.restype = _int
+        L.mxq_gemm_nvfp4_grouped_gather.argtypes = [
+            _p, _p, _p, _i64, _p, _p, _i64, _p, _p, _p, _i64, _i64, _p, _i64, _p]
+        L.mxq_moe_gate_up_swiglu_nvfp4_gather.restype = _int
+        L.mxq_moe_gate_up_swiglu_nvfp4_gather.argtypes = [
+            _p, _p, _p, _i64, _p, _p, _i64, _p, _p, _p, _i64, _i64, _p, _i64, _p]
         L.dequantize_nvfp4.restype = _int
         L.dequantize_nvfp4.argtypes = [_p, _p, _p, _int, _i64, _i64, _i64,
                                        _int, _p, _p]
@@ -460,6 +466,68 @@ def moe_gate_up_swiglu(a_codes: torch.Tensor, a_scales: torch.Tensor,
         ctypes.cast(off_arr, ctypes.c_void_p), G, w_codes.data_ptr(),
         w_scales.data_ptr(), w_group_scales.data_ptr(), F, K, h.data_ptr(), F,
         _stream(a_codes.device)), "mxq_moe_gate_up_swiglu_nvfp4")
+    return h
+
+
+def _gather_operand(x: Nvfp4Quantized, row_index: torch.Tensor):
+    if x.scale_layout != SCALE_LINEAR:
+        raise ValueError("the gathered GEMMs take the tokens' block scales in "
+                         "the linear layout (nvfp4_quantize_per_token(x, "
+                         "'linear'))")
+    if (row_index.dtype != torch.int32 or row_index.dim() != 1
+            or row_index.device != x.codes.device or not row_index.is_contiguous()):
+        raise ValueError("row_index must be a contiguous int32 vector on the "
+                         "tokens' device")
+    T_src, half = x.codes.shape
+    return T_src, half * 2
+
+
+def gemm_nvfp4_grouped_gather(x: Nvfp4Quantized, row_index: torch.Tensor,
+                              group_offsets, w_codes: torch.Tensor,
+                              w_scales: torch.Tensor,
+                              w_group_scales: torch.Tensor) -> torch.Tensor:
+    """Expert-grouped NVFP4 GEMM whose routed rows are gathered from the
+    per-token operand x (quantized once, linear scales) as the GEMM loads
+    them: row r is token row_index[r], padding rows (index outside
+    [0, T_src)) give +0 (C: mxq_gemm_nvfp4_grouped_gather)."""
+    T_src, K = _gather_operand(x, row_index)
+    offs = [int(v) for v in group_offsets]
+    G = len(offs) - 1
+    if row_index.numel() != offs[-1]:
+        raise ValueError("row_index must hold one entry per routed row")
+    N = w_codes.shape[1]
+    off_arr = (ctypes.c_int64 * len(offs))(*offs)
+    C = torch.empty((offs[-1], N), dtype=torch.float32, device=x.codes.device)
+    _check(lib().mxq_gemm_nvfp4_grouped_gather(
+        x.codes.data_ptr(), x.block_scales.data_ptr(), x.scales.data_ptr(),
+        T_src, row_index.data_ptr(), ctypes.cast(off_arr, ctypes.c_void_p), G,
+        w_codes.data_ptr(), w_scales.data_ptr(), w_group_scales.data_ptr(), N,
+        K, C.data_ptr(), N, _stream(x.codes.device)),
+        "mxq_gemm_nvfp4_grouped_gather")
+    return C
+
+
+def moe_gate_up_swiglu_gather(x: Nvfp4Quantized, row_index: torch.Tensor,
+                              group_offsets, w_codes: torch.Tensor,
+                              w_scales: torch.Tensor,
+                              w_group_scales: torch.Tensor) -> torch.Tensor:
+    """MoE gate/up GEMM with SwiGLU in the epilogue, the routed rows
+    gathered from the per-token operand x as the GEMM loads them
+    (C: mxq_moe_gate_up_swiglu_nvfp4_gather).  Returns bf16 h [rows, F]."""
+    T_src, K = _gather_operand(x, row_index)
+    offs = [int(v) for v in group_offsets]
+    G = len(offs) - 1
+    if row_index.numel() != offs[-1]:
+        raise ValueError("row_index must hold one entry per routed row")
+    F = w_codes.shape[1] // 2
+    off_arr = (ctypes.c_int64 * len(offs))(*offs)
+    h = torch.empty((offs[-1], F), dtype=torch.bfloat16, device=x.codes.device)
+    _check(lib().mxq_moe_gate_up_swiglu_nvfp4_gather(
+        x.codes.data_ptr(), x.block_scales.data_ptr(), x.scales.data_ptr(),
+        T_src, row_index.data_ptr(), ctypes.cast(off_arr, ctypes.c_void_p), G,
+        w_codes.data_ptr(), w_scales.data_ptr(), w_group_scales.data_ptr(), F,
+        K, h.data_ptr(), F, _stream(x.codes.device)),
+        "mxq_moe_gate_up_swiglu_nvfp4_gather")
     return h
 
 

@@ -563,4 +563,90 @@ mxq_status mxq_moe_gate_up_swiglu_nvfp4(
       static_cast<cudaStream_t>(stream)));
 }
 
+// Shared checks of the gathered grouped GEMMs: the per-token operand x
+// [T_src rows] with linear block scales, int32 row_index [rows].
+static mxq_status check_gather(const uint8_t* x_codes, const uint8_t* x_scales,
+                               const float* x_s, int64_t T_src,
+                               const int32_t* row_index) {
+  if (T_src <= 0 || T_src >= (1ll << 31)) return MXQ_ERR_SHAPE;
+  if (!x_codes || !x_scales || !x_s || !row_index) return MXQ_ERR_NULL;
+  if (!aligned16(x_codes) || !aligned16(x_scales) ||
+      (reinterpret_cast<uintptr_t>(row_index) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(x_s) & 3u) != 0)
+    return MXQ_ERR_ALIGN;
+  return MXQ_OK;
+}
+
+mxq_status mxq_gemm_nvfp4_grouped_gather(
+    const uint8_t* x_codes, const uint8_t* x_scales, const float* x_token_scales,
+    int64_t T_src, const int32_t* row_index, const int64_t* group_offsets,
+    int64_t num_groups, const uint8_t* w_codes, const uint8_t* w_scales,
+    const float* w_group_scales, int64_t N, int64_t K, float* C, int64_t ldc,
+    void* stream) {
+  const int fm = fault_mode();
+  if (fm == 2) return MXQ_ERR_ARG;
+  if (num_groups < 0 || num_groups > 256 || N < 0 || K < 0 || ldc < N)
+    return MXQ_ERR_SHAPE;
+  if (num_groups == 0 || N == 0) return MXQ_OK;
+  if (!group_offsets) return MXQ_ERR_NULL;
+  if (group_offsets[0] != 0) return MXQ_ERR_SHAPE;
+  for (int64_t g = 0; g < num_groups; ++g)
+    if (group_offsets[g + 1] < group_offsets[g] ||
+        group_offsets[g + 1] % 128 != 0)
+      return MXQ_ERR_SHAPE;
+  if (group_offsets[num_groups] == 0) return MXQ_OK;
+  const mxq_status st =
+      check_gather(x_codes, x_scales, x_token_scales, T_src, row_index);
+  if (st != MXQ_OK) return st;
+  if (!w_codes || !w_scales || !w_group_scales || !C) return MXQ_ERR_NULL;
+  if (N % 128 != 0 || K % 256 != 0 || K == 0) return MXQ_ERR_SHAPE;
+  if (group_offsets[num_groups] >= (1ll << 31) || num_groups * N >= (1ll << 31) ||
+      K >= (1ll << 31))
+    return MXQ_ERR_SHAPE;
+  if (!aligned16(w_codes) || !aligned16(w_scales) || !aligned16(C) ||
+      ldc % 4 != 0)
+    return MXQ_ERR_ALIGN;
+  if (fm == 1) return MXQ_ERR_CUDA;
+  return from_cuda(launch_gemm_nvfp4_grouped(
+      x_codes, x_scales, x_token_scales, group_offsets, num_groups, w_codes,
+      w_scales, w_group_scales, N, K, C, ldc,
+      static_cast<cudaStream_t>(stream), row_index, T_src));
+}
+
+mxq_status mxq_moe_gate_up_swiglu_nvfp4_gather(
+    const uint8_t* x_codes, const uint8_t* x_scales, const float* x_token_scales,
+    int64_t T_src, const int32_t* row_index, const int64_t* group_offsets,
+    int64_t num_groups, const uint8_t* w_codes, const uint8_t* w_scales,
+    const float* w_group_scales, int64_t F, int64_t K, void* h, int64_t ldh,
+    void* stream) {
+  const int fm = fault_mode();
+  if (fm == 2) return MXQ_ERR_ARG;
+  if (num_groups < 0 || num_groups > 256 || F < 0 || K < 0 || ldh < F)
+    return MXQ_ERR_SHAPE;
+  if (num_groups == 0 || F == 0) return MXQ_OK;
+  if (!group_offsets) return MXQ_ERR_NULL;
+  if (group_offsets[0] != 0) return MXQ_ERR_SHAPE;
+  for (int64_t g = 0; g < num_groups; ++g)
+    if (group_offsets[g + 1] < group_offsets[g] ||
+        group_offsets[g + 1] % 128 != 0)
+      return MXQ_ERR_SHAPE;
+  if (group_offsets[num_groups] == 0) return MXQ_OK;
+  const mxq_status st =
+      check_gather(x_codes, x_scales, x_token_scales, T_src, row_index);
+  if (st != MXQ_OK) return st;
+  if (!w_codes || !w_scales || !w_group_scales || !h) return MXQ_ERR_NULL;
+  if (F % 128 != 0 || K % 256 != 0 || K == 0) return MXQ_ERR_SHAPE;
+  if (group_offsets[num_groups] >= (1ll << 31) ||
+      num_groups * 2 * F >= (1ll << 31) || K >= (1ll << 31))
+    return MXQ_ERR_SHAPE;
+  if (!aligned16(w_codes) || !aligned16(w_scales) || !aligned16(h) ||
+      ldh % 8 != 0)
+    return MXQ_ERR_ALIGN;
+  if (fm == 1) return MXQ_ERR_CUDA;
+  return from_cuda(launch_moe_gate_up_swiglu(
+      x_codes, x_scales, x_token_scales, group_offsets, num_groups, w_codes,
+      w_scales, w_group_scales, F, K, h, ldh,
+      static_cast<cudaStream_t>(stream), row_index, T_src));
+}
+
 }  // extern "C"

@@ -52,7 +52,9 @@ constexpr int GN = 256;              // tile cols (B rows) = MMA N
 constexpr int GKB = 128;             // bytes of K per stage per row
 constexpr int GSTAGES = 3;
 constexpr int kEpiWarps = 8;         // 4 lane quarters x 2 column halves
-constexpr int GTHREADS = 32 * (3 + kEpiWarps);  // producer, MMA, waiter, epilogue
+constexpr int kSfWarp = 3 + kEpiWarps;  // gathers A's block scales (gather mode)
+// producer, MMA, waiter, epilogue, scale gatherer
+constexpr int GTHREADS = 32 * (4 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;  // accumulator 256 + scale columns
 constexpr uint32_t kSfCol0 = 256;    // 64 scale columns per stage
 constexpr uint32_t kSfColsPerStage = 64;
@@ -208,6 +210,21 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// 2-D tiled TMA gather of four rows (rows y0..y3, the box's columns from
+// x) into four consecutive box-sized rows of shared memory, completion on
+// `bar`.  The tensor map's box is one row high.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map,
+                                            int32_t x, int32_t y0, int32_t y1,
+                                            int32_t y2, int32_t y3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2),
+      "r"(y3), "r"(bar)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor (sm_100 family): start address, leading
 // and stride byte offsets (all >> 4), version 1 at bit 46, layout type at
 // bits 61-63 (0 = no swizzle, 2 = 128-byte swizzle).
@@ -243,6 +260,15 @@ struct GemmParams {
   int64_t b_sf_group_stride;   // bytes between the scale matrices of groups
   int64_t b_rows_group_stride; // rows between the groups' weights in the B map
   // NVFP4 grouped
+  // Gather mode (row_index != NULL): routed row r of A is row row_index[r]
+  // of the per-token operand (codes through the A tensor map, block scales
+  // in the linear layout at a_sf_lin, a_sf_ld bytes per row, S_tok per
+  // source row); an index outside [0, T_src) is a padding row (zero block
+  // scales and S_tok, so it contributes 0).
+  const int32_t* row_index;
+  int64_t T_src;
+  const uint8_t* a_sf_lin;
+  int64_t a_sf_ld;
   const float* s_tok;
   const float* s_w;
   int num_groups;
@@ -305,7 +331,8 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   if (warp == 0) tmem_alloc(smem_addr(&s.tmem_base), kTmemCols);
   if (threadIdx.x == 0) {
     for (int i = 0; i < GSTAGES; ++i) {
-      mbar_init(smem_addr(&s.full[i]), 1);
+      // the producer's arrive (+ the scale gatherer's in gather mode)
+      mbar_init(smem_addr(&s.full[i]), p.row_index ? 2 : 1);
       mbar_init(smem_addr(&s.empty[i]), 1);   // freed by the MMA commit
     }
     mbar_init(smem_addr(&s.acc_full), 1);
@@ -324,27 +351,52 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   const int n_sf = p.kind == 1 ? 4 : 1;  // scale tiles per stage and row block
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- producer ----------------
-      int64_t it = 0;
-      int grp_cursor = 0;
-      for (int64_t u = unit0; u < n_units; u += unit_step) {
-        const Tile t = decode_tile(p, u, &grp_cursor);
-        // B row blocks of this tile that exist (the last column tile may
-        // hold only 128 columns); rows past them are never stored.
-        const int nrb = (EPI == 1 || t.n0 + 128 < p.N) ? 2 : 1;
-        const uint32_t stage_bytes =
-            (uint32_t)(GM * GKB + GN * GKB + 512 * n_sf * (1 + nrb));
-        for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
-          const int st = (int)(it % GSTAGES);
-          const uint32_t ph = (uint32_t)((it / GSTAGES) & 1);
-          if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1, &s.abort,
-                         &g_gemm_wait_error))
-            break;
-          const uint32_t full = smem_addr(&s.full[st]);
+    // ---------------- producer ----------------
+    // Lane 0 waits for free stages and issues the copies.  In gather mode
+    // every lane holds four of the tile's source rows (rows 4 lane ..
+    // 4 lane + 3) and issues their gather4 load itself (one lane issuing
+    // all 32, with the indices passed by shuffles, took longer per stage
+    // than the stage's MMAs).
+    int64_t it = 0;
+    int grp_cursor = 0, pf_cursor = 0;
+    bool ok = true;
+    // the gather rows of a tile: loaded one tile ahead, so that their
+    // latency is not on the path of the tile's first stage
+    int32_t nxt[4] = {0, 0, 0, 0};
+    auto load_rows = [&](int64_t u, int32_t (&dst)[4]) {
+      if (!p.row_index || u >= n_units) return;
+      const Tile tt = decode_tile(p, u, &pf_cursor);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        dst[k] = p.row_index[tt.m0 + 4 * lane + k];
+    };
+    load_rows(unit0, nxt);
+    for (int64_t u = unit0; u < n_units && ok; u += unit_step) {
+      const Tile t = decode_tile(p, u, &grp_cursor);
+      int32_t src[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)                    // padding: any real row
+        src[k] = (nxt[k] >= 0 && nxt[k] < p.T_src) ? nxt[k] : 0;
+      load_rows(u + unit_step, nxt);
+      // B row blocks of this tile that exist (the last column tile may
+      // hold only 128 columns); rows past them are never stored.
+      const int nrb = (EPI == 1 || t.n0 + 128 < p.N) ? 2 : 1;
+      const uint32_t stage_bytes = (uint32_t)(
+          GM * GKB + GN * GKB + 512 * n_sf * ((p.row_index ? 0 : 1) + nrb));
+      for (int64_t kt = 0; kt < p.k_stages; ++kt, ++it) {
+        const int st = (int)(it % GSTAGES);
+        const uint32_t ph = (uint32_t)((it / GSTAGES) & 1);
+        if (lane == 0)
+          ok = mbar_wait(smem_addr(&s.empty[st]), ph ^ 1, &s.abort,
+                         &g_gemm_wait_error);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const uint32_t full = smem_addr(&s.full[st]);
+        if (lane == 0) {
           mbar_arrive_expect_tx(full, stage_bytes);
-          tma_load_2d(smem_addr(s.a[st]), &tmap_a, (int32_t)(kt * GKB),
-                      (int32_t)t.m0, full);
+          if (!p.row_index)
+            tma_load_2d(smem_addr(s.a[st]), &tmap_a, (int32_t)(kt * GKB),
+                        (int32_t)t.m0, full);
           const int64_t brow = t.grp * p.b_rows_group_stride + t.n0;
           if (EPI == 0) {
             tma_load_2d(smem_addr(s.b[st]), &tmap_b, (int32_t)(kt * GKB),
@@ -360,9 +412,10 @@ __global__ void __launch_bounds__(GTHREADS, 1)
           // The stage's n_sf scale tiles of one 128-row block are
           // consecutive in the swizzled layout: one copy per row block.
           const int64_t ct = kt * n_sf;
-          bulk_g2s(smem_addr(s.sfa[st][0]),
-                   p.a_sf + ((t.m0 / 128) * p.a_sf_ct + ct) * 512,
-                   512u * n_sf, full);
+          if (!p.row_index)
+            bulk_g2s(smem_addr(s.sfa[st][0]),
+                     p.a_sf + ((t.m0 / 128) * p.a_sf_ct + ct) * 512,
+                     512u * n_sf, full);
           for (int rb = 0; rb < nrb; ++rb) {
             const int64_t rblk =
                 EPI == 0 ? t.n0 / 128 + rb : (t.n0 + rb * p.b_up_row) / 128;
@@ -372,8 +425,17 @@ __global__ void __launch_bounds__(GTHREADS, 1)
                      512u * n_sf, full);
           }
         }
-        if (s.abort) break;
+        if (p.row_index) {
+          // the A stage: every lane gathers its 4 routed rows (128 bytes of
+          // K each) into rows 4 lane .. 4 lane + 3 of the 128-byte-swizzled
+          // tile the MMA reads, once lane 0 has set the stage's byte count
+          __syncwarp();
+          tma_gather4(smem_addr(s.a[st]) + lane * 4 * GKB, &tmap_a,
+                      (int32_t)(kt * GKB), src[0], src[1], src[2], src[3],
+                      full);
+        }
       }
+      if (s.abort) break;
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -459,6 +521,90 @@ __global__ void __launch_bounds__(GTHREADS, 1)
         }
       }
     }
+  } else if (warp == kSfWarp) {
+    // ---------------- scale gatherer (gather mode) ----------------
+    // Lane l holds the tile's routed rows l + 32 j: each stage it loads
+    // their 16 block scales of the stage (linear layout: 16 contiguous
+    // bytes of the source row, four 4-column scale tiles) before waiting
+    // for the slot, then writes each 4-byte word to its place in the
+    // 128x4 tile layout the tensor core reads, (r % 32) * 16 + (r / 32) * 4,
+    // fences the writes to the async proxy and arrives on the stage.
+    if (p.row_index) {
+      // Stages in the order the producer fills them: stage it is k-stage
+      // it % k_stages of this CTA's tile it / k_stages.  Scale words are
+      // loaded D stages ahead into two static register buffers, and a
+      // tile's source rows one tile ahead of their first use.
+      const int64_t n_my = n_units > unit0 ? (n_units - unit0 + unit_step - 1) / unit_step : 0;
+      const int64_t total = n_my * p.k_stages;
+      const int D = p.k_stages >= 2 ? 2 : 1;
+      int cursor = 0;
+      int64_t cur_i = -1;                // tile of rc; rn is tile cur_i + 1
+      const uint8_t* rc[4];
+      const uint8_t* rn[4];
+      uint32_t vc = 0, vn = 0;           // bit j: row lane + 32 j is real
+      auto fetch_rows = [&](int64_t i, const uint8_t* (&src)[4], uint32_t& vb) {
+        vb = 0;
+        if (i >= n_my) return;
+        const Tile tt = decode_tile(p, unit0 + i * unit_step, &cursor);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int32_t v = p.row_index[tt.m0 + lane + 32 * j];
+          const bool ok_v = v >= 0 && v < p.T_src;
+          vb |= (ok_v ? 1u : 0u) << j;
+          src[j] = p.a_sf_lin + (int64_t)(ok_v ? v : 0) * p.a_sf_ld;
+        }
+      };
+      auto load_stage = [&](int64_t j2, uint4 (&w)[4]) {
+        const int64_t i = j2 / p.k_stages, kt = j2 % p.k_stages;
+        if (i != cur_i) {                 // i == cur_i + 1 (or the first)
+          if (cur_i < 0) {
+            fetch_rows(i, rc, vc);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) rc[j] = rn[j];
+            vc = vn;
+          }
+          cur_i = i;
+          fetch_rows(i + 1, rn, vn);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          w[j] = (vc >> j) & 1 ? ld_stream_v4(rc[j] + kt * 16)
+                               : make_uint4(0, 0, 0, 0);  // padding: scale 0
+      };
+      bool ok = true;
+      // stage it: wait for its slot, write the words of buffer w, arrive,
+      // then load stage it + D into w
+      auto step = [&](int64_t it, uint4 (&w)[4]) {
+        const int st = (int)(it % GSTAGES);
+        const uint32_t ph = (uint32_t)((it / GSTAGES) & 1);
+        if (lane == 0)
+          ok = mbar_wait(smem_addr(&s.empty[st]), ph ^ 1, &s.abort,
+                         &g_gemm_wait_error);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = lane + 32 * j;
+          const int off = (r & 31) * 16 + (r >> 5) * 4;
+          *reinterpret_cast<uint32_t*>(&s.sfa[st][0][off]) = w[j].x;
+          *reinterpret_cast<uint32_t*>(&s.sfa[st][1][off]) = w[j].y;
+          *reinterpret_cast<uint32_t*>(&s.sfa[st][2][off]) = w[j].z;
+          *reinterpret_cast<uint32_t*>(&s.sfa[st][3][off]) = w[j].w;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&s.full[st]));
+        if (it + D < total) load_stage(it + D, w);
+      };
+      uint4 wa[4], wb[4];
+      if (total > 0) load_stage(0, wa);
+      if (D == 2 && total > 1) load_stage(1, wb);
+      for (int64_t it = 0; it < total && ok; it += D) {
+        step(it, wa);
+        if (D == 2 && it + 1 < total && ok) step(it + 1, wb);
+      }
+    }
   } else {
     // ---------------- epilogue: warps 3-10 ----------------
     // Tensor-memory lane quarter q = warp id mod 4 (lane = tile row),
@@ -504,8 +650,17 @@ __global__ void __launch_bounds__(GTHREADS, 1)
 
       const Tile t = decode_tile(p, u, &grp_cursor);
       float rs = 1.0f;
-      if (p.kind == 1)
-        rs = __fmul_rn(p.s_tok[t.m0 + q * 32 + lane], p.s_w[t.grp]);
+      bool pad = false;               // gather mode: a padding row, stored as +0
+      if (p.kind == 1) {
+        if (p.row_index) {
+          // gather mode: the routed row's source token
+          const int32_t v = p.row_index[t.m0 + q * 32 + lane];
+          pad = !(v >= 0 && v < p.T_src);
+          rs = pad ? 0.0f : __fmul_rn(p.s_tok[v], p.s_w[t.grp]);
+        } else {
+          rs = __fmul_rn(p.s_tok[t.m0 + q * 32 + lane], p.s_w[t.grp]);
+        }
+      }
       uint8_t* row = box + lane * 128;
       if (EPI == 0) {
         const int64_t x0 = t.n0 + h * 128;
@@ -526,6 +681,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
               v.y = __fmul_rn(v.y, rs);
               v.z = __fmul_rn(v.z, rs);
               v.w = __fmul_rn(v.w, rs);
+              if (pad) v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
             *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) = v;
           }
@@ -560,7 +716,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
             float h0, h1;
             fmul2(g0, g1, s0, s1, h0, h1);
             fmul2(h0, h1, u0, u1, h0, h1);
-            w[k] = f32x2_to_bf16x2(h0, h1);
+            w[k] = pad ? 0u : f32x2_to_bf16x2(h0, h1);
           }
           *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) =
               make_uint4(w[0], w[1], w[2], w[3]);
@@ -600,10 +756,12 @@ cudaError_t make_tmap_c(CUtensorMap* map, float* C, int64_t rows,
                           (uint64_t)ldc * 4, 32, 32);
 }
 
-// A operand as a byte matrix [a_rows x a_row_bytes].
+// A operand as a byte matrix [a_rows x a_row_bytes], loaded in boxes of
+// box_rows rows (GM for tiles, 1 for the gather4 loads of gather mode).
 struct AOperand {
   const uint8_t* base;
   int64_t row_bytes, rows;
+  uint32_t box_rows = GM;
 };
 
 // One CTA per SM (or per tile when there are fewer tiles).
@@ -628,7 +786,7 @@ cudaError_t launch_gemm(const AOperand& a, const CUtensorMap& tb,
   }
   CUtensorMap ta;
   err = make_tmap_2d_u8(&ta, a.base, (uint64_t)a.row_bytes, (uint64_t)a.rows,
-                        (uint64_t)a.row_bytes, (uint32_t)GM);
+                        (uint64_t)a.row_bytes, a.box_rows);
   if (err != cudaSuccess) return err;
   const int64_t grid = imin<int64_t>(tiles, sm_count(dev));
   return launch_pdl(kern, dim3((unsigned)grid), dim3(GTHREADS), smem, stream,
@@ -659,6 +817,17 @@ void grouped_params(GemmParams& p, const uint8_t* a_scales, const float* a_s,
     *tiles_m += (group_offsets[g + 1] - group_offsets[g]) / GM;
     p.tile_end[g] = *tiles_m;
   }
+}
+
+// Gather mode of the two grouped launchers: A's rows are rows row_index[r]
+// of the per-token operand x (codes [T_src x K/2], linear block scales
+// [T_src x K/16], S [T_src]).
+void gather_params(GemmParams& p, const int32_t* row_index, int64_t T_src,
+                   const uint8_t* x_scales_lin, int64_t K) {
+  p.row_index = row_index;
+  p.T_src = T_src;
+  p.a_sf_lin = x_scales_lin;
+  p.a_sf_ld = K / 16;
 }
 
 }  // namespace
@@ -707,7 +876,8 @@ cudaError_t launch_gemm_nvfp4_grouped(
     const uint8_t* a_codes, const uint8_t* a_scales, const float* a_s,
     const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
     const uint8_t* w_scales, const float* w_s, int64_t N, int64_t K, float* C,
-    int64_t ldc, cudaStream_t stream) {
+    int64_t ldc, cudaStream_t stream, const int32_t* row_index,
+    int64_t T_src) {
   // Packed E2M1: K/2 bytes per row; all groups' weights as one
   // [num_groups * N x K/2] byte matrix.
   CUtensorMap tb;
@@ -724,19 +894,22 @@ cudaError_t launch_gemm_nvfp4_grouped(
   p.tile_cols = GN;
   p.C = C;
   p.ldc = ldc;
+  if (row_index) gather_params(p, row_index, T_src, a_scales, K);
   if (tiles_m == 0) return cudaSuccess;
   CUtensorMap tc;
   err = make_tmap_c(&tc, C, p.M, N, ldc);
   if (err != cudaSuccess) return err;
-  return launch_gemm<0>(AOperand{a_codes, K / 2, p.M}, tb, tc, p,
-                        tiles_m * p.tiles_n, stream);
+  const AOperand a = row_index ? AOperand{a_codes, K / 2, T_src, 1}
+                               : AOperand{a_codes, K / 2, p.M};
+  return launch_gemm<0>(a, tb, tc, p, tiles_m * p.tiles_n, stream);
 }
 
 cudaError_t launch_moe_gate_up_swiglu(
     const uint8_t* a_codes, const uint8_t* a_scales, const float* a_s,
     const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
     const uint8_t* w_scales, const float* w_s, int64_t F, int64_t K,
-    void* out, int64_t ldo, cudaStream_t stream) {
+    void* out, int64_t ldo, cudaStream_t stream, const int32_t* row_index,
+    int64_t T_src) {
   // weights: [num_groups * 2F x K/2] bytes, gate rows then up rows per
   // group, loaded as 128-row boxes (gate block and matching up block)
   CUtensorMap tb;
@@ -754,13 +927,15 @@ cudaError_t launch_moe_gate_up_swiglu(
   p.b_up_row = F;
   p.C = nullptr;
   p.ldc = ldo;
+  if (row_index) gather_params(p, row_index, T_src, a_scales, K);
   if (tiles_m == 0) return cudaSuccess;
   CUtensorMap tc;                       // bf16 h [rows x F], 32 x 64 boxes
   err = make_tmap_2d_bf16(&tc, out, (uint64_t)F, (uint64_t)p.M,
                           (uint64_t)ldo * 2, 64, 32, true);
   if (err != cudaSuccess) return err;
-  return launch_gemm<1>(AOperand{a_codes, K / 2, p.M}, tb, tc, p,
-                        tiles_m * p.tiles_n, stream);
+  const AOperand a = row_index ? AOperand{a_codes, K / 2, T_src, 1}
+                               : AOperand{a_codes, K / 2, p.M};
+  return launch_gemm<1>(a, tb, tc, p, tiles_m * p.tiles_n, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -114,17 +114,23 @@ cudaError_t launch_gemm_mxfp8(const uint8_t* a_codes, const uint8_t* a_scales,
                               const uint8_t* bt_scales, int64_t M, int64_t N,
                               int64_t K, float* C, int64_t ldc,
                               cudaStream_t stream);
+// row_index != NULL (gather mode): A's routed row r is row row_index[r] of
+// the per-token operand (a_codes [T_src x K/2], a_scales its LINEAR block
+// scales [T_src x K/16], a_s [T_src]); indices outside [0, T_src) are
+// padding rows, which contribute 0.
 cudaError_t launch_gemm_nvfp4_grouped(
     const uint8_t* a_codes, const uint8_t* a_scales, const float* a_s,
     const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
     const uint8_t* w_scales, const float* w_s, int64_t N, int64_t K, float* C,
-    int64_t ldc, cudaStream_t stream);
+    int64_t ldc, cudaStream_t stream, const int32_t* row_index = nullptr,
+    int64_t T_src = 0);
 // h = silu(gate) * up over the grouped gate/up GEMM, bf16 [rows x F].
 cudaError_t launch_moe_gate_up_swiglu(
     const uint8_t* a_codes, const uint8_t* a_scales, const float* a_s,
     const int64_t* group_offsets, int64_t num_groups, const uint8_t* w_codes,
     const uint8_t* w_scales, const float* w_s, int64_t F, int64_t K,
-    void* out, int64_t ldo, cudaStream_t stream);
+    void* out, int64_t ldo, cudaStream_t stream,
+    const int32_t* row_index = nullptr, int64_t T_src = 0);
 
 // Scale-matrix size in bytes for either layout.
 inline int64_t scale_bytes(int64_t rows, int64_t cols, int swizzled) {

@@ -298,3 +298,42 @@ def test_guard_grouped_nvfp4_and_swiglu(mxq):
        "swiglu")
     h.check("h")
     same(h, ref2, "h")
+
+
+def test_guard_gather_in_gemm(mxq):
+    """The routing gather inside the grouped GEMMs' operand load."""
+    q = mxq
+    L = q.lib()
+    T_src, H, F, E = 300, 512, 128, 3
+    x = dev_bf16(W.gemm_tokens(T_src, H, seed=6))
+    xq = q.nvfp4_quantize_per_token(x, "linear")
+    rows = [128, 256, 128]
+    offs = np.concatenate([[0], np.cumsum(rows)])
+    Mt = int(offs[-1])
+    idx = (np.arange(Mt, dtype=np.int32) * 7) % T_src
+    idx[::5] = -1
+    idx_dev = torch.from_numpy(idx).cuda()
+    wts = [dev_bf16(np.concatenate(W.moe_expert(e, hidden=H, ffn=F, seed=6)[:2]))
+           for e in range(E)]
+    tw = q.nvfp4_quantize_weight_shared([[w] for w in wts])
+    off_arr = (ctypes.c_int64 * (E + 1))(*[int(v) for v in offs])
+    ref = q.gemm_nvfp4_grouped_gather(xq, idx_dev, offs, tw.codes, tw.block_scales,
+                                      tw.scales)
+    C = Guarded(Mt * 2 * F * 4)
+    ok(q, L.mxq_gemm_nvfp4_grouped_gather(
+        xq.codes.data_ptr(), xq.block_scales.data_ptr(), xq.scales.data_ptr(), T_src,
+        idx_dev.data_ptr(), ctypes.cast(off_arr, ctypes.c_void_p), E,
+        tw.codes.data_ptr(), tw.block_scales.data_ptr(), tw.scales.data_ptr(), 2 * F,
+        H, C.ptr, 2 * F, stream()), "grouped gather")
+    C.check("C")
+    same(C, ref, "C")
+    ref2 = q.moe_gate_up_swiglu_gather(xq, idx_dev, offs, tw.codes, tw.block_scales,
+                                       tw.scales)
+    h = Guarded(Mt * F * 2)
+    ok(q, L.mxq_moe_gate_up_swiglu_nvfp4_gather(
+        xq.codes.data_ptr(), xq.block_scales.data_ptr(), xq.scales.data_ptr(), T_src,
+        idx_dev.data_ptr(), ctypes.cast(off_arr, ctypes.c_void_p), E,
+        tw.codes.data_ptr(), tw.block_scales.data_ptr(), tw.scales.data_ptr(), F, H,
+        h.ptr, F, stream()), "swiglu gather")
+    h.check("h")
+    same(h, ref2, "h")

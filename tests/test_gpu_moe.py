@@ -163,3 +163,71 @@ def test_moe_forward_full_size_sampled(mxq):
                                    tw.scales.cpu().numpy()[e:e + 1])
         _check_h(hn[r0:r1], ref, f"expert {e}")
         assert np.all(hn[r1:int(offs[e + 1])] == 0), "padding rows"
+
+
+# --------------------------------------------------------------------------
+# The routing gather inside the GEMM's operand load: the unique tokens are
+# quantized once (per-token quantization does not depend on the batch) and
+# each routed row is gathered by the GEMM.  The outputs must be the bytes of
+# the path that writes the gathered operand first.
+# --------------------------------------------------------------------------
+def _gather_case(q, T_src, H, F, E, k, seed):
+    tokens = W.gemm_tokens(T_src, H, seed=seed)
+    route = W.topk_routing(T_src, E, k, seed=seed)
+    idx, offs, _ = W.expert_gather_index(route, E)
+    x = dev_bf16(tokens)
+    idx_dev = torch.from_numpy(idx).cuda()
+    experts = [W.moe_expert(e, hidden=H, ffn=F, seed=seed) for e in range(E)]
+    tw = q.nvfp4_quantize_weight_shared(
+        [[dev_bf16(g), dev_bf16(u)] for g, u, _ in experts])
+    return x, idx_dev, offs, tw
+
+
+@pytest.mark.parametrize("T_src,H,F,E,k", [(300, 512, 128, 5, 2),
+                                           (1000, 1024, 384, 16, 4),
+                                           (4096, 2048, 768, 128, 8)])
+def test_gather_in_gemm_matches_materialized(mxq, T_src, H, F, E, k):
+    q = mxq
+    x, idx, offs, tw = _gather_case(q, T_src, H, F, E, k, seed=T_src + E)
+    ref_a = q.nvfp4_quantize_per_token_gather(x, idx)
+    ref_h = q.moe_gate_up_swiglu(ref_a.codes, ref_a.block_scales, ref_a.scales,
+                                 offs, tw.codes, tw.block_scales, tw.scales)
+    ref_c = q.gemm_nvfp4_grouped(ref_a.codes, ref_a.block_scales, ref_a.scales,
+                                 offs, tw.codes, tw.block_scales, tw.scales)
+    xq = q.nvfp4_quantize_per_token(x, "linear")
+    h = q.moe_gate_up_swiglu_gather(xq, idx, offs, tw.codes, tw.block_scales,
+                                    tw.scales)
+    c = q.gemm_nvfp4_grouped_gather(xq, idx, offs, tw.codes, tw.block_scales,
+                                    tw.scales)
+    torch.cuda.synchronize()
+    assert q.get_last_error() == q.MXQ_OK
+    assert torch.equal(h.view(torch.int16), ref_h.view(torch.int16))
+    assert torch.equal(c.view(torch.int32), ref_c.view(torch.int32))
+
+
+def test_gather_in_gemm_index_edges(mxq):
+    """Padding (-1), out-of-range and repeated indices, the last token."""
+    q = mxq
+    T_src, H, F = 200, 512, 256
+    x = dev_bf16(W.gemm_tokens(T_src, H, seed=41))
+    rows = [256, 128]
+    idx = np.arange(384, dtype=np.int32) % T_src
+    idx[5::9] = -1
+    idx[7] = T_src
+    idx[11] = T_src - 1
+    idx[200:260] = 3
+    offs = np.array([0, 256, 384])
+    experts = [W.moe_expert(e, hidden=H, ffn=F, seed=41) for e in range(2)]
+    tw = q.nvfp4_quantize_weight_shared(
+        [[dev_bf16(g), dev_bf16(u)] for g, u, _ in experts])
+    idx_dev = torch.from_numpy(idx).cuda()
+    ref_a = q.nvfp4_quantize_per_token_gather(x, idx_dev)
+    ref_h = q.moe_gate_up_swiglu(ref_a.codes, ref_a.block_scales, ref_a.scales,
+                                 offs, tw.codes, tw.block_scales, tw.scales)
+    xq = q.nvfp4_quantize_per_token(x, "linear")
+    h = q.moe_gate_up_swiglu_gather(xq, idx_dev, offs, tw.codes,
+                                    tw.block_scales, tw.scales)
+    torch.cuda.synchronize()
+    assert torch.equal(h.view(torch.int16), ref_h.view(torch.int16))
+    pad = (idx < 0) | (idx >= T_src)
+    assert torch.all(h[torch.from_numpy(pad).cuda()].view(torch.int16) == 0)
