@@ -11,14 +11,13 @@
 //          the inner one exact)
 //
 // Design (sm_103a): pure streaming, grid-stride over 16-element units with
-// four 256-thread CTAs per SM.  A thread converts 16 values per unit: a
+// eight 256-thread CTAs per SM.  A thread converts 16 values per unit: a
 // 16-byte (MXFP8) or 8-byte (NVFP4) code load, one scale byte, and one
-// 32-byte bf16 store.  With a per-row S (activations) the NVFP4 kernel
-// takes four units per step, one grid stride apart, and issues all their
-// loads before the first conversion, so four units' loads are in flight
-// per thread (one at a time left it waiting on load latency) while the
-// work still splits evenly over the grid in single units; the MXFP8
-// kernel and the per-group NVFP4 one measured best one unit at a time.  The codes widen exactly through
+// 32-byte bf16 store.  The NVFP4 kernel takes two units per step, one grid
+// stride apart, and issues both units' loads before the first conversion
+// (one at a time left it waiting on load latency: the ragged 132106 x 2048
+// batch 138 -> 108 us) while the work still splits evenly over the grid in
+// single units; the MXFP8 kernel measured best one unit at a time.  The codes widen exactly through
 // cvt.rn.f16x2.{e4m3x2,e2m1x2}; the scale multiply is one binary32
 // multiply and the bf16 rounding one cvt.rn.bf16x2.f32.  Index math is
 // 32-bit whenever every index fits.
@@ -30,10 +29,13 @@ namespace mxq {
 namespace {
 
 constexpr int DQ_THREADS = 256;
-constexpr int DQ_CTAS_PER_SM = 4;
+// Eight CTAs per SM (all 64 warps; at most 48 registers a thread): with
+// four, too few loads were in flight per SM (8192 x 4096 MXFP8 19.1 ->
+// 17.5 us, 128 gate/up NVFP4 weights 187 -> 162 us with two units a step).
+constexpr int DQ_CTAS_PER_SM = 8;
 constexpr int DQ_UNROLL_MXFP8 = 1;         // units per thread per step
-constexpr int DQ_UNROLL_NVFP4_ROW = 4;     // NVFP4, S per row
-constexpr int DQ_UNROLL_NVFP4_BATCH = 1;   // NVFP4, S per weight group
+constexpr int DQ_UNROLL_NVFP4_ROW = 2;     // NVFP4, S per row
+constexpr int DQ_UNROLL_NVFP4_BATCH = 2;   // NVFP4, S per weight group
 
 // MXFP8: a thread converts 16 codes (one 16-byte load, half a 1x32 block)
 // into 32 bytes of bf16 per step.  Idx is uint32_t when every index fits.

@@ -370,7 +370,8 @@ cudaError_t launch_fp8blk_dequantize(const uint8_t* codes, const float* scales,
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   const int64_t n16 = rows * (cols >> 4);
-  const unsigned grid = fb_grid(n16, FB_THREADS, dev, 4);
+  // all 64 warps of an SM (8192 x 4096 tiles: 18.7 -> 18.3 us against 4 CTAs)
+  const unsigned grid = fb_grid(n16, FB_THREADS, dev, 8);
   const int wide = (reinterpret_cast<uintptr_t>(y) & 31u) == 0;
   return launch_pdl(fp8blk_dequant_kernel, dim3(grid), dim3(FB_THREADS), 0,
                     stream, false, codes, scales, rows, cols,
