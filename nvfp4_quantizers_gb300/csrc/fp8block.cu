@@ -208,14 +208,19 @@ __global__ void __launch_bounds__(FB_THREADS)
 }
 
 // Backward-orientation conversion: tile (ti, tj) of X [M x K] is dequantized
-// into shared memory transposed (column-major bf16, column pitch 136
-// halfwords), then each of its 128 columns is quantized as one 1x128 tile
-// of X^T.
-//   Dequantize: a thread takes two adjacent rows and 32 columns and writes
-//   each column's pair of rows as one 32-bit word (consecutive lanes hold
-//   consecutive row pairs: no bank conflicts); its loads of the CTA's next
-//   tile are issued right after, so they are in flight while this tile is
-//   quantized.
+// into shared memory transposed (column-major bf16, 256 bytes a column),
+// then each of its 128 columns is quantized as one 1x128 tile of X^T.
+//   Dequantize: a thread takes 8 rows and 8 columns (one 8-byte code load
+//   per row: a warp's loads are two whole 128-byte rows), converts them,
+//   transposes the 8 x 8 bf16 block in registers (byte permutes) and
+//   writes each column's 8 rows as one 16-byte store.  Chunk k (rows
+//   8k .. 8k + 7) of column c sits at chunk k ^ ((c / 8) % 16) of the
+//   column, so the 8 lanes of a store phase (8 column groups, one row
+//   group) hit 8 different bank quads.  Its loads of the CTA's next tile
+//   are issued right after, so they are in flight while this tile is
+//   quantized.  (Two rows and 4-byte stores per column made the kernel
+//   shared-memory-instruction bound: 512 store instructions a tile
+//   against 128.)
 //   Quantize: a warp takes 16 columns, 8 at a time, a lane 4 rows of each,
 //   so every code store is 128 contiguous bytes per warp.  The 8 column
 //   maxima are reduced together by a reduce-scatter over the lanes (lane
@@ -227,58 +232,74 @@ __global__ void __launch_bounds__(FB_THREADS)
 //   8 reciprocals by shuffle.  (A thread per column, with no cross-lane
 //   reduction, measured slower: its 16-byte stores land in 32 different
 //   rows of X^T.)
-constexpr int kPitch = 136;
-constexpr int kPitchW = kPitch / 2;       // 32-bit words per column
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p));
+  return v;
+}
+
+// Byte offset of rows 8k .. 8k + 7 of column c in the transposed tile.
+__device__ __forceinline__ int rt_chunk(int c, int k) {
+  return c * 256 + ((k ^ ((c >> 3) & 15)) << 4);
+}
 
 __global__ void __launch_bounds__(FB_THREADS)
     fp8blk_requant_t_kernel(const uint8_t* __restrict__ codes,
                             const float* __restrict__ scales, int64_t M,
                             int64_t K, uint8_t* __restrict__ codes_t,
                             float* __restrict__ scales_t) {
-  __shared__ __align__(16) uint32_t sm[128 * kPitchW];
+  __shared__ __align__(16) uint8_t sm[128 * 256];
   const int64_t nti = M >> 7, ntj = K >> 7;
   const int64_t ntiles = nti * ntj;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pr = threadIdx.x & 63;                  // row pair 2 pr, 2 pr + 1
-  const int cq = (threadIdx.x >> 6) * 32;           // 32-column quarter
+  const int cg = threadIdx.x & 15;                  // columns 8 cg .. + 7
+  const int rg = threadIdx.x >> 4;                  // rows 8 rg .. + 7
   const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
   const int mycol = (lane >> 2) & 7;                // column whose scales
   pdl_wait();                                       // this lane derives
-  // the codes and scales of this thread's two rows of a tile; the next
+  // the codes and scales of this thread's 8 rows of a tile; the next
   // tile's are loaded while the current one is quantized
-  uint4 cv[4];
-  float S0 = 0.0f, S1 = 0.0f;
+  uint2 cv[8];
+  float Sr[8];
   auto load_tile = [&](int64_t tile) {
     const int64_t ti = tile / ntj, tj = tile - ti * ntj;
-    const int64_t ra = ti * 128 + 2 * pr;
-    S0 = scales[ra * ntj + tj];
-    S1 = scales[(ra + 1) * ntj + tj];
-    const uint8_t* src = codes + ra * K + tj * 128 + cq;
-    cv[0] = ld_stream_v4(src);
-    cv[1] = ld_stream_v4(src + 16);
-    cv[2] = ld_stream_v4(src + K);
-    cv[3] = ld_stream_v4(src + K + 16);
+    const int64_t ra = ti * 128 + 8 * rg;
+    const uint8_t* src = codes + ra * K + tj * 128 + 8 * cg;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      Sr[i] = scales[(ra + i) * ntj + tj];
+      cv[i] = ld_stream_v2(src + i * K);
+    }
   };
   if ((int64_t)blockIdx.x < ntiles) load_tile(blockIdx.x);
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const int64_t ti = tile / ntj, tj = tile - ti * ntj;
     const int64_t r0 = ti * 128, c0 = tj * 128;
+    // w[i][j]: row i, columns 2j and 2j + 1 (low half = column 2j)
+    uint32_t w[8][4];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {                   // 16-column halves
-      uint4 lo0, hi0, lo1, hi1;
-      decode16(cv[k], S0, lo0, hi0);
-      decode16(cv[2 + k], S1, lo1, hi1);
-      const uint32_t w0[8] = {lo0.x, lo0.y, lo0.z, lo0.w,
-                              hi0.x, hi0.y, hi0.z, hi0.w};
-      const uint32_t w1[8] = {lo1.x, lo1.y, lo1.z, lo1.w,
-                              hi1.x, hi1.y, hi1.z, hi1.w};
+    for (int i = 0; i < 8; ++i) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int col = cq + 16 * k + 2 * e;
-        // column col: (row 2 pr, row 2 pr + 1) = the low halves
-        sm[col * kPitchW + pr] = __byte_perm(w0[e], w1[e], 0x5410);
-        sm[(col + 1) * kPitchW + pr] = __byte_perm(w0[e], w1[e], 0x7632);
+      for (int j = 0; j < 4; ++j) {
+        float a, b;
+        e4m3x2_to_f32(((j < 2 ? cv[i].x : cv[i].y) >> ((j & 1) * 16)) & 0xFFFFu,
+                      a, b);
+        fmul2(a, b, Sr[i], Sr[i], a, b);
+        w[i][j] = f32x2_to_bf16x2(a, b);
       }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int j = c >> 1;
+      const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
+      // column 8 cg + c, rows 8 rg .. 8 rg + 7 as four row pairs
+      const uint4 col = make_uint4(__byte_perm(w[0][j], w[1][j], sel),
+                                   __byte_perm(w[2][j], w[3][j], sel),
+                                   __byte_perm(w[4][j], w[5][j], sel),
+                                   __byte_perm(w[6][j], w[7][j], sel));
+      *reinterpret_cast<uint4*>(&sm[rt_chunk(8 * cg + c, rg)]) = col;
     }
     if (tile + gridDim.x < ntiles) load_tile(tile + gridDim.x);
     __syncthreads();
@@ -289,8 +310,9 @@ __global__ void __launch_bounds__(FB_THREADS)
       uint32_t m[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
+        // rows 4 lane .. 4 lane + 3: half (lane & 1) of chunk lane / 2
         v[j] = *reinterpret_cast<const uint2*>(
-            &sm[(cbase + j) * kPitchW + 2 * lane]);
+            &sm[rt_chunk(cbase + j, lane >> 1) + (lane & 1) * 8]);
         m[j] = bf16x2_hmax(bf16x2_maxabs(v[j].x, v[j].y) & 0x7FFF7FFFu);
       }
       // reduce-scatter of the 8 column maxima (bf16 bit patterns of
