@@ -365,6 +365,9 @@ mxq_status nvfp4_quantize_per_token_rht_sr(const void* x, int64_t T,
 /* block_rows = 128: 128x128 blocks (rows % 128 == 0).  cols % 128 == 0.  */
 /* codes u8 [rows x cols]; scales f32 [rows/block_rows x cols/128],       */
 /* row-major.  All pointers 16-byte aligned.                              */
+/* [bounded waits] (block_rows = 128): a device-side wait that gives up   */
+/* is reported by the next mxq_get_last_error(), not by this call's       */
+/* status.                                                               */
 /* --------------------------------------------------------------------- */
 mxq_status fp8_block_quantize(const void* x, int64_t rows, int64_t cols,
                               int64_t ldx, int block_rows, uint8_t* codes,

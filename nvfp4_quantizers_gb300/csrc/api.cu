@@ -190,11 +190,13 @@ int64_t mxq_scale_bytes(int64_t rows, int64_t cols, int scale_layout) {
 mxq_status mxq_get_last_error(void) {
   cudaError_t e = cudaDeviceSynchronize();
   unsigned int word = 0, word2 = 0;
-  unsigned int word3 = 0;
+  unsigned int word3 = 0, word4 = 0;
   cudaError_t e2 = mxfp8_take_wait_error(&word);
   if (e2 == cudaSuccess) e2 = nvfp4_take_wait_error(&word2);
   if (e2 == cudaSuccess) e2 = gemm_take_wait_error(&word3);
-  if (e2 == cudaSuccess && (word | word2 | word3) != 0) return MXQ_ERR_TIMEOUT;
+  if (e2 == cudaSuccess) e2 = fp8blk_take_wait_error(&word4);
+  if (e2 == cudaSuccess && (word | word2 | word3 | word4) != 0)
+    return MXQ_ERR_TIMEOUT;
   cudaError_t last = cudaGetLastError();
   if (e != cudaSuccess || e2 != cudaSuccess || last != cudaSuccess)
     return MXQ_ERR_CUDA;

@@ -40,7 +40,7 @@ constexpr int DQ_UNROLL_NVFP4_BATCH = 2;   // NVFP4, S per weight group
 // MXFP8: a thread converts 16 codes (one 16-byte load, half a 1x32 block)
 // into 32 bytes of bf16 per step.  Idx is uint32_t when every index fits.
 template <typename Idx, int DQ_UNROLL>
-__global__ void __launch_bounds__(DQ_THREADS)
+__global__ void __launch_bounds__(DQ_THREADS, DQ_CTAS_PER_SM)
     dequant_mxfp8_kernel(const uint8_t* __restrict__ codes,
                          const uint8_t* __restrict__ scales, Idx rows,
                          Idx cols, int swizzled, int wide,
@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(DQ_THREADS)
 // rows_per_batch rows, each with its own scale matrix (scale_stride bytes
 // apart); S is per row (global row index) or per batch entry.
 template <typename Idx, int DQ_UNROLL>
-__global__ void __launch_bounds__(DQ_THREADS)
+__global__ void __launch_bounds__(DQ_THREADS, DQ_CTAS_PER_SM)
     dequant_nvfp4_kernel(const uint8_t* __restrict__ codes,
                          const uint8_t* __restrict__ scales,
                          const float* __restrict__ S, int per_batch,

@@ -21,8 +21,8 @@
 // Design (sm_103a): HBM-streaming.  Tiles: 8 lanes per 1x128 tile, 32
 // bytes of bf16 per lane in one load (two tiles per lane in flight), amax
 // by three shuffles, 16 codes per lane in one 16-byte store.  Blocks: one
-// CTA per 128x128 block in a grid-stride loop, 64 values per thread held
-// in registers across the block reduction.  Dequantizer: one 16-code unit
+// CTA per 128x128 block in a grid-stride loop, the block staged in shared
+// memory by one TMA load (bounded wait).  Dequantizer: one 16-code unit
 // per thread per step, one 32-byte store.  Conversion: all of a thread's
 // code loads issued before it decodes, and eight columns quantized per
 // step with one reduce-scatter for all of them.
@@ -126,29 +126,75 @@ __global__ void __launch_bounds__(FB_THREADS)
   pdl_launch_dependents();
 }
 
-// 128x128 blocks: thread t holds row t % 128 of the block, columns
-// (t / 128) * 64 .. + 63.
-__global__ void __launch_bounds__(FB_THREADS)
-    fp8blk_block_kernel(const uint16_t* __restrict__ x, int64_t rows,
-                        int64_t cols, int64_t ldx, uint8_t* __restrict__ codes,
-                        float* __restrict__ scales, int wide) {
+// 128x128 blocks: a CTA takes one block at a time, brought into shared
+// memory by one 2-D TMA load (128 x 128 bf16, 32 KiB); the next block's
+// load is issued as soon as every thread has read the current one, so it
+// lands while the codes are stored.  Six CTAs per SM: the block stays in
+// shared memory, not registers, so that six blocks per SM (912 on the
+// GPU) are in flight at once; with the block held in registers (64 values
+// a thread) only four fit, and the 1024 blocks of an [8192 x 2048] weight
+// took two full rounds of load latency.  A warp reads two rows per
+// step, 16 bytes a lane (conflict-free), once for the amax and again to
+// encode; the codes of a lane's 8 values leave in one 8-byte store (a
+// warp writes two whole 128-byte rows).
+constexpr int FB_BLK_CTAS = 6;
+
+__device__ unsigned int g_fp8blk_wait_error = 0;
+
+__device__ __forceinline__ uint32_t absmax8(const uint4& v) {
+  return bf16x2_hmax(bf16x2_maxabs(bf16x2_maxabs(v.x, v.y),
+                                   bf16x2_maxabs(v.z, v.w)) &
+                     0x7FFF7FFFu);
+}
+
+__global__ void __launch_bounds__(FB_THREADS, FB_BLK_CTAS)
+    fp8blk_block_kernel(const __grid_constant__ CUtensorMap tmap,
+                        int64_t rows, int64_t cols,
+                        uint8_t* __restrict__ codes,
+                        float* __restrict__ scales) {
+  __shared__ __align__(128) uint4 blk[128 * 16];   // row r: chunks 16 r ..
+  __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t red[FB_THREADS / 32];
+  __shared__ int abort_flag;
   const int64_t nbc = cols >> 7;
   const int64_t nblk = (rows >> 7) * nbc;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rr = threadIdx.x & 127, cc = (threadIdx.x >> 7) * 64;
+  const int ch = lane & 15;                         // 16-byte chunk of a row
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(b, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
   pdl_wait();
-  for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
-    const int64_t bi = blk / nbc, bj = blk - bi * nbc;
-    const uint16_t* p = x + (bi * 128 + rr) * ldx + bj * 128 + cc;
-    uint4 v[8];
-    uint32_t m = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      load16(p + k * 16, wide, v[2 * k], v[2 * k + 1]);
+  auto issue = [&](int64_t k) {                     // thread 0
+    const int64_t bi = k / nbc, bj = k - bi * nbc;
+    mbar_arrive_expect_tx(b, 128 * 128 * 2);
+    tma_load_2d(smem_addr(blk), &tmap, (int32_t)(bj * 128),
+                (int32_t)(bi * 128), b);
+  };
+  bool pending = false;                             // thread 0: a load in flight
+  if (threadIdx.x == 0 && (int64_t)blockIdx.x < nblk) {
+    issue(blockIdx.x);
+    pending = true;
+  }
+  uint32_t ph = 0;
+  for (int64_t k = blockIdx.x; k < nblk; k += gridDim.x) {
+    const bool ok = mbar_wait(b, ph, &abort_flag, &g_fp8blk_wait_error);
+    if (ok) {                           // else the load may still land:
+      ph ^= 1u;                         // phase ph stays the one in flight
+      if (threadIdx.x == 0) pending = false;
     }
+    // rows p * 16 + warp * 2 + lane / 16, p = 0 .. 7
+    uint32_t m = 0;
+    if (ok) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) m = max(m, absmax16(v[2 * k], v[2 * k + 1]));
+      for (int pp = 0; pp < 8; ++pp) {
+        const int r = pp * 16 + warp * 2 + (lane >> 4);
+        m = max(m, absmax8(blk[r * 16 + ch]));
+      }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(FULL, m, o));
     if (lane == 0) red[warp] = m;
@@ -156,14 +202,40 @@ __global__ void __launch_bounds__(FB_THREADS)
     uint32_t a = red[0];
 #pragma unroll
     for (int w = 1; w < FB_THREADS / 32; ++w) a = max(a, red[w]);
-    __syncthreads();                    // red is rewritten by the next block
     float S, enc;
     fb_scales(a, S, enc);
-    uint8_t* q = codes + (bi * 128 + rr) * cols + bj * 128 + cc;
+    uint2 cw[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      st_v4(q + k * 16, encode16(v[2 * k], v[2 * k + 1], enc));
-    if (threadIdx.x == 0) scales[blk] = S;
+    for (int pp = 0; pp < 8; ++pp) {
+      const int r = pp * 16 + warp * 2 + (lane >> 4);
+      const uint4 v = blk[r * 16 + ch];
+      cw[pp] = make_uint2(bf16x2_scale_e4m3x2(v.x, enc, enc) |
+                              (bf16x2_scale_e4m3x2(v.y, enc, enc) << 16),
+                          bf16x2_scale_e4m3x2(v.z, enc, enc) |
+                              (bf16x2_scale_e4m3x2(v.w, enc, enc) << 16));
+    }
+    __syncthreads();                    // blk and red are free again
+    if (threadIdx.x == 0 && k + gridDim.x < nblk && !abort_flag) {
+      issue(k + gridDim.x);
+      pending = true;
+    }
+    if (ok) {
+      const int64_t bi = k / nbc, bj = k - bi * nbc;
+#pragma unroll
+      for (int pp = 0; pp < 8; ++pp) {
+        const int r = pp * 16 + warp * 2 + (lane >> 4);
+        st_v2(codes + (bi * 128 + r) * cols + bj * 128 + ch * 8, cw[pp].x,
+              cw[pp].y);
+      }
+      if (threadIdx.x == 0) scales[k] = S;
+    }
+  }
+  if (threadIdx.x == 0 && pending) {
+    // after a wait gave up: let the load in flight (phase ph) land before
+    // the CTA exits (bounded)
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(b, ph) && global_timer_ns() - t0 < kWaitLimitNs) {
+    }
   }
   pdl_launch_dependents();
 }
@@ -186,7 +258,7 @@ __device__ __forceinline__ void decode16(const uint4& c, float S, uint4& lo,
 
 // Dequantize codes [rows x cols] with scales per block of brows x 128
 // (brows_log2 = 0 or 7).
-__global__ void __launch_bounds__(FB_THREADS)
+__global__ void __launch_bounds__(FB_THREADS, 8)
     fp8blk_dequant_kernel(const uint8_t* __restrict__ codes,
                           const float* __restrict__ scales, int64_t rows,
                           int64_t cols, int brows_log2, int wide,
@@ -379,9 +451,13 @@ cudaError_t launch_fp8blk_quantize(const void* x, int64_t rows, int64_t cols,
                       stream, false, xs, rows, cols, ldx, codes, scales, wide);
   }
   const int64_t nblk = (rows >> 7) * (cols >> 7);
-  const unsigned grid = fb_grid(nblk, 1, dev, 4);
+  CUtensorMap tmap;
+  err = make_tmap_2d_bf16(&tmap, x, (uint64_t)cols, (uint64_t)rows,
+                          (uint64_t)ldx * 2, 128, 128, false);
+  if (err != cudaSuccess) return err;
+  const unsigned grid = fb_grid(nblk, 1, dev, FB_BLK_CTAS);
   return launch_pdl(fp8blk_block_kernel, dim3(grid), dim3(FB_THREADS), 0,
-                    stream, false, xs, rows, cols, ldx, codes, scales, wide);
+                    stream, false, tmap, rows, cols, codes, scales);
 }
 
 cudaError_t launch_fp8blk_dequantize(const uint8_t* codes, const float* scales,
@@ -398,6 +474,13 @@ cudaError_t launch_fp8blk_dequantize(const uint8_t* codes, const float* scales,
   return launch_pdl(fp8blk_dequant_kernel, dim3(grid), dim3(FB_THREADS), 0,
                     stream, false, codes, scales, rows, cols,
                     block_rows == 1 ? 0 : 7, wide, static_cast<uint16_t*>(y));
+}
+
+cudaError_t fp8blk_take_wait_error(unsigned int* word) {
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_fp8blk_wait_error, sizeof(*word));
+  if (e != cudaSuccess || *word == 0) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_fp8blk_wait_error, &zero, sizeof(zero));
 }
 
 cudaError_t launch_fp8blk_requant_t(const uint8_t* codes, const float* scales,

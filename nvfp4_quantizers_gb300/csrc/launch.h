@@ -148,6 +148,8 @@ cudaError_t launch_nvfp4_rht_sr(const void* x, int64_t T, int64_t H,
 
 // fp8block.cu
 // block_rows 1 (1x128 tiles) or 128 (128x128 blocks).
+// Reads (and clears when set) the error word of the bounded device waits.
+cudaError_t fp8blk_take_wait_error(unsigned int* word);
 cudaError_t launch_fp8blk_quantize(const void* x, int64_t rows, int64_t cols,
                                    int64_t ldx, int block_rows,
                                    uint8_t* codes, float* scales,
