@@ -26,8 +26,9 @@
 //
 // Design (sm_103a): one warp per row (grid-stride), a lane per 16-value
 // block.  Pass 1 loads (up to four blocks per lane at once), transforms and
-// reduces the row's amax; pass 2 reloads (from L1/L2), transforms again and
-// encodes, so no row is held in registers whatever its length.
+// reduces the row's amax; pass 2 encodes.  Rows of up to 4 x 32 blocks keep
+// their transformed values in registers between the passes; longer rows
+// are reloaded (from L1/L2) and transformed again in pass 2.
 #include <float.h>
 
 #include "common.cuh"
@@ -145,37 +146,98 @@ __device__ __forceinline__ float block_amax(const float (&v)[16]) {
   return m;
 }
 
-// E2M1 code of v by stochastic rounding with u in [0, 1): the grid spacing
-// is 0.5 below 2, 1 below 4 and 2 below 6, so (|v| - lo) / (hi - lo) is
-// exact in binary32.
+// E2M1 code of v by stochastic rounding with u in [0, 1), without
+// branches: the grid spacing d around a = min(|v|, 6) is 0.5 below 2, 1
+// below 4 and 2 up to 6, i.e. 2^(e - 1) with e = max(floor(log2 a), 0);
+// f = floor(a / d) (0 .. 3) puts lo = f d, the grid value at or below a,
+// at code f + 2e (exact: d is a power of two), and the code steps up iff
+// u d < a - lo, which is u < (a - lo) / (hi - lo) with both sides scaled
+// by d (exact).
 __device__ __forceinline__ uint32_t sr_e2m1(float v, float u) {
   const uint32_t neg = __float_as_uint(v) >> 31;
   const float a = fminf(fabsf(v), 6.0f);
-  uint32_t idx;
-  float frac;
-  if (a < 2.0f) {
-    const float lo = floorf(a * 2.0f);            // 0..3 half-steps
-    idx = (uint32_t)lo;
-    frac = a * 2.0f - lo;
-  } else if (a < 4.0f) {
-    const float lo = floorf(a);                   // 2 or 3
-    idx = (uint32_t)lo + 2u;
-    frac = a - lo;
-  } else if (a < 6.0f) {
-    idx = 6u;                                     // 4
-    frac = (a - 4.0f) * 0.5f;
-  } else {
-    idx = 7u;                                     // 6
-    frac = 0.0f;
-  }
-  if (u < frac) ++idx;
+  const int e = max((int)(__float_as_uint(a) >> 23) - 127, 0);
+  const float d = __uint_as_float((uint32_t)(126 + e) << 23);
+  const float inv_d = __uint_as_float((uint32_t)(128 - e) << 23);
+  const float f = floorf(__fmul_rn(a, inv_d));
+  uint32_t idx = (uint32_t)f + 2u * (uint32_t)e;
+  if (__fmul_rn(u, d) < __fsub_rn(a, __fmul_rn(f, d))) ++idx;
   return idx | (neg << 3);
 }
 
-// SR is a template parameter: without stochastic rounding the kernel needs
-// no Philox state and fits 4 CTAs per SM instead of 2.
+// Block scale and codes of block b of a row from its 16 transformed values
+// v (1/4 applied), then the stores: 8 bytes of codes, and (lanes 0, 4, ...)
+// the 32-bit word of four consecutive block scales.  All 32 lanes call it.
 template <bool SR>
-__global__ void __launch_bounds__(RS_THREADS, SR ? 2 : 4)
+__device__ __forceinline__ void encode_store(
+    const float (&v)[16], float S, float six_s, int64_t row, int64_t b,
+    bool real, bool valid, int64_t H, int64_t nb, int64_t col_tiles,
+    uint64_t seed, int swizzled, int lane, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales) {
+  uint32_t sb = 0;
+  if (S != 0.0f)
+    sb = cvt_e4m3x2(__fdiv_rn(block_amax(v), six_s), 0.0f) & 0xFFu;
+  const float d = __fmul_rn(e4m3_to_f32(sb), S);
+  float enc = 0.0f;
+  if (d != 0.0f) enc = fminf(__frcp_rn(d), FLT_MAX);
+  float q[16];
+#pragma unroll
+  for (int i = 0; i < 16; i += 2)
+    fmul2(v[i], v[i + 1], enc, enc, q[i], q[i + 1]);
+  uint32_t lo, hi;
+  if (!SR) {
+    lo = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[0]));
+    hi = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[8]));
+  } else {
+    uint32_t c[16];
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      uint64_t o[4];
+      philox4x64((uint64_t)row, (uint64_t)(b * 2 + g), 0, 0, seed, 2, o);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint64_t wd = o[k >> 1];
+        const uint32_t w = (uint32_t)((k & 1) ? (wd >> 32) : wd);
+        const float u = __uint2float_rn(w >> 8) * 0x1p-24f;
+        c[g * 8 + k] = sr_e2m1(q[g * 8 + k], u);
+      }
+    }
+    lo = hi = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      lo |= c[k] << (4 * k);
+      hi |= c[8 + k] << (4 * k);
+    }
+  }
+  if (real && valid) st_v2(codes + row * (H >> 1) + b * 8, lo, hi);
+  // lanes 4i .. 4i+3 hold four consecutive blocks: one 32-bit word
+  const uint32_t pair = sb | (__shfl_down_sync(FULL, sb, 1) << 8);
+  const uint32_t word = pair | (__shfl_down_sync(FULL, pair, 2) << 16);
+  if ((lane & 3) == 0) {
+    if (swizzled) {
+      if (b < 4 * col_tiles)
+        *reinterpret_cast<uint32_t*>(scales + swz_offset(row, b, col_tiles)) =
+            word;
+    } else if (real) {
+      if ((nb & 3) == 0) {
+        if (b < nb)
+          *reinterpret_cast<uint32_t*>(scales + row * nb + b) = word;
+      } else {
+        for (int k = 0; k < 4; ++k)
+          if (b + k < nb) scales[row * nb + b + k] = (uint8_t)(word >> (8 * k));
+      }
+    }
+  }
+}
+
+// SR is a template parameter: without stochastic rounding the kernel needs
+// no Philox state.  KEEP (no SR, rows of at most 4 x 32 blocks, e.g. hidden
+// 2048): pass 1 keeps each lane's transformed blocks in registers (64
+// values) and pass 2 encodes them, instead of reloading and transforming
+// the row again (ragged 132106 x 2048 with the RHT: 211 -> 179 us);
+// otherwise pass 2 reloads the row (from L1/L2) and transforms it again.
+template <bool SR, bool KEEP>
+__global__ void __launch_bounds__(RS_THREADS, (SR || KEEP) ? 2 : 4)
     nvfp4_rht_sr_kernel(const uint16_t* __restrict__ x, int64_t T,
                         int64_t T_pad, int64_t H, int64_t ldx, uint64_t seed,
                         int flags, uint8_t* __restrict__ codes,
@@ -185,7 +247,6 @@ __global__ void __launch_bounds__(RS_THREADS, SR ? 2 : 4)
   const int64_t warp_id = ((int64_t)blockIdx.x * RS_THREADS + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * RS_THREADS) >> 5;
   const bool rht = (flags & 1) != 0;
-  constexpr bool sr = SR;
   const int64_t nb = H >> 4;
   const int64_t col_tiles = (nb + 3) >> 2;
   const int64_t iters = (nb + 31) >> 5;           // warp-uniform
@@ -207,7 +268,8 @@ __global__ void __launch_bounds__(RS_THREADS, SR ? 2 : 4)
     // ---- pass 1: the row's amax over the (transformed) values; up to
     // four of a lane's blocks loaded before any is transformed ----
     float am = 0.0f;
-    for (int64_t j0 = 0; j0 < iters; j0 += kChunk) {
+    float kept[KEEP ? kChunk : 1][16];
+    for (int64_t j0 = 0; j0 < (KEEP ? 1 : iters); j0 += kChunk) {
       uint4 raw[2 * kChunk];
 #pragma unroll
       for (int k = 0; k < kChunk; ++k) {
@@ -225,6 +287,10 @@ __global__ void __launch_bounds__(RS_THREADS, SR ? 2 : 4)
         float v[16];
         block_values<false>(raw[2 * k], raw[2 * k + 1], rht, smask, v);
         am = fmaxf(am, block_amax(v));
+        if (KEEP) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) kept[KEEP ? k : 0][i] = v[i];
+        }
       }
     }
 #pragma unroll
@@ -236,71 +302,37 @@ __global__ void __launch_bounds__(RS_THREADS, SR ? 2 : 4)
     const float six_s = __fmul_rn(6.0f, S);
     if (real && lane == 0) S_out[row] = S;
     // ---- pass 2: block scales and codes ----
-    for (int64_t j = 0; j < iters; ++j) {
-      const int64_t b = j * 32 + lane;
-      const bool valid = b < nb;
-      float v[16];
-      if (real && valid) {
-        const uint4 a0 = *reinterpret_cast<const uint4*>(xr + b * 16);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(xr + b * 16 + 8);
-        block_values(a0, a1, rht, smask, v);
-      } else {
+    if (KEEP) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+      for (int k = 0; k < kChunk; ++k) {
+        if (k >= iters) break;                    // warp-uniform
+        const int64_t b = k * 32 + lane;
+        const bool valid = b < nb;
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          v[i] = (real && valid)
+                     ? (rht ? __fmul_rn(kept[KEEP ? k : 0][i], 0.25f)
+                            : kept[KEEP ? k : 0][i])
+                     : 0.0f;
+        encode_store<SR>(v, S, six_s, row, b, real, valid, H, nb, col_tiles,
+                         seed, swizzled, lane, codes, scales);
       }
-      uint32_t sb = 0;
-      if (S != 0.0f)
-        sb = cvt_e4m3x2(__fdiv_rn(block_amax(v), six_s), 0.0f) & 0xFFu;
-      const float d = __fmul_rn(e4m3_to_f32(sb), S);
-      float enc = 0.0f;
-      if (d != 0.0f) enc = fminf(__frcp_rn(d), FLT_MAX);
-      float q[16];
+    } else {
+      for (int64_t j = 0; j < iters; ++j) {
+        const int64_t b = j * 32 + lane;
+        const bool valid = b < nb;
+        float v[16];
+        if (real && valid) {
+          const uint4 a0 = *reinterpret_cast<const uint4*>(xr + b * 16);
+          const uint4 a1 = *reinterpret_cast<const uint4*>(xr + b * 16 + 8);
+          block_values(a0, a1, rht, smask, v);
+        } else {
 #pragma unroll
-      for (int i = 0; i < 16; i += 2)
-        fmul2(v[i], v[i + 1], enc, enc, q[i], q[i + 1]);
-      uint32_t lo, hi;
-      if (!sr) {
-        lo = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[0]));
-        hi = cvt_e2m1x8(*reinterpret_cast<const float(*)[8]>(&q[8]));
-      } else {
-        uint32_t c[16];
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          uint64_t o[4];
-          philox4x64((uint64_t)row, (uint64_t)(b * 2 + g), 0, 0, seed, 2, o);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t wd = o[k >> 1];
-            const uint32_t w = (uint32_t)((k & 1) ? (wd >> 32) : wd);
-            const float u = __uint2float_rn(w >> 8) * 0x1p-24f;
-            c[g * 8 + k] = sr_e2m1(q[g * 8 + k], u);
-          }
+          for (int i = 0; i < 16; ++i) v[i] = 0.0f;
         }
-        lo = hi = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          lo |= c[k] << (4 * k);
-          hi |= c[8 + k] << (4 * k);
-        }
-      }
-      if (real && valid) st_v2(codes + row * (H >> 1) + b * 8, lo, hi);
-      // lanes 4i .. 4i+3 hold four consecutive blocks: one 32-bit word
-      const uint32_t pair = sb | (__shfl_down_sync(FULL, sb, 1) << 8);
-      const uint32_t word = pair | (__shfl_down_sync(FULL, pair, 2) << 16);
-      if ((lane & 3) == 0) {
-        if (swizzled) {
-          if (b < 4 * col_tiles)
-            *reinterpret_cast<uint32_t*>(scales + swz_offset(row, b, col_tiles)) =
-                word;
-        } else if (real) {
-          if ((nb & 3) == 0) {
-            if (b < nb)
-              *reinterpret_cast<uint32_t*>(scales + row * nb + b) = word;
-          } else {
-            for (int k = 0; k < 4; ++k)
-              if (b + k < nb) scales[row * nb + b + k] = (uint8_t)(word >> (8 * k));
-          }
-        }
+        encode_store<SR>(v, S, six_s, row, b, real, valid, H, nb, col_tiles,
+                         seed, swizzled, lane, codes, scales);
       }
     }
   }
@@ -319,19 +351,21 @@ cudaError_t launch_nvfp4_rht_sr(const void* x, int64_t T, int64_t H,
   if (err != cudaSuccess) return err;
   const int64_t T_pad = swizzled ? (T + 127) / 128 * 128 : T;
   const int64_t per_cta = RS_THREADS / 32;
+  // Rows kept in registers only without SR: the Philox state and the kept
+  // values together spill (ragged 132106 x 2048 with SR: 786 -> 874 us).
+  const bool keep = !(flags & 2) && ((H >> 4) + 31) / 32 <= kChunk;
   int64_t grid = (T_pad + per_cta - 1) / per_cta;
   const int64_t cap = (int64_t)sm_count(dev) * 8;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  if (flags & 2)
-    return launch_pdl(nvfp4_rht_sr_kernel<true>, dim3((unsigned)grid),
-                      dim3(RS_THREADS), 0, stream, false,
-                      static_cast<const uint16_t*>(x), T, T_pad, H, ldx, seed,
-                      flags, codes, scales, token_scales, swizzled);
-  return launch_pdl(nvfp4_rht_sr_kernel<false>, dim3((unsigned)grid),
-                    dim3(RS_THREADS), 0, stream, false,
-                    static_cast<const uint16_t*>(x), T, T_pad, H, ldx, seed,
-                    flags, codes, scales, token_scales, swizzled);
+#define MXQ_RHT_LAUNCH(SR_, KEEP_)                                          \
+  launch_pdl(nvfp4_rht_sr_kernel<SR_, KEEP_>, dim3((unsigned)grid),        \
+             dim3(RS_THREADS), 0, stream, false,                           \
+             static_cast<const uint16_t*>(x), T, T_pad, H, ldx, seed, flags, \
+             codes, scales, token_scales, swizzled)
+  if (flags & 2) return MXQ_RHT_LAUNCH(true, false);
+  return keep ? MXQ_RHT_LAUNCH(false, true) : MXQ_RHT_LAUNCH(false, false);
+#undef MXQ_RHT_LAUNCH
 }
 
 }  // namespace mxq
