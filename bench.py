@@ -1242,10 +1242,12 @@ def run_reference(args):
 PROFILE_WORKLOADS = (
     "rowcol_8192x4096", "rowcol_8192x2048", "dequant_mxfp8_8192x4096",
     "per_token_ragged", "dequant_nvfp4_ragged", "rht_ragged",
+    "rht_sr_ragged",
     "weight_gate_up_128", "weight_down_128", "weight_step_8pairs",
     "weight_gate_up_128_given_scale",
     "dequant_nvfp4_gate_up_128", "fp8_block_1x128", "fp8_block_128x128",
-    "fp8_block_requant_t", "gemm_mxfp8", "gemm_nvfp4_grouped",
+    "fp8_block_dequant_1x128", "fp8_block_requant_t", "gemm_mxfp8",
+    "gemm_nvfp4_grouped",
     "moe_gate_up_swiglu", "moe_gate_up_swiglu_gather", "gemm_bf16_dq")
 
 
@@ -1276,11 +1278,13 @@ def run_profile(args):
         _, o = ops.rowcol(dev16(W.mxfp8_random(8192, 4096)))
         _()
         call = ops.dq_mxfp8(o[0].view(8192, 4096), o[1])
-    elif name in ("per_token_ragged", "dequant_nvfp4_ragged", "rht_ragged"):
+    elif name in ("per_token_ragged", "dequant_nvfp4_ragged", "rht_ragged",
+                  "rht_sr_ragged"):
         x = dev16(W.ragged_tokens(W.ragged_lengths(), H))
         T = x.shape[0]
-        call, o = ops.per_token(x, rht_flags=q.NVFP4_RHT
-                                if name == "rht_ragged" else None)
+        flags = {"rht_ragged": q.NVFP4_RHT,
+                 "rht_sr_ragged": q.NVFP4_RHT | q.NVFP4_SR}.get(name)
+        call, o = ops.per_token(x, rht_flags=flags)
         if name == "dequant_nvfp4_ragged":
             call()
             call = ops.dq_nvfp4(o[0], o[1], o[2], q.S_PER_ROW, 1, T, H)
@@ -1314,6 +1318,9 @@ def run_profile(args):
         if name == "fp8_block_requant_t":
             call()
             call = ops.fp8blk_rt(o[0], o[1], 8192, 4096)
+        elif name == "fp8_block_dequant_1x128":
+            call()
+            call = ops.fp8blk_dq(o[0], o[1], 8192, 4096, 1)
     elif name.startswith(("gemm", "moe")):
         gemm_calls = _gemm_workloads(q, W, dev)
         call = gemm_calls[name]
