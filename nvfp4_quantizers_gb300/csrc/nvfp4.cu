@@ -772,6 +772,9 @@ cudaError_t launch_nvfp4_weight_shared(
   p.nE = (p.R_pad + rows_per_task - 1) / rows_per_task;
   p.win = kWindowBytes / (p.R * K * 2);
   if (p.win < 1) p.win = 1;
+  // a call whose whole input stays in L2 runs as one window (8 gate/up
+  // pairs of [1024 x 2048], 64 MB: 44.6 -> 40.8 us)
+  if (num_groups * p.R * K * 2 <= (64ll << 20)) p.win = num_groups;
   p.lead = kLeadWindows;
   p.done = ws ? ws + kWsHeaderWords + num_groups : nullptr;
   p.codes = codes;

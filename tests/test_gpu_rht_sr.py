@@ -62,8 +62,11 @@ def test_ragged_tokens(mxq, flags, lay):
     check(mxq, x, 1234, flags, lay)
 
 
-@pytest.mark.parametrize("H", [16, 48, 160, 2048])
+@pytest.mark.parametrize("H", [16, 48, 160, 1552, 2048, 2064, 4096])
 def test_hidden_sizes(mxq, H):
+    """Rows of up to 128 blocks keep their transformed values in registers
+    between the passes (1552: 97 blocks, a ragged last step); longer rows
+    (2064: 129 blocks, 4096) are transformed again in the second pass."""
     x = W.ragged_tokens([37], H=H)
     for flags in (1, 3):
         check(mxq, x, 99, flags, "swizzled")
