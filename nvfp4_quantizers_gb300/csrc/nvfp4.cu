@@ -77,6 +77,13 @@ __device__ __forceinline__ uint32_t warp_max(uint32_t a) {
   return a;
 }
 
+// Maximum over each half of the warp (lanes 0-15 and 16-31 separately).
+__device__ __forceinline__ uint32_t half_warp_max(uint32_t a) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) a = max(a, __shfl_xor_sync(FULL, a, o));
+  return a;
+}
+
 // pol != 0: the rows are read for the last time (the weight quantizer's
 // second pass): their lines are marked first to evict in L2.
 __device__ __forceinline__ void load_block(Blk& v, const uint16_t* row,
@@ -143,7 +150,7 @@ __device__ __forceinline__ void store_block(const RowOut& o, int64_t b,
   // assemble them, lowest block in the lowest byte, in lane 4i
   const uint32_t pair = sb | (__shfl_down_sync(FULL, sb, 1) << 8);
   const uint32_t word = pair | (__shfl_down_sync(FULL, pair, 2) << 16);
-  if ((lane & 3) == 0) {
+  if ((lane & 3) == 0 && o.scales) {      // no scales: a row past the matrix
     if (o.swizzled) {
       if (b < ((o.nblocks + 3) & ~int64_t(3)))
         *reinterpret_cast<uint32_t*>(o.scales +
@@ -162,19 +169,23 @@ __device__ __forceinline__ void store_block(const RowOut& o, int64_t b,
 // One row of H values is spread over WPR warps; warp w of the row owns
 // blocks [w*R*32, (w+1)*R*32), lane l the blocks w*R*32 + r*32 + l.  The
 // row's amax is combined across its warps through shared memory and a
-// named barrier (id 1 + row slot, 32*WPR threads).
-template <int R, int WPR>
+// named barrier (id 1 + row slot, 32*WPR threads).  LPR = 16: each half of
+// the warp takes its own row (WPR = 1), lane l of a half the blocks
+// r*16 + l (rows of 33 to 48 blocks: 3 blocks a lane, no idle lanes).
+template <int R, int WPR, int LPR = 32>
 __device__ __forceinline__ void encode_row_warps(
     const uint16_t* row, bool load, bool write, float S_given, bool use_given,
     const RowOut& o, int row_slot, int wpart, int lane, uint32_t* red,
     float* S_used, uint64_t pol = 0) {
-  const int64_t blk0 = (int64_t)wpart * R * 32;
+  static_assert(LPR == 32 || (LPR == 16 && WPR == 1), "lanes per row");
+  const int l = lane & (LPR - 1);
+  const int64_t blk0 = (int64_t)wpart * R * LPR;
   Blk v[R];
   uint32_t am[R];
   uint32_t a = 0;
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const int64_t b = blk0 + r * 32 + lane;
+    const int64_t b = blk0 + r * LPR + l;
     load_block(v[r], row, b, load && b < o.nblocks, o.wide, pol);
   }
 #pragma unroll
@@ -184,7 +195,7 @@ __device__ __forceinline__ void encode_row_warps(
   }
   float S = S_given;
   if (!use_given) {
-    a = warp_max(a);
+    a = LPR == 32 ? warp_max(a) : half_warp_max(a);
     if (WPR > 1) {
       if (lane == 0) red[row_slot * WPR + wpart] = a;
       named_barrier_sync(1 + row_slot, 32 * WPR);
@@ -195,10 +206,10 @@ __device__ __forceinline__ void encode_row_warps(
   const float six_s = __fmul_rn(6.0f, S);
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    if (blk0 + r * 32 >= o.nblocks) break;             // warp-uniform
+    if (blk0 + r * LPR >= o.nblocks) break;            // warp-uniform
     uint32_t lo, hi, sb;
     encode_block(v[r], am[r], S, six_s, lo, hi, sb);
-    store_block(o, blk0 + r * 32 + lane, write, lo, hi, sb, lane);
+    store_block(o, blk0 + r * LPR + l, write, lo, hi, sb, lane);
   }
   *S_used = S;
 }
@@ -483,11 +494,11 @@ __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
                : "memory");
 }
 
-template <int R, int WPR>
+template <int R, int WPR, int LPR>
 __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
     nvfp4_weight_kernel(const __grid_constant__ GroupTable tab,
                         const __grid_constant__ GroupParams p) {
-  constexpr int ROWS = CTA_WARPS / WPR;
+  constexpr int ROWS = CTA_WARPS / WPR * (32 / LPR);  // rows per row set
   __shared__ uint32_t red[CTA_WARPS];
   __shared__ int s_abort;
   __shared__ int64_t s_task[2];
@@ -499,7 +510,9 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
   __shared__ __align__(16) uint8_t s_sc[kStage8 ? 8 : 1][kStage8 ? 256 : 4];
   __shared__ float s_S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int slot = warp / WPR, wpart = warp % WPR;
+  // LPR = 16: the two halves of a warp take rows 2 warp and 2 warp + 1
+  const int slot = LPR == 32 ? warp / WPR : 2 * warp + (lane >> 4);
+  const int wpart = LPR == 32 ? warp % WPR : 0;
   if (threadIdx.x == 0) s_abort = 0;
   __syncthreads();
   pdl_wait();
@@ -617,22 +630,28 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
     const int64_t r = staged ? (idx >> 4) * 128 + 2 * (idx & 15) + (s8 & 1) +
                                    32 * (s8 >> 1)
                              : (idx * kRowSetsPerTask + rs) * ROWS + slot;
-    if (r < p.R_pad && !s_abort) {                      // uniform over the row
-      const bool real = r < p.R;
+    // uniform over the row; with half-warp rows the two halves may
+    // differ, so a warp with one row in range runs the other half idle
+    // (no loads, no stores)
+    const bool active = r < p.R_pad && !s_abort;
+    if (LPR == 32 ? active : __any_sync(FULL, active)) {
+      const bool real = active && r < p.R;
       const uint16_t* row = nullptr;
       if (real) {
         int pi = 0;
         while (pi + 1 < p.num_parts && r >= p.part_row0[pi + 1]) ++pi;
         row = tab.part[gl][pi] + (r - p.part_row0[pi]) * p.K;
       }
-      if (r == 0 && wpart == 0 && lane == 0) p.group_scales[g] = S;
+      if (active && r == 0 && wpart == 0 && (lane & (LPR - 1)) == 0)
+        p.group_scales[g] = S;
       RowOut o{p.codes + (g * p.R + r) * (p.K >> 1),
-               p.scales + g * p.scale_stride, r, ((p.K >> 4) + 3) >> 2,
-               p.K >> 4, p.swizzled, p.wide,
+               active ? p.scales + g * p.scale_stride : nullptr, r,
+               ((p.K >> 4) + 3) >> 2, p.K >> 4, p.swizzled, p.wide,
                staged ? s_sc[s8 % (kStage8 ? 8 : 1)] : nullptr};
       float S_used;
-      encode_row_warps<R, WPR>(row, real, real, S, true, o, slot, wpart, lane,
-                               red, &S_used, p.S_in ? 0 : pol_last);
+      encode_row_warps<R, WPR, LPR>(row, real, real, S, true, o, slot, wpart,
+                                    lane, red, &S_used,
+                                    p.S_in ? 0 : pol_last);
     }
     }
     if (staged) {
@@ -665,6 +684,7 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, 4)
 // warp) and WPR warps per row; 0 = rows too long (one CTA per row).
 struct RowShape {
   int R, WPR;
+  int LPR = 32;           // lanes per row (16: two rows per warp)
 };
 RowShape pick_shape(int64_t H) {
   const int64_t nb = H >> 4;
@@ -675,6 +695,14 @@ RowShape pick_shape(int64_t H) {
   if (nb <= 512) return {4, 4};
   if (nb <= 1024) return {4, 8};
   return {0, 0};
+}
+// The weight quantizer's encode: rows of 33 to 48 blocks take half a warp
+// each, 3 blocks a lane (with a full warp and 2 blocks a lane a quarter of
+// the lanes idled in the second pass: 128 down projections [2048 x 768]).
+RowShape pick_weight_shape(int64_t K) {
+  const int64_t nb = K >> 4;
+  if (nb > 32 && nb <= 48) return {3, 1, 16};
+  return pick_shape(K);
 }
 
 }  // namespace
@@ -724,14 +752,14 @@ cudaError_t nvfp4_take_wait_error(unsigned int* word) {
 
 namespace {
 
-template <int R, int WPR>
+template <int R, int WPR, int LPR = 32>
 cudaError_t launch_weight_tasks(const GroupTable& tab, const GroupParams& p,
                                 int dev, cudaStream_t stream) {
   static int occ[64] = {};
   int n = (dev >= 0 && dev < 64) ? occ[dev] : 0;
   if (n == 0) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &n, nvfp4_weight_kernel<R, WPR>, CTA_WARPS * 32, 0);
+        &n, nvfp4_weight_kernel<R, WPR, LPR>, CTA_WARPS * 32, 0);
     if (e != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;
     if (dev >= 0 && dev < 64) occ[dev] = n;
@@ -739,7 +767,7 @@ cudaError_t launch_weight_tasks(const GroupTable& tab, const GroupParams& p,
   const unsigned grid = (unsigned)(n * sm_count(dev));
   // No co-residency is needed: a CTA only waits for tasks that running
   // CTAs hold.
-  return launch_pdl(nvfp4_weight_kernel<R, WPR>, dim3(grid),
+  return launch_pdl(nvfp4_weight_kernel<R, WPR, LPR>, dim3(grid),
                     dim3(CTA_WARPS * 32), 0, stream, false, tab, p);
 }
 
@@ -750,7 +778,7 @@ cudaError_t launch_nvfp4_weight_shared(
     const int64_t* part_rows, int64_t K, uint8_t* codes, uint8_t* scales,
     float* group_scales, const float* group_scales_in, int swizzled,
     uint32_t* ws, cudaStream_t stream) {
-  const RowShape sh = pick_shape(K);
+  const RowShape sh = pick_weight_shape(K);
   if (sh.R == 0) return cudaErrorInvalidValue;   // K > 16384: not supported
   GroupParams p;
   p.num_parts = num_parts;
@@ -768,7 +796,8 @@ cudaError_t launch_nvfp4_weight_shared(
   p.R_pad = swizzled ? (p.R + 127) / 128 * 128 : p.R;
   p.K = K;
   p.nA = (p.part_chunk0[num_parts] + kTaskChunks - 1) / kTaskChunks;
-  const int64_t rows_per_task = RowSets(sh.R, sh.WPR) * (CTA_WARPS / sh.WPR);
+  const int64_t rows_per_task =
+      RowSets(sh.R, sh.WPR) * (CTA_WARPS / sh.WPR) * (32 / sh.LPR);
   p.nE = (p.R_pad + rows_per_task - 1) / rows_per_task;
   p.win = kWindowBytes / (p.R * K * 2);
   if (p.win < 1) p.win = 1;
@@ -815,7 +844,8 @@ cudaError_t launch_nvfp4_weight_shared(
     p.g0 = g0;
     p.ng = ng;
     p.counter = ws ? ws + 1 + g0 / kMaxGroupsPerLaunch : nullptr;
-    if (sh.R == 1) err = launch_weight_tasks<1, 1>(tab, p, dev, stream);
+    if (sh.LPR == 16) err = launch_weight_tasks<3, 1, 16>(tab, p, dev, stream);
+    else if (sh.R == 1) err = launch_weight_tasks<1, 1>(tab, p, dev, stream);
     else if (sh.R == 2) err = launch_weight_tasks<2, 1>(tab, p, dev, stream);
     else if (sh.WPR == 1) err = launch_weight_tasks<4, 1>(tab, p, dev, stream);
     else if (sh.WPR == 2) err = launch_weight_tasks<4, 2>(tab, p, dev, stream);

@@ -155,7 +155,8 @@ def test_guard_nvfp4_gather(mxq):
 
 @pytest.mark.parametrize("lay", ["swizzled", "linear"])
 @pytest.mark.parametrize("rows,K,G", [((100, 60), 48, 3), ((768, 768), 2048, 2),
-                                      ((2048,), 768, 2), ((33,), 4096, 3)])
+                                      ((2048,), 768, 2), ((33,), 4096, 3),
+                                      ((77, 30), 640, 3)])
 def test_guard_nvfp4_weights_and_dequant(mxq, lay, rows, K, G):
     q = mxq
     L = q.lib()

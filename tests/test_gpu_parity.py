@@ -497,6 +497,8 @@ def test_weight_full_moe_layer_sampled(mxq):
 @pytest.mark.parametrize("rows,K,G", [
     ((768, 768), 2048, 3),      # gate/up pairs
     ((2048,), 768, 5),          # down projections, 48 blocks per row
+    ((77, 30), 640, 3),         # 40 blocks per row: half-warp rows, odd row count
+    ((5,), 528, 4),             # 33 blocks per row, 5 rows: one half idle
     ((200, 56), 512, 7),        # ~256 KiB groups, parts of 200 and 56 rows
     ((33,), 4096, 9),           # 33 rows of 4096: a partial scale tile
     ((1000,), 1552, 2),         # 97 blocks per row: byte scale stores
