@@ -1053,57 +1053,95 @@ def load_traffic(kernel_name):
 
 
 def run_e2e(q, dev, x_bits, args):
-    """The step through the public API with host buffers: every step copies
-    X from pinned host memory to the device, runs the seven operations and
-    reads every code, scale and FP32 scale back into pinned host memory.
-    Steps alternate between two streams (and two sets of host result
-    buffers), so one step's copies overlap the neighbouring steps' kernels
-    and opposite-direction copies, as a pipelined producer would run them."""
+    """The step through the C ABI with host buffers: every step copies X from
+    pinned host memory to the device, runs the seven operations on it and
+    reads every code, scale and FP32 scale back into pinned host memory
+    (one copy each way: a step's outputs sit in one device buffer).  Steps
+    rotate over three streams, each with its own device buffers, workspace
+    and host result buffer, so one step's copies overlap the neighbouring
+    steps' kernels and opposite-direction copies, as a pipelined producer
+    would run them."""
     import torch
+    L = q.lib()
+    lay = q.SCALE_SWIZZLED
+    NS = 3
     x_pin = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    n_e2e = max(4, min(20, args.steps // 50))
-    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    n_e2e = max(6, min(30, args.steps // 50))
+    streams = [torch.cuda.Stream(dev) for _ in range(NS)]
+    # the outputs read back, in one device buffer (256-byte aligned views)
+    sizes = [("rc", M * K), ("rs", q.scale_bytes(M, K // 32)), ("cc", K * M),
+             ("cs", q.scale_bytes(K, M // 32)), ("tc", M * K // 2),
+             ("ts", q.scale_bytes(M, K // 16)), ("tS", 4 * M),
+             ("wc", PAIRS * 2 * PART_ROWS * WK // 2),
+             ("ws", PAIRS * q.scale_bytes(2 * PART_ROWS, WK // 16)),
+             ("wS", 4 * PAIRS)]
+    offs, o = {}, 0
+    for nm, n in sizes:
+        offs[nm] = o
+        o += (n + 255) // 256 * 256
+    total_out = o
+    d2h = sum(n for _, n in sizes)
+    ws_bytes = int(L.nvfp4_quantize_weight_shared_workspace_size(PAIRS))
+    rows_tab = (ctypes.c_int64 * 2)(PART_ROWS, PART_ROWS)
+    sets = []
+    for i in range(NS):
+        x = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        ob = torch.empty(total_out, dtype=torch.uint8, device=dev)
+        hb = torch.empty(total_out, dtype=torch.uint8).pin_memory()
+        y = [torch.empty(M * K, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+        wsp = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+        flat = x.view(2 * PAIRS, PART_ROWS, WK)
+        tab = (ctypes.c_void_p * (2 * PAIRS))(
+            *[flat[k].data_ptr() for k in range(2 * PAIRS)])
+        a = {nm: ob.data_ptr() + offs[nm] for nm, _ in sizes}
+        st = ctypes.c_void_p(streams[i].cuda_stream)
+        calls = [
+            (L.mxfp8_quantize_rowcol, (x.data_ptr(), M, K, K, a["rc"], a["rs"],
+                                       a["cc"], a["cs"], lay, st)),
+            (L.dequantize_mxfp8, (a["rc"], a["rs"], M, K, lay, y[0].data_ptr(), st)),
+            (L.dequantize_mxfp8, (a["cc"], a["cs"], K, M, lay, y[1].data_ptr(), st)),
+            (L.nvfp4_quantize_per_token, (x.data_ptr(), M, K, K, a["tc"], a["ts"],
+                                          a["tS"], lay, st)),
+            (L.dequantize_nvfp4, (a["tc"], a["ts"], a["tS"], q.S_PER_ROW, 1, M, K,
+                                  lay, y[2].data_ptr(), st)),
+            (L.nvfp4_quantize_weight_shared,
+             (PAIRS, 2, ctypes.cast(tab, ctypes.c_void_p),
+              ctypes.cast(rows_tab, ctypes.c_void_p), WK, a["wc"], a["ws"],
+              a["wS"], None, lay, wsp.data_ptr(), wsp.numel(), st)),
+            (L.dequantize_nvfp4, (a["wc"], a["ws"], a["wS"], q.S_PER_BATCH, PAIRS,
+                                  2 * PART_ROWS, WK, lay, y[3].data_ptr(), st)),
+        ]
+        sets.append((x, ob, hb, y, wsp, tab, calls))
 
-    def once():
-        x = x_pin.to(dev, non_blocking=True)
-        r = q.mxfp8_quantize_rowcol(x)
-        q.dequantize_mxfp8(r.row_codes, r.row_scales)
-        q.dequantize_mxfp8(r.col_codes_t, r.col_scales_t)
-        t = q.nvfp4_quantize_per_token(x)
-        q.dequantize_nvfp4(t.codes, t.block_scales, t.scales)
-        parts = x.view(2 * PAIRS, PART_ROWS, WK)
-        w = q.nvfp4_quantize_weight_shared(
-            [[parts[2 * g], parts[2 * g + 1]] for g in range(PAIRS)])
-        q.dequantize_nvfp4(w.codes, w.block_scales, w.scales)
-        return [r.row_codes, r.row_scales, r.col_codes_t, r.col_scales_t,
-                t.codes, t.block_scales, t.scales, w.codes, w.block_scales,
-                w.scales]
+    def step(i):
+        x, ob, hb, _, _, _, calls = sets[i % NS]
+        with torch.cuda.stream(streams[i % NS]):
+            x.copy_(x_pin, non_blocking=True)
+            for fn, a in calls:
+                st = fn(*a)
+                if st != 0:
+                    raise RuntimeError(f"e2e: {q.status_string(st)}")
+            hb.copy_(ob, non_blocking=True)
 
-    def step(i, hosts):
-        s = streams[i % 2]
-        with torch.cuda.stream(s):
-            for h, a in zip(hosts[i % 2], once()):
-                h.copy_(a, non_blocking=True)
-
-    with torch.cuda.stream(streams[0]):
-        res = once()
-    torch.cuda.synchronize(dev)
-    hosts = [[torch.empty(a.shape, dtype=a.dtype).pin_memory() for a in res]
-             for _ in range(2)]
-    for i in range(4):
-        step(i, hosts)
+    for i in range(2 * NS):
+        step(i)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for i in range(n_e2e):
-        step(i, hosts)
+        step(i)
     torch.cuda.synchronize(dev)
     dt = (time.perf_counter() - t0) / n_e2e
+    st = q.get_last_error()
+    if st != 0:
+        raise RuntimeError(f"e2e: {q.status_string(st)}")
     step_bytes = sum(op_bytes().values())
-    d2h = sum(a.numel() * a.element_size() for a in res)
     return {"value": round(step_bytes / dt / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": int(x_bits.nbytes),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(dt * 1e3, 3),
-            "steps": n_e2e, "streams": 2}
+            "steps": n_e2e, "streams": NS,
+            "api": "C ABI (libmxq) with preallocated device buffers; one "
+                   "H2D copy of X and one D2H copy of all codes and scales "
+                   "per step"}
 
 
 # --------------------------------------------------------------------------
