@@ -366,12 +366,13 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 // ---------------------------------------------------------------------------
 constexpr int kMaxGroupsPerLaunch = 256;
 constexpr int64_t kTaskChunks = 4096;         // 16-byte chunks per amax task
-// Encode task: RowSets(R, WPR) sets of ROWS rows.  Rows of at most 1024
-// values (R <= 2 blocks per lane) take 4 sets, 32 rows (short rows would
-// otherwise make small tasks whose fixed cost dominates: 128 down
-// projections [2048 x 768], 210 -> 190 us); longer rows take 2 (4 sets
-// measured slower at 2048 values, and with WPR = 2 the 8 rows of 2 sets
-// fill whole swizzled scale sectors).
+// Encode task: RowSets(R, WPR) sets of ROWS rows (ROWS = 8 / WPR, or 16
+// with half-warp rows).  Rows of at most 1024 values on full warps (R <= 2
+// blocks per lane) take 4 sets, 32 rows (short rows would otherwise make
+// small tasks whose fixed cost dominates); longer rows take 2, and so do
+// half-warp rows (2 x 16 = 32 rows: the down projections); 4 sets measured
+// slower at 2048 values, and with WPR = 2 the 8 rows of 2 sets fill whole
+// swizzled scale sectors.
 __host__ __device__ constexpr int RowSets(int r, int wpr) {
   return (wpr == 1 && r <= 2) ? 4 : 2;
 }
