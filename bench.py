@@ -465,19 +465,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {
-            "workload": WORKLOAD,
-            "M": M, "K": K, "scale_layout": "swizzled",
-            "weight_pairs": f"{PAIRS} x 2 x [{PART_ROWS} x {WK}]",
-            "l2": ("inputs larger than L2: 3 rotating input copies and 2 "
-                   "rotating output sets, every kernel reads data last "
-                   "touched >= one step (~680 MB) earlier"),
-            "parallelism": f"weak: one independent replica per GPU x{world}",
-            "streams": ("1 (serial)" if args.serial else
-                        "3: the rowcol kernel alone, then the MXFP8 "
-                        "dequantizations, the per-token chain and the weight "
-                        "chain (higher stream priority) concurrently"),
-        },
+        "config": step_config(world, args.serial),
         "pct_hbm_peak": round(100 * value / world / peak, 1),
         "roofline": {
             "kernel": dom,
@@ -1236,6 +1224,23 @@ def cpu_baseline(args, min_s=10.0, max_passes=40, single_min_s=5.0):
                            f"7 operations on one thread, {t1:.1f} s")}}
 
 
+def step_config(world, serial=False):
+    """The workload's `config`, the same for both arms of the bench."""
+    return {
+        "workload": WORKLOAD,
+        "M": M, "K": K, "scale_layout": "swizzled",
+        "weight_pairs": f"{PAIRS} x 2 x [{PART_ROWS} x {WK}]",
+        "l2": ("inputs larger than L2: 3 rotating input copies and 2 "
+               "rotating output sets, every kernel reads data last "
+               "touched >= one step (~680 MB) earlier"),
+        "parallelism": f"weak: one independent replica per GPU x{world}",
+        "streams": ("1 (serial)" if serial else
+                    "3: the rowcol kernel alone, then the MXFP8 "
+                    "dequantizations, the per-token chain and the weight "
+                    "chain (higher stream priority) concurrently"),
+    }
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -1265,12 +1270,15 @@ def run_reference(args):
         "ms_per_step": round(1e3 * statistics.mean(dts), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": M, "K": K,
-                   "sample_rows": rows},
+        "config": step_config(world),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT,
                          "cores": cores, "kind": "oracle",
                          "cpu_model": cpu_model(),
-                         "sample": f"{rows} of 8192 rows per step"},
+                         "sample": (f"{rows} of the {M} rows of X through "
+                                    "the step's 7 operations per step "
+                                    "(32-row slices over all cores); value "
+                                    "= the step's algorithmic bytes scaled "
+                                    "to the sampled rows / time")},
         "e2e": {"value": round(value, 4), "unit": UNIT,
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
