@@ -413,6 +413,28 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src,
       : "memory");
 }
 
+// Shared -> global 2-D tensor store, tracked by the issuing thread's bulk
+// groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map,
+                                             uint32_t src, int32_t x,
+                                             int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, "
+      "%2}], [%3];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until no committed store group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Programmatic dependent launch.  Every kernel calls pdl_wait() before its
 // first global-memory access: it returns once the previous kernel on the
 // stream has completed and its writes are visible (and at once when the

@@ -188,28 +188,6 @@ __device__ __forceinline__ bool stage_handoff(bool abort_in) {
   return r != 0;
 }
 
-// Shared -> global 2-D tensor store, tracked by the issuing thread's bulk
-// groups.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map,
-                                             uint32_t src, int32_t x,
-                                             int32_t y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, "
-      "%2}], [%3];" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(x), "r"(y), "r"(src)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Wait until no committed store group still reads shared memory.
-__device__ __forceinline__ void bulk_wait_read_0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // 2-D tiled TMA gather of four rows (rows y0..y3, the box's columns from
 // x) into four consecutive box-sized rows of shared memory, completion on
 // `bar`.  The tensor map's box is one row high.

@@ -11,8 +11,8 @@
 //  * Persistent CTAs of 8 warps, 3 per SM.  128x128 bf16 tiles (32 KB)
 //    stream into a 2-stage shared-memory ring per CTA with 2-D TMA
 //    (cp.async.bulk.tensor), completion tracked by mbarriers; thread 0
-//    issues each load as soon as all warps are done with the stage it
-//    refills.
+//    refills a stage as soon as the tile's column codes, staged in it,
+//    have left by their TMA store.
 //  * Each tile arrives as two [128 x 64] halves with the 128-byte TMA
 //    swizzle (16-byte chunk q of row r stored at chunk q ^ (r % 8)), which
 //    makes both read patterns below free of shared-memory bank conflicts.
@@ -26,11 +26,14 @@
 //    registers, 2 CTAs of 3 stages: 27.0 -> 26.6 us per launch in the
 //    step).
 //  * Scaling uses packed f32x2 multiplies (exact: the scale is a power of
-//    two); each 1x32 block's row codes and each 32x1 block's column codes
-//    (the columnwise copy is written transposed) are 32 contiguous bytes,
-//    written with one 32-byte store (two 16-byte stores if a code buffer
-//    is only 16-byte aligned): full-sector writes cut the kernel's time by
-//    a sixth against 16-byte stores.
+//    two); each 1x32 block's row codes are 32 contiguous bytes, written
+//    with one 32-byte store (two 16-byte stores if the buffer is only
+//    16-byte aligned): full-sector writes cut the kernel's time by a sixth
+//    against 16-byte stores.  The column codes (the columnwise copy is
+//    written transposed) go into the tile's own stage once every warp has
+//    read it, and leave as one 128 x 128-byte TMA store: from registers
+//    each lane's 32-byte runs landed in 64 different rows of X^T per warp
+//    instruction.
 //  * A 128x128 tile owns exactly one 512-byte tile of the swizzled row
 //    scales and one of the swizzled column scales; both are assembled in
 //    shared memory and written out as one coalesced 512-byte store each
@@ -59,7 +62,6 @@ struct alignas(1024) Smem {
   alignas(16) uint8_t rscale[2][512];
   alignas(16) uint8_t cscale[2][512];
   alignas(8) uint64_t full[STAGES];
-  alignas(8) uint64_t empty[STAGES];
   int abort;
 };
 
@@ -90,6 +92,7 @@ __device__ __forceinline__ int stage_pos(int r, int c, int swizzled) {
 
 __global__ void __launch_bounds__(THREADS, 3)
     mxfp8_rowcol_kernel(const __grid_constant__ CUtensorMap tmap,
+                        const __grid_constant__ CUtensorMap tmap_c,
                         const Params p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(
@@ -98,10 +101,7 @@ __global__ void __launch_bounds__(THREADS, 3)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(smem_addr(&s.full[i]), 1);
-      mbar_init(smem_addr(&s.empty[i]), CONSUMER_WARPS);
-    }
+    for (int i = 0; i < STAGES; ++i) mbar_init(smem_addr(&s.full[i]), 1);
     s.abort = 0;
     fence_barrier_init();
   }
@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(THREADS, 3)
       }
     }
 
+    uint32_t q_lo[8], q_hi[8];            // this lane's two columns' codes
     if (ok && p.do_col) {
       uint32_t col[32];
 #pragma unroll
@@ -214,7 +215,6 @@ __global__ void __launch_bounds__(THREADS, 3)
       const uint32_t s_hi = e8m0_from_amax_bits(m >> 16);
       const float inv_lo = e8m0_inv_scale(s_lo);
       const float inv_hi = e8m0_inv_scale(s_hi);
-      uint32_t q_lo[8], q_hi[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         float l0, l1, l2, l3, h0, h1, h2, h3;
@@ -229,26 +229,44 @@ __global__ void __launch_bounds__(THREADS, 3)
         q_lo[j] = cvt_e4m3x2(l0, l1) | (cvt_e4m3x2(l2, l3) << 16);
         q_hi[j] = cvt_e4m3x2(h0, h1) | (cvt_e4m3x2(h2, h3) << 16);
       }
-      if (mb * 32 < rows_valid && c < cols_valid) {
-        uint8_t* dst = p.col_codes + (k0 + c) * p.M + m0 + mb * 32;
-        st_32B(dst, make_uint4(q_lo[0], q_lo[1], q_lo[2], q_lo[3]),
-               make_uint4(q_lo[4], q_lo[5], q_lo[6], q_lo[7]), p.wide);
-        st_32B(dst + p.M, make_uint4(q_hi[0], q_hi[1], q_hi[2], q_hi[3]),
-               make_uint4(q_hi[4], q_hi[5], q_hi[6], q_hi[7]), p.wide);
-      }
       s.cscale[par][stage_pos(c, mb, p.swizzled)] = (uint8_t)s_lo;
       s.cscale[par][stage_pos(c + 1, mb, p.swizzled)] = (uint8_t)s_hi;
     }
+    // Every warp must be done reading the tile before its stage takes the
+    // tile's column codes: [128 columns x 128 rows] bytes, column c's
+    // 32-byte run of block mb at bytes 32 mb of row c, in the 128-byte
+    // swizzle of the store's tensor map (16-byte chunk q of row r at
+    // q ^ (r % 8)); one TMA store then writes the whole tile.
+    if (p.do_col) named_barrier_sync(2, CONSUMER_WARPS * 32);  // uniform
+    if (ok && p.do_col) {
+      uint8_t* cst = reinterpret_cast<uint8_t*>(s.tile[stage]);
+      const int q0 = 2 * mb;
+      *reinterpret_cast<uint4*>(cst + c * 128 + ((q0 ^ (c & 7)) << 4)) =
+          make_uint4(q_lo[0], q_lo[1], q_lo[2], q_lo[3]);
+      *reinterpret_cast<uint4*>(cst + c * 128 + (((q0 + 1) ^ (c & 7)) << 4)) =
+          make_uint4(q_lo[4], q_lo[5], q_lo[6], q_lo[7]);
+      *reinterpret_cast<uint4*>(cst + (c + 1) * 128 + ((q0 ^ ((c + 1) & 7)) << 4)) =
+          make_uint4(q_hi[0], q_hi[1], q_hi[2], q_hi[3]);
+      *reinterpret_cast<uint4*>(cst + (c + 1) * 128 +
+                                (((q0 + 1) ^ ((c + 1) & 7)) << 4)) =
+          make_uint4(q_hi[4], q_hi[5], q_hi[6], q_hi[7]);
+      fence_proxy_async_smem();
+    }
 
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&s.empty[stage]));
-    // Refill: once all eight warps have read this stage, thread 0 loads the
-    // tile STAGES iterations ahead into it.
+    // All scale bytes (and the column codes) of this tile are staged.
+    named_barrier_sync(1, CONSUMER_WARPS * 32);
+    // Thread 0: the column codes leave by one TMA store (rows and columns
+    // past M and K are clipped by the tensor map); once the store has read
+    // the stage, the tile STAGES iterations ahead is loaded into it.
     if (threadIdx.x == 0) {
+      if (ok && p.do_col) {
+        tma_store_2d(&tmap_c, smem_addr(s.tile[stage]), (int32_t)m0,
+                     (int32_t)k0);
+        bulk_commit();
+        bulk_wait_read_0();
+      }
       const uint32_t next = t + (uint32_t)STAGES * gridDim.x;
-      if (next < p.num_tiles &&
-          mbar_wait(smem_addr(&s.empty[stage]), phase, &s.abort,
-                    &g_mxfp8_wait_error)) {
+      if (next < p.num_tiles && !s.abort) {
         const uint32_t nm = next / p.tiles_k, nk = next - nm * p.tiles_k;
         const uint32_t full = smem_addr(&s.full[stage]);
         mbar_arrive_expect_tx(full, TILE_BYTES);
@@ -258,10 +276,6 @@ __global__ void __launch_bounds__(THREADS, 3)
                     (int32_t)(nk * BK + HALF_COLS), (int32_t)(nm * BM), full);
       }
     }
-    __syncwarp();
-
-    // All scale bytes of this tile are staged.
-    named_barrier_sync(1, CONSUMER_WARPS * 32);
 
     if (ok) {
       if (p.swizzled) {
@@ -290,6 +304,7 @@ __global__ void __launch_bounds__(THREADS, 3)
     if (++stage == STAGES) { stage = 0; phase ^= 1; }
     par ^= 1;
   }
+  if (threadIdx.x == 0) bulk_wait_all();
   pdl_launch_dependents();
 }
 
@@ -335,6 +350,15 @@ cudaError_t launch_mxfp8_rowcol(const void* x, int64_t M, int64_t K,
   cudaError_t err = make_tmap_2d_bf16(&tmap, x, (uint64_t)K, (uint64_t)M,
                                       (uint64_t)ldx * 2, HALF_COLS, BM, true);
   if (err != cudaSuccess) return err;
+  // the columnwise codes X^T [K x M], stored by 128 x 128-byte boxes
+  CUtensorMap tmap_c;
+  if (col_codes) {
+    err = make_tmap_2d_bytes(&tmap_c, col_codes, (uint64_t)M, (uint64_t)K,
+                             (uint64_t)M, BM, BK);
+    if (err != cudaSuccess) return err;
+  } else {
+    tmap_c = tmap;                      // unused
+  }
   Params p;
   p.M = M;
   p.K = K;
@@ -367,7 +391,7 @@ cudaError_t launch_mxfp8_rowcol(const void* x, int64_t M, int64_t K,
   }
   const int64_t grid = imin<int64_t>((int64_t)p.num_tiles, (int64_t)sm_count(dev) * 3);
   return launch_pdl(mxfp8_rowcol_kernel, dim3((unsigned)grid), dim3(THREADS),
-                    smem, stream, false, tmap, p);
+                    smem, stream, false, tmap, tmap_c, p);
 }
 
 }  // namespace mxq
