@@ -234,10 +234,12 @@ __device__ __forceinline__ void encode_store(
 // no Philox state.  KEEP (no SR, rows of at most 4 x 32 blocks, e.g. hidden
 // 2048): pass 1 keeps each lane's transformed blocks in registers (64
 // values) and pass 2 encodes them, instead of reloading and transforming
-// the row again (ragged 132106 x 2048 with the RHT: 211 -> 179 us);
-// otherwise pass 2 reloads the row (from L1/L2) and transforms it again.
+// the row again (ragged 132106 x 2048 with the RHT: 211 -> 179 us); it
+// runs 3 CTAs per SM at 80 registers with a few values spilled to L1
+// (2 CTAs at 120 registers: 178 -> 170 us); otherwise pass 2 reloads the
+// row (from L1/L2) and transforms it again.
 template <bool SR, bool KEEP>
-__global__ void __launch_bounds__(RS_THREADS, (SR || KEEP) ? 2 : 4)
+__global__ void __launch_bounds__(RS_THREADS, SR ? 2 : (KEEP ? 3 : 4))
     nvfp4_rht_sr_kernel(const uint16_t* __restrict__ x, int64_t T,
                         int64_t T_pad, int64_t H, int64_t ldx, uint64_t seed,
                         int flags, uint8_t* __restrict__ codes,
