@@ -495,8 +495,11 @@ __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
                : "memory");
 }
 
+// Half-warp rows (the down projections) run 5 CTAs per SM (137 -> 126 us
+// at 128 experts); the full-warp shapes 4 (5 measured slower: gate/up 255
+// -> 292 us).
 template <int R, int WPR, int LPR>
-__global__ void __launch_bounds__(CTA_WARPS * 32, 4)
+__global__ void __launch_bounds__(CTA_WARPS * 32, LPR == 16 ? 5 : 4)
     nvfp4_weight_kernel(const __grid_constant__ GroupTable tab,
                         const __grid_constant__ GroupParams p) {
   constexpr int ROWS = CTA_WARPS / WPR * (32 / LPR);  // rows per row set
