@@ -365,7 +365,14 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 // one word per group serialises the hundreds of CTAs that finish together.
 // ---------------------------------------------------------------------------
 constexpr int kMaxGroupsPerLaunch = 256;
-constexpr int64_t kTaskChunks = 4096;         // 16-byte chunks per amax task
+// An amax task covers a whole number of rounds of kRoundChunks (one 32-byte
+// load pair per thread per round), about 1/kAmaxTasksPerGroup of its
+// group, from 2 to 8 rounds (64 to 256 KiB): fewer, longer amax tasks mean
+// fewer task claims and CTA barriers (128 gate/up pairs: 64 KiB tasks 255
+// us, 128 KiB 240, 256 KiB 234, 512 KiB 310; down: 126, 121, 127, 163).
+constexpr int64_t kRoundChunks = CTA_WARPS * 32 * 8;
+constexpr int64_t kAmaxTasksPerGroup = 24;
+constexpr int64_t kMinAmaxTasks = 1024;
 // Encode task: RowSets(R, WPR) sets of ROWS rows (ROWS = 8 / WPR, or 16
 // with half-warp rows).  Rows of at most 1024 values on full warps (R <= 2
 // blocks per lane) take 4 sets, 32 rows (short rows would otherwise make
@@ -379,6 +386,26 @@ __host__ __device__ constexpr int RowSets(int r, int wpr) {
 constexpr int kWsHeaderWords = 64;            // [1 + launch] = task counters
 constexpr int64_t kWindowBytes = 24ll << 20;  // input bytes per window
 constexpr int64_t kLeadWindows = 1;           // amax windows ahead, L
+
+// This thread's maximum over NR rounds of 32-byte loads from base (all of
+// a round's loads issued before its reduction; unrolled, so that the
+// compiler may issue a round's loads ahead of the previous reduction).
+template <int NR>
+__device__ __forceinline__ uint32_t rounds_amax(const uint16_t* base) {
+  uint32_t a = 0;
+#pragma unroll
+  for (int rr = 0; rr < NR; ++rr) {
+    uint4 v[8];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+      ld_stream_v8(base + ((int64_t)(rr * 4 + jj) * (CTA_WARPS * 32) +
+                           threadIdx.x) * 16,
+                   v[2 * jj], v[2 * jj + 1]);
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) a = max(a, chunk_absmax(v[jj]));
+  }
+  return a;
+}
 
 // Error word of the bounded waits of this translation unit.
 __device__ unsigned int g_nvfp4_wait_error = 0;
@@ -395,6 +422,7 @@ struct GroupParams {
   int64_t g0;                         // global index of local group 0
   int ng;                             // groups in this launch
   int64_t nA, nE;                     // amax / encode tasks per group
+  int64_t task_chunks;                // 16-byte chunks per amax task
   int64_t win;                        // groups per window (>= 1)
   int64_t lead;                       // windows of amax tasks ahead, L
   uint8_t* codes;                     // group g at g * R * K/2
@@ -547,31 +575,23 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, LPR == 16 ? 5 : 4)
     int64_t idx;
     task_of(p, t, &is_a, &gl, &idx);
     if (is_a) {
-      // ---- amax of 64 KiB of group gl ----
+      // ---- amax of one task (2, 4 or 8 rounds, 64 to 256 KiB) of group gl ----
       uint32_t a = 0;
-      const int64_t q0 = idx * kTaskChunks;
+      const int64_t q0 = idx * p.task_chunks;
       // The task's chunks usually lie in one part: then one base pointer
       // and 32-byte loads (pairs of chunks); otherwise a part lookup per
       // 16-byte chunk.
       int pi = 0;
       while (pi + 1 < p.num_parts && q0 >= p.part_chunk0[pi + 1]) ++pi;
-      const bool one_part = p.wide && q0 + kTaskChunks <= p.part_chunk0[pi + 1];
+      const bool one_part = p.wide && q0 + p.task_chunks <= p.part_chunk0[pi + 1];
       if (one_part && !s_abort) {
         const uint16_t* base = tab.part[gl][pi] + (q0 - p.part_chunk0[pi]) * 8;
-#pragma unroll
-        for (int rr = 0; rr < (int)(kTaskChunks / (CTA_WARPS * 32 * 8)); ++rr) {
-          uint4 v[8];
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-            ld_stream_v8(base + ((int64_t)(rr * 4 + jj) * (CTA_WARPS * 32) +
-                                 threadIdx.x) * 16,
-                         v[2 * jj], v[2 * jj + 1]);
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) a = max(a, chunk_absmax(v[jj]));
-        }
+        const int64_t nr = p.task_chunks / kRoundChunks;
+        a = nr == 8 ? rounds_amax<8>(base) : nr == 4 ? rounds_amax<4>(base)
+                                                     : rounds_amax<2>(base);
       } else {
 #pragma unroll
-        for (int rr = 0; rr < (int)(kTaskChunks / (CTA_WARPS * 32 * 8)); ++rr) {
+        for (int64_t rr = 0; rr < p.task_chunks / kRoundChunks; ++rr) {
           uint4 v[8];
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
@@ -799,7 +819,20 @@ cudaError_t launch_nvfp4_weight_shared(
   p.R = p.part_row0[num_parts];
   p.R_pad = swizzled ? (p.R + 127) / 128 * 128 : p.R;
   p.K = K;
-  p.nA = (p.part_chunk0[num_parts] + kTaskChunks - 1) / kTaskChunks;
+  {
+    // 2, 4 or 8 rounds: about kAmaxTasksPerGroup tasks per group, but at
+    // least kMinAmaxTasks in the call (a small call needs many tasks to
+    // fill the GPU)
+    const int64_t gc = p.part_chunk0[num_parts];
+    int64_t rounds = 8;
+    while (rounds > 2 && (gc / (rounds * kRoundChunks) < kAmaxTasksPerGroup ||
+                          num_groups * ((gc + rounds * kRoundChunks - 1) /
+                                        (rounds * kRoundChunks)) <
+                              kMinAmaxTasks))
+      rounds /= 2;
+    p.task_chunks = rounds * kRoundChunks;
+    p.nA = (gc + p.task_chunks - 1) / p.task_chunks;
+  }
   const int64_t rows_per_task =
       RowSets(sh.R, sh.WPR) * (CTA_WARPS / sh.WPR) * (32 / sh.LPR);
   p.nE = (p.R_pad + rows_per_task - 1) / rows_per_task;
