@@ -387,26 +387,6 @@ constexpr int kWsHeaderWords = 64;            // [1 + launch] = task counters
 constexpr int64_t kWindowBytes = 24ll << 20;  // input bytes per window
 constexpr int64_t kLeadWindows = 1;           // amax windows ahead, L
 
-// This thread's maximum over NR rounds of 32-byte loads from base (all of
-// a round's loads issued before its reduction; unrolled, so that the
-// compiler may issue a round's loads ahead of the previous reduction).
-template <int NR>
-__device__ __forceinline__ uint32_t rounds_amax(const uint16_t* base) {
-  uint32_t a = 0;
-#pragma unroll
-  for (int rr = 0; rr < NR; ++rr) {
-    uint4 v[8];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
-      ld_stream_v8(base + ((int64_t)(rr * 4 + jj) * (CTA_WARPS * 32) +
-                           threadIdx.x) * 16,
-                   v[2 * jj], v[2 * jj + 1]);
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) a = max(a, chunk_absmax(v[jj]));
-  }
-  return a;
-}
-
 // Error word of the bounded waits of this translation unit.
 __device__ unsigned int g_nvfp4_wait_error = 0;
 
@@ -422,7 +402,6 @@ struct GroupParams {
   int64_t g0;                         // global index of local group 0
   int ng;                             // groups in this launch
   int64_t nA, nE;                     // amax / encode tasks per group
-  int64_t task_chunks;                // 16-byte chunks per amax task
   int64_t win;                        // groups per window (>= 1)
   int64_t lead;                       // windows of amax tasks ahead, L
   uint8_t* codes;                     // group g at g * R * K/2
@@ -526,11 +505,12 @@ __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
 // Half-warp rows (the down projections) run 5 CTAs per SM (137 -> 126 us
 // at 128 experts); the full-warp shapes 4 (5 measured slower: gate/up 255
 // -> 292 us).
-template <int R, int WPR, int LPR>
+template <int R, int WPR, int LPR, int NR>
 __global__ void __launch_bounds__(CTA_WARPS * 32, LPR == 16 ? 5 : 4)
     nvfp4_weight_kernel(const __grid_constant__ GroupTable tab,
                         const __grid_constant__ GroupParams p) {
   constexpr int ROWS = CTA_WARPS / WPR * (32 / LPR);  // rows per row set
+  constexpr int64_t kTaskChunks = NR * kRoundChunks;  // per amax task
   __shared__ uint32_t red[CTA_WARPS];
   __shared__ int s_abort;
   __shared__ int64_t s_task[2];
@@ -577,21 +557,34 @@ __global__ void __launch_bounds__(CTA_WARPS * 32, LPR == 16 ? 5 : 4)
     if (is_a) {
       // ---- amax of one task (2, 4 or 8 rounds, 64 to 256 KiB) of group gl ----
       uint32_t a = 0;
-      const int64_t q0 = idx * p.task_chunks;
+      const int64_t q0 = idx * kTaskChunks;
       // The task's chunks usually lie in one part: then one base pointer
       // and 32-byte loads (pairs of chunks); otherwise a part lookup per
       // 16-byte chunk.
       int pi = 0;
       while (pi + 1 < p.num_parts && q0 >= p.part_chunk0[pi + 1]) ++pi;
-      const bool one_part = p.wide && q0 + p.task_chunks <= p.part_chunk0[pi + 1];
+      const bool one_part = p.wide && q0 + kTaskChunks <= p.part_chunk0[pi + 1];
       if (one_part && !s_abort) {
         const uint16_t* base = tab.part[gl][pi] + (q0 - p.part_chunk0[pi]) * 8;
-        const int64_t nr = p.task_chunks / kRoundChunks;
-        a = nr == 8 ? rounds_amax<8>(base) : nr == 4 ? rounds_amax<4>(base)
-                                                     : rounds_amax<2>(base);
+        // NR rounds of 32-byte loads, a round's loads issued before its
+        // reduction.  NR is a template parameter and the loop is written
+        // here rather than in a helper: either change alone measured 181
+        // instead of 174 us for the encode tasks at 128 gate/up pairs with
+        // the scales given (a different register allocation of the loop).
+#pragma unroll
+        for (int rr = 0; rr < NR; ++rr) {
+          uint4 v[8];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            ld_stream_v8(base + ((int64_t)(rr * 4 + jj) * (CTA_WARPS * 32) +
+                                 threadIdx.x) * 16,
+                         v[2 * jj], v[2 * jj + 1]);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) a = max(a, chunk_absmax(v[jj]));
+        }
       } else {
 #pragma unroll
-        for (int64_t rr = 0; rr < p.task_chunks / kRoundChunks; ++rr) {
+        for (int rr = 0; rr < NR; ++rr) {
           uint4 v[8];
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
@@ -776,14 +769,14 @@ cudaError_t nvfp4_take_wait_error(unsigned int* word) {
 
 namespace {
 
-template <int R, int WPR, int LPR = 32>
-cudaError_t launch_weight_tasks(const GroupTable& tab, const GroupParams& p,
-                                int dev, cudaStream_t stream) {
+template <int R, int WPR, int LPR, int NR>
+cudaError_t launch_weight_nr(const GroupTable& tab, const GroupParams& p,
+                             int dev, cudaStream_t stream) {
   static int occ[64] = {};
   int n = (dev >= 0 && dev < 64) ? occ[dev] : 0;
   if (n == 0) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &n, nvfp4_weight_kernel<R, WPR, LPR>, CTA_WARPS * 32, 0);
+        &n, nvfp4_weight_kernel<R, WPR, LPR, NR>, CTA_WARPS * 32, 0);
     if (e != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;
     if (dev >= 0 && dev < 64) occ[dev] = n;
@@ -791,8 +784,17 @@ cudaError_t launch_weight_tasks(const GroupTable& tab, const GroupParams& p,
   const unsigned grid = (unsigned)(n * sm_count(dev));
   // No co-residency is needed: a CTA only waits for tasks that running
   // CTAs hold.
-  return launch_pdl(nvfp4_weight_kernel<R, WPR, LPR>, dim3(grid),
+  return launch_pdl(nvfp4_weight_kernel<R, WPR, LPR, NR>, dim3(grid),
                     dim3(CTA_WARPS * 32), 0, stream, false, tab, p);
+}
+
+// rounds: 2, 4 or 8 rounds of kRoundChunks per amax task
+template <int R, int WPR, int LPR = 32>
+cudaError_t launch_weight_tasks(const GroupTable& tab, const GroupParams& p,
+                                int rounds, int dev, cudaStream_t stream) {
+  if (rounds == 8) return launch_weight_nr<R, WPR, LPR, 8>(tab, p, dev, stream);
+  if (rounds == 4) return launch_weight_nr<R, WPR, LPR, 4>(tab, p, dev, stream);
+  return launch_weight_nr<R, WPR, LPR, 2>(tab, p, dev, stream);
 }
 
 }  // namespace
@@ -819,19 +821,19 @@ cudaError_t launch_nvfp4_weight_shared(
   p.R = p.part_row0[num_parts];
   p.R_pad = swizzled ? (p.R + 127) / 128 * 128 : p.R;
   p.K = K;
+  int64_t rounds;
   {
     // 2, 4 or 8 rounds: about kAmaxTasksPerGroup tasks per group, but at
     // least kMinAmaxTasks in the call (a small call needs many tasks to
     // fill the GPU)
     const int64_t gc = p.part_chunk0[num_parts];
-    int64_t rounds = 8;
+    rounds = 8;
     while (rounds > 2 && (gc / (rounds * kRoundChunks) < kAmaxTasksPerGroup ||
                           num_groups * ((gc + rounds * kRoundChunks - 1) /
                                         (rounds * kRoundChunks)) <
                               kMinAmaxTasks))
       rounds /= 2;
-    p.task_chunks = rounds * kRoundChunks;
-    p.nA = (gc + p.task_chunks - 1) / p.task_chunks;
+    p.nA = (gc + rounds * kRoundChunks - 1) / (rounds * kRoundChunks);
   }
   const int64_t rows_per_task =
       RowSets(sh.R, sh.WPR) * (CTA_WARPS / sh.WPR) * (32 / sh.LPR);
@@ -881,13 +883,13 @@ cudaError_t launch_nvfp4_weight_shared(
     p.g0 = g0;
     p.ng = ng;
     p.counter = ws ? ws + 1 + g0 / kMaxGroupsPerLaunch : nullptr;
-    if (sh.LPR == 16) err = launch_weight_tasks<3, 1, 16>(tab, p, dev, stream);
-    else if (sh.R == 1) err = launch_weight_tasks<1, 1>(tab, p, dev, stream);
-    else if (sh.R == 2) err = launch_weight_tasks<2, 1>(tab, p, dev, stream);
-    else if (sh.WPR == 1) err = launch_weight_tasks<4, 1>(tab, p, dev, stream);
-    else if (sh.WPR == 2) err = launch_weight_tasks<4, 2>(tab, p, dev, stream);
-    else if (sh.WPR == 4) err = launch_weight_tasks<4, 4>(tab, p, dev, stream);
-    else err = launch_weight_tasks<4, 8>(tab, p, dev, stream);
+    if (sh.LPR == 16) err = launch_weight_tasks<3, 1, 16>(tab, p, (int)rounds, dev, stream);
+    else if (sh.R == 1) err = launch_weight_tasks<1, 1>(tab, p, (int)rounds, dev, stream);
+    else if (sh.R == 2) err = launch_weight_tasks<2, 1>(tab, p, (int)rounds, dev, stream);
+    else if (sh.WPR == 1) err = launch_weight_tasks<4, 1>(tab, p, (int)rounds, dev, stream);
+    else if (sh.WPR == 2) err = launch_weight_tasks<4, 2>(tab, p, (int)rounds, dev, stream);
+    else if (sh.WPR == 4) err = launch_weight_tasks<4, 4>(tab, p, (int)rounds, dev, stream);
+    else err = launch_weight_tasks<4, 8>(tab, p, (int)rounds, dev, stream);
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;
