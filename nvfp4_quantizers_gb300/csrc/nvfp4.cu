@@ -502,11 +502,13 @@ __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
                : "memory");
 }
 
-// Half-warp rows (the down projections) run 5 CTAs per SM (137 -> 126 us
-// at 128 experts); the full-warp shapes 4 (5 measured slower: gate/up 255
-// -> 292 us).
+// Half-warp rows (the down projections) run 5 CTAs per SM at 48 registers
+// (137 -> 126 us at 128 experts); the full-warp shapes 4 at 56 (5 measured
+// slower: gate/up 255 -> 292 us; the 64 registers of 4 CTAs per SM spilled
+// 16-24 bytes in the encode loop, 56 spill none at 2048 values a row: 128
+// gate/up pairs 234.7 -> 229.6 us).
 template <int R, int WPR, int LPR, int NR>
-__global__ void __launch_bounds__(CTA_WARPS * 32, LPR == 16 ? 5 : 4)
+__global__ void __maxnreg__(LPR == 16 ? 48 : 56)
     nvfp4_weight_kernel(const __grid_constant__ GroupTable tab,
                         const __grid_constant__ GroupParams p) {
   constexpr int ROWS = CTA_WARPS / WPR * (32 / LPR);  // rows per row set
