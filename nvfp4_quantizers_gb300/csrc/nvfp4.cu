@@ -24,8 +24,9 @@
 // IEEE intrinsics and cvt.rn.satfinite.e2m1x2; one 8-byte code store per
 // block, four block scales gathered by shuffles into one 32-bit store (four
 // consecutive scale columns are contiguous in both layouts).  Weight groups
-// use one persistent task-list kernel (see below): all amax tasks, then all
-// encode tasks, so the second read of a group is served from L2.
+// use one persistent task-list kernel (see below): the amax tasks of a
+// window of groups run ahead of that window's encode tasks, so the second
+// read of a group is served from L2.
 #include <float.h>
 
 #include "common.cuh"
@@ -342,9 +343,9 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 
 // ---------------------------------------------------------------------------
 // Weight groups: one persistent kernel working through a task list.  Per
-// group g there are nA amax tasks (64 KiB of the group each) and nE encode
-// tasks (2 or 4 sets of ROWS rows); an encode task needs its group's S, i.e.
-// every amax task of the group.  Groups are taken in windows of about
+// group g there are nA amax tasks (64 to 256 KiB of the group each) and
+// nE encode tasks (2 or 4 sets of ROWS rows); an encode task needs its
+// group's S, i.e. every amax task of the group.  Groups are taken in windows of about
 // 24 MB of input, and the list runs A(0) A(1) E(0) A(2) E(1) ... E(last):
 // the amax tasks of a window, then those of the next window, then the
 // encode tasks of the first one (task_of has the general form with the
