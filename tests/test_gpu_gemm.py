@@ -107,8 +107,8 @@ def test_gemm_nvfp4_grouped_small(mxq, rows, K, N):
 
 def test_gemm_mxfp8_many_tiles_per_cta(mxq):
     """320 output tiles over at most 152 persistent CTAs: every CTA runs
-    two or three tiles, alternating its two tensor-memory accumulators,
-    and the 3-stage K loop wraps the 4-deep operand ring across tiles.
+    two or three tiles through its tensor-memory accumulator, and the
+    3-stage K loop wraps the 4-deep operand ring across tiles.
     Every element of C is checked."""
     C, ref = _mxfp8_case(mxq, 2048, 384, 2560, seed=11)
     assert rel_fro(C, ref) <= TOL
@@ -118,6 +118,37 @@ def test_gemm_mxfp8_many_tiles_per_cta(mxq):
         for j in range(0, 2560, 128):
             assert rel_fro(C[i:i + 128, j:j + 128],
                            ref[i:i + 128, j:j + 128]) <= TOL, (i, j)
+
+
+def test_gemm_mxfp8_strided_unaligned_c(mxq):
+    """C with a row stride of N + 4 floats and its base 16 bytes past a
+    32-byte boundary (the epilogue's 16-byte store path instead of whole
+    32-byte sectors), N = 384 so the second column tile holds 128 valid
+    columns: C is byte-identical to the contiguous call's, and every byte
+    around it keeps its sentinel."""
+    M, K, N = 256, 256, 384
+    rng = np.random.default_rng(21)
+    A = W.to_bf16_bits(rng.standard_normal((M, K)))
+    B = W.to_bf16_bits(0.02 * rng.standard_normal((K, N)))
+    qa = mxq.mxfp8_quantize_rowcol(dev_bf16(A), rowwise=True, colwise=False)
+    qb = mxq.mxfp8_quantize_rowcol(dev_bf16(B), rowwise=False, colwise=True)
+    ref = mxq.gemm_mxfp8(qa.row_codes, qa.row_scales, qb.col_codes_t,
+                         qb.col_scales_t)
+    ldc = N + 4
+    buf = torch.full((M * ldc + 8,), -7.0, dtype=torch.float32, device="cuda")
+    C = buf[4:4 + M * ldc]
+    assert C.data_ptr() % 32 == 16
+    st = mxq.lib().mxq_gemm_mxfp8(
+        qa.row_codes.data_ptr(), qa.row_scales.data_ptr(),
+        qb.col_codes_t.data_ptr(), qb.col_scales_t.data_ptr(), M, N, K,
+        C.data_ptr(), ldc, torch.cuda.current_stream().cuda_stream)
+    assert st == 0, mxq.status_string(st)
+    torch.cuda.synchronize()
+    got = C.view(M, ldc)
+    assert torch.equal(got[:, :N].contiguous().view(torch.int32),
+                       ref.view(torch.int32))
+    assert bool((got[:, N:] == -7.0).all())
+    assert bool((buf[:4] == -7.0).all()) and bool((buf[4 + M * ldc:] == -7.0).all())
 
 
 def test_gemm_nvfp4_grouped_many_tiles_per_cta(mxq):

@@ -116,10 +116,51 @@ def _moe_case(q, rows_per_group, F, K, seed):
                                       ([128, 256, 0, 128], 256, 512),
                                       ([384, 128, 256], 384, 1024)])
 def test_moe_swiglu_small(mxq, rows, F, K):
-    """Ragged groups (one empty), F with odd and even tile counts (2-CTA
-    clusters only for even), several stages per tile."""
+    """Ragged groups (one empty), F with odd and even tile counts, several
+    stages per tile."""
     got, ref, _ = _moe_case(mxq, rows, F, K, seed=sum(rows) + F + K)
     _check_h(got, ref, f"rows={rows} F={F} K={K}")
+
+
+def test_moe_swiglu_strided_unaligned_h(mxq):
+    """h with a row stride of F + 8 bf16 and its base 16 bytes past a
+    32-byte boundary (the epilogue's 16-byte store path): h is
+    byte-identical to the contiguous call's, and every byte around it keeps
+    its sentinel."""
+    rng = np.random.default_rng(31)
+    F, K, rows = 256, 512, [128, 256]
+    T_src = 256
+    x = W.to_bf16_bits(rng.standard_normal((T_src, K)).astype(np.float32))
+    idx = rng.integers(0, T_src, sum(rows)).astype(np.int32)
+    offs = np.array([0, rows[0], rows[0] + rows[1]], np.int64)
+    Wg = [W.to_bf16_bits(0.05 * rng.standard_normal((F, K)).astype(np.float32))
+          for _ in rows]
+    Wu = [W.to_bf16_bits(0.05 * rng.standard_normal((F, K)).astype(np.float32))
+          for _ in rows]
+    ta = mxq.nvfp4_quantize_per_token_gather(dev_bf16(x),
+                                             torch.from_numpy(idx).cuda())
+    tw = mxq.nvfp4_quantize_weight_shared(
+        [[dev_bf16(Wg[g]), dev_bf16(Wu[g])] for g in range(len(rows))])
+    ref = mxq.moe_gate_up_swiglu(ta.codes, ta.block_scales, ta.scales, offs,
+                                 tw.codes, tw.block_scales, tw.scales)
+    M = int(offs[-1])
+    ldh = F + 8
+    buf = torch.full((M * ldh + 16,), 12345, dtype=torch.int16, device="cuda")
+    h = buf[8:8 + M * ldh]
+    assert h.data_ptr() % 32 == 16
+    import ctypes
+    off_arr = (ctypes.c_int64 * len(offs))(*[int(v) for v in offs])
+    st = mxq.lib().mxq_moe_gate_up_swiglu_nvfp4(
+        ta.codes.data_ptr(), ta.block_scales.data_ptr(), ta.scales.data_ptr(),
+        ctypes.cast(off_arr, ctypes.c_void_p), len(rows), tw.codes.data_ptr(),
+        tw.block_scales.data_ptr(), tw.scales.data_ptr(), F, K, h.data_ptr(),
+        ldh, torch.cuda.current_stream().cuda_stream)
+    assert st == 0, mxq.status_string(st)
+    torch.cuda.synchronize()
+    got = h.view(M, ldh)
+    assert torch.equal(got[:, :F].contiguous(), ref.view(torch.int16))
+    assert bool((got[:, F:] == 12345).all())
+    assert bool((buf[:8] == 12345).all()) and bool((buf[8 + M * ldh:] == 12345).all())
 
 
 def test_moe_swiglu_many_tiles_per_cta(mxq):
