@@ -272,6 +272,15 @@ def test_nvfp4_hidden_sizes(mxq, H):
 
 
 @pytest.mark.parametrize("lay", LAYOUTS)
+def test_nvfp4_tokens_16_byte_aligned(mxq, lay):
+    """Tokens whose rows start 16 bytes past a 32-byte boundary (the
+    16-byte load path), hidden 2048 and 768."""
+    for H in (2048, 768):
+        x = W.ragged_tokens([3, 130, 61], H=H)
+        check_nvfp4_tokens(mxq, x, lay, x_dev=_dev_bf16_shift16(x))
+
+
+@pytest.mark.parametrize("lay", LAYOUTS)
 def test_nvfp4_edge_tokens(mxq, lay):
     """All-zero token, subnormal FP32 scale, all +-2688, all +-bf16 max,
     one huge channel (block scales that round to zero), E2M1 midpoints."""
@@ -348,8 +357,20 @@ def test_nvfp4_full_ragged_batch_sampled(mxq):
 # --------------------------------------------------------------------------
 # NVFP4 weights with a shared FP32 scale
 # --------------------------------------------------------------------------
-def check_weight_groups(q, groups_bits, lay, S_in=None):
-    groups = [[dev_bf16(p) for p in g] for g in groups_bits]
+def _dev_bf16_shift16(bits):
+    """bits on the device 16 bytes past a 32-byte boundary (inside a
+    larger allocation), so that 32-byte loads are not allowed."""
+    rows, cols = bits.shape
+    buf = torch.empty(rows * cols + 8, dtype=torch.bfloat16, device="cuda")
+    view = buf[8:8 + rows * cols].view(rows, cols)
+    view.copy_(dev_bf16(bits))
+    assert view.data_ptr() % 32 == 16
+    return view
+
+
+def check_weight_groups(q, groups_bits, lay, S_in=None, shift16=False):
+    place = _dev_bf16_shift16 if shift16 else dev_bf16
+    groups = [[place(p) for p in g] for g in groups_bits]
     S_dev = None if S_in is None else torch.from_numpy(S_in).cuda()
     r = q.nvfp4_quantize_weight_shared(groups, S_dev, lay)
     y = q.dequantize_nvfp4(r.codes, r.block_scales, r.scales, lay)
@@ -427,6 +448,22 @@ def test_weight_wide_rows_and_slices(mxq, lay):
                W.to_bf16_bits(rng.standard_normal((200, 1552)) * 0.5 * s)]
               for s in (2e-3, 1.0, 50.0)]
     check_weight_groups(mxq, groups, lay)
+
+
+@pytest.mark.parametrize("lay", LAYOUTS)
+def test_weight_parts_16_byte_aligned(mxq, lay):
+    """Parts whose base lies 16 bytes past a 32-byte boundary: every amax
+    task takes the general path (a part lookup per 16-byte chunk) and every
+    row the 16-byte loads; gate/up-like pairs (2048 values a row) and
+    down-like parts (768 values a row, half-warp rows)."""
+    rng = np.random.default_rng(13)
+    pairs = [[W.to_bf16_bits(rng.standard_normal((200, 2048)) * s),
+              W.to_bf16_bits(rng.standard_normal((300, 2048)) * 0.5 * s)]
+             for s in (0.01, 3.0)]
+    check_weight_groups(mxq, pairs, lay, shift16=True)
+    downs = [[W.to_bf16_bits(rng.standard_normal((256, 768)) * s)]
+             for s in (0.2, 40.0, 1e-3)]
+    check_weight_groups(mxq, downs, lay, shift16=True)
 
 
 def test_weight_windows(mxq):
