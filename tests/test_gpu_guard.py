@@ -8,6 +8,8 @@ scale column), single rows, a 32-row tail, N = 128 mod 256 for the GEMMs --
 and the bands must be untouched afterwards, so a kernel that writes past
 either end of any output is caught.  The bytes between the bands must equal
 the outputs of the same call through the Python binding (fresh buffers).
+Every test runs twice: with each output 32-byte aligned, and with each
+output 16 bytes past a 32-byte boundary (the kernels' 16-byte store paths).
 """
 import ctypes
 
@@ -22,6 +24,15 @@ pytestmark = pytest.mark.gpu
 
 BAND = 4096
 CANARY = 0xA5
+SHIFT = 0            # bytes past a 32-byte boundary for every output
+
+
+@pytest.fixture(params=[0, 16], ids=["aligned32", "shift16"], autouse=True)
+def _output_shift(request):
+    global SHIFT
+    SHIFT = request.param
+    yield
+    SHIFT = 0
 
 
 @pytest.fixture(scope="module")
@@ -40,23 +51,25 @@ class Guarded:
 
     def __init__(self, nbytes):
         self.n = int(nbytes)
-        self.buf = torch.full((BAND + self.n + BAND,), CANARY, dtype=torch.uint8,
-                              device="cuda")
+        self.lo = BAND + SHIFT
+        self.buf = torch.full((self.lo + self.n + BAND,), CANARY,
+                              dtype=torch.uint8, device="cuda")
+        assert (self.buf.data_ptr() + self.lo) % 32 == SHIFT
 
     @property
     def ptr(self):
-        return self.buf.data_ptr() + BAND
+        return self.buf.data_ptr() + self.lo
 
     def body(self):
-        return self.buf[BAND:BAND + self.n]
+        return self.buf[self.lo:self.lo + self.n]
 
     def check(self, what):
         torch.cuda.synchronize()
-        lo = self.buf[:BAND].cpu().numpy()
-        hi = self.buf[BAND + self.n:].cpu().numpy()
+        lo = self.buf[:self.lo].cpu().numpy()
+        hi = self.buf[self.lo + self.n:].cpu().numpy()
         bad_lo = np.nonzero(lo != CANARY)[0]
         bad_hi = np.nonzero(hi != CANARY)[0]
-        assert bad_lo.size == 0, f"{what}: {bad_lo.size} bytes written before the buffer (last at -{BAND - bad_lo[-1]})"
+        assert bad_lo.size == 0, f"{what}: {bad_lo.size} bytes written before the buffer (last at -{self.lo - bad_lo[-1]})"
         assert bad_hi.size == 0, f"{what}: {bad_hi.size} bytes written after the buffer (first at +{bad_hi[0]})"
 
 
