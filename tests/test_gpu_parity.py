@@ -160,6 +160,14 @@ def test_mxfp8_strided_input(mxq):
                 x_dev=dev)
 
 
+def test_mxfp8_input_16_byte_aligned(mxq):
+    """The input 16 bytes past a 32-byte boundary (the tensor maps need 16),
+    with a ragged 96-row tail tile and a 32-column tail."""
+    x = W.mxfp8_random(224, 416, seed=9)
+    check_mxfp8(mxq, x, "swizzled", x_dev=_dev_bf16_shift16(x))
+    check_mxfp8(mxq, x, "linear", x_dev=_dev_bf16_shift16(x))
+
+
 def _bands(M, n, seed):
     rng = np.random.default_rng(seed)
     b = rng.choice(M // 32, n, replace=False)
