@@ -346,15 +346,15 @@ __global__ void __launch_bounds__(CTA_WARPS * 32)
 // group g there are nA amax tasks (64 to 256 KiB of the group each) and
 // nE encode tasks (2 or 4 sets of ROWS rows); an encode task needs its
 // group's S, i.e. every amax task of the group.  Groups are taken in windows of about
-// 24 MB of input, and the list runs A(0) A(1) E(0) A(2) E(1) ... E(last):
-// the amax tasks of a window, then those of the next window, then the
-// encode tasks of the first one (task_of has the general form with the
-// amax tasks L windows ahead; L = 1 measured best: 24 MB windows 248 us,
-// 32 MB 261 us, 48 MB 287 us, 16 MB x L = 2 262 us for 128 gate/up pairs).
+// 12 MB of input, and the list runs A(0) .. A(L-1), then A(w+L) E(w) for
+// w = 0, 1, ...: the amax tasks L windows ahead of the encode tasks, with
+// L windows making about 36 MB (128 gate/up pairs: 12 MB x 3 or 6 MB x 6
+// 224 us; 24 MB x 1 230 us, 6 MB x 5 249 us, 12 MB x 4 231 us: a shorter
+// lead leaves encode tasks waiting for S, a longer one overflows L2).
 // CTAs take tasks in list order from an atomic counter, so an encode task
 // only ever waits (bounded) for amax tasks that running CTAs already hold,
-// and by the time it is handed out a window of amax tasks and one of encode
-// tasks separate it from its group's; the two windows in flight stay in
+// and by the time it is handed out L windows of amax and encode tasks
+// separate it from its group's; the windows in flight stay in
 // the 126 MB L2, so the encode tasks read their rows back from L2 however
 // many groups a call holds (those reads mark the lines first to evict, so
 // lines still waiting for their second read outlive the ones read twice).
@@ -385,8 +385,8 @@ __host__ __device__ constexpr int RowSets(int r, int wpr) {
   return (wpr == 1 && r <= 2) ? 4 : 2;
 }
 constexpr int kWsHeaderWords = 64;            // [1 + launch] = task counters
-constexpr int64_t kWindowBytes = 24ll << 20;  // input bytes per window
-constexpr int64_t kLeadWindows = 1;           // amax windows ahead, L
+constexpr int64_t kWindowBytes = 12ll << 20;  // input bytes per window
+constexpr int64_t kLeadBytes = 36ll << 20;    // amax lead, L windows
 
 // Error word of the bounded waits of this translation unit.
 __device__ unsigned int g_nvfp4_wait_error = 0;
@@ -846,7 +846,8 @@ cudaError_t launch_nvfp4_weight_shared(
   // a call whose whole input stays in L2 runs as one window (8 gate/up
   // pairs of [1024 x 2048], 64 MB: 44.6 -> 40.8 us)
   if (num_groups * p.R * K * 2 <= (64ll << 20)) p.win = num_groups;
-  p.lead = kLeadWindows;
+  p.lead = kLeadBytes / (p.win * p.R * K * 2);
+  if (p.lead < 1) p.lead = 1;
   p.done = ws ? ws + kWsHeaderWords + num_groups : nullptr;
   p.codes = codes;
   p.scales = scales;
